@@ -1,0 +1,406 @@
+#!/usr/bin/env python
+"""Benchmark: GDN chunked-prefill forward + backward through the C ABI.
+
+One step = gdr_fwd (o, final_state, A) followed by gdr_bwd (dq, dk, dv, dbeta,
+dg, dh0) over one synthetic batch: every step of the hot path.  The default
+workload is the context-parallel forward case B=1, T=8192, Hq=4, Hv=8,
+K=V=128 (bf16 q/k/v, fp32 g/beta, 30% of v-heads with g == 0) with do ~ N(0,1)
+and dht ~ N(0, 0.1) drawn for the backward.
+
+Timing: W untimed warm-up steps, then K steps bracketed by a barrier and
+torch.cuda.synchronize() on both sides; each step is timed with CUDA events on
+the launching stream after an L2 flush (a 256 MiB write), and the value is the
+tokens of all ranks divided by the slowest rank's summed step time.  Each
+kernel is also bracketed by caller-owned events (gdr_opts.events); the
+dominant kernel's algorithmic work over its measured duration gives the
+roofline fraction.
+
+``--impl reference`` times the fp64 CPU oracle (the reference arm of this
+build) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "GDN chunked-prefill fwd/bwd Mtokens/s at 1 GB300; % of bf16 roofline"
+DEFAULT_WORKLOAD = "fwd_bf16_T8192_hq4_hv8_d128"
+FLUSH_BYTES = 256 << 20
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        return {"hbm_gbs": pk["hbm_gbs"], "bf16_tflops": pk["bf16_tflops"],
+                "bf16_tflops_sustained": pk.get("bf16_tflops_sustained", pk["bf16_tflops"]),
+                "sm_max_mhz": pk.get("sm_max_mhz", 2070.0), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2070.0,
+            "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work per kernel launch (inputs read once, outputs written once)
+# ---------------------------------------------------------------------------
+C = 64
+
+
+def kernel_work(name, spec, in_bytes, o_bytes, nchunk_heads):
+    """(flops, bytes) of one launch of kernel `name` over the whole problem.
+
+    Units: one (chunk, v-head) pair; tokens-heads = tokens * Hv.  Counts dense
+    contractions (2 flops per MAC, causal products halved) and the HBM bytes the
+    kernel must move at least: its inputs once and its outputs once."""
+    K, V, Hv, Hq = spec.K, spec.V, spec.Hv, spec.Hq
+    G = Hv // Hq
+    th = spec.tokens * Hv                      # token-heads
+    qk = spec.tokens * Hq * K * in_bytes       # one of q or k
+    vv = spec.tokens * Hv * V * in_bytes
+    gb = spec.tokens * Hv * 4                  # one of g or beta
+    A = spec.tokens * Hv * C * 4
+    st = spec.n_seqs * Hv * K * V * 4          # one state tensor
+    wy_fl = nchunk_heads * (2 * C * C * K / G + 2 * C * C * K / G   # K K^T, Q K^T (shared by the group)
+                            + C ** 3 / 3 * 2                        # triangular inverse
+                            + 2 * C * C * K / 2 + 2 * C * C * V / 2)  # W, U (triangular A)
+    scan_fl = nchunk_heads * (6 * C * K * V + C * C * V)
+    if name.endswith("wy"):
+        return wy_fl, 2 * qk + vv + 2 * gb + A
+    if name.endswith("wy_from_A"):
+        return wy_fl - nchunk_heads * (C ** 3 / 3 * 2), 2 * qk + vv + 2 * gb + A
+    if name.endswith("scan"):
+        return scan_fl, 2 * qk + vv + 2 * gb + th * V * o_bytes + st
+    if name.endswith("scan_states"):
+        return nchunk_heads * 4 * C * K * V, 2 * qk + vv + 2 * gb
+    if name.endswith("dh"):
+        return nchunk_heads * (6 * C * K * V + C * C * V), 2 * qk + vv + 2 * gb + st * 2
+    if name.endswith("bwd_chunk"):
+        return (nchunk_heads * (10 * C * K * V + 14 * C * C * K + 4 * C ** 3),
+                2 * qk * (1 + 1) + vv * 3 + 2 * gb * 2 + A)
+    if "cp_" in name or name in ("tables",) or name.startswith("group_sum"):
+        return 0.0, 0.0
+    return 0.0, 0.0
+
+
+# ---------------------------------------------------------------------------
+# clocks sampler
+# ---------------------------------------------------------------------------
+class Clocks:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self, t0, t1):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = [l for (ts, l) in self.lines if t0 - 0.15 <= ts <= t1 + 0.15] or [l for (_, l) in self.lines]
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            parts = [p.strip() for p in r.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle arm
+# ---------------------------------------------------------------------------
+def oracle_sample(x, spec, t_sample, heads_sample):
+    """Run the fp64 oracle forward+backward on the first t_sample tokens of every
+    sequence's first batch element, over the first `heads_sample` qk-heads."""
+    import oracle
+    G = spec.Hv // spec.Hq
+    hq = slice(0, heads_sample)
+    hv = slice(0, heads_sample * G)
+    T = min(t_sample, spec.T if spec.lengths is None else spec.lengths[0])
+    q = x["q"][:1, :T, hq]
+    k = x["k"][:1, :T, hq]
+    v = x["v"][:1, :T, hv]
+    g = x["g"][:1, :T, hv]
+    beta = x["beta"][:1, :T, hv]
+    h0 = None if x["h0"] is None else x["h0"][:1, hv]
+    do = x["do"][:1, :T, hv]
+    dht = x["dht"][:1, hv]
+    nthreads = os.cpu_count() or 1
+    t0 = time.perf_counter()
+    oracle.fwd(q, k, v, g, beta, x["scale"], h0=h0, nthreads=nthreads, vblock=16)
+    oracle.bwd(q, k, v, g, beta, x["scale"], do, dht=dht, h0=h0, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    # throughput in full-workload tokens: each token carries Hv heads of work
+    eq_tokens = T * (heads_sample * G) / spec.Hv
+    return eq_tokens / dt / 1e6, dt, T, nthreads
+
+
+def run_reference(args, spec, rank, world):
+    from gated_deltanet_chunked_delta_gb300 import inputs
+    if rank != 0:
+        return
+    x = inputs.make(spec, seed=0)
+    import oracle
+    oracle.build()
+    t_sample, heads = args.ref_tokens, spec.Hq
+    vals = []
+    for i in range(args.warmup + args.steps):
+        v, dt, T, nth = oracle_sample(x, spec, t_sample, heads)
+        if i >= args.warmup:
+            vals.append(v)
+    value = statistics.mean(vals)
+    line = {"metric": METRIC, "impl": "reference", "value": value, "unit": "Mtokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": _config(spec, args),
+            "cpu_baseline": {"value": value, "unit": "Mtokens/s", "cores": nth, "kind": "oracle",
+                             "sample": f"oracle fwd+bwd on tokens [0,{T}) of sequence 0, all {spec.Hv} v-heads; "
+                                       f"throughput in full-workload tokens"},
+            "e2e": {"value": value, "unit": "Mtokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def _config(spec, args):
+    return {"workload": spec.name, "B": spec.B, "T": spec.T, "Hq": spec.Hq, "Hv": spec.Hv, "K": spec.K,
+            "V": spec.V, "lengths": list(spec.lengths) if spec.lengths else None,
+            "in_dtype": spec.in_dtype, "o_dtype": spec.out_dtype,
+            "step": "gdr_fwd(o, final_state, A) + gdr_bwd(dq, dk, dv, dbeta, dg, dh0)",
+            "l2": f"flushed before every timed step ({FLUSH_BYTES >> 20} MiB write)",
+            "parallelism": f"independent replicas x{args.gpus} (no collective)"}
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gdr", choices=["gdr", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--path", default="auto", choices=["auto", "simt", "tc"])
+    ap.add_argument("--cp", type=int, default=0, help="cp_segments (0 auto, 1 off, n forced)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-tokens", type=int, default=1024, help="tokens per oracle step (reference arm)")
+    ap.add_argument("--cpu-tokens", type=int, default=4096, help="tokens of the cpu_baseline sample")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    from gated_deltanet_chunked_delta_gb300 import inputs
+    base = inputs.resolve(args.workload)
+    from dataclasses import replace
+    spec = replace(base, bwd=True)
+
+    if args.impl == "reference":
+        run_reference(args, spec, rank, world)
+        return
+
+    import gated_deltanet_chunked_delta_gb300 as gdr
+    gdr.load()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    path = {"auto": gdr.GDR_PATH_AUTO, "simt": gdr.GDR_PATH_SIMT, "tc": gdr.GDR_PATH_TC}[args.path]
+    peaks = _peaks()
+
+    x = inputs.make(spec, seed=0)
+    keys = ("q", "k", "v", "g", "beta", "h0", "do", "dht", "cu_seqlens")
+    d = {k: (x[k].to(dev) if torch.is_tensor(x[k]) else None) for k in keys}
+    cu_host = x["cu_seqlens"]
+    o_dtype = torch.float32 if spec.out_dtype == "f32" else torch.bfloat16
+    prob = gdr.Problem(d["q"], d["v"], d["cu_seqlens"], cu_host)
+    opts = gdr.make_opts(args.cp, path)
+    ws_f = gdr.alloc_workspace(gdr.fwd_workspace_size(prob, opts), dev)
+    ws_b = gdr.alloc_workspace(gdr.bwd_workspace_size(prob, opts), dev)
+    N, B, T, Hv, K, V = prob.N, spec.B, spec.T, spec.Hv, spec.K, spec.V
+    out_f = {"o": torch.empty(B, T, Hv, V, device=dev, dtype=o_dtype),
+             "final_state": torch.empty(N, Hv, K, V, device=dev),
+             "A": torch.empty(B, T, Hv, 64, device=dev)}
+    out_b = {"dq": torch.empty_like(d["q"]), "dk": torch.empty_like(d["k"]), "dv": torch.empty_like(d["v"]),
+             "dbeta": torch.empty_like(d["g"]), "dg": torch.empty_like(d["g"]),
+             "dh0": torch.empty(N, Hv, K, V, device=dev)}
+    tf = gdr.KernelTimer(32)
+    tb = gdr.KernelTimer(32)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(timer_f=None, timer_b=None):
+        gdr.gdr_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], x["scale"], h0=d["h0"], cu_seqlens=d["cu_seqlens"],
+                    cu_seqlens_host=cu_host, out=out_f, workspace=ws_f, cp_segments=args.cp, path=path,
+                    timer=timer_f)
+        gdr.gdr_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], out_f["A"], d["do"], dht=d["dht"],
+                    scale=x["scale"], h0=d["h0"], cu_seqlens=d["cu_seqlens"], cu_seqlens_host=cu_host,
+                    out=out_b, workspace=ws_b, cp_segments=args.cp, path=path, timer=timer_b)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    gdr.check_status()
+
+    clocks = Clocks(local)
+    clocks.start()
+    time.sleep(0.3)
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    per_kernel = {}
+    launches = 0
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    for i in range(args.steps):
+        flush.zero_()
+        e0[i].record(stream)
+        step(tf, tb)
+        e1[i].record(stream)
+        torch.cuda.synchronize()
+        for timer in (tf, tb):
+            launches += timer.count.value
+            for nm, ms in timer.elapsed():
+                per_kernel.setdefault(nm, []).append(ms)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t_wall1 = time.time()
+    clk = clocks.stop(t_wall0, t_wall1)
+    step_ms = [a.elapsed_time(b) for a, b in zip(e0, e1)]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    gdr.check_status()
+
+    tokens = spec.tokens
+    value = tokens * world * args.steps / (total_ms / 1e3) / 1e6
+
+    # e2e: pinned host buffers, copies inside the timed region
+    hin = {k: (x[k].pin_memory() if torch.is_tensor(x[k]) and k != "cu_seqlens" else None) for k in keys}
+    hout = {k: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for k, t in {**out_f, **out_b}.items()}
+    h2d = sum(t.numel() * t.element_size() for t in hin.values() if t is not None)
+    d2h = sum(t.numel() * t.element_size() for t in hout.values())
+    ee0 = torch.cuda.Event(enable_timing=True)
+    ee1 = torch.cuda.Event(enable_timing=True)
+    e2e_ms = []
+    for i in range(max(3, args.steps // 2)):
+        ee0.record(stream)
+        for k, t in hin.items():
+            if t is not None:
+                d[k].copy_(t, non_blocking=True)
+        step()
+        for k, t in {**out_f, **out_b}.items():
+            hout[k].copy_(t, non_blocking=True)
+        ee1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms.append(ee0.elapsed_time(ee1))
+    e2e_val = tokens * world / (statistics.mean(e2e_ms) / 1e3) / 1e6
+
+    # roofline of the dominant kernel
+    nch_heads = prob.num_chunks() * Hv
+    in_b = 2 if spec.in_dtype == "bf16" else 4
+    o_b = 4 if spec.out_dtype == "f32" else 2
+    agg = {nm: (sum(v), len(v)) for nm, v in per_kernel.items()}
+    dom = max(agg, key=lambda n: agg[n][0])
+    dom_ms = agg[dom][0] / agg[dom][1]
+    fl, by = kernel_work(dom, spec, in_b, o_b, nch_heads)
+    tc_peak = peaks["bf16_tflops"]
+    alu_peak = 152 * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12  # fp32 FFMA, TFLOP/s
+    if dom.startswith("simt"):
+        t_c, t_m = fl / (alu_peak * 1e12), by / (peaks["hbm_gbs"] * 1e9)
+        if t_c >= t_m:
+            roof = {"bound": "alu", "achieved": fl / (dom_ms / 1e3) / 1e12, "peak": alu_peak, "unit": "TFLOP/s"}
+        else:
+            roof = {"bound": "hbm", "achieved": by / (dom_ms / 1e3) / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    else:
+        t_c, t_m = fl / (tc_peak * 1e12), by / (peaks["hbm_gbs"] * 1e9)
+        if t_c >= t_m:
+            roof = {"bound": "tensor", "achieved": fl / (dom_ms / 1e3) / 1e12, "peak": tc_peak, "unit": "TFLOP/s"}
+        else:
+            roof = {"bound": "hbm", "achieved": by / (dom_ms / 1e3) / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    roof["kernel"] = dom
+    roof["peak_source"] = peaks["source"]
+
+    # whole-step roofline (the metric's "% of bf16 roofline")
+    th = tokens * Hv
+    step_flops = th * (166.6e3 + 491.5e3) * (K * V / (128 * 128))
+    step_bytes = (2 * tokens * spec.Hq * K * in_b * 2 + tokens * Hv * V * in_b * 2 + tokens * Hv * 4 * 4
+                  + tokens * Hv * V * o_b + tokens * Hv * 64 * 4 * 2 + tokens * Hv * V * in_b
+                  + 4 * N * Hv * K * V * 4)
+    step_roof_ms = max(step_flops / (tc_peak * 1e12), step_bytes / (peaks["hbm_gbs"] * 1e9)) * 1e3
+
+    kernels = {nm: {"launches": n, "ms_total": round(t, 4), "share": round(t / sum(a for a, _ in agg.values()), 4)}
+               for nm, (t, n) in sorted(agg.items(), key=lambda kv: -kv[1][0])}
+    line = {"metric": METRIC, "value": value, "unit": "Mtokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if spec.in_dtype == "bf16" else "f32",
+            "data": "synthetic", "config": _config(spec, args),
+            "roofline": roof,
+            "step_roofline_frac": step_roof_ms / (total_ms / args.steps),
+            "kernels": kernels,
+            "e2e": {"value": e2e_val, "unit": "Mtokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches, "clocks": clk}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        v, dt, Ts, nth = oracle_sample(x, spec, args.cpu_tokens, spec.Hq)
+        line["cpu_baseline"] = {"value": v, "unit": "Mtokens/s", "cores": nth, "kind": "oracle",
+                                "sample": f"oracle fwd+bwd on tokens [0,{Ts}) of sequence 0, all {spec.Hv} "
+                                          f"v-heads ({dt:.1f} s); throughput in full-workload tokens"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

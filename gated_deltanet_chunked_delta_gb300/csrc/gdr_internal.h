@@ -1,0 +1,105 @@
+// gdr_internal.h -- host/device shared definitions of libgdr (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gdr {
+
+constexpr int kChunk = 64;  // tokens per chunk
+
+// Per sequence: token range, chunk range and segment range (context-parallel split).
+struct SeqInfo {
+    int tok0, len, chunk0, nch;
+    int seg0, nseg, pad0, pad1;
+};
+// Per chunk: owning sequence, first token (flattened), number of tokens, index in sequence.
+struct ChunkInfo {
+    int seq, tok0, len, local;
+};
+// Per segment: owning sequence, first global chunk, number of chunks, index in sequence.
+struct SegInfo {
+    int seq, chunk0, nch, idx;
+};
+
+// Caller-owned event brackets around every kernel launch of one call.
+struct Timing {
+    void **events;
+    const char **names;
+    int max_events;
+    int count;
+};
+
+// Records the opening event of a launch named `name` (no-op without timing).
+inline void tm_begin(Timing *t, const char *name, cudaStream_t st) {
+    if (!t) return;
+    const int i = t->count;
+    if (t->events && 2 * i + 1 < t->max_events) {
+        cudaEventRecord(static_cast<cudaEvent_t>(t->events[2 * i]), st);
+        if (t->names) t->names[i] = name;
+    }
+}
+inline void tm_end(Timing *t, cudaStream_t st) {
+    if (!t) return;
+    const int i = t->count++;
+    if (t->events && 2 * i + 1 < t->max_events) cudaEventRecord(static_cast<cudaEvent_t>(t->events[2 * i + 1]), st);
+}
+
+// Everything a kernel may need.  Pointers that a launch does not use are null.
+struct Params {
+    // inputs
+    const void *q, *k, *v;  // [Ttot,Hq,K], [Ttot,Hq,K], [Ttot,Hv,V]
+    const float *g, *beta;  // [Ttot,Hv]
+    const float *h0;        // [N,Hv,K,V] or null
+    const float *A_in;      // [Ttot,Hv,64] (backward)
+    const void *dout;       // [Ttot,Hv,V] (backward)
+    const float *dht;       // [N,Hv,K,V] or null (backward)
+    float scale;
+    // outputs
+    void *o;                // [Ttot,Hv,V]
+    float *final_state;     // [N,Hv,K,V] or null
+    float *A_out;           // [Ttot,Hv,64] or null
+    float *h_out;           // [NT,Hv,K,V] or null
+    void *dq, *dk, *dv;     // backward
+    float *dbeta, *dg, *dh0;
+    // sizes
+    int Ttot, Hq, Hv, K, V;
+    int N, NT, NSEG;
+    // tables (workspace)
+    const SeqInfo *seq;
+    const ChunkInfo *chunk;
+    const SegInfo *seg;
+    // workspace arrays
+    float *gam;     // [NT,Hv,64]
+    float *W;       // [NT,Hv,64,K]
+    float *U;       // [NT,Hv,64,V]
+    float *P;       // [NT,Hv,64,64]
+    float *Hseg;    // [NSEG,Hv,K,V]
+    float *Mseg;    // [NSEG,Hv,K,K]
+    float *Sstart;  // [NSEG,Hv,K,V]
+    float *hbuf;    // [NT,Hv,K,V]   (backward: states before each chunk)
+    float *dhbuf;   // [NT,Hv,K,V]   (backward: gradient of the state after each chunk)
+    float *dubuf;   // [NT,Hv,64,V]  (backward: gradient of the chunk pseudo-values)
+    float *dqp, *dkp;  // [Ttot,Hv,K] per-v-head partial dq, dk
+    // tensor-core path operands (bf16, laid out as the MMA tiles want them)
+    void *Wb;       // [NT,Hv,64,K]   W
+    void *Ub;       // [NT,Hv,64,V]   U
+    void *Pb;       // [NT,Hv,64,64]  scale * (Q K^T o D o tril_incl)
+    void *KTb;      // [NT,Hv,K,64]   Kt^T, Kt = diag(e^{gamma_n - gamma}) K
+    int debug;
+    long long timeout_spins;
+    Timing *tm;  // host-side only: launch timing (may be null)
+};
+
+}  // namespace gdr
+
+// Host-side entry points of each translation unit (called from gdr_api.cu).
+namespace gdr {
+int simt_fwd(const Params &p, int in_f32, int o_f32, int use_cp, cudaStream_t st);
+int simt_bwd(const Params &p, int in_f32, int use_cp, cudaStream_t st);
+unsigned simt_take_status(cudaStream_t st);
+int simt_wy_tc(const Params &p, int from_A, cudaStream_t st);
+int simt_cp_combine(const Params &p, cudaStream_t st);
+int prep_tables(const int32_t *cu_dev, int N, int T_fixed, int seg_len, SeqInfo *seq,
+                ChunkInfo *chunk, SegInfo *seg, cudaStream_t st);
+}  // namespace gdr

@@ -1,0 +1,88 @@
+"""Helpers shared by the GPU parity tests: run the C ABI through the binding
+and the fp64 oracle on the same seeded inputs, and measure the error as
+max|x - ref| / rms(ref) per tensor."""
+import numpy as np
+import torch
+
+import oracle
+from gated_deltanet_chunked_delta_gb300 import inputs
+
+TOL = {"f32": 2e-3, "bf16": 2e-2}
+
+
+# Unit roundoff of a stored bf16 value (8 significant bits, round to nearest).
+BF16_U = 2.0 ** -8
+
+
+def err(x, ref):
+    """max|x - ref| / rms(ref).  For a tensor stored in bf16 the stored value
+    cannot be nearer to the fp64 result than its own rounding, so the error
+    counted is what exceeds that rounding: max(|x - ref| - u |x|, 0)."""
+    slack = 0.0
+    if torch.is_tensor(x):
+        if x.dtype == torch.bfloat16:
+            slack = BF16_U * 1.01
+        x = x.detach().float().cpu().double().numpy()
+    else:
+        x = np.asarray(x, np.float64)
+    ref = np.asarray(ref, np.float64)
+    if not x.size:
+        return 0.0
+    d = np.maximum(np.abs(x - ref) - slack * np.abs(x), 0.0)
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    if rms == 0.0:
+        return float(np.max(d))
+    return float(np.max(d)) / rms
+
+
+def raw_err(x, ref):
+    """The plain max|x - ref| / rms(ref), rounding of the stored value included."""
+    x = x.detach().float().cpu().double().numpy() if torch.is_tensor(x) else np.asarray(x, np.float64)
+    ref = np.asarray(ref, np.float64)
+    rms = float(np.sqrt(np.mean(ref * ref))) or 1.0
+    return float(np.max(np.abs(x - ref))) / rms if x.size else 0.0
+
+
+def to_dev(x, dev="cuda"):
+    return {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in x.items()}
+
+
+def gpu_fwd(gdr, d, **kw):
+    return gdr.gdr_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["scale"], h0=d["h0"],
+                       cu_seqlens=d["cu_seqlens"], **kw)
+
+
+def gpu_bwd(gdr, d, A, **kw):
+    return gdr.gdr_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], A, d["do"], dht=d.get("dht"),
+                       scale=d["scale"], h0=d["h0"], cu_seqlens=d["cu_seqlens"], **kw)
+
+
+def oracle_fwd(x, want_h=False):
+    return oracle.fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], h0=x["h0"],
+                      cu_seqlens=x["cu_seqlens"], want_h=want_h)
+
+
+def oracle_bwd(x):
+    return oracle.bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], x["do"], dht=x.get("dht"),
+                      h0=x["h0"], cu_seqlens=x["cu_seqlens"])
+
+
+def oracle_A(x):
+    return oracle.A_matrix(x["k"], x["g"], x["beta"], cu_seqlens=x["cu_seqlens"])
+
+
+def select_heads(x, hq):
+    """Inputs restricted to qk-head hq and the v-heads of its group."""
+    spec = x["spec"]
+    G = spec.Hv // spec.Hq
+    hv = slice(hq * G, (hq + 1) * G)
+    y = dict(x)
+    y["q"] = x["q"][:, :, hq:hq + 1].contiguous()
+    y["k"] = x["k"][:, :, hq:hq + 1].contiguous()
+    for key in ("v", "g", "beta", "do"):
+        if key in x and x[key] is not None:
+            y[key] = x[key][:, :, hv].contiguous()
+    for key in ("h0", "dht"):
+        if key in x and x[key] is not None:
+            y[key] = x[key][:, hv].contiguous()
+    return y, hv

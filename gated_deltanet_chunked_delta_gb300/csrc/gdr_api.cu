@@ -140,7 +140,10 @@ int make_plan(const gdr_shape *s, const gdr_opts *o, int want_path, int in_f32, 
 size_t al(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Layout {
-    size_t seq, chunk, seg, gam, W, U, P, Hseg, Mseg, Sstart, hbuf, dhbuf, dubuf, dqp, dkp, total;
+    size_t seq, chunk, seg, gam, W, U, P, Hseg, Mseg, Sstart, hbuf, dhbuf, dubuf, dqp, dkp;
+    size_t Aimg, Pimg, Aux;
+    bool f32_tiles, bf16_tiles;
+    size_t total;
 };
 
 Layout layout(const gdr_shape *s, const Plan &pl, bool bwd) {
@@ -152,9 +155,16 @@ Layout layout(const gdr_shape *s, const Plan &pl, bool bwd) {
     L.chunk = take(sizeof(ChunkInfo) * NT);
     L.seg = take(sizeof(SegInfo) * NS);
     L.gam = take(4 * NT * Hv * 64);
-    L.W = take(4 * NT * Hv * 64 * K);
-    L.U = take(4 * NT * Hv * 64 * V);
-    L.P = take(4 * NT * Hv * 64 * 64);
+    // fp32 chunk tiles serve the CUDA-core kernels (the whole CUDA-core path, and
+    // the backward of both paths); bf16 tiles feed the tensor-core scans.
+    L.f32_tiles = pl.path == GDR_PATH_SIMT || bwd;
+    L.bf16_tiles = pl.path == GDR_PATH_TC;
+    L.W = L.f32_tiles ? take(4 * NT * Hv * 64 * K) : 0;
+    L.U = L.f32_tiles ? take(4 * NT * Hv * 64 * V) : 0;
+    L.P = L.f32_tiles ? take(4 * NT * Hv * 64 * 64) : 0;
+    L.Aimg = L.bf16_tiles ? take(16384 * NT * Hv) : 0;
+    L.Pimg = L.bf16_tiles ? take(16384 * NT * Hv) : 0;
+    L.Aux = L.bf16_tiles ? take(512 * NT * Hv) : 0;
     if (pl.use_cp) {
         L.Hseg = take(4 * NS * Hv * K * V);
         L.Mseg = take(4 * NS * Hv * K * K);
@@ -237,9 +247,12 @@ int fill_params(const gdr_shape *s, const Plan &pl, const Layout &L, void *ws, P
     p->seg = reinterpret_cast<SegInfo *>(w + L.seg);
     auto F = [&](size_t off, bool on) { return on ? reinterpret_cast<float *>(w + off) : nullptr; };
     p->gam = F(L.gam, true);
-    p->W = F(L.W, true);
-    p->U = F(L.U, true);
-    p->P = F(L.P, true);
+    p->W = F(L.W, L.f32_tiles);
+    p->U = F(L.U, L.f32_tiles);
+    p->P = F(L.P, L.f32_tiles);
+    p->Aimg = F(L.Aimg, L.bf16_tiles);
+    p->Pimg = F(L.Pimg, L.bf16_tiles);
+    p->Aux = F(L.Aux, L.bf16_tiles);
     p->Hseg = F(L.Hseg, pl.use_cp);
     p->Mseg = F(L.Mseg, pl.use_cp);
     p->Sstart = F(L.Sstart, pl.use_cp);
@@ -249,7 +262,7 @@ int fill_params(const gdr_shape *s, const Plan &pl, const Layout &L, void *ws, P
     p->dqp = F(L.dqp, L.dqp != 0);
     p->dkp = F(L.dkp, L.dkp != 0);
     p->debug = o ? o->debug_checks : 0;
-    p->timeout_spins = (o && o->timeout_spins > 0) ? o->timeout_spins : (1LL << 26);
+    p->timeout_spins = (o && o->timeout_spins > 0) ? o->timeout_spins : (1LL << 22);
     return GDR_OK;
 }
 

@@ -81,11 +81,10 @@ struct Params {
     float *dhbuf;   // [NT,Hv,K,V]   (backward: gradient of the state after each chunk)
     float *dubuf;   // [NT,Hv,64,V]  (backward: gradient of the chunk pseudo-values)
     float *dqp, *dkp;  // [Ttot,Hv,K] per-v-head partial dq, dk
-    // tensor-core path operands (bf16, laid out as the MMA tiles want them)
-    void *Wb;       // [NT,Hv,64,K]   W
-    void *Ub;       // [NT,Hv,64,V]   U
-    void *Pb;       // [NT,Hv,64,64]  scale * (Q K^T o D o tril_incl)
-    void *KTb;      // [NT,Hv,K,64]   Kt^T, Kt = diag(e^{gamma_n - gamma}) K
+    // tensor-core path chunk tiles (bf16 shared-memory images, hi and lo terms, 16 KiB each)
+    void *Aimg;     // [NT,Hv] x A
+    void *Pimg;     // [NT,Hv] x P' = scale diag(e^{gamma - gamma_n}) (Q K^T o tril_incl)
+    void *Aux;      // [NT,Hv] x (gamma[64], beta[64]) fp32
     int debug;
     long long timeout_spins;
     Timing *tm;  // host-side only: launch timing (may be null)
@@ -98,7 +97,6 @@ namespace gdr {
 int simt_fwd(const Params &p, int in_f32, int o_f32, int use_cp, cudaStream_t st);
 int simt_bwd(const Params &p, int in_f32, int use_cp, cudaStream_t st);
 unsigned simt_take_status(cudaStream_t st);
-int simt_wy_tc(const Params &p, int from_A, cudaStream_t st);
 int simt_cp_combine(const Params &p, cudaStream_t st);
 int prep_tables(const int32_t *cu_dev, int N, int T_fixed, int seg_len, SeqInfo *seq,
                 ChunkInfo *chunk, SegInfo *seg, cudaStream_t st);

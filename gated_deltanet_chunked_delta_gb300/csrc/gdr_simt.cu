@@ -58,7 +58,7 @@ __device__ __forceinline__ bool bad(const Params &p, bool cond) {
 // K1: per (chunk, v-head): gamma, A (inverted, or read back in the backward),
 // P, W, U.  256 threads.
 // ---------------------------------------------------------------------------
-template <typename TI, int KD, int VD, bool kTC = false>
+template <typename TI, int KD, int VD>
 __global__ void __launch_bounds__(256) k_wy(Params p, int from_A) {
     constexpr int DM = KD > VD ? KD : VD;
     constexpr int LD = DM + 1;
@@ -137,16 +137,8 @@ __global__ void __launch_bounds__(256) k_wy(Params p, int from_A) {
             for (int i = 0; i < KD; ++i) d += Xs[r * LD + i] * Ks[s * LD + i];
             val = p.scale * __expf(gam[r] - gam[s]) * d;
         }
-        if (kTC)
-            stf((__nv_bfloat16 *)p.Pb, ch * 64 * 64 + idx, val);
-        else
-            p.P[ch * 64 * 64 + idx] = val;
+        p.P[ch * 64 * 64 + idx] = val;
     }
-    if (kTC)  // Kt^T[k][r] = e^{gamma_n - gamma_r} k_r  (zero past the chunk end)
-        for (int idx = tid; idx < KD * 64; idx += 256) {
-            const int i = idx >> 6, r = idx & 63;
-            stf((__nv_bfloat16 *)p.KTb, ch * KD * 64 + idx, __expf(gam[63] - gam[r]) * Ks[r * LD + i]);
-        }
     __syncthreads();
     for (int idx = tid; idx < 64 * KD; idx += 256) {
         const int r = idx / KD, i = idx % KD;
@@ -161,19 +153,13 @@ __global__ void __launch_bounds__(256) k_wy(Params p, int from_A) {
         const int r = idx / KD, i = idx % KD;
         float acc = 0.f;
         for (int s = 0; s <= r; ++s) acc += Am[r * 65 + s] * Ks[s * LD + i];
-        if (kTC)
-            stf((__nv_bfloat16 *)p.Wb, ch * 64 * KD + idx, acc);
-        else
-            p.W[ch * 64 * KD + idx] = acc;
+        p.W[ch * 64 * KD + idx] = acc;
     }
     for (int idx = tid; idx < 64 * VD; idx += 256) {
         const int r = idx / VD, jj = idx % VD;
         float acc = 0.f;
         for (int s = 0; s <= r; ++s) acc += Am[r * 65 + s] * Xs[s * LD + jj];
-        if (kTC)
-            stf((__nv_bfloat16 *)p.Ub, ch * 64 * VD + idx, acc);
-        else
-            p.U[ch * 64 * VD + idx] = acc;
+        p.U[ch * 64 * VD + idx] = acc;
     }
     if (tid < 64) p.gam[((size_t)c * p.Hv + h) * 64 + tid] = gam[tid];
 }
@@ -852,12 +838,6 @@ int simt_fwd(const Params &p, int in_f32, int o_f32, int use_cp, cudaStream_t st
 
 int simt_bwd(const Params &p, int in_f32, int use_cp, cudaStream_t st) {
     return in_f32 ? bwd_dims<float>(p, use_cp, st) : bwd_dims<__nv_bfloat16>(p, use_cp, st);
-}
-
-int simt_wy_tc(const Params &p, int from_A, cudaStream_t st) {
-    if (p.K != 128 || p.V != 128) return 1;
-    return launch(from_A ? "simt_wy_tc_from_A" : "simt_wy_tc", k_wy<__nv_bfloat16, 128, 128, true>,
-                  dim3(p.NT, p.Hv), smem_wy<128, 128>(), st, p, from_A) != cudaSuccess;
 }
 
 int simt_cp_combine(const Params &p, cudaStream_t st) {

@@ -1,32 +1,26 @@
 // gdr_tc.cu -- tcgen05 tensor-core path of the GDN chunked prefill (bf16
 // operands, fp32 accumulation, K = V = 128, 64-token chunks).
 //
-// The inter-chunk state scan (FlashQLA pages, page 1 "efficiency problem":
-// the scan kernel can only launch batch x heads blocks; page 1 "two fused
-// kernels and automatic CP": a chunk-parallel kernel, then the scan, with the
-// context-parallel step between them) runs one CTA per (segment, v-head) and
-// keeps the fp32 state in tensor memory, transposed: TMEM lane v holds row v
-// of S^T (column v of S), 128 columns of k.  Per chunk:
-//
-//   MMA1  D1 = S^T [W ; Q]^T          (M=128 lanes v, N=64 or 128, K=128)
-//         -> (W S)^T and (Q S)^T
-//   epi   Ut^T = U^T - (W S)^T   (bf16 into shared memory, the next A operand)
-//   MMA2  D2 = Ut^T P^T               (M=128, N=64, K=64)  -> (P Ut)^T
-//   MMA3  S^T += Ut^T Kt              (M=128, N=128, K=64), after the epilogue
-//         scaled S^T by e^{gamma_n} in place
-//   epi   O = scale e^{gamma} o (Q S) + P Ut   (row r of O from column r of D)
-//
-// Roles: warps 0-3 are the epilogue (thread t <-> TMEM lane t), warp 4 issues
-// TMA loads of the chunk tiles into a two-stage ring, warp 5 allocates tensor
-// memory and issues the MMAs from one thread.  Every wait is a bounded poll;
-// a wait that runs out sets the device status word, raises a shared abort
-// flag that every role polls, and the CTA drains and frees its tensor memory.
-//
-// Modes: kFwd emits o (and h, final_state); kStates only stores the state
-// before every chunk (the backward's recompute); kSummary runs the
-// context-parallel segment summary, carrying two states: S from 0 with
-// pseudo-values U, and M from I with zero pseudo-values (the columns of
-// X = [S | M] evolve independently), and writes H = S_end and M = M_end.
+// FlashQLA pages: the forward splits into a chunk-parallel kernel and the
+// inter-chunk state scan with the context-parallel step between them (page 1,
+// "two fused kernels and automatic CP"); the scan alone can only launch
+// batch x heads blocks (page 1, "efficiency problem"), which the segment split
+// fixes.  The pages also claim an algebraic reformulation that cuts
+// tensor-core, CUDA-core and SFU work without losing precision, but give no
+// formula; the one used here is this build's own:
+//   * the chunk's pseudo-values are formed as Ut = A R with the residual
+//     R = diag(b) (V - diag(e^gamma) K S0) built from the exact bf16 inputs and
+//     a two-term (hi + lo bf16) split of the fp32 state, so the cancellation in
+//     v - S^T k happens in fp32 and W = A diag(b e^gamma) K, U = A diag(b) V
+//     never need to be formed;
+//   * the state update uses K itself (read as an MN-major operand) with the
+//     decay e^{gamma_n - gamma_r} folded into the left operand, so no decayed
+//     copy of K is stored;
+//   * the intra-chunk attention P = scale (Q K^T o D o tril) is stored as
+//     P' = scale diag(e^{gamma - gamma_n}) (Q K^T o tril), which needs one
+//     exponential per row instead of one per entry.
+// The state lives in tensor memory, transposed: TMEM lane v holds row v of
+// S^T, 128 fp32 columns of k.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -38,7 +32,7 @@ namespace {
 
 __device__ unsigned g_tc_status;
 
-constexpr int kFwd = 0, kStates = 1, kSummary = 2;
+constexpr int kFwd = 0, kStates = 1, kSum = 2;
 
 // ---------------------------------------------------------------------------
 // PTX wrappers
@@ -87,13 +81,6 @@ __device__ __forceinline__ void drain_wait(uint64_t *b, uint32_t parity, long lo
         if (mbar_try(b, parity)) return;
 }
 
-__device__ __forceinline__ void tma2d(void *dst, const CUtensorMap *m, int x, int y, uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-            su32(dst)),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(su32(bar))
-        : "memory");
-}
 __device__ __forceinline__ void tma3d(void *dst, const CUtensorMap *m, int x, int y, int z, uint64_t *bar) {
     asm volatile(
         "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
@@ -112,20 +99,24 @@ __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.a
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
-// 1024 bytes apart (tile bases are 1024-byte aligned).
-__device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
+// Shared-memory matrix descriptor for a 128-byte-swizzled bf16 tile (bases
+// 1024-byte aligned).  K-major: rows of 64 K-elements (128 B), 8-row groups
+// 1024 bytes apart; the leading byte offset is unused.  MN-major: rows along
+// K of 64 MN-elements, 8-row groups 1024 bytes apart, and `lbo` bytes between
+// consecutive 64-element blocks along MN.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo = 16) {
     uint64_t d = 0;
     d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-    d |= (uint64_t)1 << 16;             // leading byte offset (unused for this layout)
-    d |= (uint64_t)(1024 >> 4) << 32;   // stride byte offset
-    d |= (uint64_t)1 << 46;             // descriptor version
-    d |= (uint64_t)2 << 61;             // 128-byte swizzle
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;  // leading byte offset
+    d |= (uint64_t)(1024 >> 4) << 32;              // stride byte offset
+    d |= (uint64_t)1 << 46;                        // descriptor version
+    d |= (uint64_t)2 << 61;                        // 128-byte swizzle
     return d;
 }
-// Instruction descriptor: bf16 x bf16 -> fp32, both operands K-major.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+// Instruction descriptor: bf16 x bf16 -> fp32; a_mn / b_mn select MN-major operands.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn = 0, int b_mn = 0) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 __device__ __forceinline__ void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
     asm volatile(
@@ -187,67 +178,307 @@ __device__ __forceinline__ void st_row32(char *tile, int rows, int row, int col0
     }
 }
 
-__device__ __forceinline__ float ldbf(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
 
 // ---------------------------------------------------------------------------
-// the scan kernel
+// chunk-tile images kept in the workspace (bf16, byte-for-byte the shared-
+// memory image the scan's MMAs read, so the scan fetches them with plain bulk
+// copies).  Each fp32 matrix is stored as two bf16 terms, hi = bf16(x) and
+// lo = bf16(x - hi), which together carry ~16 significant bits:
+//   A image   [hi | lo], each [64 rows r][128 B], 128-byte swizzled: A[r][s] over s
+//   P' image  same layout: P'[r][s] = scale e^{gamma_r - gamma_n} (q_r . k_s), s <= r
+//   aux       gamma[64], beta[64] (fp32; rows past the chunk end: gamma_n, 0)
 // ---------------------------------------------------------------------------
-struct TcMaps {
-    CUtensorMap W, U, P, KT, Q;
+constexpr int kImg = 8192;       // one bf16 term
+constexpr int kImg2 = 2 * kImg;  // hi and lo
+constexpr int kAux = 512;
+
+__device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+
+// Row `row` of a [hi | lo] pair of 128-byte-swizzled 64-column bf16 images.
+__device__ __forceinline__ void st_img_row2(char *img, int row, const float *x /* 64 */) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        float hi[8], lw[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            hi[e] = bf16_round(x[8 * j + e]);
+            lw[e] = x[8 * j + e] - hi[e];
+        }
+        uint4 vh, vl;
+        vh.x = pack_bf16(hi[0], hi[1]); vh.y = pack_bf16(hi[2], hi[3]);
+        vh.z = pack_bf16(hi[4], hi[5]); vh.w = pack_bf16(hi[6], hi[7]);
+        vl.x = pack_bf16(lw[0], lw[1]); vl.y = pack_bf16(lw[2], lw[3]);
+        vl.z = pack_bf16(lw[4], lw[5]); vl.w = pack_bf16(lw[6], lw[7]);
+        const int off = row * 128 + ((j ^ (row & 7)) << 4);
+        *reinterpret_cast<uint4 *>(img + off) = vh;
+        *reinterpret_cast<uint4 *>(img + kImg + off) = vl;
+    }
+}
+
+struct ChunkMaps {
+    CUtensorMap K, Q;  // 3-D over k and q: (K, Hq, Ttot), box (64, 1, 64), 128-byte swizzle
 };
 
-// One pipeline stage (all offsets 1024-byte aligned):
-//   B1  [2 atoms][rows][128 B] swizzled: W rows 0-63 (+ Q rows 64-127 in kFwd)
-//   U   [64][128] bf16 plain row-major
-//   P   [64 rows][128 B] swizzled (kFwd only)
-//   KT  [128 rows][128 B] swizzled
-//   gamma, 64 fp32
+// ---------------------------------------------------------------------------
+// Chunk-parallel kernel: one CTA per (chunk, qk-head), looping over the v-heads
+// of the group.  [K ; Q] K^T on tcgen05 (shared by the group), then per v-head
+// the gate cumsum, L, the unit-lower-triangular inverse A = (I + L)^-1 on the
+// CUDA cores (blocked: 16x16 diagonal blocks, then block levels), and P'.
+// With from_A (the backward) A is read back from the forward's output.
+// ---------------------------------------------------------------------------
+constexpr int kChunkSmem = 1024 + 32768 + 2 * 64 * 65 * 4 + 3 * 16 * 17 * 4 + 2 * 64 * 4 + 128;
+
+__global__ void __launch_bounds__(128) k_chunk_tc(Params p, const __grid_constant__ ChunkMaps maps, int from_A) {
+    extern __shared__ __align__(1024) char smraw[];
+    char *sm = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+    char *tile = sm;                                             // [2 atoms][128 rows][128 B]: K rows 0-63, Q 64-127
+    float *Ls = reinterpret_cast<float *>(sm + 32768);           // [64][65]
+    float *As = Ls + 64 * 65;                                    // [64][65]
+    float *Tt = As + 64 * 65;                                    // [3][16][17]
+    float *gam = Tt + 3 * 16 * 17;                               // [64]
+    float *bet = gam + 64;                                       // [64]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(bet + 64);     // tma, mma
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2);
+    volatile int *abort = reinterpret_cast<volatile int *>(bars + 3);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c = blockIdx.x, hq = blockIdx.y;
+    const ChunkInfo ci = p.chunk[c];
+    const int len = ci.len, tok0 = ci.tok0;
+    const int G = p.Hv / p.Hq;
+    const long long cap = p.timeout_spins;
+
+    if (tid == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        *abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
+                     "r"(64));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    if (tid == 0) {
+        mbar_expect_tx(&bars[0], 32768);
+        tma3d(tile, &maps.K, 0, hq, tok0, &bars[0]);
+        tma3d(tile + 16384, &maps.K, 64, hq, tok0, &bars[0]);
+        tma3d(tile + 8192, &maps.Q, 0, hq, tok0, &bars[0]);
+        tma3d(tile + 16384 + 8192, &maps.Q, 64, hq, tok0, &bars[0]);
+        if (bwait(&bars[0], 0, cap, abort)) {
+            tc_fence_after();
+            const uint32_t id = idesc_bf16(128, 64);
+            const uint32_t a0 = su32(tile);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                mma(tmem, sdesc(a0 + off), sdesc(a0 + off), id, kk > 0);
+            }
+            mma_commit(&bars[1]);
+        }
+    }
+    // row t of [K K^T ; Q K^T] (garbage rows past the chunk end are masked by
+    // beta = 0 and by the triangles below)
+    float row[64];
+    bool ok = bwait(&bars[1], 0, cap, abort);
+    tc_fence_after();
+    if (ok) {
+        uint32_t r[32];
+        const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16);
+        tmem_ld32(ta, r);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) row[i] = __uint_as_float(r[i]);
+        tmem_ld32(ta + 32, r);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) row[32 + i] = __uint_as_float(r[i]);
+    }
+    __syncthreads();
+    for (int j = 0; j < G && !*abort; ++j) {
+        const int h = hq * G + j;
+        const size_t ch = (size_t)c * p.Hv + h;
+        if (tid < 64) {
+            gam[tid] = tid < len ? p.g[(size_t)(tok0 + tid) * p.Hv + h] : 0.f;
+            bet[tid] = tid < len ? p.beta[(size_t)(tok0 + tid) * p.Hv + h] : 0.f;
+        }
+        __syncthreads();
+        if (tid < 32) {  // inclusive cumsum over 64 values, two per lane
+            float a = gam[2 * lane], b = gam[2 * lane + 1];
+            float s = a + b;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float n = __shfl_up_sync(0xffffffffu, s, o);
+                if (lane >= o) s += n;
+            }
+            const float excl = s - (a + b);
+            gam[2 * lane] = excl + a;
+            gam[2 * lane + 1] = s;
+        }
+        __syncthreads();
+        const float gC = gam[63];
+        if (tid < 64) {
+            float *aux = reinterpret_cast<float *>(reinterpret_cast<char *>(p.Aux) + ch * kAux);
+            aux[tid] = gam[tid];
+            aux[64 + tid] = bet[tid];
+        }
+        if (tid < 64) {
+            const int rr = tid;
+            if (!from_A) {
+                const float br = bet[rr], gr = gam[rr];
+#pragma unroll
+                for (int s = 0; s < 64; ++s) Ls[rr * 65 + s] = s < rr ? br * __expf(gr - gam[s]) * row[s] : 0.f;
+            }
+        } else {
+            const int rr = tid - 64;
+            const float f = p.scale * __expf(gam[rr] - gC);
+            float x[64];
+#pragma unroll
+            for (int s = 0; s < 64; ++s) x[s] = s <= rr ? f * row[s] : 0.f;
+            st_img_row2(reinterpret_cast<char *>(p.Pimg) + ch * kImg2, rr, x);
+        }
+        for (int e = tid; e < 64 * 64; e += 128) {
+            const int rr = e >> 6, s = e & 63;
+            if (from_A)
+                As[rr * 65 + s] = rr < len ? p.A_in[((size_t)(tok0 + rr) * p.Hv + h) * 64 + s] : (rr == s ? 1.f : 0.f);
+            else
+                As[rr * 65 + s] = 0.f;
+        }
+        __syncthreads();
+        if (!from_A) {
+            // diagonal 16x16 blocks: warp w inverts block w, lane j owns column j
+            if (lane < 16) {
+                const int b = 16 * warp, jj = lane;
+                for (int rr = jj; rr < 16; ++rr) {
+                    float acc = rr == jj ? 1.f : 0.f;
+                    for (int s = jj; s < rr; ++s) acc -= Ls[(b + rr) * 65 + b + s] * As[(b + s) * 65 + b + jj];
+                    As[(b + rr) * 65 + b + jj] = acc;
+                }
+            }
+            __syncthreads();
+            // block levels: A_ij = -A_ii sum_{k=j}^{i-1} L_ik A_kj, i - j = d
+            for (int d = 1; d < 4; ++d) {
+                const int nb = 4 - d;
+                for (int e = tid; e < nb * 256; e += 128) {
+                    const int blk = e >> 8, i = d + blk, jb = i - d, rr = (e >> 4) & 15, cc = e & 15;
+                    float acc = 0.f;
+                    for (int kb = jb; kb < i; ++kb)
+                        for (int m = 0; m < 16; ++m)
+                            acc += Ls[(16 * i + rr) * 65 + 16 * kb + m] * As[(16 * kb + m) * 65 + 16 * jb + cc];
+                    Tt[blk * 272 + rr * 17 + cc] = acc;
+                }
+                __syncthreads();
+                for (int e = tid; e < nb * 256; e += 128) {
+                    const int blk = e >> 8, i = d + blk, jb = i - d, rr = (e >> 4) & 15, cc = e & 15;
+                    float acc = 0.f;
+                    for (int m = 0; m <= rr; ++m) acc -= As[(16 * i + rr) * 65 + 16 * i + m] * Tt[blk * 272 + m * 17 + cc];
+                    As[(16 * i + rr) * 65 + 16 * jb + cc] = acc;
+                }
+                __syncthreads();
+            }
+        }
+        if (tid < 64) {
+            const int rr = tid;
+            float x[64];
+#pragma unroll
+            for (int s = 0; s < 64; ++s) x[s] = As[rr * 65 + s];
+            st_img_row2(reinterpret_cast<char *>(p.Aimg) + ch * kImg2, rr, x);
+            if (p.A_out && !from_A && rr < len) {
+                float4 *dst = reinterpret_cast<float4 *>(p.A_out + ((size_t)(tok0 + rr) * p.Hv + h) * 64);
+#pragma unroll
+                for (int s = 0; s < 16; ++s) dst[s] = make_float4(x[4 * s], x[4 * s + 1], x[4 * s + 2], x[4 * s + 3]);
+            }
+        }
+        __syncthreads();
+    }
+    if (tid == 0) {  // no copy may still be in flight when the CTA leaves
+        drain_wait(&bars[0], 0, cap);
+        drain_wait(&bars[1], 0, cap);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(64));
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Scan kernel.  One CTA per (segment, v-head) (x2 in kSum: the S and the M
+// states run in separate CTAs).  Per chunk, with S^T in TMEM (lane v):
+//   (a)  S^T -> bf16 hi + lo (A operands); S^T *= e^{gamma_n} in place
+//   MMA1 D1 = S^T [K ; Q]^T                               -> (K S)^T, (Q S)^T
+//   (c)  R^T = (diag(b) (V - diag(e^gamma) K S))^T        -> bf16 hi + lo
+//   MMA1b D1b = R^T A^T = Ut^T
+//   (c2) Y^T = (diag(e^{gamma_n - gamma}) Ut)^T           -> bf16 hi + lo
+//   MMA2 D2 = Y^T P'^T = (P Ut)^T                         (kFwd)
+//   MMA3 S^T += Y^T K     (K tile read MN-major)          = (e^{gamma_n} S + Kt^T Ut)^T
+//   (e)  O = scale diag(e^gamma) Q S + P Ut               (kFwd)
+// Every operand that is not an exact bf16 input (S, R, A, Y, P') enters as two
+// bf16 terms: x y ~ x_hi y_hi + x_lo y_hi + x_hi y_lo (one term when y is an
+// input), accumulated in fp32.  With single bf16 operands the max-abs error
+// of o and of the state settles near 2e-2 of their RMS on these workloads;
+// with the split it is ~1e-4.  The residual R is formed from the exact inputs,
+// so the cancellation in v - S^T k happens in fp32.
+// ---------------------------------------------------------------------------
+struct ScanMaps {
+    CUtensorMap K, Q, V;  // 3-D over k, q (box 64 x 1 x 64, swizzled) and v (box 128 x 1 x 64, plain)
+};
+
 template <int MODE>
-struct Stage {
-    static constexpr int kAtom = MODE == kFwd ? 16384 : 8192;  // bytes per 64-column atom of B1
+struct ScanStage {
+    static constexpr int kRows = MODE == kFwd ? 128 : 64;  // rows per 64-column atom of B1 (K, then Q)
+    static constexpr int kAtom = kRows * 128;
     static constexpr int kB1 = 0;
-    static constexpr int kU = 2 * kAtom;
-    static constexpr int kP = kU + 16384;
-    static constexpr int kKT = kP + (MODE == kFwd ? 8192 : 0);
-    static constexpr int kGam = kKT + 16384;
-    static constexpr int kBytes = kGam + 1024;
-    static constexpr uint32_t kTx = 2 * 8192 * (MODE == kFwd ? 2 : 1) + 16384 + (MODE == kFwd ? 8192 : 0) + 16384 + 256;
+    static constexpr int kV = 2 * kAtom;          // [64][128] bf16 plain row-major
+    static constexpr int kA = kV + 16384;         // A image, hi | lo
+    static constexpr int kP = kA + kImg2;         // P' image, hi | lo (kFwd)
+    static constexpr int kBytes = kP + (MODE == kFwd ? kImg2 : 0);
 };
-constexpr int kSB = 32768;       // S^T in bf16: [2 atoms][128][128 B]
-constexpr int kUT = 16384;       // Ut^T in bf16: [128][128 B]
+// One 64 KiB operand region, reused within a chunk: S^T hi | lo (2 x 32 KiB,
+// [2 atoms][128][128 B]) while MMA1 reads it, then R^T hi | lo (2 x 16 KiB,
+// [128][128 B]) in its first half and Y^T hi | lo in its second half.
+constexpr int kOps = 65536;
 
 template <int MODE>
 __host__ __device__ constexpr int scan_smem() {
-    return 1024 /* alignment slack */ + 2 * Stage<MODE>::kBytes + (MODE == kSummary ? 2 : 1) * (kSB + kUT) + 256;
+    return 1024 + 2 * ScanStage<MODE>::kBytes + kOps + 2 * kAux + 256;
 }
 
 template <int MODE, typename TO>
-__global__ void __launch_bounds__(192, 1) k_scan_tc(Params p, const __grid_constant__ TcMaps maps) {
+__global__ void __launch_bounds__(192, 1) k_scan_tc(Params p, const __grid_constant__ ScanMaps maps) {
     extern __shared__ __align__(1024) char smraw[];
     char *sm = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
-    constexpr int NX = MODE == kSummary ? 2 : 1;  // number of carried states
-    using SL = Stage<MODE>;
+    using SL = ScanStage<MODE>;
     static_assert(scan_smem<MODE>() <= 227 * 1024, "shared memory budget");
     char *stage0 = sm;
-    char *SB = sm + 2 * SL::kBytes;               // NX x kSB
-    char *UT = SB + NX * kSB;                     // NX x kUT
-    uint64_t *bars = reinterpret_cast<uint64_t *>(UT + NX * kUT);
+    char *SBh = sm + 2 * SL::kBytes;
+    char *SBl = SBh + 32768;
+    char *RTh = SBh, *RTl = SBh + 16384;
+    char *YTh = SBh + 32768, *YTl = SBh + 49152;
+    char *aux0 = SBh + kOps;  // 2 x kAux, one per stage
+    uint64_t *bars = reinterpret_cast<uint64_t *>(aux0 + 2 * kAux);
     uint64_t *full = bars;        // [2]
     uint64_t *empty = bars + 2;   // [2]
     uint64_t *bar_sb = bars + 4;
     uint64_t *bar_m1 = bars + 5;
-    uint64_t *bar_ut = bars + 6;
-    uint64_t *bar_m2 = bars + 7;
-    uint64_t *bar_drain = bars + 8;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 9);
-    volatile int *abort = reinterpret_cast<volatile int *>(bars + 10);
+    uint64_t *bar_rt = bars + 6;
+    uint64_t *bar_m1b = bars + 7;
+    uint64_t *bar_ut = bars + 8;
+    uint64_t *bar_m3 = bars + 9;
+    uint64_t *bar_drain = bars + 10;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 11);
+    volatile int *abort = reinterpret_cast<volatile int *>(bars + 12);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int sidx = blockIdx.x, h = blockIdx.y;
+    const bool isM = MODE == kSum && blockIdx.z == 1;  // the composed-transition state
     const SegInfo sg = p.seg[sidx];
     const SeqInfo sq = p.seq[sg.seq];
     const int hq = h / (p.Hv / p.Hq);
-    const int nch = sg.nch;
+    const int nch = (MODE == kSum && sg.idx >= sq.nseg - 1) ? 0 : sg.nch;  // last segment: no summary
     const long long cap = p.timeout_spins;
 
     if (tid == 0) {
@@ -257,8 +488,10 @@ __global__ void __launch_bounds__(192, 1) k_scan_tc(Params p, const __grid_const
         mbar_init(&empty[1], 129);
         mbar_init(bar_sb, 128);
         mbar_init(bar_m1, 1);
+        mbar_init(bar_rt, 128);
+        mbar_init(bar_m1b, 1);
         mbar_init(bar_ut, 128);
-        mbar_init(bar_m2, 1);
+        mbar_init(bar_m3, 1);
         mbar_init(bar_drain, 1);
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -272,10 +505,7 @@ __global__ void __launch_bounds__(192, 1) k_scan_tc(Params p, const __grid_const
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    // TMEM columns
-    const uint32_t tS = tmem;                                   // S^T (and M^T at +128 in summary mode)
-    const uint32_t tD1 = tmem + (MODE == kSummary ? 256 : 128); // 128 (fwd) or 64 per state
-    const uint32_t tD2 = tmem + 256;                            // fwd: (P Ut)^T, 64 columns
+    const uint32_t tS = tmem, tD1 = tmem + 128, tD1b = tmem + 256, tD2 = tmem + 320;
 
     if (warp == 4) {
         // ---------------- TMA producer ----------------
@@ -285,23 +515,25 @@ __global__ void __launch_bounds__(192, 1) k_scan_tc(Params p, const __grid_const
                 const int s = cc & 1;
                 if (cc >= 2 && !bwait(&empty[s], ((cc >> 1) & 1) ^ 1, cap, abort)) break;
                 const int c = sg.chunk0 + cc;
-                const ChunkInfo ci = p.chunk[c];
-                const int row = (c * p.Hv + h) * 64;
+                const int tok0 = p.chunk[c].tok0;
+                const size_t ch = (size_t)c * p.Hv + h;
                 char *st = stage0 + s * SL::kBytes;
-                mbar_expect_tx(&full[s], SL::kTx);
-                tma2d(st + SL::kB1, &maps.W, 0, row, &full[s]);
-                tma2d(st + SL::kB1 + SL::kAtom, &maps.W, 64, row, &full[s]);
+                uint32_t tx = 2 * 8192 + kImg2 + kAux;
+                if (MODE == kFwd) tx += 2 * 8192 + kImg2;
+                if (!isM) tx += 16384;
+                mbar_expect_tx(&full[s], tx);
+                tma3d(st + SL::kB1, &maps.K, 0, hq, tok0, &full[s]);
+                tma3d(st + SL::kB1 + SL::kAtom, &maps.K, 64, hq, tok0, &full[s]);
                 if (MODE == kFwd) {
-                    tma3d(st + SL::kB1 + 8192, &maps.Q, 0, hq, ci.tok0, &full[s]);
-                    tma3d(st + SL::kB1 + SL::kAtom + 8192, &maps.Q, 64, hq, ci.tok0, &full[s]);
-                    tma2d(st + SL::kP, &maps.P, 0, row, &full[s]);
+                    tma3d(st + SL::kB1 + 8192, &maps.Q, 0, hq, tok0, &full[s]);
+                    tma3d(st + SL::kB1 + SL::kAtom + 8192, &maps.Q, 64, hq, tok0, &full[s]);
+                    bulk_g2s(st + SL::kP, reinterpret_cast<const char *>(p.Pimg) + ch * kImg2, kImg2, &full[s]);
                 }
-                tma2d(st + SL::kU, &maps.U, 0, row, &full[s]);
-                tma2d(st + SL::kKT, &maps.KT, 0, (c * p.Hv + h) * 128, &full[s]);
-                bulk_g2s(st + SL::kGam, p.gam + (size_t)(c * p.Hv + h) * 64, 256, &full[s]);
+                if (!isM) tma3d(st + SL::kV, &maps.V, 0, h, tok0, &full[s]);
+                bulk_g2s(st + SL::kA, reinterpret_cast<const char *>(p.Aimg) + ch * kImg2, kImg2, &full[s]);
+                bulk_g2s(aux0 + s * kAux, reinterpret_cast<const char *>(p.Aux) + ch * kAux, kAux, &full[s]);
                 issued = cc + 1;
             }
-            // never leave with copies in flight: wait for the last stages that were issued
             for (int cc = issued - 2 < 0 ? 0 : issued - 2; cc < issued; ++cc)
                 drain_wait(&full[cc & 1], (cc >> 1) & 1, cap);
         }
@@ -309,127 +541,168 @@ __global__ void __launch_bounds__(192, 1) k_scan_tc(Params p, const __grid_const
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
             const uint32_t id1 = idesc_bf16(128, MODE == kFwd ? 128 : 64);
-            const uint32_t id2 = idesc_bf16(128, 64);
-            const uint32_t id3 = idesc_bf16(128, 128);
+            const uint32_t id64 = idesc_bf16(128, 64);
+            const uint32_t id3 = idesc_bf16(128, 128, 0, 1);
             for (int cc = 0; cc < nch; ++cc) {
                 const int s = cc & 1;
                 char *st = stage0 + s * SL::kBytes;
                 if (!bwait(&full[s], (cc >> 1) & 1, cap, abort)) break;
                 if (!bwait(bar_sb, cc & 1, cap, abort)) break;
                 tc_fence_after();
-                for (int x = 0; x < NX; ++x) {
-                    const uint32_t a0 = su32(SB + x * kSB), b0 = su32(st + SL::kB1);
+                const uint32_t b1 = su32(st + SL::kB1);
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const uint32_t a0 = su32(half ? SBl : SBh);
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         const uint32_t ko = (kk & 3) * 32;
-                        mma(tD1 + x * 64, sdesc(a0 + (kk >> 2) * 16384 + ko), sdesc(b0 + (kk >> 2) * SL::kAtom + ko),
-                            id1, kk > 0);
+                        mma(tD1, sdesc(a0 + (kk >> 2) * 16384 + ko), sdesc(b1 + (kk >> 2) * SL::kAtom + ko), id1,
+                            (half | kk) != 0);
                     }
                 }
                 mma_commit(bar_m1);
+                if (!bwait(bar_rt, cc & 1, cap, abort)) break;
+                tc_fence_after();
+                {
+                    const uint32_t rh = su32(RTh), rl = su32(RTl), ah = su32(st + SL::kA), al = ah + kImg;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint32_t o = kk * 32;
+                        mma(tD1b, sdesc(rh + o), sdesc(ah + o), id64, kk > 0);
+                        mma(tD1b, sdesc(rl + o), sdesc(ah + o), id64, 1);
+                        mma(tD1b, sdesc(rh + o), sdesc(al + o), id64, 1);
+                    }
+                }
+                mma_commit(bar_m1b);
                 if (!bwait(bar_ut, cc & 1, cap, abort)) break;
                 tc_fence_after();
+                const uint32_t yh = su32(YTh), yl = su32(YTl);
                 if (MODE == kFwd) {
-                    const uint32_t a0 = su32(UT), b0 = su32(st + SL::kP);
+                    const uint32_t ph = su32(st + SL::kP), pl = ph + kImg;
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) mma(tD2, sdesc(a0 + kk * 32), sdesc(b0 + kk * 32), id2, kk > 0);
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint32_t o = kk * 32;
+                        mma(tD2, sdesc(yh + o), sdesc(ph + o), id64, kk > 0);
+                        mma(tD2, sdesc(yl + o), sdesc(ph + o), id64, 1);
+                        mma(tD2, sdesc(yh + o), sdesc(pl + o), id64, 1);
+                    }
                 }
-                for (int x = 0; x < NX; ++x) {
-                    const uint32_t a0 = su32(UT + x * kUT), b0 = su32(st + SL::kKT);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) mma(tS + x * 128, sdesc(a0 + kk * 32), sdesc(b0 + kk * 32), id3, 1);
+                for (int kk = 0; kk < 4; ++kk) {
+                    mma(tS, sdesc(yh + kk * 32), sdesc(b1 + kk * 2048, SL::kAtom), id3, 1);
+                    mma(tS, sdesc(yl + kk * 32), sdesc(b1 + kk * 2048, SL::kAtom), id3, 1);
                 }
-                mma_commit(bar_m2);
+                mma_commit(bar_m3);
                 mma_commit(&empty[s]);
             }
-            // every MMA issued above has completed before the CTA tears down
             mma_commit(bar_drain);
             drain_wait(bar_drain, 0, cap);
         }
     } else {
         // ---------------- epilogue: warps 0-3, thread t <-> TMEM lane t ----------------
         const int t = tid;
-        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        const uint32_t lo = (uint32_t)(warp * 32) << 16;
         uint32_t r[32];
-        // initial state(s)
-        for (int x = 0; x < NX; ++x) {
-            for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < 4; ++j) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int k = 32 * j + i;
-                    float v0;
-                    if (MODE == kSummary)
-                        v0 = (x == 1 && k == t) ? 1.f : 0.f;
-                    else if (sg.idx == 0)
-                        v0 = p.h0 ? p.h0[(((size_t)sg.seq * p.Hv + h) * 128 + k) * 128 + t] : 0.f;
-                    else
-                        v0 = p.Sstart[(((size_t)sidx * p.Hv + h) * 128 + k) * 128 + t];
-                    r[i] = __float_as_uint(v0);
-                }
-                tmem_st32(tS + x * 128 + 32 * j + lane_off, r);
+            for (int i = 0; i < 32; ++i) {
+                const int k = 32 * j + i;
+                float v0;
+                if (MODE == kSum)
+                    v0 = (isM && k == t) ? 1.f : 0.f;
+                else if (sg.idx == 0)
+                    v0 = p.h0 ? p.h0[(((size_t)sg.seq * p.Hv + h) * 128 + k) * 128 + t] : 0.f;
+                else
+                    v0 = p.Sstart[(((size_t)sidx * p.Hv + h) * 128 + k) * 128 + t];
+                r[i] = __float_as_uint(v0);
             }
+            tmem_st32(tS + 32 * j + lo, r);
         }
         tmem_wait_st();
         float *hdst = MODE == kFwd ? p.h_out : (MODE == kStates ? p.hbuf : nullptr);
         for (int cc = 0; cc < nch; ++cc) {
             const int s = cc & 1;
             char *st = stage0 + s * SL::kBytes;
-            const float *gam = reinterpret_cast<const float *>(st + SL::kGam);
+            const float *gam = reinterpret_cast<const float *>(aux0 + s * kAux);
+            const float *bet = gam + 64;
             const int c = sg.chunk0 + cc;
-            if (cc > 0 && !bwait(bar_m2, (cc - 1) & 1, cap, abort)) break;
+            if (cc > 0 && !bwait(bar_m3, (cc - 1) & 1, cap, abort)) break;
             tc_fence_after();
             if (!bwait(&full[s], (cc >> 1) & 1, cap, abort)) break;
-            const float dec = __expf(gam[63]);
-            // (a) S^T row t -> bf16 A operand; S^T *= e^{gamma_n} in place; h = S
-            for (int x = 0; x < NX; ++x) {
-                for (int j = 0; j < 4; ++j) {
-                    tmem_ld32(tS + x * 128 + 32 * j + lane_off, r);
-                    float f[32];
+            const float gC = gam[63];
+            const float dec = __expf(gC);
+            // (a)
+            for (int j = 0; j < 4; ++j) {
+                tmem_ld32(tS + 32 * j + lo, r);
+                float f[32], hi[32], lw[32];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(r[i]);
-                    st_row32(SB + x * kSB, 128, t, 32 * j, f);
-                    if (hdst)
-#pragma unroll 8
-                        for (int i = 0; i < 32; ++i)
-                            hdst[(((size_t)c * p.Hv + h) * 128 + 32 * j + i) * 128 + t] = f[i];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(f[i] * dec);
-                    tmem_st32(tS + x * 128 + 32 * j + lane_off, r);
+                for (int i = 0; i < 32; ++i) {
+                    f[i] = __uint_as_float(r[i]);
+                    hi[i] = bf16_round(f[i]);
+                    lw[i] = f[i] - hi[i];
                 }
+                st_row32(SBh, 128, t, 32 * j, hi);
+                st_row32(SBl, 128, t, 32 * j, lw);
+                if (hdst)
+#pragma unroll 8
+                    for (int i = 0; i < 32; ++i) hdst[(((size_t)c * p.Hv + h) * 128 + 32 * j + i) * 128 + t] = f[i];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(f[i] * dec);
+                tmem_st32(tS + 32 * j + lo, r);
             }
             tmem_wait_st();
             fence_async_smem();
             tc_fence_before();
             mbar_arrive(bar_sb);
-            // (c) Ut^T = U^T - (W S)^T
+            // (c) R^T[t][s] = b_s (V[s][t] - e^{gamma_s} (K S)^T[t][s])
             if (!bwait(bar_m1, cc & 1, cap, abort)) break;
             tc_fence_after();
-            const __nv_bfloat16 *Us = reinterpret_cast<const __nv_bfloat16 *>(st + SL::kU);
-            for (int x = 0; x < NX; ++x) {
-                for (int j = 0; j < 2; ++j) {
-                    tmem_ld32(tD1 + x * 64 + 32 * j + lane_off, r);
-                    float f[32];
+            const __nv_bfloat16 *Vs = reinterpret_cast<const __nv_bfloat16 *>(st + SL::kV);
+            for (int j = 0; j < 2; ++j) {
+                tmem_ld32(tD1 + 32 * j + lo, r);
+                float f[32], lw[32];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const float u = x == 0 ? ldbf(Us + (32 * j + i) * 128 + t) : 0.f;
-                        f[i] = u - __uint_as_float(r[i]);
-                    }
-                    st_row32(UT + x * kUT, 128, t, 32 * j, f);
+                for (int i = 0; i < 32; ++i) {
+                    const int s2 = 32 * j + i;
+                    const float vv = isM ? 0.f : __bfloat162float(Vs[s2 * 128 + t]);
+                    const float x = bet[s2] * (vv - __expf(gam[s2]) * __uint_as_float(r[i]));
+                    f[i] = bf16_round(x);
+                    lw[i] = x - f[i];
                 }
+                st_row32(RTh, 128, t, 32 * j, f);
+                st_row32(RTl, 128, t, 32 * j, lw);
+            }
+            fence_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar_rt);
+            // (c2) Y^T[t][r] = e^{gamma_n - gamma_r} Ut^T[t][r]
+            if (!bwait(bar_m1b, cc & 1, cap, abort)) break;
+            tc_fence_after();
+            for (int j = 0; j < 2; ++j) {
+                tmem_ld32(tD1b + 32 * j + lo, r);
+                float f[32], lw[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float x = __expf(gC - gam[32 * j + i]) * __uint_as_float(r[i]);
+                    f[i] = bf16_round(x);
+                    lw[i] = x - f[i];
+                }
+                st_row32(YTh, 128, t, 32 * j, f);
+                st_row32(YTl, 128, t, 32 * j, lw);
             }
             fence_async_smem();
             tc_fence_before();
             mbar_arrive(bar_ut);
-            // (e) output
+            // (e)
             if (MODE == kFwd) {
-                if (!bwait(bar_m2, cc & 1, cap, abort)) break;
+                if (!bwait(bar_m3, cc & 1, cap, abort)) break;
                 tc_fence_after();
                 const ChunkInfo ci = p.chunk[c];
                 TO *o = reinterpret_cast<TO *>(p.o);
                 for (int j = 0; j < 2; ++j) {
                     uint32_t r2[32];
-                    tmem_ld32(tD1 + 64 + 32 * j + lane_off, r);
-                    tmem_ld32(tD2 + 32 * j + lane_off, r2);
+                    tmem_ld32(tD1 + 64 + 32 * j + lo, r);
+                    tmem_ld32(tD2 + 32 * j + lo, r2);
 #pragma unroll 8
                     for (int i = 0; i < 32; ++i) {
                         const int rr = 32 * j + i;
@@ -447,30 +720,28 @@ __global__ void __launch_bounds__(192, 1) k_scan_tc(Params p, const __grid_const
             tc_fence_before();
             mbar_arrive(&empty[s]);
         }
-        // final state(s)
         if (!*abort) {
-            if (nch > 0 && MODE != kFwd) bwait(bar_m2, (nch - 1) & 1, cap, abort);
+            if (nch > 0 && MODE != kFwd) bwait(bar_m3, (nch - 1) & 1, cap, abort);
             tc_fence_after();
         }
         if (!*abort) {
-            const bool last = sg.idx == sq.nseg - 1;
-            for (int x = 0; x < NX; ++x) {
-                float *dst = nullptr;
-                size_t base = 0;
-                if (MODE == kSummary) {
-                    dst = x == 0 ? p.Hseg : p.Mseg;
+            float *dst = nullptr;
+            size_t base = 0;
+            if (MODE == kSum) {
+                if (sg.idx < sq.nseg - 1) {
+                    dst = isM ? p.Mseg : p.Hseg;
                     base = ((size_t)sidx * p.Hv + h) * 128 * 128;
-                } else if (last && p.final_state) {
-                    dst = p.final_state;
-                    base = ((size_t)sg.seq * p.Hv + h) * 128 * 128;
                 }
-                if (!dst) continue;
+            } else if (sg.idx == sq.nseg - 1 && p.final_state) {
+                dst = p.final_state;
+                base = ((size_t)sg.seq * p.Hv + h) * 128 * 128;
+            }
+            if (dst)
                 for (int j = 0; j < 4; ++j) {
-                    tmem_ld32(tS + x * 128 + 32 * j + lane_off, r);
+                    tmem_ld32(tS + 32 * j + lo, r);
 #pragma unroll 8
                     for (int i = 0; i < 32; ++i) dst[base + (size_t)(32 * j + i) * 128 + t] = __uint_as_float(r[i]);
                 }
-            }
         }
     }
     tc_fence_before();
@@ -501,55 +772,43 @@ EncodeFn encoder() {
     return fn;
 }
 
-bool make_map(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims, const cuuint64_t *strides_bytes,
-              const cuuint32_t *box, bool swizzle) {
+// 3-D bf16 map over a [Ttot, H, 128] tensor, box (bx, 1, 64).
+bool map3(CUtensorMap *m, const void *base, int H, int Ttot, int bx, bool swizzle) {
     EncodeFn fn = encoder();
     if (!fn) return false;
+    cuuint64_t d[3] = {128, (cuuint64_t)H, (cuuint64_t)Ttot};
+    cuuint64_t s[2] = {256, (cuuint64_t)H * 256};
+    cuuint32_t b[3] = {(cuuint32_t)bx, 1, 64};
     cuuint32_t es[3] = {1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), dims, strides_bytes, box, es,
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), d, s, b, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool build_maps(const Params &p, TcMaps *m) {
-    const cuuint64_t rows = (cuuint64_t)p.NT * p.Hv * 64;
-    {
-        cuuint64_t d[2] = {128, rows}, s[1] = {256};
-        cuuint32_t b[2] = {64, 64};
-        if (!make_map(&m->W, p.Wb, 2, d, s, b, true)) return false;
-    }
-    {
-        cuuint64_t d[2] = {128, rows}, s[1] = {256};
-        cuuint32_t b[2] = {128, 64};
-        if (!make_map(&m->U, p.Ub, 2, d, s, b, false)) return false;
-    }
-    {
-        cuuint64_t d[2] = {64, rows}, s[1] = {128};
-        cuuint32_t b[2] = {64, 64};
-        if (!make_map(&m->P, p.Pb, 2, d, s, b, true)) return false;
-    }
-    {
-        cuuint64_t d[2] = {64, (cuuint64_t)p.NT * p.Hv * 128}, s[1] = {128};
-        cuuint32_t b[2] = {64, 128};
-        if (!make_map(&m->KT, p.KTb, 2, d, s, b, true)) return false;
-    }
-    {
-        cuuint64_t d[3] = {128, (cuuint64_t)p.Hq, (cuuint64_t)p.Ttot};
-        cuuint64_t s[2] = {256, (cuuint64_t)p.Hq * 256};
-        cuuint32_t b[3] = {64, 1, 64};
-        if (!make_map(&m->Q, p.q, 3, d, s, b, true)) return false;
-    }
-    return true;
+int launch_chunk(const char *name, const Params &p, int from_A, cudaStream_t st) {
+    ChunkMaps maps;
+    if (!map3(&maps.K, p.k, p.Hq, p.Ttot, 64, true) || !map3(&maps.Q, p.q, p.Hq, p.Ttot, 64, true)) return 1;
+    if (p.NT == 0) return 0;
+    if (cudaFuncSetAttribute(k_chunk_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kChunkSmem) != cudaSuccess)
+        return 1;
+    tm_begin(p.tm, name, st);
+    k_chunk_tc<<<dim3(p.NT, p.Hq), 128, kChunkSmem, st>>>(p, maps, from_A);
+    tm_end(p.tm, st);
+    return cudaGetLastError() != cudaSuccess;
 }
 
 template <int MODE, typename TO>
-int launch_scan(const char *name, const Params &p, const TcMaps &maps, cudaStream_t st) {
+int launch_scan(const char *name, const Params &p, cudaStream_t st) {
     if (p.NSEG == 0) return 0;
+    ScanMaps maps;
+    if (!map3(&maps.K, p.k, p.Hq, p.Ttot, 64, true) || !map3(&maps.Q, p.q, p.Hq, p.Ttot, 64, true) ||
+        !map3(&maps.V, p.v, p.Hv, p.Ttot, 128, false))
+        return 1;
     auto kern = k_scan_tc<MODE, TO>;
     const int smem = scan_smem<MODE>();
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 1;
     tm_begin(p.tm, name, st);
-    kern<<<dim3(p.NSEG, p.Hv), 192, smem, st>>>(p, maps);
+    kern<<<dim3(p.NSEG, p.Hv, MODE == kSum ? 2 : 1), 192, smem, st>>>(p, maps);
     tm_end(p.tm, st);
     return cudaGetLastError() != cudaSuccess;
 }
@@ -559,15 +818,12 @@ int launch_scan(const char *name, const Params &p, const TcMaps &maps, cudaStrea
 int tc_supported(int K, int V) { return K == 128 && V == 128; }
 
 int tc_fwd(const Params &p, int o_f32, int use_cp, cudaStream_t st) {
-    if (simt_wy_tc(p, 0, st)) return 1;
-    TcMaps maps;
-    if (!build_maps(p, &maps)) return 1;
+    if (launch_chunk("tc_chunk", p, 0, st)) return 1;
     if (use_cp) {
-        if (launch_scan<kSummary, float>("tc_cp_summary", p, maps, st)) return 1;
+        if (launch_scan<kSum, float>("tc_cp_summary", p, st)) return 1;
         if (simt_cp_combine(p, st)) return 1;
     }
-    return o_f32 ? launch_scan<kFwd, float>("tc_scan", p, maps, st)
-                 : launch_scan<kFwd, __nv_bfloat16>("tc_scan", p, maps, st);
+    return o_f32 ? launch_scan<kFwd, float>("tc_scan", p, st) : launch_scan<kFwd, __nv_bfloat16>("tc_scan", p, st);
 }
 
 int tc_bwd(const Params &p, int use_cp, cudaStream_t st) { return simt_bwd(p, 0, use_cp, st); }

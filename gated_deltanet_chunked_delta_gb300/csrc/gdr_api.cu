@@ -277,6 +277,11 @@ int launch_prep(const gdr_shape *s, const Plan &pl, const Params &p, cudaStream_
 
 }  // namespace
 
+namespace gdr {
+// Records a message for gdr_last_error() on behalf of another translation unit.
+int set_last_error(int code, const char *msg) { return fail(code, "%s", msg); }
+}  // namespace gdr
+
 extern "C" {
 
 long long gdr_num_chunks(const gdr_shape *shape) {

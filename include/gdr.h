@@ -153,6 +153,26 @@ GDR_API int gdr_bwd(const gdr_shape *shape, gdr_buf q, gdr_buf k, gdr_buf v, con
             float *dh0, void *workspace, size_t workspace_bytes, const gdr_opts *opts,
             void *stream);
 
+/*
+ * gdr_fwd without a workspace, for callers that cannot allocate device memory
+ * (a plugin inside a host program that owns all device memory and offers no
+ * allocator, or a path that must not call cudaMalloc because it may
+ * synchronise the device).  The pages have no counterpart; this is a library
+ * convenience.  Arguments and results are those of gdr_fwd, minus the
+ * workspace: the call uses a fixed 64 MiB array compiled into the library,
+ * which every GPU that loads the library keeps until the process exits.
+ * Problems whose gdr_fwd_workspace_size() exceeds 64 MiB are rejected with
+ * GDR_ERR_WORKSPACE before anything is launched.  The first call on each
+ * device looks the array's device address up (cudaGetSymbolAddress); make that
+ * first call before any stream capture.  All calls share the one array: calls
+ * whose work overlaps on the GPU (different streams, or another thread) race
+ * and corrupt each other's results, so serialise them.  Nothing carried over
+ * from an earlier call is read.  The call itself allocates nothing.
+ */
+GDR_API int gdr_fwd_noalloc(const gdr_shape *shape, gdr_buf q, gdr_buf k, gdr_buf v, const float *g,
+                            const float *beta, float scale, const float *h0, gdr_buf o, float *final_state,
+                            float *A, float *h, const gdr_opts *opts, void *stream);
+
 /* Synchronises `stream`, then reads and clears the device status word:
  * GDR_OK, GDR_ERR_TIMEOUT, GDR_ERR_DEVICE, or GDR_ERR_CUDA. */
 GDR_API int gdr_check_status(void *stream);

@@ -155,9 +155,9 @@ Layout layout(const gdr_shape *s, const Plan &pl, bool bwd) {
     L.chunk = take(sizeof(ChunkInfo) * NT);
     L.seg = take(sizeof(SegInfo) * NS);
     L.gam = take(4 * NT * Hv * 64);
-    // fp32 chunk tiles serve the CUDA-core kernels (the whole CUDA-core path, and
-    // the backward of both paths); bf16 tiles feed the tensor-core scans.
-    L.f32_tiles = pl.path == GDR_PATH_SIMT || bwd;
+    // fp32 chunk tiles serve the CUDA-core path; bf16 tile images feed the
+    // tensor-core kernels.
+    L.f32_tiles = pl.path == GDR_PATH_SIMT;
     L.bf16_tiles = pl.path == GDR_PATH_TC;
     L.W = L.f32_tiles ? take(4 * NT * Hv * 64 * K) : 0;
     L.U = L.f32_tiles ? take(4 * NT * Hv * 64 * V) : 0;

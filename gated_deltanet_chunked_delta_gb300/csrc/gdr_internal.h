@@ -98,6 +98,7 @@ int simt_fwd(const Params &p, int in_f32, int o_f32, int use_cp, cudaStream_t st
 int simt_bwd(const Params &p, int in_f32, int use_cp, cudaStream_t st);
 unsigned simt_take_status(cudaStream_t st);
 int simt_cp_combine(const Params &p, cudaStream_t st);
+int simt_bwd_chunk(const Params &p, cudaStream_t st);
 int prep_tables(const int32_t *cu_dev, int N, int T_fixed, int seg_len, SeqInfo *seq,
                 ChunkInfo *chunk, SegInfo *seg, cudaStream_t st);
 }  // namespace gdr

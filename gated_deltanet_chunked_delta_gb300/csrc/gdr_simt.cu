@@ -840,6 +840,25 @@ int simt_bwd(const Params &p, int in_f32, int use_cp, cudaStream_t st) {
     return in_f32 ? bwd_dims<float>(p, use_cp, st) : bwd_dims<__nv_bfloat16>(p, use_cp, st);
 }
 
+int simt_bwd_chunk(const Params &p, cudaStream_t st) {
+    if (p.K != 128 || p.V != 128) return 1;
+    cudaError_t e = launch("simt_bwd_chunk", k_bwd_chunk<__nv_bfloat16, 128, 128>, dim3(p.NT, p.Hv),
+                           smem_bwd_chunk<128, 128>(), st, p);
+    if (e != cudaSuccess) return 1;
+    const long long n = (long long)p.Ttot * p.Hq * 128;
+    if (n > 0) {
+        const int blocks = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
+        tm_begin(p.tm, "group_sum_dq", st);
+        k_group_sum<__nv_bfloat16><<<blocks, 256, 0, st>>>(p.dqp, (__nv_bfloat16 *)p.dq, n, p.Hq, p.Hv / p.Hq, 128);
+        tm_end(p.tm, st);
+        tm_begin(p.tm, "group_sum_dk", st);
+        k_group_sum<__nv_bfloat16><<<blocks, 256, 0, st>>>(p.dkp, (__nv_bfloat16 *)p.dk, n, p.Hq, p.Hv / p.Hq, 128);
+        tm_end(p.tm, st);
+        if (cudaGetLastError() != cudaSuccess) return 1;
+    }
+    return 0;
+}
+
 int simt_cp_combine(const Params &p, cudaStream_t st) {
     if (p.K == 128 && p.V == 128)
         return launch("cp_combine", k_cp_combine<128, 128>, dim3(p.N, p.Hv, 4), sizeof(float) * 128 * 33, st, p) !=

@@ -75,9 +75,13 @@ __device__ __forceinline__ bool bwait(uint64_t *b, uint32_t parity, long long ca
         }
     }
 }
-// Bounded wait that ignores the abort flag (used while draining).
-__device__ __forceinline__ void drain_wait(uint64_t *b, uint32_t parity, long long cap) {
-    for (long long i = 0; i < cap; ++i)
+// Bounded wait that ignores the abort flag, used while draining a CTA's own
+// copies and MMAs before it leaves.  Its cap is fixed and generous, not the
+// caller's timeout: work that was issued with valid addresses completes, and
+// leaving before it does would let it land in freed shared memory.
+constexpr long long kDrainCap = 1LL << 24;
+__device__ __forceinline__ void drain_wait(uint64_t *b, uint32_t parity) {
+    for (long long i = 0; i < kDrainCap; ++i)
         if (mbar_try(b, parity)) return;
 }
 
@@ -263,6 +267,7 @@ __global__ void __launch_bounds__(128) k_chunk_tc(Params p, const __grid_constan
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    bool mma_issued = false;
     if (tid == 0) {
         mbar_expect_tx(&bars[0], 32768);
         tma3d(tile, &maps.K, 0, hq, tok0, &bars[0]);
@@ -279,6 +284,7 @@ __global__ void __launch_bounds__(128) k_chunk_tc(Params p, const __grid_constan
                 mma(tmem, sdesc(a0 + off), sdesc(a0 + off), id, kk > 0);
             }
             mma_commit(&bars[1]);
+            mma_issued = true;
         }
     }
     // row t of [K K^T ; Q K^T] (garbage rows past the chunk end are masked by
@@ -333,7 +339,8 @@ __global__ void __launch_bounds__(128) k_chunk_tc(Params p, const __grid_constan
             }
         } else {
             const int rr = tid - 64;
-            const float f = p.scale * __expf(gam[rr] - gC);
+            // rows past the chunk end are zero (the backward mixes rows through P'^T)
+            const float f = rr < len ? p.scale * __expf(gam[rr] - gC) : 0.f;
             float x[64];
 #pragma unroll
             for (int s = 0; s < 64; ++s) x[s] = s <= rr ? f * row[s] : 0.f;
@@ -393,9 +400,9 @@ __global__ void __launch_bounds__(128) k_chunk_tc(Params p, const __grid_constan
         }
         __syncthreads();
     }
-    if (tid == 0) {  // no copy may still be in flight when the CTA leaves
-        drain_wait(&bars[0], 0, cap);
-        drain_wait(&bars[1], 0, cap);
+    if (tid == 0) {  // no copy or MMA of this CTA may still be in flight when it leaves
+        drain_wait(&bars[0], 0);
+        if (mma_issued) drain_wait(&bars[1], 0);
     }
     tc_fence_before();
     __syncthreads();
@@ -535,7 +542,7 @@ __global__ void __launch_bounds__(192, 1) k_scan_tc(Params p, const __grid_const
                 issued = cc + 1;
             }
             for (int cc = issued - 2 < 0 ? 0 : issued - 2; cc < issued; ++cc)
-                drain_wait(&full[cc & 1], (cc >> 1) & 1, cap);
+                drain_wait(&full[cc & 1], (cc >> 1) & 1);
         }
     } else if (warp == 5) {
         // ---------------- MMA issuer ----------------
@@ -596,7 +603,7 @@ __global__ void __launch_bounds__(192, 1) k_scan_tc(Params p, const __grid_const
                 mma_commit(&empty[s]);
             }
             mma_commit(bar_drain);
-            drain_wait(bar_drain, 0, cap);
+            drain_wait(bar_drain, 0);
         }
     } else {
         // ---------------- epilogue: warps 0-3, thread t <-> TMEM lane t ----------------
@@ -753,6 +760,301 @@ __global__ void __launch_bounds__(192, 1) k_scan_tc(Params p, const __grid_const
 }
 
 // ---------------------------------------------------------------------------
+// Reverse state scan of the backward: one CTA per (sequence, v-head), over the
+// chunks from last to first, with dS^T (the gradient of the state after the
+// chunk, transposed: lane v) in TMEM.  With dY = P'^T dO + K dS1 (the
+// gradient of Y = diag(e^{gamma_n - gamma}) Ut), dUt = diag(e^{gamma_n -
+// gamma}) dY and dR = A^T dUt:
+//   (a)  store dS1; dS1^T -> bf16 hi + lo; dS^T *= e^{gamma_n} in place
+//   MMA-a D1 = dS1^T K^T + dO^T P'         = dY^T  (dO and P' read MN-major)
+//   (c)  store dUt; dUt^T -> bf16 hi + lo
+//   MMA-b D2 = dUt^T A                     = dR^T  (A read MN-major)
+//   (c2) X^T = [ (diag(scale e^gamma) dO)^T | -(diag(b e^gamma) dR)^T ] -> hi + lo
+//   MMA-c dS^T += X^T [Q ; K]              (the stacked Q, K tile read MN-major)
+// which is dS0 = e^{gamma_n} dS1 + Qt^T dO - W^T dUt with W = A diag(b e^gamma) K.
+// ---------------------------------------------------------------------------
+struct DhMaps {
+    CUtensorMap K, Q, dO;  // 3-D, box (64, 1, 64), 128-byte swizzle
+};
+struct DhStage {
+    static constexpr int kQK = 0;         // [2 atoms][128 rows][128 B]: Q rows 0-63, K rows 64-127
+    static constexpr int kdO = 32768;     // [2 atoms (v halves)][64 rows][128 B]
+    static constexpr int kA = 49152;      // A image, hi | lo
+    static constexpr int kP = 65536;      // P' image, hi | lo
+    static constexpr int kBytes = 81920;
+};
+constexpr int kDhSmem = 1024 + 2 * DhStage::kBytes + kOps + 2 * kAux + 256;
+
+__global__ void __launch_bounds__(192, 1) k_dh_tc(Params p, const __grid_constant__ DhMaps maps) {
+    extern __shared__ __align__(1024) char smraw[];
+    char *sm = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+    static_assert(kDhSmem <= 227 * 1024, "shared memory budget");
+    using SL = DhStage;
+    char *stage0 = sm;
+    char *SBh = sm + 2 * SL::kBytes;    // dS1^T hi | lo, then dUt^T hi | lo, then X^T hi | lo
+    char *SBl = SBh + 32768;
+    char *UTh = SBh, *UTl = SBh + 16384;
+    char *XTh = SBh, *XTl = SBh + 32768;
+    char *aux0 = SBh + kOps;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(aux0 + 2 * kAux);
+    uint64_t *full = bars;
+    uint64_t *empty = bars + 2;
+    uint64_t *bar_sb = bars + 4;
+    uint64_t *bar_m1 = bars + 5;
+    uint64_t *bar_ut = bars + 6;
+    uint64_t *bar_m2 = bars + 7;
+    uint64_t *bar_x = bars + 8;
+    uint64_t *bar_m3 = bars + 9;
+    uint64_t *bar_drain = bars + 10;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 11);
+    volatile int *abort = reinterpret_cast<volatile int *>(bars + 12);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int n = blockIdx.x, h = blockIdx.y;
+    const SeqInfo sq = p.seq[n];
+    const int hq = h / (p.Hv / p.Hq);
+    const int nch = sq.nch;
+    const long long cap = p.timeout_spins;
+
+    if (tid == 0) {
+        mbar_init(&full[0], 1);
+        mbar_init(&full[1], 1);
+        mbar_init(&empty[0], 129);
+        mbar_init(&empty[1], 129);
+        mbar_init(bar_sb, 128);
+        mbar_init(bar_m1, 1);
+        mbar_init(bar_ut, 128);
+        mbar_init(bar_m2, 1);
+        mbar_init(bar_x, 128);
+        mbar_init(bar_m3, 1);
+        mbar_init(bar_drain, 1);
+        *abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 5) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
+                     "r"(256));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tS = tmem, tD1 = tmem + 128, tD2 = tmem + 192;
+
+    if (warp == 4) {
+        if (lane == 0) {
+            int issued = 0;
+            for (int cc = 0; cc < nch; ++cc) {
+                const int s = cc & 1;
+                if (cc >= 2 && !bwait(&empty[s], ((cc >> 1) & 1) ^ 1, cap, abort)) break;
+                const int c = sq.chunk0 + nch - 1 - cc;
+                const int tok0 = p.chunk[c].tok0;
+                const size_t ch = (size_t)c * p.Hv + h;
+                char *st = stage0 + s * SL::kBytes;
+                mbar_expect_tx(&full[s], 32768 + 16384 + 2 * kImg2 + kAux);
+                tma3d(st + SL::kQK, &maps.Q, 0, hq, tok0, &full[s]);
+                tma3d(st + SL::kQK + 16384, &maps.Q, 64, hq, tok0, &full[s]);
+                tma3d(st + SL::kQK + 8192, &maps.K, 0, hq, tok0, &full[s]);
+                tma3d(st + SL::kQK + 16384 + 8192, &maps.K, 64, hq, tok0, &full[s]);
+                tma3d(st + SL::kdO, &maps.dO, 0, h, tok0, &full[s]);
+                tma3d(st + SL::kdO + 8192, &maps.dO, 64, h, tok0, &full[s]);
+                bulk_g2s(st + SL::kA, reinterpret_cast<const char *>(p.Aimg) + ch * kImg2, kImg2, &full[s]);
+                bulk_g2s(st + SL::kP, reinterpret_cast<const char *>(p.Pimg) + ch * kImg2, kImg2, &full[s]);
+                bulk_g2s(aux0 + s * kAux, reinterpret_cast<const char *>(p.Aux) + ch * kAux, kAux, &full[s]);
+                issued = cc + 1;
+            }
+            for (int cc = issued - 2 < 0 ? 0 : issued - 2; cc < issued; ++cc)
+                drain_wait(&full[cc & 1], (cc >> 1) & 1);
+        }
+    } else if (warp == 5) {
+        if (lane == 0) {
+            const uint32_t idK = idesc_bf16(128, 64);           // dS1^T K^T
+            const uint32_t idOP = idesc_bf16(128, 64, 1, 1);    // dO^T P'
+            const uint32_t idA = idesc_bf16(128, 64, 0, 1);     // dUt^T A
+            const uint32_t idQK = idesc_bf16(128, 128, 0, 1);   // X^T [Q ; K]
+            for (int cc = 0; cc < nch; ++cc) {
+                const int s = cc & 1;
+                char *st = stage0 + s * SL::kBytes;
+                if (!bwait(&full[s], (cc >> 1) & 1, cap, abort)) break;
+                if (!bwait(bar_sb, cc & 1, cap, abort)) break;
+                tc_fence_after();
+                const uint32_t qk = su32(st + SL::kQK), kr = qk + 8192;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const uint32_t a0 = su32(half ? SBl : SBh);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t o = (kk >> 2) * 16384 + (kk & 3) * 32;
+                        mma(tD1, sdesc(a0 + o), sdesc(kr + o), idK, (half | kk) != 0);
+                    }
+                }
+                {
+                    const uint32_t dO = su32(st + SL::kdO), ph = su32(st + SL::kP), pl = ph + kImg;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        mma(tD1, sdesc(dO + kk * 2048, 8192), sdesc(ph + kk * 2048, 8192), idOP, 1);
+                        mma(tD1, sdesc(dO + kk * 2048, 8192), sdesc(pl + kk * 2048, 8192), idOP, 1);
+                    }
+                }
+                mma_commit(bar_m1);
+                if (!bwait(bar_ut, cc & 1, cap, abort)) break;
+                tc_fence_after();
+                {
+                    const uint32_t uh = su32(UTh), ul = su32(UTl), ah = su32(st + SL::kA), al = ah + kImg;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint32_t o = kk * 32, ob = kk * 2048;
+                        mma(tD2, sdesc(uh + o), sdesc(ah + ob, 8192), idA, kk > 0);
+                        mma(tD2, sdesc(ul + o), sdesc(ah + ob, 8192), idA, 1);
+                        mma(tD2, sdesc(uh + o), sdesc(al + ob, 8192), idA, 1);
+                    }
+                }
+                mma_commit(bar_m2);
+                if (!bwait(bar_x, cc & 1, cap, abort)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const uint32_t a0 = su32(half ? XTl : XTh);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma(tS, sdesc(a0 + (kk >> 2) * 16384 + (kk & 3) * 32), sdesc(qk + kk * 2048, 16384), idQK, 1);
+                }
+                mma_commit(bar_m3);
+                mma_commit(&empty[s]);
+            }
+            mma_commit(bar_drain);
+            drain_wait(bar_drain, 0);
+        }
+    } else {
+        const int t = tid;
+        const uint32_t lo = (uint32_t)(warp * 32) << 16;
+        uint32_t r[32];
+        for (int j = 0; j < 4; ++j) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int k = 32 * j + i;
+                r[i] = __float_as_uint(p.dht ? p.dht[(((size_t)n * p.Hv + h) * 128 + k) * 128 + t] : 0.f);
+            }
+            tmem_st32(tS + 32 * j + lo, r);
+        }
+        tmem_wait_st();
+        for (int cc = 0; cc < nch; ++cc) {
+            const int s = cc & 1;
+            char *st = stage0 + s * SL::kBytes;
+            const float *gam = reinterpret_cast<const float *>(aux0 + s * kAux);
+            const float *bet = gam + 64;
+            const int c = sq.chunk0 + nch - 1 - cc;
+            const int len = p.chunk[c].len;
+            const size_t ch = (size_t)c * p.Hv + h;
+            if (cc > 0 && !bwait(bar_m3, (cc - 1) & 1, cap, abort)) break;
+            tc_fence_after();
+            if (!bwait(&full[s], (cc >> 1) & 1, cap, abort)) break;
+            const float gC = gam[63];
+            const float dec = __expf(gC);
+            // (a)
+            for (int j = 0; j < 4; ++j) {
+                tmem_ld32(tS + 32 * j + lo, r);
+                float f[32], hi[32], lw[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    f[i] = __uint_as_float(r[i]);
+                    hi[i] = bf16_round(f[i]);
+                    lw[i] = f[i] - hi[i];
+                }
+                st_row32(SBh, 128, t, 32 * j, hi);
+                st_row32(SBl, 128, t, 32 * j, lw);
+#pragma unroll 8
+                for (int i = 0; i < 32; ++i) p.dhbuf[(ch * 128 + 32 * j + i) * 128 + t] = f[i];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(f[i] * dec);
+                tmem_st32(tS + 32 * j + lo, r);
+            }
+            tmem_wait_st();
+            fence_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar_sb);
+            // (c) dUt^T[t][r] = e^{gamma_n - gamma_r} dY^T[t][r]
+            if (!bwait(bar_m1, cc & 1, cap, abort)) break;
+            tc_fence_after();
+            for (int j = 0; j < 2; ++j) {
+                tmem_ld32(tD1 + 32 * j + lo, r);
+                float f[32], lw[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int rr = 32 * j + i;
+                    const float x = rr < len ? __expf(gC - gam[rr]) * __uint_as_float(r[i]) : 0.f;
+                    p.dubuf[(ch * 64 + rr) * 128 + t] = x;
+                    f[i] = bf16_round(x);
+                    lw[i] = x - f[i];
+                }
+                st_row32(UTh, 128, t, 32 * j, f);
+                st_row32(UTl, 128, t, 32 * j, lw);
+            }
+            fence_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar_ut);
+            // (c2) X^T = [scale e^{gamma_s} dO[s][t] | -b_s e^{gamma_s} dR^T[t][s]]
+            if (!bwait(bar_m2, cc & 1, cap, abort)) break;
+            tc_fence_after();
+            {
+                const char *dO = st + SL::kdO + (t >> 6) * 8192;
+                const int cv = t & 63;
+                for (int j = 0; j < 2; ++j) {
+                    float f[32], lw[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int s2 = 32 * j + i;
+                        const __nv_bfloat16 dv = *reinterpret_cast<const __nv_bfloat16 *>(
+                            dO + s2 * 128 + ((((cv >> 3) ^ (s2 & 7)) << 4) | ((cv & 7) << 1)));
+                        const float x = s2 < len ? p.scale * __expf(gam[s2]) * __bfloat162float(dv) : 0.f;
+                        f[i] = bf16_round(x);
+                        lw[i] = x - f[i];
+                    }
+                    st_row32(XTh, 128, t, 32 * j, f);
+                    st_row32(XTl, 128, t, 32 * j, lw);
+                }
+                for (int j = 0; j < 2; ++j) {
+                    tmem_ld32(tD2 + 32 * j + lo, r);
+                    float f[32], lw[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int s2 = 32 * j + i;
+                        const float x = -bet[s2] * __expf(gam[s2]) * __uint_as_float(r[i]);
+                        f[i] = bf16_round(x);
+                        lw[i] = x - f[i];
+                    }
+                    st_row32(XTh, 128, t, 64 + 32 * j, f);
+                    st_row32(XTl, 128, t, 64 + 32 * j, lw);
+                }
+            }
+            fence_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar_x);
+            tc_fence_before();
+            mbar_arrive(&empty[s]);
+        }
+        if (!*abort) {
+            if (nch > 0) bwait(bar_m3, (nch - 1) & 1, cap, abort);
+            tc_fence_after();
+        }
+        if (!*abort && p.dh0)
+            for (int j = 0; j < 4; ++j) {
+                tmem_ld32(tS + 32 * j + lo, r);
+#pragma unroll 8
+                for (int i = 0; i < 32; ++i)
+                    p.dh0[(((size_t)n * p.Hv + h) * 128 + 32 * j + i) * 128 + t] = __uint_as_float(r[i]);
+            }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(256));
+    }
+}
+
+// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -813,6 +1115,19 @@ int launch_scan(const char *name, const Params &p, cudaStream_t st) {
     return cudaGetLastError() != cudaSuccess;
 }
 
+int launch_dh(const Params &p, cudaStream_t st) {
+    if (p.N == 0) return 0;
+    DhMaps maps;
+    if (!map3(&maps.K, p.k, p.Hq, p.Ttot, 64, true) || !map3(&maps.Q, p.q, p.Hq, p.Ttot, 64, true) ||
+        !map3(&maps.dO, p.dout, p.Hv, p.Ttot, 64, true))
+        return 1;
+    if (cudaFuncSetAttribute(k_dh_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kDhSmem) != cudaSuccess) return 1;
+    tm_begin(p.tm, "tc_dh", st);
+    k_dh_tc<<<dim3(p.N, p.Hv), 192, kDhSmem, st>>>(p, maps);
+    tm_end(p.tm, st);
+    return cudaGetLastError() != cudaSuccess;
+}
+
 }  // namespace
 
 int tc_supported(int K, int V) { return K == 128 && V == 128; }
@@ -826,7 +1141,21 @@ int tc_fwd(const Params &p, int o_f32, int use_cp, cudaStream_t st) {
     return o_f32 ? launch_scan<kFwd, float>("tc_scan", p, st) : launch_scan<kFwd, __nv_bfloat16>("tc_scan", p, st);
 }
 
-int tc_bwd(const Params &p, int use_cp, cudaStream_t st) { return simt_bwd(p, 0, use_cp, st); }
+int tc_bwd(const Params &p, int use_cp, cudaStream_t st) {
+    // a8: A image, P' image and gates from the forward's A; states before every chunk
+    if (launch_chunk("tc_chunk_from_A", p, 1, st)) return 1;
+    if (use_cp) {
+        if (launch_scan<kSum, float>("tc_cp_summary", p, st)) return 1;
+        if (simt_cp_combine(p, st)) return 1;
+    }
+    Params ps = p;
+    ps.final_state = nullptr;
+    if (launch_scan<kStates, float>("tc_scan_states", ps, st)) return 1;
+    // a9: reverse state scan
+    if (launch_dh(p, st)) return 1;
+    // a10, a11: chunk-local gradients
+    return simt_bwd_chunk(p, st);
+}
 
 unsigned tc_take_status(cudaStream_t st) {
     unsigned v = 0, z = 0;

@@ -60,36 +60,44 @@ C = 64
 def kernel_work(name, spec, in_bytes, o_bytes, nchunk_heads):
     """(flops, bytes) of one launch of kernel `name` over the whole problem.
 
-    Units: one (chunk, v-head) pair; tokens-heads = tokens * Hv.  Counts dense
-    contractions (2 flops per MAC, causal products halved) and the HBM bytes the
-    kernel must move at least: its inputs once and its outputs once."""
+    Unit: one (chunk, v-head) pair of C = 64 tokens.  Flops count the dense
+    contractions the kernel's step of the method needs (2 per MAC, causal
+    products halved), not the extra terms of split operands; bytes count its
+    inputs read once and outputs written once (the workspace tiles it passes to
+    the next kernel are not algorithmic).  Overhead kernels (the context-parallel
+    summaries and combines, the tables, the group sums) count zero."""
     K, V, Hv, Hq = spec.K, spec.V, spec.Hv, spec.Hq
     G = Hv // Hq
     th = spec.tokens * Hv                      # token-heads
     qk = spec.tokens * Hq * K * in_bytes       # one of q or k
-    vv = spec.tokens * Hv * V * in_bytes
-    gb = spec.tokens * Hv * 4                  # one of g or beta
+    vv = spec.tokens * Hv * V * in_bytes       # one of v, o (input dtype) or do
+    gb = spec.tokens * Hv * 4                  # one of g, beta, dg, dbeta
     A = spec.tokens * Hv * C * 4
     st = spec.n_seqs * Hv * K * V * 4          # one state tensor
-    wy_fl = nchunk_heads * (2 * C * C * K / G + 2 * C * C * K / G   # K K^T, Q K^T (shared by the group)
-                            + C ** 3 / 3 * 2                        # triangular inverse
-                            + 2 * C * C * K / 2 + 2 * C * C * V / 2)  # W, U (triangular A)
-    scan_fl = nchunk_heads * (6 * C * K * V + C * C * V)
-    if name.endswith("wy"):
-        return wy_fl, 2 * qk + vv + 2 * gb + A
-    if name.endswith("wy_from_A"):
-        return wy_fl - nchunk_heads * (C ** 3 / 3 * 2), 2 * qk + vv + 2 * gb + A
-    if name.endswith("scan"):
-        return scan_fl, 2 * qk + vv + 2 * gb + th * V * o_bytes + st
-    if name.endswith("scan_states"):
-        return nchunk_heads * 4 * C * K * V, 2 * qk + vv + 2 * gb
-    if name.endswith("dh"):
-        return nchunk_heads * (6 * C * K * V + C * C * V), 2 * qk + vv + 2 * gb + st * 2
-    if name.endswith("bwd_chunk"):
-        return (nchunk_heads * (10 * C * K * V + 14 * C * C * K + 4 * C ** 3),
-                2 * qk * (1 + 1) + vv * 3 + 2 * gb * 2 + A)
-    if "cp_" in name or name in ("tables",) or name.startswith("group_sum"):
-        return 0.0, 0.0
+    n = nchunk_heads
+    mac = {
+        # [K;Q] K^T (shared by the group), the triangular inverse
+        "chunk": n * (2 * C * C * K / G + C ** 3 / 3),
+        # K S0, Q S0, K^T Y; A R; P' Y (causal)
+        "scan": n * (3 * C * K * V + C * C * V + C * C * V / 2),
+        "scan_states": n * (2 * C * K * V + C * C * V),
+        # dS1 K^T, X [Q ; K]; dO^T P' (causal); dUt A
+        "dh": n * (3 * C * K * V + C * C * V / 2 + C * C * V),
+        # K S0, dO S0^T, dKS S0^T, Y dS1^T; A R, A^T dUt, dUt R^T, dO Y^T;
+        # Q K^T, K K^T, dP'' K, dP''^T Q, MM K, MM^T K; A^T dA A^T
+        "bwd_chunk": n * (4 * C * K * V + 3.5 * C * C * V + 6 * C * C * K + 2 * C ** 3),
+    }
+    byt = {
+        "chunk": 2 * qk + 2 * gb + A,
+        "scan": 2 * qk + vv + th * V * o_bytes + st,
+        "scan_states": qk + vv,
+        "dh": 2 * qk + vv + 2 * st,
+        "bwd_chunk": 2 * qk + 2 * vv + A + 2 * gb + (2 * qk + vv) + 2 * gb,
+    }
+    base = name.split("_", 1)[1] if name.startswith(("tc_", "mma_", "simt_")) else name
+    base = {"chunk_from_A": "chunk", "wy": "chunk", "wy_from_A": "chunk"}.get(base, base)
+    if base in mac:
+        return 2.0 * mac[base], float(byt[base])
     return 0.0, 0.0
 
 

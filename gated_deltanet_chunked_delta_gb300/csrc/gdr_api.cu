@@ -11,8 +11,8 @@
 // scan would otherwise leave SMs idle -- evaluated against this device's SM
 // count.  The pages' cost model (steps 2.1 and 3 cost ~L, step 2.2 ~N/L) is
 // garbled where it names the optimum; minimising a*L + b*N/L gives
-// L* = sqrt(b N / a), which is what the plan below approximates by filling
-// the SMs with the fewest segments.
+// L* = sqrt(b N / a).  The plan below minimises that cost directly, with the
+// per-step costs measured on GB300 and the waves of one-CTA-per-SM scans.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -114,15 +114,31 @@ int make_plan(const gdr_shape *s, const gdr_opts *o, int want_path, int in_f32, 
     int seg_len = std::max(1, maxc);
     if (forced > 1) {
         seg_len = std::max(1, (maxc + forced - 1) / forced);
+    } else if (forced == 0 && maxc > 1 && path == GDR_PATH_TC) {
+        // One scan CTA per (segment, v-head), one CTA per SM.  Estimated time in
+        // chunk steps of the longest segment: the scan's waves times the segment
+        // length, plus (when split) the summary's waves (two states, each ~0.8 of
+        // a scan step) and the sequential combine (~0.7 of a step per segment).
+        const long long B = (long long)pl->N * s->Hv, S = device_sms();
+        double best = 1e300;
+        for (int nseg = 1; nseg <= 64 && nseg <= maxc; ++nseg) {
+            const int L = (maxc + nseg - 1) / nseg;
+            if (nseg > 1 && L < 4) break;
+            const double waves = (double)((B * nseg + S - 1) / S);
+            double t = waves * L;
+            if (nseg > 1) t += (double)((2 * B * nseg + S - 1) / S) * L * 0.8 + 0.7 * nseg;
+            if (t < best - 1e-9) {
+                best = t;
+                seg_len = L;
+            }
+        }
     } else if (forced == 0 && maxc > 1) {
-        // units of parallel work without CP; each unit is one CTA of the scan
-        const int col_blocks = path == GDR_PATH_TC ? 1 : s->V / 32;
-        const long long base = (long long)pl->N * s->Hv * col_blocks;
-        const long long target = (long long)device_sms() * (path == GDR_PATH_TC ? 1 : 2);
+        // CUDA-core path: 32-column CTAs, two per SM
+        const long long base = (long long)pl->N * s->Hv * (s->V / 32);
+        const long long target = (long long)device_sms() * 2;
         if (base < target) {
             const long long want = (target + base - 1) / base;
-            const int min_len = path == GDR_PATH_TC ? 8 : 4;
-            seg_len = std::max<int>(min_len, (int)((maxc + want - 1) / want));
+            seg_len = std::max<int>(4, (int)((maxc + want - 1) / want));
             seg_len = std::min(seg_len, maxc);
         }
     }
@@ -162,9 +178,9 @@ Layout layout(const gdr_shape *s, const Plan &pl, bool bwd) {
     L.W = L.f32_tiles ? take(4 * NT * Hv * 64 * K) : 0;
     L.U = L.f32_tiles ? take(4 * NT * Hv * 64 * V) : 0;
     L.P = L.f32_tiles ? take(4 * NT * Hv * 64 * 64) : 0;
-    L.Aimg = L.bf16_tiles ? take(16384 * NT * Hv) : 0;
-    L.Pimg = L.bf16_tiles ? take(16384 * NT * Hv) : 0;
-    L.Aux = L.bf16_tiles ? take(512 * NT * Hv) : 0;
+    L.Aimg = L.bf16_tiles ? take((size_t)kTileImgBytes * NT * Hv) : 0;
+    L.Pimg = L.bf16_tiles ? take((size_t)kTileImgBytes * NT * Hv) : 0;
+    L.Aux = L.bf16_tiles ? take((size_t)kAuxBytes * NT * Hv) : 0;
     if (pl.use_cp) {
         L.Hseg = take(4 * NS * Hv * K * V);
         L.Mseg = take(4 * NS * Hv * K * K);

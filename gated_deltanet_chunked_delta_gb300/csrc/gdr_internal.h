@@ -7,6 +7,9 @@
 namespace gdr {
 
 constexpr int kChunk = 64;  // tokens per chunk
+// Tensor-core path per-(chunk, v-head) workspace records (bytes).
+constexpr int kTileImgBytes = 16384;  // one bf16 hi | lo pair of 64x64 images (A, P')
+constexpr int kAuxBytes = 768;        // beta, e^gamma, e^{gamma_n - gamma}: 3 x 64 fp32
 
 // Per sequence: token range, chunk range and segment range (context-parallel split).
 struct SeqInfo {
@@ -98,7 +101,9 @@ int simt_fwd(const Params &p, int in_f32, int o_f32, int use_cp, cudaStream_t st
 int simt_bwd(const Params &p, int in_f32, int use_cp, cudaStream_t st);
 unsigned simt_take_status(cudaStream_t st);
 int simt_cp_combine(const Params &p, cudaStream_t st);
-int simt_bwd_chunk(const Params &p, cudaStream_t st);
+int simt_cp_combine_rev(const Params &p, cudaStream_t st);
+int simt_group_sum(const Params &p, cudaStream_t st);   // dq, dk from per-v-head partials (bf16)
+int mma_bwd_chunk(const Params &p, cudaStream_t st);    // chunk-local gradients, warp MMAs
 int prep_tables(const int32_t *cu_dev, int N, int T_fixed, int seg_len, SeqInfo *seq,
                 ChunkInfo *chunk, SegInfo *seg, cudaStream_t st);
 }  // namespace gdr

@@ -234,43 +234,135 @@ __global__ void __launch_bounds__(256) k_cp_summary(Params p) {
 }
 
 // ---------------------------------------------------------------------------
-// K3 (context parallel, step 2): per (sequence, v-head, 32 state columns):
-// S_start(j+1) = M_j S_start(j) + H_j, in segment order.
+// K3 (context parallel, step 2): per (sequence, v-head, 8 state columns):
+// S_start(j+1) = M_j S_start(j) + H_j, in segment order.  Each M_j is staged
+// in shared memory with coalesced loads; two threads share a row of M_j.
 // ---------------------------------------------------------------------------
+constexpr int kCombCols = 8;
+
 template <int KD, int VD>
 __global__ void __launch_bounds__(256) k_cp_combine(Params p) {
     extern __shared__ float sm[];
-    float *S = sm;  // [KD][33]
-    const int n = blockIdx.x, h = blockIdx.y, v0 = blockIdx.z * 32, tid = threadIdx.x;
+    float *Ms = sm;                  // [KD][KD+1]
+    float *S = Ms + KD * (KD + 1);   // [KD][8]
+    const int n = blockIdx.x, h = blockIdx.y, v0 = blockIdx.z * kCombCols, tid = threadIdx.x;
     const SeqInfo sq = p.seq[n];
     if (sq.nseg <= 1) return;
-    for (int idx = tid; idx < KD * 32; idx += 256) {
-        const int i = idx >> 5, j = idx & 31;
-        S[i * 33 + j] = p.h0 ? p.h0[(((size_t)n * p.Hv + h) * KD + i) * VD + v0 + j] : 0.f;
+    for (int idx = tid; idx < KD * kCombCols; idx += 256) {
+        const int i = idx >> 3, j = idx & 7;
+        S[idx] = p.h0 ? p.h0[(((size_t)n * p.Hv + h) * KD + i) * VD + v0 + j] : 0.f;
     }
-    const int jj = tid & 31, i0 = tid >> 5;
-    constexpr int NM = KD / 8;
-    float acc[NM];
     for (int s = 0; s < sq.nseg - 1; ++s) {
-        __syncthreads();
         const size_t sgi = (size_t)sq.seg0 + s;
-        const float *M = p.Mseg + (sgi * p.Hv + h) * KD * KD;
+        const float4 *M4 = reinterpret_cast<const float4 *>(p.Mseg + (sgi * p.Hv + h) * KD * KD);
         const float *Hs = p.Hseg + (sgi * p.Hv + h) * KD * VD;
-#pragma unroll
-        for (int m = 0; m < NM; ++m) acc[m] = Hs[(i0 + 8 * m) * VD + v0 + jj];
-        for (int l = 0; l < KD; ++l) {
-            const float sl = S[l * 33 + jj];
-#pragma unroll
-            for (int m = 0; m < NM; ++m) acc[m] += M[(i0 + 8 * m) * KD + l] * sl;
+        float *dst = p.Sstart + ((sgi + 1) * p.Hv + h) * KD * VD;
+        __syncthreads();
+        for (int idx = tid; idx < KD * KD / 4; idx += 256) {
+            const float4 m = M4[idx];
+            const int row = idx / (KD / 4), c = 4 * (idx % (KD / 4));
+            float *d = Ms + row * (KD + 1) + c;
+            d[0] = m.x; d[1] = m.y; d[2] = m.z; d[3] = m.w;
         }
         __syncthreads();
-        float *dst = p.Sstart + ((sgi + 1) * p.Hv + h) * KD * VD;
+        float acc[2][4];
+        int rows[2];
+        const int nout = KD * 2;  // (row, half of the 8 columns)
 #pragma unroll
-        for (int m = 0; m < NM; ++m) {
-            S[(i0 + 8 * m) * 33 + jj] = acc[m];
-            dst[(i0 + 8 * m) * VD + v0 + jj] = acc[m];
+        for (int u = 0; u < 2; ++u) {
+            const int o = tid + 256 * u;
+            rows[u] = o < nout ? (o >> 1) : -1;
+            if (rows[u] < 0) continue;
+            const int j0 = (o & 1) * 4;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[u][e] = Hs[rows[u] * VD + v0 + j0 + e];
+            for (int l = 0; l < KD; ++l) {
+                const float m = Ms[rows[u] * (KD + 1) + l];
+                const float4 sv = *reinterpret_cast<const float4 *>(S + l * kCombCols + j0);
+                acc[u][0] += m * sv.x;
+                acc[u][1] += m * sv.y;
+                acc[u][2] += m * sv.z;
+                acc[u][3] += m * sv.w;
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            if (rows[u] < 0) continue;
+            const int o = tid + 256 * u, j0 = (o & 1) * 4;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                S[rows[u] * kCombCols + j0 + e] = acc[u][e];
+                dst[rows[u] * VD + v0 + j0 + e] = acc[u][e];
+            }
         }
     }
+}
+
+// Reverse combine of the segmented backward scan, per (sequence, v-head, 8
+// columns): dS_end(last) = dht; dS_end(j) = N_{j+1} dS_end(j+1) + G_{j+1},
+// with N in Mseg and G in Hseg; dS_end(j) goes to Sstart[j].
+template <int KD, int VD>
+__global__ void __launch_bounds__(256) k_cp_combine_rev(Params p) {
+    extern __shared__ float sm[];
+    float *Ms = sm;                  // [KD][KD+1]
+    float *S = Ms + KD * (KD + 1);   // [KD][8]
+    const int n = blockIdx.x, h = blockIdx.y, v0 = blockIdx.z * kCombCols, tid = threadIdx.x;
+    const SeqInfo sq = p.seq[n];
+    if (sq.nseg <= 1) return;
+    for (int idx = tid; idx < KD * kCombCols; idx += 256) {
+        const int i = idx >> 3, j = idx & 7;
+        S[idx] = p.dht ? p.dht[(((size_t)n * p.Hv + h) * KD + i) * VD + v0 + j] : 0.f;
+    }
+    for (int s = sq.nseg - 1; s >= 1; --s) {
+        const size_t sgi = (size_t)sq.seg0 + s;
+        const float4 *M4 = reinterpret_cast<const float4 *>(p.Mseg + (sgi * p.Hv + h) * KD * KD);
+        const float *Hs = p.Hseg + (sgi * p.Hv + h) * KD * VD;
+        float *dst = p.Sstart + ((sgi - 1) * p.Hv + h) * KD * VD;
+        __syncthreads();
+        for (int idx = tid; idx < KD * KD / 4; idx += 256) {
+            const float4 m = M4[idx];
+            const int row = idx / (KD / 4), c = 4 * (idx % (KD / 4));
+            float *d = Ms + row * (KD + 1) + c;
+            d[0] = m.x; d[1] = m.y; d[2] = m.z; d[3] = m.w;
+        }
+        __syncthreads();
+        float acc[2][4];
+        int rows[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int o = tid + 256 * u;
+            rows[u] = o < KD * 2 ? (o >> 1) : -1;
+            if (rows[u] < 0) continue;
+            const int j0 = (o & 1) * 4;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[u][e] = Hs[rows[u] * VD + v0 + j0 + e];
+            for (int l = 0; l < KD; ++l) {
+                const float m = Ms[rows[u] * (KD + 1) + l];
+                const float4 sv = *reinterpret_cast<const float4 *>(S + l * kCombCols + j0);
+                acc[u][0] += m * sv.x;
+                acc[u][1] += m * sv.y;
+                acc[u][2] += m * sv.z;
+                acc[u][3] += m * sv.w;
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            if (rows[u] < 0) continue;
+            const int o = tid + 256 * u, j0 = (o & 1) * 4;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                S[rows[u] * kCombCols + j0 + e] = acc[u][e];
+                dst[rows[u] * VD + v0 + j0 + e] = acc[u][e];
+            }
+        }
+    }
+}
+
+template <int KD>
+constexpr size_t smem_combine() {
+    return sizeof(float) * (KD * (KD + 1) + KD * kCombCols);
 }
 
 // ---------------------------------------------------------------------------
@@ -764,7 +856,7 @@ int fwd_impl(const Params &p, int use_cp, cudaStream_t st) {
         e = launch("simt_cp_summary", k_cp_summary<TI, KD, VD>, dim3(p.NSEG, p.Hv, (VD + KD) / 32),
                    smem_summary<KD, VD>(), st, p);
         if (e != cudaSuccess) return 1;
-        e = launch("simt_cp_combine", k_cp_combine<KD, VD>, dim3(p.N, p.Hv, VD / 32), sizeof(float) * KD * 33,
+        e = launch("simt_cp_combine", k_cp_combine<KD, VD>, dim3(p.N, p.Hv, VD / kCombCols), smem_combine<KD>(),
                    st, p);
         if (e != cudaSuccess) return 1;
     }
@@ -783,7 +875,7 @@ int bwd_impl(const Params &p0, int use_cp, cudaStream_t st) {
         e = launch("simt_cp_summary", k_cp_summary<TI, KD, VD>, dim3(p.NSEG, p.Hv, (VD + KD) / 32),
                    smem_summary<KD, VD>(), st, p);
         if (e != cudaSuccess) return 1;
-        e = launch("simt_cp_combine", k_cp_combine<KD, VD>, dim3(p.N, p.Hv, VD / 32), sizeof(float) * KD * 33,
+        e = launch("simt_cp_combine", k_cp_combine<KD, VD>, dim3(p.N, p.Hv, VD / kCombCols), smem_combine<KD>(),
                    st, p);
         if (e != cudaSuccess) return 1;
     }
@@ -840,11 +932,7 @@ int simt_bwd(const Params &p, int in_f32, int use_cp, cudaStream_t st) {
     return in_f32 ? bwd_dims<float>(p, use_cp, st) : bwd_dims<__nv_bfloat16>(p, use_cp, st);
 }
 
-int simt_bwd_chunk(const Params &p, cudaStream_t st) {
-    if (p.K != 128 || p.V != 128) return 1;
-    cudaError_t e = launch("simt_bwd_chunk", k_bwd_chunk<__nv_bfloat16, 128, 128>, dim3(p.NT, p.Hv),
-                           smem_bwd_chunk<128, 128>(), st, p);
-    if (e != cudaSuccess) return 1;
+int simt_group_sum(const Params &p, cudaStream_t st) {
     const long long n = (long long)p.Ttot * p.Hq * 128;
     if (n > 0) {
         const int blocks = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
@@ -859,10 +947,17 @@ int simt_bwd_chunk(const Params &p, cudaStream_t st) {
     return 0;
 }
 
+int simt_cp_combine_rev(const Params &p, cudaStream_t st) {
+    if (p.K == 128 && p.V == 128)
+        return launch("cp_combine_rev", k_cp_combine_rev<128, 128>, dim3(p.N, p.Hv, 128 / kCombCols),
+                      smem_combine<128>(), st, p) != cudaSuccess;
+    return 1;
+}
+
 int simt_cp_combine(const Params &p, cudaStream_t st) {
     if (p.K == 128 && p.V == 128)
-        return launch("cp_combine", k_cp_combine<128, 128>, dim3(p.N, p.Hv, 4), sizeof(float) * 128 * 33, st, p) !=
-               cudaSuccess;
+        return launch("cp_combine", k_cp_combine<128, 128>, dim3(p.N, p.Hv, 128 / kCombCols), smem_combine<128>(), st,
+                      p) != cudaSuccess;
     return 1;
 }
 

@@ -190,11 +190,14 @@ __device__ __forceinline__ void st_row32(char *tile, int rows, int row, int col0
 // lo = bf16(x - hi), which together carry ~16 significant bits:
 //   A image   [hi | lo], each [64 rows r][128 B], 128-byte swizzled: A[r][s] over s
 //   P' image  same layout: P'[r][s] = scale e^{gamma_r - gamma_n} (q_r . k_s), s <= r
-//   aux       gamma[64], beta[64] (fp32; rows past the chunk end: gamma_n, 0)
+//   aux       beta[64], e^gamma[64], e^{gamma_n - gamma}[64] (fp32; rows past
+//             the chunk end: beta 0, gamma = gamma_n), the row factors every
+//             scan epilogue needs, computed once per chunk
 // ---------------------------------------------------------------------------
 constexpr int kImg = 8192;       // one bf16 term
 constexpr int kImg2 = 2 * kImg;  // hi and lo
-constexpr int kAux = 512;
+static_assert(kImg2 == kTileImgBytes, "tile image size");
+constexpr int kAux = kAuxBytes;
 
 __device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
 
@@ -327,8 +330,9 @@ __global__ void __launch_bounds__(128) k_chunk_tc(Params p, const __grid_constan
         const float gC = gam[63];
         if (tid < 64) {
             float *aux = reinterpret_cast<float *>(reinterpret_cast<char *>(p.Aux) + ch * kAux);
-            aux[tid] = gam[tid];
-            aux[64 + tid] = bet[tid];
+            aux[tid] = bet[tid];
+            aux[64 + tid] = __expf(gam[tid]);
+            aux[128 + tid] = __expf(gC - gam[tid]);
         }
         if (tid < 64) {
             const int rr = tid;
@@ -414,7 +418,9 @@ __global__ void __launch_bounds__(128) k_chunk_tc(Params p, const __grid_constan
 
 // ---------------------------------------------------------------------------
 // Scan kernel.  One CTA per (segment, v-head) (x2 in kSum: the S and the M
-// states run in separate CTAs).  Per chunk, with S^T in TMEM (lane v):
+// states run in separate CTAs).  Warps 0-7: epilogue (two warpgroups that
+// split the columns of every phase), warp 8: TMA producer (two-stage ring),
+// warp 9: tensor-memory allocation and the MMA issue (one thread).  Per chunk, with S^T in TMEM (lane v):
 //   (a)  S^T -> bf16 hi + lo (A operands); S^T *= e^{gamma_n} in place
 //   MMA1 D1 = S^T [K ; Q]^T                               -> (K S)^T, (Q S)^T
 //   (c)  R^T = (diag(b) (V - diag(e^gamma) K S))^T        -> bf16 hi + lo
@@ -455,7 +461,7 @@ __host__ __device__ constexpr int scan_smem() {
 }
 
 template <int MODE, typename TO>
-__global__ void __launch_bounds__(192, 1) k_scan_tc(Params p, const __grid_constant__ ScanMaps maps) {
+__global__ void __launch_bounds__(320, 1) k_scan_tc(Params p, const __grid_constant__ ScanMaps maps) {
     extern __shared__ __align__(1024) char smraw[];
     char *sm = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
     using SL = ScanStage<MODE>;
@@ -491,19 +497,19 @@ __global__ void __launch_bounds__(192, 1) k_scan_tc(Params p, const __grid_const
     if (tid == 0) {
         mbar_init(&full[0], 1);
         mbar_init(&full[1], 1);
-        mbar_init(&empty[0], 129);
-        mbar_init(&empty[1], 129);
-        mbar_init(bar_sb, 128);
+        mbar_init(&empty[0], 257);
+        mbar_init(&empty[1], 257);
+        mbar_init(bar_sb, 256);
         mbar_init(bar_m1, 1);
-        mbar_init(bar_rt, 128);
+        mbar_init(bar_rt, 256);
         mbar_init(bar_m1b, 1);
-        mbar_init(bar_ut, 128);
+        mbar_init(bar_ut, 256);
         mbar_init(bar_m3, 1);
         mbar_init(bar_drain, 1);
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 5) {
+    if (warp == 9) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
                      "r"(512));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
@@ -514,7 +520,7 @@ __global__ void __launch_bounds__(192, 1) k_scan_tc(Params p, const __grid_const
     const uint32_t tmem = *tmem_slot;
     const uint32_t tS = tmem, tD1 = tmem + 128, tD1b = tmem + 256, tD2 = tmem + 320;
 
-    if (warp == 4) {
+    if (warp == 8) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
             int issued = 0;
@@ -544,7 +550,7 @@ __global__ void __launch_bounds__(192, 1) k_scan_tc(Params p, const __grid_const
             for (int cc = issued - 2 < 0 ? 0 : issued - 2; cc < issued; ++cc)
                 drain_wait(&full[cc & 1], (cc >> 1) & 1);
         }
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
             const uint32_t id1 = idesc_bf16(128, MODE == kFwd ? 128 : 64);
@@ -606,11 +612,13 @@ __global__ void __launch_bounds__(192, 1) k_scan_tc(Params p, const __grid_const
             drain_wait(bar_drain, 0);
         }
     } else {
-        // ---------------- epilogue: warps 0-3, thread t <-> TMEM lane t ----------------
-        const int t = tid;
-        const uint32_t lo = (uint32_t)(warp * 32) << 16;
+        // ---------------- epilogue: warps 0-7, two warpgroups splitting the columns;
+        // thread t of a warpgroup <-> TMEM lane t ----------------
+        const int wg = warp >> 2;  // two epilogue warpgroups split the columns
+        const int t = tid & 127;
+        const uint32_t lo = (uint32_t)((warp & 3) * 32) << 16;
         uint32_t r[32];
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 2 * wg; j < 2 * wg + 2; ++j) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 const int k = 32 * j + i;
@@ -630,16 +638,15 @@ __global__ void __launch_bounds__(192, 1) k_scan_tc(Params p, const __grid_const
         for (int cc = 0; cc < nch; ++cc) {
             const int s = cc & 1;
             char *st = stage0 + s * SL::kBytes;
-            const float *gam = reinterpret_cast<const float *>(aux0 + s * kAux);
-            const float *bet = gam + 64;
+            const float *bet = reinterpret_cast<const float *>(aux0 + s * kAux);
+            const float *eg = bet + 64, *eL = bet + 128;
             const int c = sg.chunk0 + cc;
             if (cc > 0 && !bwait(bar_m3, (cc - 1) & 1, cap, abort)) break;
             tc_fence_after();
             if (!bwait(&full[s], (cc >> 1) & 1, cap, abort)) break;
-            const float gC = gam[63];
-            const float dec = __expf(gC);
+            const float dec = eg[63];
             // (a)
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 2 * wg; j < 2 * wg + 2; ++j) {
                 tmem_ld32(tS + 32 * j + lo, r);
                 float f[32], hi[32], lw[32];
 #pragma unroll
@@ -651,7 +658,7 @@ __global__ void __launch_bounds__(192, 1) k_scan_tc(Params p, const __grid_const
                 st_row32(SBh, 128, t, 32 * j, hi);
                 st_row32(SBl, 128, t, 32 * j, lw);
                 if (hdst)
-#pragma unroll 8
+#pragma unroll
                     for (int i = 0; i < 32; ++i) hdst[(((size_t)c * p.Hv + h) * 128 + 32 * j + i) * 128 + t] = f[i];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(f[i] * dec);
@@ -665,14 +672,14 @@ __global__ void __launch_bounds__(192, 1) k_scan_tc(Params p, const __grid_const
             if (!bwait(bar_m1, cc & 1, cap, abort)) break;
             tc_fence_after();
             const __nv_bfloat16 *Vs = reinterpret_cast<const __nv_bfloat16 *>(st + SL::kV);
-            for (int j = 0; j < 2; ++j) {
+            for (int j = wg; j < wg + 1; ++j) {
                 tmem_ld32(tD1 + 32 * j + lo, r);
                 float f[32], lw[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     const int s2 = 32 * j + i;
                     const float vv = isM ? 0.f : __bfloat162float(Vs[s2 * 128 + t]);
-                    const float x = bet[s2] * (vv - __expf(gam[s2]) * __uint_as_float(r[i]));
+                    const float x = bet[s2] * (vv - eg[s2] * __uint_as_float(r[i]));
                     f[i] = bf16_round(x);
                     lw[i] = x - f[i];
                 }
@@ -685,12 +692,12 @@ __global__ void __launch_bounds__(192, 1) k_scan_tc(Params p, const __grid_const
             // (c2) Y^T[t][r] = e^{gamma_n - gamma_r} Ut^T[t][r]
             if (!bwait(bar_m1b, cc & 1, cap, abort)) break;
             tc_fence_after();
-            for (int j = 0; j < 2; ++j) {
+            for (int j = wg; j < wg + 1; ++j) {
                 tmem_ld32(tD1b + 32 * j + lo, r);
                 float f[32], lw[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    const float x = __expf(gC - gam[32 * j + i]) * __uint_as_float(r[i]);
+                    const float x = eL[32 * j + i] * __uint_as_float(r[i]);
                     f[i] = bf16_round(x);
                     lw[i] = x - f[i];
                 }
@@ -706,14 +713,14 @@ __global__ void __launch_bounds__(192, 1) k_scan_tc(Params p, const __grid_const
                 tc_fence_after();
                 const ChunkInfo ci = p.chunk[c];
                 TO *o = reinterpret_cast<TO *>(p.o);
-                for (int j = 0; j < 2; ++j) {
+                for (int j = wg; j < wg + 1; ++j) {
                     uint32_t r2[32];
                     tmem_ld32(tD1 + 64 + 32 * j + lo, r);
                     tmem_ld32(tD2 + 32 * j + lo, r2);
-#pragma unroll 8
+#pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         const int rr = 32 * j + i;
-                        const float val = p.scale * __expf(gam[rr]) * __uint_as_float(r[i]) + __uint_as_float(r2[i]);
+                        const float val = p.scale * eg[rr] * __uint_as_float(r[i]) + __uint_as_float(r2[i]);
                         if (rr < ci.len) {
                             const size_t off = ((size_t)(ci.tok0 + rr) * p.Hv + h) * 128 + t;
                             if constexpr (sizeof(TO) == 4)
@@ -744,16 +751,16 @@ __global__ void __launch_bounds__(192, 1) k_scan_tc(Params p, const __grid_const
                 base = ((size_t)sg.seq * p.Hv + h) * 128 * 128;
             }
             if (dst)
-                for (int j = 0; j < 4; ++j) {
+                for (int j = 2 * wg; j < 2 * wg + 2; ++j) {
                     tmem_ld32(tS + 32 * j + lo, r);
-#pragma unroll 8
+#pragma unroll
                     for (int i = 0; i < 32; ++i) dst[base + (size_t)(32 * j + i) * 128 + t] = __uint_as_float(r[i]);
                 }
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512));
     }
@@ -772,7 +779,16 @@ __global__ void __launch_bounds__(192, 1) k_scan_tc(Params p, const __grid_const
 //   (c2) X^T = [ (diag(scale e^gamma) dO)^T | -(diag(b e^gamma) dR)^T ] -> hi + lo
 //   MMA-c dS^T += X^T [Q ; K]              (the stacked Q, K tile read MN-major)
 // which is dS0 = e^{gamma_n} dS1 + Qt^T dO - W^T dUt with W = A diag(b e^gamma) K.
+//
+// The map dS1 -> dS0 is affine, so the reverse scan splits into segments
+// exactly like the forward (the context-parallel backward): kDhSum summarises
+// every segment but the first from dS = 0 (G, with the dO terms) and, in a
+// second CTA, from dS = I without the dO terms (N, the composed transposed
+// transitions); a reverse combine gives every segment's true end gradient
+// (dS_end(j) = N_{j+1} dS_end(j+1) + G_{j+1}); kDhFull re-runs each segment
+// from it and stores dS1 and dUt of every chunk, and dh0 for the first.
 // ---------------------------------------------------------------------------
+constexpr int kDhFull = 0, kDhSum = 1;
 struct DhMaps {
     CUtensorMap K, Q, dO;  // 3-D, box (64, 1, 64), 128-byte swizzle
 };
@@ -785,7 +801,8 @@ struct DhStage {
 };
 constexpr int kDhSmem = 1024 + 2 * DhStage::kBytes + kOps + 2 * kAux + 256;
 
-__global__ void __launch_bounds__(192, 1) k_dh_tc(Params p, const __grid_constant__ DhMaps maps) {
+template <int DM>
+__global__ void __launch_bounds__(320, 1) k_dh_tc(Params p, const __grid_constant__ DhMaps maps) {
     extern __shared__ __align__(1024) char smraw[];
     char *sm = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
     static_assert(kDhSmem <= 227 * 1024, "shared memory budget");
@@ -810,28 +827,32 @@ __global__ void __launch_bounds__(192, 1) k_dh_tc(Params p, const __grid_constan
     volatile int *abort = reinterpret_cast<volatile int *>(bars + 12);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int n = blockIdx.x, h = blockIdx.y;
-    const SeqInfo sq = p.seq[n];
+    const int sidx = blockIdx.x, h = blockIdx.y;
+    const SegInfo sg = p.seg[sidx];
+    const SeqInfo sq = p.seq[sg.seq];
+    const int n = sg.seq;
+    const bool isN = DM == kDhSum && blockIdx.z == 1;  // the composed-transition state
     const int hq = h / (p.Hv / p.Hq);
-    const int nch = sq.nch;
+    const int nch = (DM == kDhSum && sg.idx == 0) ? 0 : sg.nch;  // the first segment needs no summary
+    const int cend = sg.chunk0 + sg.nch;                        // chunks run cend-1 down to chunk0
     const long long cap = p.timeout_spins;
 
     if (tid == 0) {
         mbar_init(&full[0], 1);
         mbar_init(&full[1], 1);
-        mbar_init(&empty[0], 129);
-        mbar_init(&empty[1], 129);
-        mbar_init(bar_sb, 128);
+        mbar_init(&empty[0], 257);
+        mbar_init(&empty[1], 257);
+        mbar_init(bar_sb, 256);
         mbar_init(bar_m1, 1);
-        mbar_init(bar_ut, 128);
+        mbar_init(bar_ut, 256);
         mbar_init(bar_m2, 1);
-        mbar_init(bar_x, 128);
+        mbar_init(bar_x, 256);
         mbar_init(bar_m3, 1);
         mbar_init(bar_drain, 1);
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 5) {
+    if (warp == 9) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
                      "r"(256));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
@@ -842,13 +863,13 @@ __global__ void __launch_bounds__(192, 1) k_dh_tc(Params p, const __grid_constan
     const uint32_t tmem = *tmem_slot;
     const uint32_t tS = tmem, tD1 = tmem + 128, tD2 = tmem + 192;
 
-    if (warp == 4) {
+    if (warp == 8) {
         if (lane == 0) {
             int issued = 0;
             for (int cc = 0; cc < nch; ++cc) {
                 const int s = cc & 1;
                 if (cc >= 2 && !bwait(&empty[s], ((cc >> 1) & 1) ^ 1, cap, abort)) break;
-                const int c = sq.chunk0 + nch - 1 - cc;
+                const int c = cend - 1 - cc;
                 const int tok0 = p.chunk[c].tok0;
                 const size_t ch = (size_t)c * p.Hv + h;
                 char *st = stage0 + s * SL::kBytes;
@@ -867,7 +888,7 @@ __global__ void __launch_bounds__(192, 1) k_dh_tc(Params p, const __grid_constan
             for (int cc = issued - 2 < 0 ? 0 : issued - 2; cc < issued; ++cc)
                 drain_wait(&full[cc & 1], (cc >> 1) & 1);
         }
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         if (lane == 0) {
             const uint32_t idK = idesc_bf16(128, 64);           // dS1^T K^T
             const uint32_t idOP = idesc_bf16(128, 64, 1, 1);    // dO^T P'
@@ -889,7 +910,7 @@ __global__ void __launch_bounds__(192, 1) k_dh_tc(Params p, const __grid_constan
                         mma(tD1, sdesc(a0 + o), sdesc(kr + o), idK, (half | kk) != 0);
                     }
                 }
-                {
+                if (!isN) {
                     const uint32_t dO = su32(st + SL::kdO), ph = su32(st + SL::kP), pl = ph + kImg;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
@@ -927,14 +948,22 @@ __global__ void __launch_bounds__(192, 1) k_dh_tc(Params p, const __grid_constan
             drain_wait(bar_drain, 0);
         }
     } else {
-        const int t = tid;
-        const uint32_t lo = (uint32_t)(warp * 32) << 16;
+        const int wg = warp >> 2;  // two epilogue warpgroups split the columns
+        const int t = tid & 127;
+        const uint32_t lo = (uint32_t)((warp & 3) * 32) << 16;
         uint32_t r[32];
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 2 * wg; j < 2 * wg + 2; ++j) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 const int k = 32 * j + i;
-                r[i] = __float_as_uint(p.dht ? p.dht[(((size_t)n * p.Hv + h) * 128 + k) * 128 + t] : 0.f);
+                float v0;
+                if (DM == kDhSum)
+                    v0 = (isN && k == t) ? 1.f : 0.f;
+                else if (sg.idx == sq.nseg - 1)
+                    v0 = p.dht ? p.dht[(((size_t)n * p.Hv + h) * 128 + k) * 128 + t] : 0.f;
+                else
+                    v0 = p.Sstart[(((size_t)sidx * p.Hv + h) * 128 + k) * 128 + t];
+                r[i] = __float_as_uint(v0);
             }
             tmem_st32(tS + 32 * j + lo, r);
         }
@@ -942,18 +971,17 @@ __global__ void __launch_bounds__(192, 1) k_dh_tc(Params p, const __grid_constan
         for (int cc = 0; cc < nch; ++cc) {
             const int s = cc & 1;
             char *st = stage0 + s * SL::kBytes;
-            const float *gam = reinterpret_cast<const float *>(aux0 + s * kAux);
-            const float *bet = gam + 64;
-            const int c = sq.chunk0 + nch - 1 - cc;
+            const float *bet = reinterpret_cast<const float *>(aux0 + s * kAux);
+            const float *eg = bet + 64, *eL = bet + 128;
+            const int c = cend - 1 - cc;
             const int len = p.chunk[c].len;
             const size_t ch = (size_t)c * p.Hv + h;
             if (cc > 0 && !bwait(bar_m3, (cc - 1) & 1, cap, abort)) break;
             tc_fence_after();
             if (!bwait(&full[s], (cc >> 1) & 1, cap, abort)) break;
-            const float gC = gam[63];
-            const float dec = __expf(gC);
+            const float dec = eg[63];
             // (a)
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 2 * wg; j < 2 * wg + 2; ++j) {
                 tmem_ld32(tS + 32 * j + lo, r);
                 float f[32], hi[32], lw[32];
 #pragma unroll
@@ -964,8 +992,9 @@ __global__ void __launch_bounds__(192, 1) k_dh_tc(Params p, const __grid_constan
                 }
                 st_row32(SBh, 128, t, 32 * j, hi);
                 st_row32(SBl, 128, t, 32 * j, lw);
-#pragma unroll 8
-                for (int i = 0; i < 32; ++i) p.dhbuf[(ch * 128 + 32 * j + i) * 128 + t] = f[i];
+                if (DM == kDhFull)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) p.dhbuf[(ch * 128 + 32 * j + i) * 128 + t] = f[i];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(f[i] * dec);
                 tmem_st32(tS + 32 * j + lo, r);
@@ -977,14 +1006,14 @@ __global__ void __launch_bounds__(192, 1) k_dh_tc(Params p, const __grid_constan
             // (c) dUt^T[t][r] = e^{gamma_n - gamma_r} dY^T[t][r]
             if (!bwait(bar_m1, cc & 1, cap, abort)) break;
             tc_fence_after();
-            for (int j = 0; j < 2; ++j) {
+            for (int j = wg; j < wg + 1; ++j) {
                 tmem_ld32(tD1 + 32 * j + lo, r);
                 float f[32], lw[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     const int rr = 32 * j + i;
-                    const float x = rr < len ? __expf(gC - gam[rr]) * __uint_as_float(r[i]) : 0.f;
-                    p.dubuf[(ch * 64 + rr) * 128 + t] = x;
+                    const float x = rr < len ? eL[rr] * __uint_as_float(r[i]) : 0.f;
+                    if (DM == kDhFull) p.dubuf[(ch * 64 + rr) * 128 + t] = x;
                     f[i] = bf16_round(x);
                     lw[i] = x - f[i];
                 }
@@ -1000,27 +1029,27 @@ __global__ void __launch_bounds__(192, 1) k_dh_tc(Params p, const __grid_constan
             {
                 const char *dO = st + SL::kdO + (t >> 6) * 8192;
                 const int cv = t & 63;
-                for (int j = 0; j < 2; ++j) {
+                for (int j = wg; j < wg + 1; ++j) {
                     float f[32], lw[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         const int s2 = 32 * j + i;
                         const __nv_bfloat16 dv = *reinterpret_cast<const __nv_bfloat16 *>(
                             dO + s2 * 128 + ((((cv >> 3) ^ (s2 & 7)) << 4) | ((cv & 7) << 1)));
-                        const float x = s2 < len ? p.scale * __expf(gam[s2]) * __bfloat162float(dv) : 0.f;
+                        const float x = (s2 < len && !isN) ? p.scale * eg[s2] * __bfloat162float(dv) : 0.f;
                         f[i] = bf16_round(x);
                         lw[i] = x - f[i];
                     }
                     st_row32(XTh, 128, t, 32 * j, f);
                     st_row32(XTl, 128, t, 32 * j, lw);
                 }
-                for (int j = 0; j < 2; ++j) {
+                for (int j = wg; j < wg + 1; ++j) {
                     tmem_ld32(tD2 + 32 * j + lo, r);
                     float f[32], lw[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         const int s2 = 32 * j + i;
-                        const float x = -bet[s2] * __expf(gam[s2]) * __uint_as_float(r[i]);
+                        const float x = -bet[s2] * eg[s2] * __uint_as_float(r[i]);
                         f[i] = bf16_round(x);
                         lw[i] = x - f[i];
                     }
@@ -1038,17 +1067,27 @@ __global__ void __launch_bounds__(192, 1) k_dh_tc(Params p, const __grid_constan
             if (nch > 0) bwait(bar_m3, (nch - 1) & 1, cap, abort);
             tc_fence_after();
         }
-        if (!*abort && p.dh0)
-            for (int j = 0; j < 4; ++j) {
-                tmem_ld32(tS + 32 * j + lo, r);
-#pragma unroll 8
-                for (int i = 0; i < 32; ++i)
-                    p.dh0[(((size_t)n * p.Hv + h) * 128 + 32 * j + i) * 128 + t] = __uint_as_float(r[i]);
+        if (!*abort) {
+            float *dst = nullptr;
+            size_t base = 0;
+            if (DM == kDhFull && sg.idx == 0 && p.dh0) {
+                dst = p.dh0;
+                base = ((size_t)n * p.Hv + h) * 128 * 128;
+            } else if (DM == kDhSum && sg.idx > 0) {
+                dst = isN ? p.Mseg : p.Hseg;
+                base = ((size_t)sidx * p.Hv + h) * 128 * 128;
             }
+            if (dst)
+                for (int j = 2 * wg; j < 2 * wg + 2; ++j) {
+                    tmem_ld32(tS + 32 * j + lo, r);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) dst[base + (size_t)(32 * j + i) * 128 + t] = __uint_as_float(r[i]);
+                }
+        }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(256));
     }
@@ -1110,20 +1149,22 @@ int launch_scan(const char *name, const Params &p, cudaStream_t st) {
     const int smem = scan_smem<MODE>();
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 1;
     tm_begin(p.tm, name, st);
-    kern<<<dim3(p.NSEG, p.Hv, MODE == kSum ? 2 : 1), 192, smem, st>>>(p, maps);
+    kern<<<dim3(p.NSEG, p.Hv, MODE == kSum ? 2 : 1), 320, smem, st>>>(p, maps);
     tm_end(p.tm, st);
     return cudaGetLastError() != cudaSuccess;
 }
 
-int launch_dh(const Params &p, cudaStream_t st) {
-    if (p.N == 0) return 0;
+template <int DM>
+int launch_dh(const char *name, const Params &p, cudaStream_t st) {
+    if (p.NSEG == 0) return 0;
     DhMaps maps;
     if (!map3(&maps.K, p.k, p.Hq, p.Ttot, 64, true) || !map3(&maps.Q, p.q, p.Hq, p.Ttot, 64, true) ||
         !map3(&maps.dO, p.dout, p.Hv, p.Ttot, 64, true))
         return 1;
-    if (cudaFuncSetAttribute(k_dh_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kDhSmem) != cudaSuccess) return 1;
-    tm_begin(p.tm, "tc_dh", st);
-    k_dh_tc<<<dim3(p.N, p.Hv), 192, kDhSmem, st>>>(p, maps);
+    auto kern = k_dh_tc<DM>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kDhSmem) != cudaSuccess) return 1;
+    tm_begin(p.tm, name, st);
+    kern<<<dim3(p.NSEG, p.Hv, DM == kDhSum ? 2 : 1), 320, kDhSmem, st>>>(p, maps);
     tm_end(p.tm, st);
     return cudaGetLastError() != cudaSuccess;
 }
@@ -1151,10 +1192,15 @@ int tc_bwd(const Params &p, int use_cp, cudaStream_t st) {
     Params ps = p;
     ps.final_state = nullptr;
     if (launch_scan<kStates, float>("tc_scan_states", ps, st)) return 1;
-    // a9: reverse state scan
-    if (launch_dh(p, st)) return 1;
+    // a9: reverse state scan (segmented like the forward when the plan splits)
+    if (use_cp) {
+        if (launch_dh<kDhSum>("tc_dh_summary", p, st)) return 1;
+        if (simt_cp_combine_rev(p, st)) return 1;
+    }
+    if (launch_dh<kDhFull>("tc_dh", p, st)) return 1;
     // a10, a11: chunk-local gradients
-    return simt_bwd_chunk(p, st);
+    if (mma_bwd_chunk(p, st)) return 1;
+    return simt_group_sum(p, st);
 }
 
 unsigned tc_take_status(cudaStream_t st) {

@@ -209,7 +209,7 @@ def _stream(stream):
 
 def gdr_fwd(q, k, v, g, beta, scale=None, h0=None, cu_seqlens=None, cu_seqlens_host=None, *, o_dtype=None,
             output_final_state=True, want_A=True, want_h=False, cp_segments=0, path=GDR_PATH_AUTO,
-            debug_checks=0, workspace=None, out=None, stream=None, timer=None):
+            debug_checks=0, timeout_spins=0, workspace=None, out=None, stream=None, timer=None):
     """Forward.  Returns dict(o, final_state, A, h) (entries None when not requested).
 
     ``out`` may hold preallocated output tensors under the same keys."""
@@ -218,7 +218,7 @@ def gdr_fwd(q, k, v, g, beta, scale=None, h0=None, cu_seqlens=None, cu_seqlens_h
     prob = Problem(q, v, cu_seqlens, cu_seqlens_host)
     if scale is None:
         scale = prob.K ** -0.5
-    opts = make_opts(cp_segments, path, debug_checks, timer=timer)
+    opts = make_opts(cp_segments, path, debug_checks, timeout_spins, timer=timer)
     out = dict(out or {})
     dev = q.device
     if out.get("o") is None:
@@ -243,15 +243,15 @@ def gdr_fwd(q, k, v, g, beta, scale=None, h0=None, cu_seqlens=None, cu_seqlens_h
 
 
 def gdr_bwd(q, k, v, g, beta, A, do, dht=None, scale=None, h0=None, cu_seqlens=None, cu_seqlens_host=None, *,
-            want_dh0=True, cp_segments=0, path=GDR_PATH_AUTO, debug_checks=0, workspace=None, out=None,
-            stream=None, timer=None):
+            want_dh0=True, cp_segments=0, path=GDR_PATH_AUTO, debug_checks=0, timeout_spins=0, workspace=None,
+            out=None, stream=None, timer=None):
     """Backward.  Returns dict(dq, dk, dv, dbeta, dg, dh0)."""
     _check_dev(q, k, v, g, beta, A, do, dht, h0, cu_seqlens)
     lib = load()
     prob = Problem(q, v, cu_seqlens, cu_seqlens_host)
     if scale is None:
         scale = prob.K ** -0.5
-    opts = make_opts(cp_segments, path, debug_checks, timer=timer)
+    opts = make_opts(cp_segments, path, debug_checks, timeout_spins, timer=timer)
     out = dict(out or {})
     dev = q.device
     for key, like in (("dq", q), ("dk", k), ("dv", v)):

@@ -33,9 +33,6 @@ typedef __nv_bfloat16 bf16;
 constexpr int L128 = 136;  // padded row strides (bf16 elements), conflict-free fragment loads
 constexpr int L64 = 72;
 
-__device__ __forceinline__ uint32_t pk(bf16 a, bf16 b) {
-    return (uint32_t)__bfloat16_as_ushort(a) | ((uint32_t)__bfloat16_as_ushort(b) << 16);
-}
 __device__ __forceinline__ void split(float x, bf16 &h, bf16 &l) {
     h = __float2bfloat16_rn(x);
     l = __float2bfloat16_rn(x - __bfloat162float(h));
@@ -112,6 +109,18 @@ __device__ __forceinline__ float rowsum4(float x) {
     return x;
 }
 
+// 8 consecutive bf16 (one 16-byte vector) of a row-major [rows][128] tensor
+// row, or zeros past the chunk end.
+__device__ __forceinline__ uint4 ld8(const bf16 *base, bool in) {
+    return in ? *reinterpret_cast<const uint4 *>(base) : make_uint4(0u, 0u, 0u, 0u);
+}
+__device__ __forceinline__ void split4(const float4 v, bf16 *h, bf16 *l) {
+    split(v.x, h[0], l[0]);
+    split(v.y, h[1], l[1]);
+    split(v.z, h[2], l[2]);
+    split(v.w, h[3], l[3]);
+}
+
 struct Smem {
     bf16 K[64 * L128];
     bf16 Qb[64 * L128];           // Q (after the half loop)
@@ -146,20 +155,28 @@ __global__ void __launch_bounds__(256, 1) k_bwd_chunk_mma(Params p) {
     const bf16 *qin = reinterpret_cast<const bf16 *>(p.q);
     const bf16 *vin = reinterpret_cast<const bf16 *>(p.v);
     const bf16 *din = reinterpret_cast<const bf16 *>(p.dout);
-    const bf16 zb = __float2bfloat16_rn(0.f);
 
     // ---- setup: K, A, gates ----
-    for (int idx = tid; idx < 64 * 64; idx += 256) {
-        const int r = idx >> 6, kk = (idx & 63) * 2;
-        const size_t off = ((size_t)(tok0 + r) * p.Hq + hq) * 128 + kk;
-        const bool in = r < len;
-        S.K[r * L128 + kk] = in ? kin[off] : zb;
-        S.K[r * L128 + kk + 1] = in ? kin[off + 1] : zb;
-    }
-    for (int idx = tid; idx < 64 * 64; idx += 256) {
-        const int r = idx >> 6, s = idx & 63;
-        const float a = r < len ? p.A_in[((size_t)(tok0 + r) * p.Hv + h) * 64 + s] : (r == s ? 1.f : 0.f);
-        split(a, S.Ah[r * L64 + s], S.Al[r * L64 + s]);
+    {
+        // K: 64 rows x 16 vectors of 8; A: 64 rows x 16 float4 (identity rows past the chunk end)
+        uint4 kv[4];
+        float4 av[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = tid + 256 * u, r = e >> 4, c8 = (e & 15) * 8;
+            kv[u] = ld8(kin + ((size_t)(tok0 + r) * p.Hq + hq) * 128 + c8, r < len);
+            const int c4 = (e & 15) * 4;
+            if (r < len)
+                av[u] = *reinterpret_cast<const float4 *>(p.A_in + ((size_t)(tok0 + r) * p.Hv + h) * 64 + c4);
+            else
+                av[u] = make_float4(r == c4, r == c4 + 1, r == c4 + 2, r == c4 + 3);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = tid + 256 * u, r = e >> 4;
+            *reinterpret_cast<uint4 *>(&S.K[r * L128 + (e & 15) * 8]) = kv[u];
+            split4(av[u], &S.Ah[r * L64 + (e & 15) * 4], &S.Al[r * L64 + (e & 15) * 4]);
+        }
     }
     if (tid < 64) {
         S.gam[tid] = tid < len ? p.g[(size_t)(tok0 + tid) * p.Hv + h] : 0.f;
@@ -200,17 +217,43 @@ __global__ void __launch_bounds__(256, 1) k_bwd_chunk_mma(Params p) {
     for (int half = 0; half < 2; ++half) {
         const int v0 = 64 * half;
         __syncthreads();
-        for (int idx = tid; idx < 128 * 64; idx += 256) {
-            const int kk = idx >> 6, vv = idx & 63;
-            split(S0g[kk * 128 + v0 + vv], S.S0h[kk * L64 + vv], S.S0l[kk * L64 + vv]);
-        }
-        for (int idx = tid; idx < 64 * 64; idx += 256) {
-            const int r = idx >> 6, vv = idx & 63;
-            const size_t off = ((size_t)(tok0 + r) * p.Hv + h) * 128 + v0 + vv;
-            const bool in = r < len;
-            S.V[r * L64 + vv] = in ? vin[off] : zb;
-            S.dO[r * L64 + vv] = in ? din[off] : zb;
-            split(dUg[r * 128 + v0 + vv], S.dUh[r * L64 + vv], S.dUl[r * L64 + vv]);
+        {
+            // S0 half: 128 rows x 16 float4; V, dO halves: 64 rows x 8 vectors; dUt half: 64 x 16 float4
+            float4 sv[8], uv[4];
+            uint4 vv8[2], dv8[2];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int e = tid + 256 * u, kk = e >> 4, c4 = (e & 15) * 4;
+                sv[u] = *reinterpret_cast<const float4 *>(S0g + kk * 128 + v0 + c4);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int e = tid + 256 * u, r = e >> 4, c4 = (e & 15) * 4;
+                uv[u] = *reinterpret_cast<const float4 *>(dUg + r * 128 + v0 + c4);
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int e = tid + 256 * u, r = e >> 3, c8 = (e & 7) * 8;
+                const size_t off = ((size_t)(tok0 + r) * p.Hv + h) * 128 + v0 + c8;
+                vv8[u] = ld8(vin + off, r < len);
+                dv8[u] = ld8(din + off, r < len);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int e = tid + 256 * u, kk = e >> 4, c4 = (e & 15) * 4;
+                split4(sv[u], &S.S0h[kk * L64 + c4], &S.S0l[kk * L64 + c4]);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int e = tid + 256 * u, r = e >> 4, c4 = (e & 15) * 4;
+                split4(uv[u], &S.dUh[r * L64 + c4], &S.dUl[r * L64 + c4]);
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int e = tid + 256 * u, r = e >> 3, c8 = (e & 7) * 8;
+                *reinterpret_cast<uint4 *>(&S.V[r * L64 + c8]) = vv8[u];
+                *reinterpret_cast<uint4 *>(&S.dO[r * L64 + c8]) = dv8[u];
+            }
         }
         __syncthreads();
         // (1) KS = K S0 (this half), kept in registers; R = b (V - e^gamma KS)
@@ -304,11 +347,20 @@ __global__ void __launch_bounds__(256, 1) k_bwd_chunk_mma(Params p) {
         wmma<8, false, true>(dk, S.Rl, L64, m0, S.S0h, L64, 64 * cb, 64);
         wmma<8, false, true>(dk, S.Rh, L64, m0, S.S0l, L64, 64 * cb, 64);
         __syncthreads();  // S0 no longer needed: load dS1 into its buffers
-        for (int idx = tid; idx < 128 * 64; idx += 256) {
-            const int kk = idx >> 6, vv = idx & 63;
-            const float d = dS1g[kk * 128 + v0 + vv];
-            s0ds1 += d * S0g[kk * 128 + v0 + vv];
-            split(d, S.S0h[kk * L64 + vv], S.S0l[kk * L64 + vv]);
+        {
+            float4 dv[8], sv[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int e = tid + 256 * u, kk = e >> 4, c4 = (e & 15) * 4;
+                dv[u] = *reinterpret_cast<const float4 *>(dS1g + kk * 128 + v0 + c4);
+                sv[u] = *reinterpret_cast<const float4 *>(S0g + kk * 128 + v0 + c4);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int e = tid + 256 * u, kk = e >> 4, c4 = (e & 15) * 4;
+                s0ds1 += dv[u].x * sv[u].x + dv[u].y * sv[u].y + dv[u].z * sv[u].z + dv[u].w * sv[u].w;
+                split4(dv[u], &S.S0h[kk * L64 + c4], &S.S0l[kk * L64 + c4]);
+            }
         }
         __syncthreads();
         // (8) dK += Y dS1^T
@@ -318,12 +370,18 @@ __global__ void __launch_bounds__(256, 1) k_bwd_chunk_mma(Params p) {
     }
     __syncthreads();
     // ---- after the halves: Q, QK, KK, dP'', dA -> X -> dL, assembly ----
-    for (int idx = tid; idx < 64 * 64; idx += 256) {
-        const int r = idx >> 6, kk = (idx & 63) * 2;
-        const size_t off = ((size_t)(tok0 + r) * p.Hq + hq) * 128 + kk;
-        const bool in = r < len;
-        S.Qb[r * L128 + kk] = in ? qin[off] : zb;
-        S.Qb[r * L128 + kk + 1] = in ? qin[off + 1] : zb;
+    {
+        uint4 qv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = tid + 256 * u, r = e >> 4, c8 = (e & 15) * 8;
+            qv[u] = ld8(qin + ((size_t)(tok0 + r) * p.Hq + hq) * 128 + c8, r < len);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = tid + 256 * u, r = e >> 4;
+            *reinterpret_cast<uint4 *>(&S.Qb[r * L128 + (e & 15) * 8]) = qv[u];
+        }
     }
     {
         float w = s0ds1;

@@ -258,11 +258,18 @@ __global__ void __launch_bounds__(256) k_cp_combine(Params p) {
         const float *Hs = p.Hseg + (sgi * p.Hv + h) * KD * VD;
         float *dst = p.Sstart + ((sgi + 1) * p.Hv + h) * KD * VD;
         __syncthreads();
-        for (int idx = tid; idx < KD * KD / 4; idx += 256) {
-            const float4 m = M4[idx];
-            const int row = idx / (KD / 4), c = 4 * (idx % (KD / 4));
-            float *d = Ms + row * (KD + 1) + c;
-            d[0] = m.x; d[1] = m.y; d[2] = m.z; d[3] = m.w;
+        {
+            // all loads of this thread in flight before any store
+            constexpr int NL = KD * KD / 4 / 256;
+            float4 mv[NL];
+#pragma unroll
+            for (int u = 0; u < NL; ++u) mv[u] = M4[tid + 256 * u];
+#pragma unroll
+            for (int u = 0; u < NL; ++u) {
+                const int idx = tid + 256 * u, row = idx / (KD / 4), c = 4 * (idx % (KD / 4));
+                float *d = Ms + row * (KD + 1) + c;
+                d[0] = mv[u].x; d[1] = mv[u].y; d[2] = mv[u].z; d[3] = mv[u].w;
+            }
         }
         __syncthreads();
         float acc[2][4];
@@ -320,11 +327,18 @@ __global__ void __launch_bounds__(256) k_cp_combine_rev(Params p) {
         const float *Hs = p.Hseg + (sgi * p.Hv + h) * KD * VD;
         float *dst = p.Sstart + ((sgi - 1) * p.Hv + h) * KD * VD;
         __syncthreads();
-        for (int idx = tid; idx < KD * KD / 4; idx += 256) {
-            const float4 m = M4[idx];
-            const int row = idx / (KD / 4), c = 4 * (idx % (KD / 4));
-            float *d = Ms + row * (KD + 1) + c;
-            d[0] = m.x; d[1] = m.y; d[2] = m.z; d[3] = m.w;
+        {
+            // all loads of this thread in flight before any store
+            constexpr int NL = KD * KD / 4 / 256;
+            float4 mv[NL];
+#pragma unroll
+            for (int u = 0; u < NL; ++u) mv[u] = M4[tid + 256 * u];
+#pragma unroll
+            for (int u = 0; u < NL; ++u) {
+                const int idx = tid + 256 * u, row = idx / (KD / 4), c = 4 * (idx % (KD / 4));
+                float *d = Ms + row * (KD + 1) + c;
+                d[0] = mv[u].x; d[1] = mv[u].y; d[2] = mv[u].z; d[3] = mv[u].w;
+            }
         }
         __syncthreads();
         float acc[2][4];

@@ -172,3 +172,23 @@ def test_debug_checks_clean_run(gdr):
     d = to_dev(x)
     gpu_fwd(gdr, d, path=gdr.GDR_PATH_SIMT, debug_checks=1)
     gdr.check_status()
+
+
+def test_bounded_waits_report_timeout_and_leave_the_context_usable(gdr):
+    """Every device-side wait of the tensor-core kernels is a bounded poll.  With
+    a cap of one poll the waits run out: the kernels raise their abort flag,
+    drain their own copies and MMAs, free tensor memory and return; the host
+    reads GDR_ERR_TIMEOUT, and the next call on the same context is correct."""
+    if not gdr.tc_available():
+        pytest.skip("this build has no tensor-core path")
+    spec = inputs.small(B=1, T=64 * 40, Hq=1, Hv=2, K=128, V=128, bwd=True)
+    x = inputs.make(spec)
+    d = to_dev(x)
+    out = gpu_fwd(gdr, d, path=gdr.GDR_PATH_TC, cp_segments=4, timeout_spins=1)
+    gpu_bwd(gdr, d, out["A"], path=gdr.GDR_PATH_TC, cp_segments=4, timeout_spins=1)
+    with pytest.raises(gdr.GdrError) as info:
+        gdr.check_status()
+    assert info.value.code == 7
+    gdr.check_status()  # the status word was cleared
+    _check_fwd(gdr, spec, gdr.GDR_PATH_TC, cp=4)
+    _check_bwd(gdr, spec, gdr.GDR_PATH_TC, cp=4)

@@ -101,6 +101,14 @@ def kernel_work(name, spec, in_bytes, o_bytes, nchunk_heads):
     return 0.0, 0.0
 
 
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
+# ncu capture of the kernel on the workload; an entry is removed whenever the
+# kernel changes (the summaries under profiles/ give the commands).
+TRAFFIC = {
+    ("mma_bwd_chunk", "fwd_bf16_T8192_hq4_hv8_d128"): 295.32e6,
+}
+
+
 # ---------------------------------------------------------------------------
 # clocks sampler
 # ---------------------------------------------------------------------------
@@ -374,7 +382,9 @@ def main():
         else:
             roof = {"bound": "hbm", "achieved": by / (dom_ms / 1e3) / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None
+    roof["traffic"] = TRAFFIC.get((dom, spec.name))
+    roof["algorithmic_bytes"] = by
+    roof["algorithmic_flops"] = fl
     roof["kernel"] = dom
     roof["peak_source"] = peaks["source"]
 

@@ -234,13 +234,17 @@ __global__ void __launch_bounds__(256) k_cp_summary(Params p) {
 }
 
 // ---------------------------------------------------------------------------
-// K3 (context parallel, step 2): per (sequence, v-head, 8 state columns):
-// S_start(j+1) = M_j S_start(j) + H_j, in segment order.  Each M_j is staged
-// in shared memory with coalesced loads; two threads share a row of M_j.
+// K3 (context parallel, step 2): per (sequence, v-head, 8 state columns), in
+// segment order: S_start(j+1) = M_j S_start(j) + H_j from S_start(0) = h0.
+// The reverse form serves the segmented backward scan: dS_end(last) = dht,
+// dS_end(j) = N_{j+1} dS_end(j+1) + G_{j+1} (N in Mseg, G in Hseg), written
+// to Sstart[j].  Each step's matrix is staged in shared memory; the next
+// step's matrix and offsets are loaded into registers while this step
+// computes.  Two threads share a row.
 // ---------------------------------------------------------------------------
 constexpr int kCombCols = 8;
 
-template <int KD, int VD>
+template <int KD, int VD, bool kRev>
 __global__ void __launch_bounds__(256) k_cp_combine(Params p) {
     extern __shared__ float sm[];
     float *Ms = sm;                  // [KD][KD+1]
@@ -248,44 +252,59 @@ __global__ void __launch_bounds__(256) k_cp_combine(Params p) {
     const int n = blockIdx.x, h = blockIdx.y, v0 = blockIdx.z * kCombCols, tid = threadIdx.x;
     const SeqInfo sq = p.seq[n];
     if (sq.nseg <= 1) return;
+    const float *init = kRev ? p.dht : p.h0;
     for (int idx = tid; idx < KD * kCombCols; idx += 256) {
         const int i = idx >> 3, j = idx & 7;
-        S[idx] = p.h0 ? p.h0[(((size_t)n * p.Hv + h) * KD + i) * VD + v0 + j] : 0.f;
+        S[idx] = init ? init[(((size_t)n * p.Hv + h) * KD + i) * VD + v0 + j] : 0.f;
     }
-    for (int s = 0; s < sq.nseg - 1; ++s) {
-        const size_t sgi = (size_t)sq.seg0 + s;
+    const int nsteps = sq.nseg - 1;
+    constexpr int NL = KD * KD / 4 / 256;
+    int rows[2], j0s[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int o = tid + 256 * u;
+        rows[u] = o < KD * 2 ? (o >> 1) : -1;
+        j0s[u] = (o & 1) * 4;
+    }
+    float4 mv[NL];
+    float hv[2][4];
+    // step -> the segment whose summary it applies
+    auto seg_of = [&](int step) -> size_t { return (size_t)sq.seg0 + (kRev ? (sq.nseg - 1 - step) : step); };
+    auto load = [&](int step) {
+        const size_t sgi = seg_of(step);
         const float4 *M4 = reinterpret_cast<const float4 *>(p.Mseg + (sgi * p.Hv + h) * KD * KD);
         const float *Hs = p.Hseg + (sgi * p.Hv + h) * KD * VD;
-        float *dst = p.Sstart + ((sgi + 1) * p.Hv + h) * KD * VD;
+#pragma unroll
+        for (int u = 0; u < NL; ++u) mv[u] = M4[tid + 256 * u];
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) hv[u][e] = rows[u] >= 0 ? Hs[rows[u] * VD + v0 + j0s[u] + e] : 0.f;
+    };
+    load(0);
+    for (int step = 0; step < nsteps; ++step) {
+        const size_t sgi = seg_of(step);
+        float *dst = p.Sstart + ((kRev ? sgi - 1 : sgi + 1) * p.Hv + h) * KD * VD;
         __syncthreads();
-        {
-            // all loads of this thread in flight before any store
-            constexpr int NL = KD * KD / 4 / 256;
-            float4 mv[NL];
 #pragma unroll
-            for (int u = 0; u < NL; ++u) mv[u] = M4[tid + 256 * u];
-#pragma unroll
-            for (int u = 0; u < NL; ++u) {
-                const int idx = tid + 256 * u, row = idx / (KD / 4), c = 4 * (idx % (KD / 4));
-                float *d = Ms + row * (KD + 1) + c;
-                d[0] = mv[u].x; d[1] = mv[u].y; d[2] = mv[u].z; d[3] = mv[u].w;
-            }
+        for (int u = 0; u < NL; ++u) {
+            const int idx = tid + 256 * u, row = idx / (KD / 4), c = 4 * (idx % (KD / 4));
+            float *d = Ms + row * (KD + 1) + c;
+            d[0] = mv[u].x; d[1] = mv[u].y; d[2] = mv[u].z; d[3] = mv[u].w;
         }
-        __syncthreads();
         float acc[2][4];
-        int rows[2];
-        const int nout = KD * 2;  // (row, half of the 8 columns)
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[u][e] = hv[u][e];
+        __syncthreads();
+        if (step + 1 < nsteps) load(step + 1);  // in flight during this step's products
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-            const int o = tid + 256 * u;
-            rows[u] = o < nout ? (o >> 1) : -1;
             if (rows[u] < 0) continue;
-            const int j0 = (o & 1) * 4;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[u][e] = Hs[rows[u] * VD + v0 + j0 + e];
             for (int l = 0; l < KD; ++l) {
                 const float m = Ms[rows[u] * (KD + 1) + l];
-                const float4 sv = *reinterpret_cast<const float4 *>(S + l * kCombCols + j0);
+                const float4 sv = *reinterpret_cast<const float4 *>(S + l * kCombCols + j0s[u]);
                 acc[u][0] += m * sv.x;
                 acc[u][1] += m * sv.y;
                 acc[u][2] += m * sv.z;
@@ -296,79 +315,10 @@ __global__ void __launch_bounds__(256) k_cp_combine(Params p) {
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
             if (rows[u] < 0) continue;
-            const int o = tid + 256 * u, j0 = (o & 1) * 4;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                S[rows[u] * kCombCols + j0 + e] = acc[u][e];
-                dst[rows[u] * VD + v0 + j0 + e] = acc[u][e];
-            }
-        }
-    }
-}
-
-// Reverse combine of the segmented backward scan, per (sequence, v-head, 8
-// columns): dS_end(last) = dht; dS_end(j) = N_{j+1} dS_end(j+1) + G_{j+1},
-// with N in Mseg and G in Hseg; dS_end(j) goes to Sstart[j].
-template <int KD, int VD>
-__global__ void __launch_bounds__(256) k_cp_combine_rev(Params p) {
-    extern __shared__ float sm[];
-    float *Ms = sm;                  // [KD][KD+1]
-    float *S = Ms + KD * (KD + 1);   // [KD][8]
-    const int n = blockIdx.x, h = blockIdx.y, v0 = blockIdx.z * kCombCols, tid = threadIdx.x;
-    const SeqInfo sq = p.seq[n];
-    if (sq.nseg <= 1) return;
-    for (int idx = tid; idx < KD * kCombCols; idx += 256) {
-        const int i = idx >> 3, j = idx & 7;
-        S[idx] = p.dht ? p.dht[(((size_t)n * p.Hv + h) * KD + i) * VD + v0 + j] : 0.f;
-    }
-    for (int s = sq.nseg - 1; s >= 1; --s) {
-        const size_t sgi = (size_t)sq.seg0 + s;
-        const float4 *M4 = reinterpret_cast<const float4 *>(p.Mseg + (sgi * p.Hv + h) * KD * KD);
-        const float *Hs = p.Hseg + (sgi * p.Hv + h) * KD * VD;
-        float *dst = p.Sstart + ((sgi - 1) * p.Hv + h) * KD * VD;
-        __syncthreads();
-        {
-            // all loads of this thread in flight before any store
-            constexpr int NL = KD * KD / 4 / 256;
-            float4 mv[NL];
-#pragma unroll
-            for (int u = 0; u < NL; ++u) mv[u] = M4[tid + 256 * u];
-#pragma unroll
-            for (int u = 0; u < NL; ++u) {
-                const int idx = tid + 256 * u, row = idx / (KD / 4), c = 4 * (idx % (KD / 4));
-                float *d = Ms + row * (KD + 1) + c;
-                d[0] = mv[u].x; d[1] = mv[u].y; d[2] = mv[u].z; d[3] = mv[u].w;
-            }
-        }
-        __syncthreads();
-        float acc[2][4];
-        int rows[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int o = tid + 256 * u;
-            rows[u] = o < KD * 2 ? (o >> 1) : -1;
-            if (rows[u] < 0) continue;
-            const int j0 = (o & 1) * 4;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[u][e] = Hs[rows[u] * VD + v0 + j0 + e];
-            for (int l = 0; l < KD; ++l) {
-                const float m = Ms[rows[u] * (KD + 1) + l];
-                const float4 sv = *reinterpret_cast<const float4 *>(S + l * kCombCols + j0);
-                acc[u][0] += m * sv.x;
-                acc[u][1] += m * sv.y;
-                acc[u][2] += m * sv.z;
-                acc[u][3] += m * sv.w;
-            }
-        }
-        __syncthreads();
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            if (rows[u] < 0) continue;
-            const int o = tid + 256 * u, j0 = (o & 1) * 4;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                S[rows[u] * kCombCols + j0 + e] = acc[u][e];
-                dst[rows[u] * VD + v0 + j0 + e] = acc[u][e];
+                S[rows[u] * kCombCols + j0s[u] + e] = acc[u][e];
+                dst[rows[u] * VD + v0 + j0s[u] + e] = acc[u][e];
             }
         }
     }
@@ -870,7 +820,7 @@ int fwd_impl(const Params &p, int use_cp, cudaStream_t st) {
         e = launch("simt_cp_summary", k_cp_summary<TI, KD, VD>, dim3(p.NSEG, p.Hv, (VD + KD) / 32),
                    smem_summary<KD, VD>(), st, p);
         if (e != cudaSuccess) return 1;
-        e = launch("simt_cp_combine", k_cp_combine<KD, VD>, dim3(p.N, p.Hv, VD / kCombCols), smem_combine<KD>(),
+        e = launch("simt_cp_combine", k_cp_combine<KD, VD, false>, dim3(p.N, p.Hv, VD / kCombCols), smem_combine<KD>(),
                    st, p);
         if (e != cudaSuccess) return 1;
     }
@@ -889,7 +839,7 @@ int bwd_impl(const Params &p0, int use_cp, cudaStream_t st) {
         e = launch("simt_cp_summary", k_cp_summary<TI, KD, VD>, dim3(p.NSEG, p.Hv, (VD + KD) / 32),
                    smem_summary<KD, VD>(), st, p);
         if (e != cudaSuccess) return 1;
-        e = launch("simt_cp_combine", k_cp_combine<KD, VD>, dim3(p.N, p.Hv, VD / kCombCols), smem_combine<KD>(),
+        e = launch("simt_cp_combine", k_cp_combine<KD, VD, false>, dim3(p.N, p.Hv, VD / kCombCols), smem_combine<KD>(),
                    st, p);
         if (e != cudaSuccess) return 1;
     }
@@ -963,14 +913,14 @@ int simt_group_sum(const Params &p, cudaStream_t st) {
 
 int simt_cp_combine_rev(const Params &p, cudaStream_t st) {
     if (p.K == 128 && p.V == 128)
-        return launch("cp_combine_rev", k_cp_combine_rev<128, 128>, dim3(p.N, p.Hv, 128 / kCombCols),
+        return launch("cp_combine_rev", k_cp_combine<128, 128, true>, dim3(p.N, p.Hv, 128 / kCombCols),
                       smem_combine<128>(), st, p) != cudaSuccess;
     return 1;
 }
 
 int simt_cp_combine(const Params &p, cudaStream_t st) {
     if (p.K == 128 && p.V == 128)
-        return launch("cp_combine", k_cp_combine<128, 128>, dim3(p.N, p.Hv, 128 / kCombCols), smem_combine<128>(), st,
+        return launch("cp_combine", k_cp_combine<128, 128, false>, dim3(p.N, p.Hv, 128 / kCombCols), smem_combine<128>(), st,
                       p) != cudaSuccess;
     return 1;
 }

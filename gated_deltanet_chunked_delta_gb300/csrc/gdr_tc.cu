@@ -350,23 +350,40 @@ __global__ void __launch_bounds__(128) k_chunk_tc(Params p, const __grid_constan
             for (int s = 0; s < 64; ++s) x[s] = s <= rr ? f * row[s] : 0.f;
             st_img_row2(reinterpret_cast<char *>(p.Pimg) + ch * kImg2, rr, x);
         }
-        for (int e = tid; e < 64 * 64; e += 128) {
-            const int rr = e >> 6, s = e & 63;
-            if (from_A)
-                As[rr * 65 + s] = rr < len ? p.A_in[((size_t)(tok0 + rr) * p.Hv + h) * 64 + s] : (rr == s ? 1.f : 0.f);
-            else
-                As[rr * 65 + s] = 0.f;
+        if (from_A) {
+            // 64 rows x 16 float4, eight per thread, all in flight before the stores
+            float4 av[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int e = tid + 128 * u, rr = e >> 4, c4 = (e & 15) * 4;
+                av[u] = rr < len ? *reinterpret_cast<const float4 *>(p.A_in + ((size_t)(tok0 + rr) * p.Hv + h) * 64 + c4)
+                                 : make_float4(rr == c4, rr == c4 + 1, rr == c4 + 2, rr == c4 + 3);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int e = tid + 128 * u, rr = e >> 4, c4 = (e & 15) * 4;
+                float *d = As + rr * 65 + c4;
+                d[0] = av[u].x; d[1] = av[u].y; d[2] = av[u].z; d[3] = av[u].w;
+            }
+        } else {
+            for (int e = tid; e < 64 * 64; e += 128) As[(e >> 6) * 65 + (e & 63)] = 0.f;
         }
         __syncthreads();
         if (!from_A) {
-            // diagonal 16x16 blocks: warp w inverts block w, lane j owns column j
+            // diagonal 16x16 blocks: warp w inverts block w, lane j owns column j,
+            // kept in registers (x[r] = [r == j] - sum_{s<r} L[r][s] x[s])
             if (lane < 16) {
                 const int b = 16 * warp, jj = lane;
-                for (int rr = jj; rr < 16; ++rr) {
+                float x[16];
+#pragma unroll
+                for (int rr = 0; rr < 16; ++rr) {
                     float acc = rr == jj ? 1.f : 0.f;
-                    for (int s = jj; s < rr; ++s) acc -= Ls[(b + rr) * 65 + b + s] * As[(b + s) * 65 + b + jj];
-                    As[(b + rr) * 65 + b + jj] = acc;
+#pragma unroll
+                    for (int s = 0; s < rr; ++s) acc -= Ls[(b + rr) * 65 + b + s] * x[s];
+                    x[rr] = rr < jj ? 0.f : acc;
                 }
+#pragma unroll
+                for (int rr = 0; rr < 16; ++rr) As[(b + rr) * 65 + b + jj] = x[rr];
             }
             __syncthreads();
             // block levels: A_ij = -A_ii sum_{k=j}^{i-1} L_ik A_kj, i - j = d
@@ -528,7 +545,7 @@ __global__ void __launch_bounds__(320, 1) k_scan_tc(Params p, const __grid_const
                 const int s = cc & 1;
                 if (cc >= 2 && !bwait(&empty[s], ((cc >> 1) & 1) ^ 1, cap, abort)) break;
                 const int c = sg.chunk0 + cc;
-                const int tok0 = p.chunk[c].tok0;
+                const int tok0 = sq.tok0 + kChunk * (c - sq.chunk0);
                 const size_t ch = (size_t)c * p.Hv + h;
                 char *st = stage0 + s * SL::kBytes;
                 uint32_t tx = 2 * 8192 + kImg2 + kAux;
@@ -711,7 +728,8 @@ __global__ void __launch_bounds__(320, 1) k_scan_tc(Params p, const __grid_const
             if (MODE == kFwd) {
                 if (!bwait(bar_m3, cc & 1, cap, abort)) break;
                 tc_fence_after();
-                const ChunkInfo ci = p.chunk[c];
+                const int ctok0 = sq.tok0 + kChunk * (c - sq.chunk0);
+                const int clen = min(kChunk, sq.len - kChunk * (c - sq.chunk0));
                 TO *o = reinterpret_cast<TO *>(p.o);
                 for (int j = wg; j < wg + 1; ++j) {
                     uint32_t r2[32];
@@ -721,8 +739,8 @@ __global__ void __launch_bounds__(320, 1) k_scan_tc(Params p, const __grid_const
                     for (int i = 0; i < 32; ++i) {
                         const int rr = 32 * j + i;
                         const float val = p.scale * eg[rr] * __uint_as_float(r[i]) + __uint_as_float(r2[i]);
-                        if (rr < ci.len) {
-                            const size_t off = ((size_t)(ci.tok0 + rr) * p.Hv + h) * 128 + t;
+                        if (rr < clen) {
+                            const size_t off = ((size_t)(ctok0 + rr) * p.Hv + h) * 128 + t;
                             if constexpr (sizeof(TO) == 4)
                                 o[off] = val;
                             else
@@ -870,7 +888,7 @@ __global__ void __launch_bounds__(320, 1) k_dh_tc(Params p, const __grid_constan
                 const int s = cc & 1;
                 if (cc >= 2 && !bwait(&empty[s], ((cc >> 1) & 1) ^ 1, cap, abort)) break;
                 const int c = cend - 1 - cc;
-                const int tok0 = p.chunk[c].tok0;
+                const int tok0 = sq.tok0 + kChunk * (c - sq.chunk0);
                 const size_t ch = (size_t)c * p.Hv + h;
                 char *st = stage0 + s * SL::kBytes;
                 mbar_expect_tx(&full[s], 32768 + 16384 + 2 * kImg2 + kAux);
@@ -974,7 +992,7 @@ __global__ void __launch_bounds__(320, 1) k_dh_tc(Params p, const __grid_constan
             const float *bet = reinterpret_cast<const float *>(aux0 + s * kAux);
             const float *eg = bet + 64, *eL = bet + 128;
             const int c = cend - 1 - cc;
-            const int len = p.chunk[c].len;
+            const int len = min(kChunk, sq.len - kChunk * (c - sq.chunk0));
             const size_t ch = (size_t)c * p.Hv + h;
             if (cc > 0 && !bwait(bar_m3, (cc - 1) & 1, cap, abort)) break;
             tc_fence_after();

@@ -206,8 +206,10 @@ def run_reference(args, spec, rank, world):
         if i >= args.warmup:
             vals.append(v)
     value = statistics.mean(vals)
+    # time the oracle needs for one whole step of the workload at this throughput
+    ms_full = spec.tokens / (value * 1e6) * 1e3
     line = {"metric": METRIC, "impl": "reference", "value": value, "unit": "Mtokens/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_full, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": _config(spec, args),
             "cpu_baseline": {"value": value, "unit": "Mtokens/s", "cores": nth, "kind": "oracle",
@@ -217,11 +219,26 @@ def run_reference(args, spec, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def aggregate(total_ms, tokens, steps, device):
+    """Whole-job throughput over ranks: the slowest rank's summed step time and
+    the tokens of all ranks.  Returns (Mtokens/s, max total ms)."""
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        t = torch.tensor([float(total_ms)], dtype=torch.float64, device=device)
+        n = torch.tensor([float(tokens)], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dist.all_reduce(n, op=dist.ReduceOp.SUM)
+        total_ms, tokens = float(t.item()), float(n.item())
+    return tokens * steps / (total_ms / 1e3) / 1e6, total_ms
+
+
 def _config(spec, args):
     return {"workload": spec.name, "B": spec.B, "T": spec.T, "Hq": spec.Hq, "Hv": spec.Hv, "K": spec.K,
             "V": spec.V, "lengths": list(spec.lengths) if spec.lengths else None,
             "in_dtype": spec.in_dtype, "o_dtype": spec.out_dtype,
-            "step": "gdr_fwd(o, final_state, A) + gdr_bwd(dq, dk, dv, dbeta, dg, dh0)",
+            "step": {"both": "gdr_fwd(o, final_state, A) + gdr_bwd(dq, dk, dv, dbeta, dg, dh0)",
+                     "fwd": "gdr_fwd(o, final_state, A)",
+                     "bwd": "gdr_bwd(dq, dk, dv, dbeta, dg, dh0)"}[getattr(args, "mode", "both")],
             "l2": f"flushed before every timed step ({FLUSH_BYTES >> 20} MiB write)",
             "parallelism": f"independent replicas x{args.gpus} (no collective)"}
 
@@ -238,9 +255,12 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--path", default="auto", choices=["auto", "simt", "tc"])
     ap.add_argument("--cp", type=int, default=0, help="cp_segments (0 auto, 1 off, n forced)")
+    ap.add_argument("--mode", default="both", choices=["both", "fwd", "bwd"],
+                    help="step = forward + backward (default), forward only, or backward only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-tokens", type=int, default=1024, help="tokens per oracle step (reference arm)")
-    ap.add_argument("--cpu-tokens", type=int, default=4096, help="tokens of the cpu_baseline sample")
+    ap.add_argument("--cpu-tokens", type=int, default=0,
+                    help="tokens of the cpu_baseline sample (0: the whole first sequence)")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -287,13 +307,23 @@ def main():
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step(timer_f=None, timer_b=None):
+    def run_fwd(timer=None):
         gdr.gdr_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], x["scale"], h0=d["h0"], cu_seqlens=d["cu_seqlens"],
-                    cu_seqlens_host=cu_host, out=out_f, workspace=ws_f, cp_segments=args.cp, path=path,
-                    timer=timer_f)
+                    cu_seqlens_host=cu_host, out=out_f, workspace=ws_f, cp_segments=args.cp, path=path, timer=timer)
+
+    def run_bwd(timer=None):
         gdr.gdr_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], out_f["A"], d["do"], dht=d["dht"],
                     scale=x["scale"], h0=d["h0"], cu_seqlens=d["cu_seqlens"], cu_seqlens_host=cu_host,
-                    out=out_b, workspace=ws_b, cp_segments=args.cp, path=path, timer=timer_b)
+                    out=out_b, workspace=ws_b, cp_segments=args.cp, path=path, timer=timer)
+
+    def step(timer_f=None, timer_b=None):
+        if args.mode in ("both", "fwd"):
+            run_fwd(timer_f)
+        if args.mode in ("both", "bwd"):
+            run_bwd(timer_b)
+
+    if args.mode == "bwd":
+        run_fwd()  # A for the backward, untimed
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -328,31 +358,30 @@ def main():
     t_wall1 = time.time()
     clk = clocks.stop(t_wall0, t_wall1)
     step_ms = [a.elapsed_time(b) for a, b in zip(e0, e1)]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    tokens = spec.tokens
+    value, total_ms = aggregate(sum(step_ms), tokens, args.steps, dev)
     gdr.check_status()
 
-    tokens = spec.tokens
-    value = tokens * world * args.steps / (total_ms / 1e3) / 1e6
-
-    # e2e: pinned host buffers, copies inside the timed region
-    hin = {k: (x[k].pin_memory() if torch.is_tensor(x[k]) and k != "cu_seqlens" else None) for k in keys}
-    hout = {k: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for k, t in {**out_f, **out_b}.items()}
-    h2d = sum(t.numel() * t.element_size() for t in hin.values() if t is not None)
+    # e2e: pinned host buffers, copies inside the timed region (every input of
+    # the timed calls in, every output out)
+    in_keys = ["q", "k", "v", "g", "beta", "h0"] + (["do", "dht"] if args.mode != "fwd" else [])
+    hin = {k: x[k].pin_memory() for k in in_keys if torch.is_tensor(x[k])}
+    dev_out = {**(out_f if args.mode != "bwd" else {}), **(out_b if args.mode != "fwd" else {})}
+    if args.mode == "bwd":
+        hin["A"] = out_f["A"].cpu().pin_memory()
+    hout = {k: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for k, t in dev_out.items()}
+    h2d = sum(t.numel() * t.element_size() for t in hin.values())
     d2h = sum(t.numel() * t.element_size() for t in hout.values())
+    dst_of = {**d, "A": out_f["A"]}
     ee0 = torch.cuda.Event(enable_timing=True)
     ee1 = torch.cuda.Event(enable_timing=True)
     e2e_ms = []
     for i in range(max(3, args.steps // 2)):
         ee0.record(stream)
         for k, t in hin.items():
-            if t is not None:
-                d[k].copy_(t, non_blocking=True)
+            dst_of[k].copy_(t, non_blocking=True)
         step()
-        for k, t in {**out_f, **out_b}.items():
+        for k, t in dev_out.items():
             hout[k].copy_(t, non_blocking=True)
         ee1.record(stream)
         torch.cuda.synchronize()
@@ -388,12 +417,18 @@ def main():
     roof["kernel"] = dom
     roof["peak_source"] = peaks["source"]
 
-    # whole-step roofline (the metric's "% of bf16 roofline")
+    # whole-step roofline (the metric's "% of bf16 roofline"): algorithmic flops
+    # (forward 166.6 kflop and backward 491.5 kflop per token-head at K = V = 128,
+    # G = 2) and bytes (inputs read once, outputs written once)
     th = tokens * Hv
-    step_flops = th * (166.6e3 + 491.5e3) * (K * V / (128 * 128))
-    step_bytes = (2 * tokens * spec.Hq * K * in_b * 2 + tokens * Hv * V * in_b * 2 + tokens * Hv * 4 * 4
-                  + tokens * Hv * V * o_b + tokens * Hv * 64 * 4 * 2 + tokens * Hv * V * in_b
-                  + 4 * N * Hv * K * V * 4)
+    qk_b, v_b, gb_b = tokens * spec.Hq * K * in_b, tokens * Hv * V * in_b, tokens * Hv * 4
+    A_b, st_b = tokens * Hv * 64 * 4, N * Hv * K * V * 4
+    f_fl, b_fl = th * 166.6e3, th * 491.5e3
+    f_by = 2 * qk_b + v_b + 2 * gb_b + (st_b if spec.h0 else 0) + tokens * Hv * V * o_b + st_b + A_b
+    b_by = (2 * qk_b + 2 * v_b + 2 * gb_b + A_b + (2 * st_b if spec.h0 else st_b)
+            + 2 * qk_b + v_b + 2 * gb_b + st_b)
+    step_flops = (f_fl if args.mode != "bwd" else 0) + (b_fl if args.mode != "fwd" else 0)
+    step_bytes = (f_by if args.mode != "bwd" else 0) + (b_by if args.mode != "fwd" else 0)
     step_roof_ms = max(step_flops / (tc_peak * 1e12), step_bytes / (peaks["hbm_gbs"] * 1e9)) * 1e3
 
     kernels = {nm: {"launches": n, "ms_total": round(t, 4), "share": round(t / sum(a for a, _ in agg.values()), 4)}
@@ -404,13 +439,15 @@ def main():
             "data": "synthetic", "config": _config(spec, args),
             "roofline": roof,
             "step_roofline_frac": step_roof_ms / (total_ms / args.steps),
+            "step_roofline": {"flops": step_flops, "bytes": step_bytes, "ms": step_roof_ms,
+                              "bound": "tensor" if step_flops / (tc_peak * 1e12) * 1e3 >= step_roof_ms else "hbm"},
             "kernels": kernels,
             "e2e": {"value": e2e_val, "unit": "Mtokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches, "clocks": clk}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
         oracle.build()
-        v, dt, Ts, nth = oracle_sample(x, spec, args.cpu_tokens, spec.Hq)
+        v, dt, Ts, nth = oracle_sample(x, spec, args.cpu_tokens or (1 << 30), spec.Hq)
         line["cpu_baseline"] = {"value": v, "unit": "Mtokens/s", "cores": nth, "kind": "oracle",
                                 "sample": f"oracle fwd+bwd on tokens [0,{Ts}) of sequence 0, all {spec.Hv} "
                                           f"v-heads ({dt:.1f} s); throughput in full-workload tokens"}

@@ -302,6 +302,7 @@ __global__ void __launch_bounds__(256) k_cp_combine(Params p) {
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
             if (rows[u] < 0) continue;
+#pragma unroll 16
             for (int l = 0; l < KD; ++l) {
                 const float m = Ms[rows[u] * (KD + 1) + l];
                 const float4 sv = *reinterpret_cast<const float4 *>(S + l * kCombCols + j0s[u]);

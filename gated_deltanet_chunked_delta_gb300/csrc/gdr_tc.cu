@@ -151,6 +151,21 @@ __device__ __forceinline__ void tmem_ld32(uint32_t ta, uint32_t (&r)[32]) {
         : "r"(ta));
     asm volatile("tcgen05.wait::ld.sync.aligned;" : W8(0), W8(8), W8(16), W8(24)::"memory");
 }
+// Issue only; pair with tmem_wait_ld32 / tmem_hold32 before the registers are used.
+__device__ __forceinline__ void tmem_ld32_issue(uint32_t ta, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : R8(0), R8(8), R8(16), R8(24)
+        : "r"(ta));
+}
+__device__ __forceinline__ void tmem_wait_ld32(uint32_t (&r)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" : W8(0), W8(8), W8(16), W8(24)::"memory");
+}
+// Orders the use of a second load's registers after a wait already issued.
+__device__ __forceinline__ void tmem_hold32(uint32_t (&r)[32]) {
+    asm volatile("" : W8(0), W8(8), W8(16), W8(24)::"memory");
+}
 __device__ __forceinline__ void tmem_st32(uint32_t ta, const uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
@@ -201,10 +216,15 @@ constexpr int kAux = kAuxBytes;
 
 __device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
 
-// Row `row` of a [hi | lo] pair of 128-byte-swizzled 64-column bf16 images.
-__device__ __forceinline__ void st_img_row2(char *img, int row, const float *x /* 64 */) {
+struct ChunkMaps {
+    CUtensorMap K, Q;  // 3-D over k and q: (K, Hq, Ttot), box (64, 1, 64), 128-byte swizzle
+};
+
+// Row `row`, columns [col0, col0 + 32) of a [hi | lo] pair of 128-byte-swizzled
+// 64-column bf16 images (col0 = 0 or 32).
+__device__ __forceinline__ void st_img_half2(char *img, int row, int col0, const float *x /* 32 */) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < 4; ++j) {
         float hi[8], lw[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
@@ -216,43 +236,100 @@ __device__ __forceinline__ void st_img_row2(char *img, int row, const float *x /
         vh.z = pack_bf16(hi[4], hi[5]); vh.w = pack_bf16(hi[6], hi[7]);
         vl.x = pack_bf16(lw[0], lw[1]); vl.y = pack_bf16(lw[2], lw[3]);
         vl.z = pack_bf16(lw[4], lw[5]); vl.w = pack_bf16(lw[6], lw[7]);
-        const int off = row * 128 + ((j ^ (row & 7)) << 4);
+        const int off = row * 128 + ((((col0 >> 3) + j) ^ (row & 7)) << 4);
         *reinterpret_cast<uint4 *>(img + off) = vh;
         *reinterpret_cast<uint4 *>(img + kImg + off) = vl;
     }
 }
 
-struct ChunkMaps {
-    CUtensorMap K, Q;  // 3-D over k and q: (K, Hq, Ttot), box (64, 1, 64), 128-byte swizzle
-};
-
 // ---------------------------------------------------------------------------
-// Chunk-parallel kernel: one CTA per (chunk, qk-head), looping over the v-heads
-// of the group.  [K ; Q] K^T on tcgen05 (shared by the group), then per v-head
-// the gate cumsum, L, the unit-lower-triangular inverse A = (I + L)^-1 on the
-// CUDA cores (blocked: 16x16 diagonal blocks, then block levels), and P'.
-// With from_A (the backward) A is read back from the forward's output.
+// Chunk-parallel kernel: one CTA of 128 threads per (chunk, v-head), several
+// CTAs per SM.  [K ; Q] K^T on tcgen05 (warps 0-1 read the K K^T rows, warps
+// 2-3 the Q K^T rows), the gate cumsum, L = strict_tril(diag(b) (K K^T o D)),
+// P', and the unit-lower-triangular inverse A = (I + L)^-1 on the CUDA cores
+// by row blocks of 16: the four 16x16 diagonal inverses first (one column
+// per thread), then for i = 1..3
+//     A[i, <i] = -A_ii (L[i, <i] A[<i, <i])
+// with every product register-blocked over all 128 threads.  With from_A
+// (the backward) A is read back from the forward's output instead.
 // ---------------------------------------------------------------------------
-constexpr int kChunkSmem = 1024 + 32768 + 2 * 64 * 65 * 4 + 3 * 16 * 17 * 4 + 2 * 64 * 4 + 128;
+constexpr int kLd = 68;                            // fp32 row pitch of L and A (16-byte aligned rows)
+constexpr int kTLd = 52;                           // row pitch of the 16 x 48 product scratch
+constexpr int kChunkScratch = 2 * 64 * kLd * 4;    // L and A, laid over the K/Q tile once the MMA is done
+constexpr int kChunkSmem = 1024 + (kChunkScratch > 32768 ? kChunkScratch : 32768) + 16 * kTLd * 4 + 2 * 64 * 4 + 64;
 
-__global__ void __launch_bounds__(128) k_chunk_tc(Params p, const __grid_constant__ ChunkMaps maps, int from_A) {
+// A[16i + r][c] for the thread's columns c = cg n .. cg n + n - 1, n = 2i:
+// T = L[16i:16i+16, 0:16i] A[0:16i, 0:16i], then A[16i:, 0:16i] = -A_ii T.
+template <int I>
+__device__ __forceinline__ void inv_row_block(float *Ls, float *As, float *Tt, int tid) {
+    constexpr int n = 2 * I, KD = 16 * I;
+    const int r = tid >> 3, cg = tid & 7, c0 = cg * n;
+    float acc[n];
+#pragma unroll
+    for (int u = 0; u < n; ++u) acc[u] = 0.f;
+    const float *lrow = Ls + (16 * I + r) * kLd;
+#pragma unroll
+    for (int k = 0; k < KD; k += 4) {
+        const float4 l4 = *reinterpret_cast<const float4 *>(lrow + k);
+        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float *arow = As + (k + q) * kLd + c0;
+#pragma unroll
+            for (int u = 0; u < n; u += 2) {
+                const float2 a2 = *reinterpret_cast<const float2 *>(arow + u);
+                acc[u] = fmaf(lv[q], a2.x, acc[u]);
+                acc[u + 1] = fmaf(lv[q], a2.y, acc[u + 1]);
+            }
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < n; u += 2) *reinterpret_cast<float2 *>(Tt + r * kTLd + c0 + u) = make_float2(acc[u], acc[u + 1]);
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < n; ++u) acc[u] = 0.f;
+    const float *drow = As + (16 * I + r) * kLd + 16 * I;
+#pragma unroll
+    for (int m = 0; m < 16; m += 4) {
+        const float4 d4 = *reinterpret_cast<const float4 *>(drow + m);
+        const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float *trow = Tt + (m + q) * kTLd + c0;
+#pragma unroll
+            for (int u = 0; u < n; u += 2) {
+                const float2 t2 = *reinterpret_cast<const float2 *>(trow + u);
+                acc[u] = fmaf(dv[q], t2.x, acc[u]);
+                acc[u + 1] = fmaf(dv[q], t2.y, acc[u + 1]);
+            }
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < n; u += 2)
+        *reinterpret_cast<float2 *>(As + (16 * I + r) * kLd + c0 + u) = make_float2(-acc[u], -acc[u + 1]);
+    __syncthreads();
+}
+
+__global__ void __launch_bounds__(128, 4) k_chunk_tc(Params p, const __grid_constant__ ChunkMaps maps, int from_A) {
     extern __shared__ __align__(1024) char smraw[];
     char *sm = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
-    char *tile = sm;                                             // [2 atoms][128 rows][128 B]: K rows 0-63, Q 64-127
-    float *Ls = reinterpret_cast<float *>(sm + 32768);           // [64][65]
-    float *As = Ls + 64 * 65;                                    // [64][65]
-    float *Tt = As + 64 * 65;                                    // [3][16][17]
-    float *gam = Tt + 3 * 16 * 17;                               // [64]
-    float *bet = gam + 64;                                       // [64]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(bet + 64);     // tma, mma
+    constexpr int kTileRegion = kChunkScratch > 32768 ? kChunkScratch : 32768;
+    char *tile = sm;                                              // [2 atoms][128 rows][128 B]: K rows 0-63, Q 64-127
+    float *Ls = reinterpret_cast<float *>(sm);                    // [64][kLd], over the tile after the MMA
+    float *As = Ls + 64 * kLd;                                    // [64][kLd]
+    float *Tt = reinterpret_cast<float *>(sm + kTileRegion);      // [16][kTLd]
+    float *gam = Tt + 16 * kTLd;                                  // [64]
+    float *bet = gam + 64;                                        // [64]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(bet + 64);      // tma, mma
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2);
     volatile int *abort = reinterpret_cast<volatile int *>(bars + 3);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int c = blockIdx.x, hq = blockIdx.y;
+    const int c = blockIdx.x / p.Hv, h = blockIdx.x - c * p.Hv;
+    const int hq = h / (p.Hv / p.Hq);
     const ChunkInfo ci = p.chunk[c];
     const int len = ci.len, tok0 = ci.tok0;
-    const int G = p.Hv / p.Hq;
+    const size_t ch = (size_t)c * p.Hv + h;
     const long long cap = p.timeout_spins;
 
     if (tid == 0) {
@@ -277,6 +354,14 @@ __global__ void __launch_bounds__(128) k_chunk_tc(Params p, const __grid_constan
         tma3d(tile + 16384, &maps.K, 64, hq, tok0, &bars[0]);
         tma3d(tile + 8192, &maps.Q, 0, hq, tok0, &bars[0]);
         tma3d(tile + 16384 + 8192, &maps.Q, 64, hq, tok0, &bars[0]);
+    }
+    // gates while the copies fly: g -> gam (threads 0-63), beta -> bet (64-127)
+    {
+        const int t = tid & 63;
+        const float x = t < len ? (tid < 64 ? p.g : p.beta)[(size_t)(tok0 + t) * p.Hv + h] : 0.f;
+        (tid < 64 ? gam : bet)[t] = x;
+    }
+    if (tid == 0) {
         if (bwait(&bars[0], 0, cap, abort)) {
             tc_fence_after();
             const uint32_t id = idesc_bf16(128, 64);
@@ -290,136 +375,138 @@ __global__ void __launch_bounds__(128) k_chunk_tc(Params p, const __grid_constan
             mma_issued = true;
         }
     }
-    // row t of [K K^T ; Q K^T] (garbage rows past the chunk end are masked by
-    // beta = 0 and by the triangles below)
-    float row[64];
-    bool ok = bwait(&bars[1], 0, cap, abort);
-    tc_fence_after();
-    if (ok) {
-        uint32_t r[32];
-        const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16);
-        tmem_ld32(ta, r);
+    __syncthreads();
+    if (tid < 32) {  // inclusive cumsum over 64 values, two per lane
+        const float a = gam[2 * lane], b = gam[2 * lane + 1];
+        float s = a + b;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) row[i] = __uint_as_float(r[i]);
-        tmem_ld32(ta + 32, r);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) row[32 + i] = __uint_as_float(r[i]);
+        for (int o = 1; o < 32; o <<= 1) {
+            const float n = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o) s += n;
+        }
+        gam[2 * lane] = s - b;
+        gam[2 * lane + 1] = s;
     }
     __syncthreads();
-    for (int j = 0; j < G && !*abort; ++j) {
-        const int h = hq * G + j;
-        const size_t ch = (size_t)c * p.Hv + h;
+    const float gC = gam[63];
+    if (tid < 64) {
+        float *aux = reinterpret_cast<float *>(reinterpret_cast<char *>(p.Aux) + ch * kAux);
+        aux[tid] = bet[tid];
+        aux[64 + tid] = __expf(gam[tid]);
+        aux[128 + tid] = __expf(gC - gam[tid]);
+    }
+    const bool ok = bwait(&bars[1], 0, cap, abort);
+    tc_fence_after();
+    // rows of [K K^T ; Q K^T]: warps 0-1 -> L (unless from_A), warps 2-3 -> P'
+    if (ok) {
+        const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16);
         if (tid < 64) {
-            gam[tid] = tid < len ? p.g[(size_t)(tok0 + tid) * p.Hv + h] : 0.f;
-            bet[tid] = tid < len ? p.beta[(size_t)(tok0 + tid) * p.Hv + h] : 0.f;
-        }
-        __syncthreads();
-        if (tid < 32) {  // inclusive cumsum over 64 values, two per lane
-            float a = gam[2 * lane], b = gam[2 * lane + 1];
-            float s = a + b;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float n = __shfl_up_sync(0xffffffffu, s, o);
-                if (lane >= o) s += n;
-            }
-            const float excl = s - (a + b);
-            gam[2 * lane] = excl + a;
-            gam[2 * lane + 1] = s;
-        }
-        __syncthreads();
-        const float gC = gam[63];
-        if (tid < 64) {
-            float *aux = reinterpret_cast<float *>(reinterpret_cast<char *>(p.Aux) + ch * kAux);
-            aux[tid] = bet[tid];
-            aux[64 + tid] = __expf(gam[tid]);
-            aux[128 + tid] = __expf(gC - gam[tid]);
-        }
-        if (tid < 64) {
-            const int rr = tid;
             if (!from_A) {
+                const int rr = tid;
                 const float br = bet[rr], gr = gam[rr];
+                uint32_t r0[32], r1[32];
+                tmem_ld32(ta, r0);
+                tmem_ld32(ta + 32, r1);
+                float *lrow = Ls + rr * kLd;
 #pragma unroll
-                for (int s = 0; s < 64; ++s) Ls[rr * 65 + s] = s < rr ? br * __expf(gr - gam[s]) * row[s] : 0.f;
+                for (int s = 0; s < 32; s += 4) {
+                    float4 v;
+                    v.x = s + 0 < rr ? br * __expf(gr - gam[s + 0]) * __uint_as_float(r0[s + 0]) : 0.f;
+                    v.y = s + 1 < rr ? br * __expf(gr - gam[s + 1]) * __uint_as_float(r0[s + 1]) : 0.f;
+                    v.z = s + 2 < rr ? br * __expf(gr - gam[s + 2]) * __uint_as_float(r0[s + 2]) : 0.f;
+                    v.w = s + 3 < rr ? br * __expf(gr - gam[s + 3]) * __uint_as_float(r0[s + 3]) : 0.f;
+                    *reinterpret_cast<float4 *>(lrow + s) = v;
+                }
+#pragma unroll
+                for (int s = 0; s < 32; s += 4) {
+                    float4 v;
+                    v.x = s + 32 < rr ? br * __expf(gr - gam[s + 32]) * __uint_as_float(r1[s + 0]) : 0.f;
+                    v.y = s + 33 < rr ? br * __expf(gr - gam[s + 33]) * __uint_as_float(r1[s + 1]) : 0.f;
+                    v.z = s + 34 < rr ? br * __expf(gr - gam[s + 34]) * __uint_as_float(r1[s + 2]) : 0.f;
+                    v.w = s + 35 < rr ? br * __expf(gr - gam[s + 35]) * __uint_as_float(r1[s + 3]) : 0.f;
+                    *reinterpret_cast<float4 *>(lrow + 32 + s) = v;
+                }
             }
         } else {
-            const int rr = tid - 64;
             // rows past the chunk end are zero (the backward mixes rows through P'^T)
+            const int rr = tid - 64;
             const float f = rr < len ? p.scale * __expf(gam[rr] - gC) : 0.f;
-            float x[64];
+            char *pimg = reinterpret_cast<char *>(p.Pimg) + ch * kImg2;
 #pragma unroll
-            for (int s = 0; s < 64; ++s) x[s] = s <= rr ? f * row[s] : 0.f;
-            st_img_row2(reinterpret_cast<char *>(p.Pimg) + ch * kImg2, rr, x);
+            for (int hb = 0; hb < 2; ++hb) {
+                uint32_t r0[32];
+                tmem_ld32(ta + 32 * hb, r0);
+                float x[32];
+#pragma unroll
+                for (int s = 0; s < 32; ++s) x[s] = 32 * hb + s <= rr ? f * __uint_as_float(r0[s]) : 0.f;
+                st_img_half2(pimg, rr, 32 * hb, x);
+            }
         }
-        if (from_A) {
-            // 64 rows x 16 float4, eight per thread, all in flight before the stores
-            float4 av[8];
+    }
+    __syncthreads();  // L complete; the K/Q tile is dead (the MMA that read it has completed)
+    if (from_A) {
+        // 64 rows x 16 float4, eight per thread, all in flight before the stores
+        float4 av[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int e = tid + 128 * u, rr = e >> 4, c4 = (e & 15) * 4;
-                av[u] = rr < len ? *reinterpret_cast<const float4 *>(p.A_in + ((size_t)(tok0 + rr) * p.Hv + h) * 64 + c4)
-                                 : make_float4(rr == c4, rr == c4 + 1, rr == c4 + 2, rr == c4 + 3);
-            }
+        for (int u = 0; u < 8; ++u) {
+            const int e = tid + 128 * u, rr = e >> 4, c4 = (e & 15) * 4;
+            av[u] = rr < len ? *reinterpret_cast<const float4 *>(p.A_in + ((size_t)(tok0 + rr) * p.Hv + h) * 64 + c4)
+                             : make_float4(rr == c4, rr == c4 + 1, rr == c4 + 2, rr == c4 + 3);
+        }
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int e = tid + 128 * u, rr = e >> 4, c4 = (e & 15) * 4;
-                float *d = As + rr * 65 + c4;
-                d[0] = av[u].x; d[1] = av[u].y; d[2] = av[u].z; d[3] = av[u].w;
-            }
-        } else {
-            for (int e = tid; e < 64 * 64; e += 128) As[(e >> 6) * 65 + (e & 63)] = 0.f;
+        for (int u = 0; u < 8; ++u) {
+            const int e = tid + 128 * u, rr = e >> 4, c4 = (e & 15) * 4;
+            *reinterpret_cast<float4 *>(As + rr * kLd + c4) = av[u];
         }
         __syncthreads();
-        if (!from_A) {
-            // diagonal 16x16 blocks: warp w inverts block w, lane j owns column j,
-            // kept in registers (x[r] = [r == j] - sum_{s<r} L[r][s] x[s])
-            if (lane < 16) {
-                const int b = 16 * warp, jj = lane;
-                float x[16];
-#pragma unroll
-                for (int rr = 0; rr < 16; ++rr) {
-                    float acc = rr == jj ? 1.f : 0.f;
-#pragma unroll
-                    for (int s = 0; s < rr; ++s) acc -= Ls[(b + rr) * 65 + b + s] * x[s];
-                    x[rr] = rr < jj ? 0.f : acc;
-                }
-#pragma unroll
-                for (int rr = 0; rr < 16; ++rr) As[(b + rr) * 65 + b + jj] = x[rr];
-            }
-            __syncthreads();
-            // block levels: A_ij = -A_ii sum_{k=j}^{i-1} L_ik A_kj, i - j = d
-            for (int d = 1; d < 4; ++d) {
-                const int nb = 4 - d;
-                for (int e = tid; e < nb * 256; e += 128) {
-                    const int blk = e >> 8, i = d + blk, jb = i - d, rr = (e >> 4) & 15, cc = e & 15;
-                    float acc = 0.f;
-                    for (int kb = jb; kb < i; ++kb)
-                        for (int m = 0; m < 16; ++m)
-                            acc += Ls[(16 * i + rr) * 65 + 16 * kb + m] * As[(16 * kb + m) * 65 + 16 * jb + cc];
-                    Tt[blk * 272 + rr * 17 + cc] = acc;
-                }
-                __syncthreads();
-                for (int e = tid; e < nb * 256; e += 128) {
-                    const int blk = e >> 8, i = d + blk, jb = i - d, rr = (e >> 4) & 15, cc = e & 15;
-                    float acc = 0.f;
-                    for (int m = 0; m <= rr; ++m) acc -= As[(16 * i + rr) * 65 + 16 * i + m] * Tt[blk * 272 + m * 17 + cc];
-                    As[(16 * i + rr) * 65 + 16 * jb + cc] = acc;
-                }
-                __syncthreads();
-            }
-        }
+    } else if (ok) {
         if (tid < 64) {
-            const int rr = tid;
-            float x[64];
+            // diagonal 16x16 blocks: thread (b, j) solves column j of block b in
+            // registers, x[r] = [r == j] - sum_{s<r} L[b+r][b+s] x[s]
+            const int b = 16 * (tid >> 4), jj = tid & 15;
+            float x[16];
 #pragma unroll
-            for (int s = 0; s < 64; ++s) x[s] = As[rr * 65 + s];
-            st_img_row2(reinterpret_cast<char *>(p.Aimg) + ch * kImg2, rr, x);
-            if (p.A_out && !from_A && rr < len) {
-                float4 *dst = reinterpret_cast<float4 *>(p.A_out + ((size_t)(tok0 + rr) * p.Hv + h) * 64);
+            for (int rr = 0; rr < 16; ++rr) {
+                const float *lrow = Ls + (b + rr) * kLd + b;
+                float acc = rr == jj ? 1.f : 0.f;
 #pragma unroll
-                for (int s = 0; s < 16; ++s) dst[s] = make_float4(x[4 * s], x[4 * s + 1], x[4 * s + 2], x[4 * s + 3]);
+                for (int s = 0; s < rr; ++s) acc = fmaf(-lrow[s], x[s], acc);
+                x[rr] = rr < jj ? 0.f : acc;
+            }
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr) As[(b + rr) * kLd + b + jj] = x[rr];
+        } else {
+            // zero the strictly upper blocks of A
+            const int t = tid - 64;
+#pragma unroll
+            for (int u = 0; u < 6; ++u) {
+                const int e = t + 64 * u;             // 384 float4 = 6 blocks x 16 rows x 4
+                const int blk = e >> 6, rr = (e >> 2) & 15, c4 = (e & 3) * 4;
+                const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+                const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+                *reinterpret_cast<float4 *>(As + (16 * bi + rr) * kLd + 16 * bj + c4) = make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
         __syncthreads();
+        inv_row_block<1>(Ls, As, Tt, tid);
+        inv_row_block<2>(Ls, As, Tt, tid);
+        inv_row_block<3>(Ls, As, Tt, tid);
+    }
+    if (!*abort) {
+        // A image (hi | lo) and the fp32 A output: thread -> row tid/2, 32 columns
+        const int rr = tid >> 1, c0 = 32 * (tid & 1);
+        float x[32];
+#pragma unroll
+        for (int s = 0; s < 32; s += 4) {
+            const float4 v = *reinterpret_cast<const float4 *>(As + rr * kLd + c0 + s);
+            x[s] = v.x; x[s + 1] = v.y; x[s + 2] = v.z; x[s + 3] = v.w;
+        }
+        st_img_half2(reinterpret_cast<char *>(p.Aimg) + ch * kImg2, rr, c0, x);
+        if (p.A_out && !from_A && rr < len) {
+            float4 *dst = reinterpret_cast<float4 *>(p.A_out + ((size_t)(tok0 + rr) * p.Hv + h) * 64 + c0);
+#pragma unroll
+            for (int s = 0; s < 8; ++s) dst[s] = make_float4(x[4 * s], x[4 * s + 1], x[4 * s + 2], x[4 * s + 3]);
+        }
     }
     if (tid == 0) {  // no copy or MMA of this CTA may still be in flight when it leaves
         drain_wait(&bars[0], 0);
@@ -535,7 +622,11 @@ __global__ void __launch_bounds__(320, 1) k_scan_tc(Params p, const __grid_const
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tS = tmem, tD1 = tmem + 128, tD1b = tmem + 256, tD2 = tmem + 320;
+    // S^T [0,128); D1 = [(K S)^T | (Q S)^T] alternates between [128,256) and
+    // [384,512) so the output of chunk c is read while chunk c+1 runs;
+    // Ut^T [256,320); (P Ut)^T [320,384)
+    const uint32_t tS = tmem, tD1b = tmem + 256, tD2 = tmem + 320;
+    auto tD1 = [&](int cc) -> uint32_t { return tmem + ((cc & 1) ? 384u : 128u); };
 
     if (warp == 8) {
         // ---------------- TMA producer ----------------
@@ -569,6 +660,9 @@ __global__ void __launch_bounds__(320, 1) k_scan_tc(Params p, const __grid_const
         }
     } else if (warp == 9) {
         // ---------------- MMA issuer ----------------
+        // MMA2 is issued before MMA3: both read the Y^T images, which share
+        // the operand region with the next chunk's S^T images, so bar_m3 must
+        // cover both.
         if (lane == 0) {
             const uint32_t id1 = idesc_bf16(128, MODE == kFwd ? 128 : 64);
             const uint32_t id64 = idesc_bf16(128, 64);
@@ -579,14 +673,14 @@ __global__ void __launch_bounds__(320, 1) k_scan_tc(Params p, const __grid_const
                 if (!bwait(&full[s], (cc >> 1) & 1, cap, abort)) break;
                 if (!bwait(bar_sb, cc & 1, cap, abort)) break;
                 tc_fence_after();
-                const uint32_t b1 = su32(st + SL::kB1);
+                const uint32_t b1 = su32(st + SL::kB1), d1 = tD1(cc);
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     const uint32_t a0 = su32(half ? SBl : SBh);
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         const uint32_t ko = (kk & 3) * 32;
-                        mma(tD1, sdesc(a0 + (kk >> 2) * 16384 + ko), sdesc(b1 + (kk >> 2) * SL::kAtom + ko), id1,
+                        mma(d1, sdesc(a0 + (kk >> 2) * 16384 + ko), sdesc(b1 + (kk >> 2) * SL::kAtom + ko), id1,
                             (half | kk) != 0);
                     }
                 }
@@ -652,45 +746,89 @@ __global__ void __launch_bounds__(320, 1) k_scan_tc(Params p, const __grid_const
         }
         tmem_wait_st();
         float *hdst = MODE == kFwd ? p.h_out : (MODE == kStates ? p.hbuf : nullptr);
+        // (e) O = scale diag(e^gamma) Q S + P Ut of chunk cc, run while chunk
+        // cc+1 is on the chain (after its (a), which waited for bar_m3 of cc)
+        auto out_phase = [&](int cc) {
+            const int s = cc & 1;
+            const float *eg = reinterpret_cast<const float *>(aux0 + s * kAux) + 64;
+            const int c = sg.chunk0 + cc;
+            const int ctok0 = sq.tok0 + kChunk * (c - sq.chunk0);
+            const int clen = min(kChunk, sq.len - kChunk * (c - sq.chunk0));
+            TO *o = reinterpret_cast<TO *>(p.o);
+            uint32_t r2[32];
+            const int j = wg;
+            tmem_ld32_issue(tD1(cc) + 64 + 32 * j + lo, r);
+            tmem_ld32_issue(tD2 + 32 * j + lo, r2);
+            tmem_wait_ld32(r);
+            tmem_hold32(r2);
+            TO *orow = o + ((size_t)ctok0 * p.Hv + h) * 128 + t;
+            const size_t pitch = (size_t)p.Hv * 128;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int rr = 32 * j + i;
+                const float val = p.scale * eg[rr] * __uint_as_float(r[i]) + __uint_as_float(r2[i]);
+                if (rr < clen) {
+                    if constexpr (sizeof(TO) == 4)
+                        orow[rr * pitch] = val;
+                    else
+                        orow[rr * pitch] = __float2bfloat16_rn(val);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&empty[s]);
+        };
+        bool live = true;
         for (int cc = 0; cc < nch; ++cc) {
             const int s = cc & 1;
             char *st = stage0 + s * SL::kBytes;
             const float *bet = reinterpret_cast<const float *>(aux0 + s * kAux);
             const float *eg = bet + 64, *eL = bet + 128;
             const int c = sg.chunk0 + cc;
-            if (cc > 0 && !bwait(bar_m3, (cc - 1) & 1, cap, abort)) break;
+            if (cc > 0 && !bwait(bar_m3, (cc - 1) & 1, cap, abort)) { live = false; break; }
             tc_fence_after();
-            if (!bwait(&full[s], (cc >> 1) & 1, cap, abort)) break;
+            if (!bwait(&full[s], (cc >> 1) & 1, cap, abort)) { live = false; break; }
             const float dec = eg[63];
             // (a)
-            for (int j = 2 * wg; j < 2 * wg + 2; ++j) {
-                tmem_ld32(tS + 32 * j + lo, r);
-                float f[32], hi[32], lw[32];
+            {
+                uint32_t r2[32];
+                tmem_ld32_issue(tS + 64 * wg + lo, r);
+                tmem_ld32_issue(tS + 64 * wg + 32 + lo, r2);
+                tmem_wait_ld32(r);
+                tmem_hold32(r2);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    f[i] = __uint_as_float(r[i]);
-                    hi[i] = bf16_round(f[i]);
-                    lw[i] = f[i] - hi[i];
+                for (int jj = 0; jj < 2; ++jj) {
+                    uint32_t(&rv)[32] = jj ? r2 : r;
+                    const int j = 2 * wg + jj;
+                    float f[32], hi[32], lw[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        f[i] = __uint_as_float(rv[i]);
+                        hi[i] = bf16_round(f[i]);
+                        lw[i] = f[i] - hi[i];
+                    }
+                    st_row32(SBh, 128, t, 32 * j, hi);
+                    st_row32(SBl, 128, t, 32 * j, lw);
+                    if (hdst)
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            hdst[(((size_t)c * p.Hv + h) * 128 + 32 * j + i) * 128 + t] = f[i];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) rv[i] = __float_as_uint(f[i] * dec);
+                    tmem_st32(tS + 32 * j + lo, rv);
                 }
-                st_row32(SBh, 128, t, 32 * j, hi);
-                st_row32(SBl, 128, t, 32 * j, lw);
-                if (hdst)
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) hdst[(((size_t)c * p.Hv + h) * 128 + 32 * j + i) * 128 + t] = f[i];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(f[i] * dec);
-                tmem_st32(tS + 32 * j + lo, r);
             }
             tmem_wait_st();
             fence_async_smem();
             tc_fence_before();
             mbar_arrive(bar_sb);
+            if (MODE == kFwd && cc > 0) out_phase(cc - 1);
             // (c) R^T[t][s] = b_s (V[s][t] - e^{gamma_s} (K S)^T[t][s])
-            if (!bwait(bar_m1, cc & 1, cap, abort)) break;
+            if (!bwait(bar_m1, cc & 1, cap, abort)) { live = false; break; }
             tc_fence_after();
             const __nv_bfloat16 *Vs = reinterpret_cast<const __nv_bfloat16 *>(st + SL::kV);
-            for (int j = wg; j < wg + 1; ++j) {
-                tmem_ld32(tD1 + 32 * j + lo, r);
+            {
+                const int j = wg;
+                tmem_ld32(tD1(cc) + 32 * j + lo, r);
                 float f[32], lw[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
@@ -707,9 +845,10 @@ __global__ void __launch_bounds__(320, 1) k_scan_tc(Params p, const __grid_const
             tc_fence_before();
             mbar_arrive(bar_rt);
             // (c2) Y^T[t][r] = e^{gamma_n - gamma_r} Ut^T[t][r]
-            if (!bwait(bar_m1b, cc & 1, cap, abort)) break;
+            if (!bwait(bar_m1b, cc & 1, cap, abort)) { live = false; break; }
             tc_fence_after();
-            for (int j = wg; j < wg + 1; ++j) {
+            {
+                const int j = wg;
                 tmem_ld32(tD1b + 32 * j + lo, r);
                 float f[32], lw[32];
 #pragma unroll
@@ -724,37 +863,14 @@ __global__ void __launch_bounds__(320, 1) k_scan_tc(Params p, const __grid_const
             fence_async_smem();
             tc_fence_before();
             mbar_arrive(bar_ut);
-            // (e)
-            if (MODE == kFwd) {
-                if (!bwait(bar_m3, cc & 1, cap, abort)) break;
-                tc_fence_after();
-                const int ctok0 = sq.tok0 + kChunk * (c - sq.chunk0);
-                const int clen = min(kChunk, sq.len - kChunk * (c - sq.chunk0));
-                TO *o = reinterpret_cast<TO *>(p.o);
-                for (int j = wg; j < wg + 1; ++j) {
-                    uint32_t r2[32];
-                    tmem_ld32(tD1 + 64 + 32 * j + lo, r);
-                    tmem_ld32(tD2 + 32 * j + lo, r2);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int rr = 32 * j + i;
-                        const float val = p.scale * eg[rr] * __uint_as_float(r[i]) + __uint_as_float(r2[i]);
-                        if (rr < clen) {
-                            const size_t off = ((size_t)(ctok0 + rr) * p.Hv + h) * 128 + t;
-                            if constexpr (sizeof(TO) == 4)
-                                o[off] = val;
-                            else
-                                o[off] = __float2bfloat16_rn(val);
-                        }
-                    }
-                }
+            if (MODE != kFwd) {
+                tc_fence_before();
+                mbar_arrive(&empty[s]);
             }
-            tc_fence_before();
-            mbar_arrive(&empty[s]);
         }
-        if (!*abort) {
-            if (nch > 0 && MODE != kFwd) bwait(bar_m3, (nch - 1) & 1, cap, abort);
+        if (live && !*abort && nch > 0 && bwait(bar_m3, (nch - 1) & 1, cap, abort)) {
             tc_fence_after();
+            if (MODE == kFwd) out_phase(nch - 1);
         }
         if (!*abort) {
             float *dst = nullptr;
@@ -1151,7 +1267,7 @@ int launch_chunk(const char *name, const Params &p, int from_A, cudaStream_t st)
     if (cudaFuncSetAttribute(k_chunk_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kChunkSmem) != cudaSuccess)
         return 1;
     tm_begin(p.tm, name, st);
-    k_chunk_tc<<<dim3(p.NT, p.Hq), 128, kChunkSmem, st>>>(p, maps, from_A);
+    k_chunk_tc<<<dim3(p.NT * p.Hv), 128, kChunkSmem, st>>>(p, maps, from_A);
     tm_end(p.tm, st);
     return cudaGetLastError() != cudaSuccess;
 }

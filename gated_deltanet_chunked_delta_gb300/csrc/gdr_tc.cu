@@ -75,6 +75,17 @@ __device__ __forceinline__ bool bwait(uint64_t *b, uint32_t parity, long long ca
         }
     }
 }
+// Warp-uniform bounded wait: every lane polls, and the warp proceeds only if
+// all of them saw the phase complete.
+__device__ __forceinline__ bool wbwait(uint64_t *b, uint32_t parity, long long cap, volatile int *abort) {
+    return __all_sync(0xffffffffu, bwait(b, parity, cap, abort));
+}
+// One arrival per warp (the barrier counts warps): the lanes' prior shared
+// memory writes and tensor-memory reads are ordered before lane 0's arrival.
+__device__ __forceinline__ void warp_arrive(uint64_t *b, int lane) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(b);
+}
 // Bounded wait that ignores the abort flag, used while draining a CTA's own
 // copies and MMAs before it leaves.  Its cap is fixed and generous, not the
 // caller's timeout: work that was issued with valid addresses completes, and
@@ -91,6 +102,14 @@ __device__ __forceinline__ void tma3d(void *dst, const CUtensorMap *m, int x, in
         "[%5];" ::"r"(su32(dst)),
         "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(z), "r"(su32(bar))
         : "memory");
+}
+// Shared -> global tiled store, committed as its own bulk group.
+__device__ __forceinline__ void tma_store3d(const CUtensorMap *m, const void *src, int x, int y, int z) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(su32(src)), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
@@ -130,6 +149,16 @@ __device__ __forceinline__ void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t
         "l"(a), "l"(b), "r"(idesc), "r"(acc)
         : "memory");
 }
+// Same with the A operand (M = 128 lanes x 16 K as 8 packed bf16-pair columns)
+// read from tensor memory at column address a.
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+        "r"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(bar))
                  : "memory");
@@ -151,21 +180,22 @@ __device__ __forceinline__ void tmem_ld32(uint32_t ta, uint32_t (&r)[32]) {
         : "r"(ta));
     asm volatile("tcgen05.wait::ld.sync.aligned;" : W8(0), W8(8), W8(16), W8(24)::"memory");
 }
-// Issue only; pair with tmem_wait_ld32 / tmem_hold32 before the registers are used.
-__device__ __forceinline__ void tmem_ld32_issue(uint32_t ta, uint32_t (&r)[32]) {
+#define R4(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3])
+#define W4(i) "+r"(r[i]), "+r"(r[i + 1]), "+r"(r[i + 2]), "+r"(r[i + 3])
+// 16 consecutive TMEM columns of this warp's 32 lanes, issue only.
+__device__ __forceinline__ void tmem_ld16_issue(uint32_t ta, uint32_t (&r)[16]) {
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : R8(0), R8(8), R8(16), R8(24)
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : R4(0), R4(4), R4(8), R4(12)
         : "r"(ta));
 }
-__device__ __forceinline__ void tmem_wait_ld32(uint32_t (&r)[32]) {
-    asm volatile("tcgen05.wait::ld.sync.aligned;" : W8(0), W8(8), W8(16), W8(24)::"memory");
+__device__ __forceinline__ void tmem_wait_ld16(uint32_t (&r)[16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" : W4(0), W4(4), W4(8), W4(12)::"memory");
+}
+__device__ __forceinline__ void tmem_hold16(uint32_t (&r)[16]) {
+    asm volatile("" : W4(0), W4(4), W4(8), W4(12)::"memory");
 }
 // Orders the use of a second load's registers after a wait already issued.
-__device__ __forceinline__ void tmem_hold32(uint32_t (&r)[32]) {
-    asm volatile("" : W8(0), W8(8), W8(16), W8(24)::"memory");
-}
 __device__ __forceinline__ void tmem_st32(uint32_t ta, const uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
@@ -173,12 +203,36 @@ __device__ __forceinline__ void tmem_st32(uint32_t ta, const uint32_t (&r)[32]) 
         S8(0), S8(8), S8(16), S8(24)
         : "memory");
 }
+__device__ __forceinline__ void tmem_st16(uint32_t ta, const uint32_t *r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(ta),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st8(uint32_t ta, const uint32_t *r) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(ta), "r"(r[0]),
+                 "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
 }
+
+// x = hi + lo as packed bf16 pairs: hv[i] = (bf16(x[2i]), bf16(x[2i+1])), lv the remainders.
+template <int NP>
+__device__ __forceinline__ void split_pairs(const float *x, uint32_t *hv, uint32_t *lv) {
+#pragma unroll
+    for (int e = 0; e < NP; ++e) {
+        const float a = x[2 * e], b = x[2 * e + 1];
+        hv[e] = pack_bf16(a, b);
+        lv[e] = pack_bf16(a - __uint_as_float(hv[e] << 16), b - __uint_as_float(hv[e] & 0xffff0000u));
+    }
+}
+
 
 // Row `row` of a K-major, 128-byte-swizzled bf16 tile of `rows` rows: writes
 // 32 consecutive elements starting at column `col0` (a multiple of 32).
@@ -408,23 +462,20 @@ __global__ void __launch_bounds__(128, 4) k_chunk_tc(Params p, const __grid_cons
                 tmem_ld32(ta, r0);
                 tmem_ld32(ta + 32, r1);
                 float *lrow = Ls + rr * kLd;
+                // each half computed in registers before its stores (a store
+                // into Ls may not pass a load of gam)
 #pragma unroll
-                for (int s = 0; s < 32; s += 4) {
-                    float4 v;
-                    v.x = s + 0 < rr ? br * __expf(gr - gam[s + 0]) * __uint_as_float(r0[s + 0]) : 0.f;
-                    v.y = s + 1 < rr ? br * __expf(gr - gam[s + 1]) * __uint_as_float(r0[s + 1]) : 0.f;
-                    v.z = s + 2 < rr ? br * __expf(gr - gam[s + 2]) * __uint_as_float(r0[s + 2]) : 0.f;
-                    v.w = s + 3 < rr ? br * __expf(gr - gam[s + 3]) * __uint_as_float(r0[s + 3]) : 0.f;
-                    *reinterpret_cast<float4 *>(lrow + s) = v;
-                }
+                for (int hb = 0; hb < 2; ++hb) {
+                    const uint32_t *rv = hb ? r1 : r0;
+                    float x[32];
 #pragma unroll
-                for (int s = 0; s < 32; s += 4) {
-                    float4 v;
-                    v.x = s + 32 < rr ? br * __expf(gr - gam[s + 32]) * __uint_as_float(r1[s + 0]) : 0.f;
-                    v.y = s + 33 < rr ? br * __expf(gr - gam[s + 33]) * __uint_as_float(r1[s + 1]) : 0.f;
-                    v.z = s + 34 < rr ? br * __expf(gr - gam[s + 34]) * __uint_as_float(r1[s + 2]) : 0.f;
-                    v.w = s + 35 < rr ? br * __expf(gr - gam[s + 35]) * __uint_as_float(r1[s + 3]) : 0.f;
-                    *reinterpret_cast<float4 *>(lrow + 32 + s) = v;
+                    for (int s = 0; s < 32; ++s) {
+                        const int sc = 32 * hb + s;
+                        x[s] = sc < rr ? br * __expf(gr - gam[sc]) * __uint_as_float(rv[s]) : 0.f;
+                    }
+#pragma unroll
+                    for (int s = 0; s < 32; s += 4)
+                        *reinterpret_cast<float4 *>(lrow + 32 * hb + s) = make_float4(x[s], x[s + 1], x[s + 2], x[s + 3]);
                 }
             }
         } else {
@@ -522,26 +573,34 @@ __global__ void __launch_bounds__(128, 4) k_chunk_tc(Params p, const __grid_cons
 
 // ---------------------------------------------------------------------------
 // Scan kernel.  One CTA per (segment, v-head) (x2 in kSum: the S and the M
-// states run in separate CTAs).  Warps 0-7: epilogue (two warpgroups that
-// split the columns of every phase), warp 8: TMA producer (two-stage ring),
-// warp 9: tensor-memory allocation and the MMA issue (one thread).  Per chunk, with S^T in TMEM (lane v):
+// states run in separate CTAs).  Warps 0-15: epilogue (in kFwd, warps 0-7
+// carry the state chain and warps 8-15 write the output; otherwise all 16
+// carry the chain), warp 16: TMA producer (two-stage ring), warp 17: tensor-
+// memory allocation and the MMA issue (one thread).  Every A operand comes
+// from tensor memory as packed bf16 pairs written by the epilogue, so the
+// MMAs read only their B operands from shared memory.  Per chunk, with S^T
+// in TMEM (lane v):
 //   (a)  S^T -> bf16 hi + lo (A operands); S^T *= e^{gamma_n} in place
 //   MMA1 D1 = S^T [K ; Q]^T                               -> (K S)^T, (Q S)^T
 //   (c)  R^T = (diag(b) (V - diag(e^gamma) K S))^T        -> bf16 hi + lo
 //   MMA1b D1b = R^T A^T = Ut^T
 //   (c2) Y^T = (diag(e^{gamma_n - gamma}) Ut)^T           -> bf16 hi + lo
-//   MMA2 D2 = Y^T P'^T = (P Ut)^T                         (kFwd)
 //   MMA3 S^T += Y^T K     (K tile read MN-major)          = (e^{gamma_n} S + Kt^T Ut)^T
-//   (e)  O = scale diag(e^gamma) Q S + P Ut               (kFwd)
-// Every operand that is not an exact bf16 input (S, R, A, Y, P') enters as two
-// bf16 terms: x y ~ x_hi y_hi + x_lo y_hi + x_hi y_lo (one term when y is an
-// input), accumulated in fp32.  With single bf16 operands the max-abs error
-// of o and of the state settles near 2e-2 of their RMS on these workloads;
-// with the split it is ~1e-4.  The residual R is formed from the exact inputs,
-// so the cancellation in v - S^T k happens in fp32.
+//   MMA2 D2 = Y^T P'^T = (P Ut)^T                         (kFwd)
+//   (e)  O = scale diag(e^gamma) Q S + P Ut               (kFwd, one chunk behind)
+// The state chain (S -> K S -> R -> Ut -> Y -> S) keeps every operand that
+// is not an exact bf16 input (S, R, A, Y) as two bf16 terms: x y ~ x_hi y_hi
+// + x_lo y_hi + x_hi y_lo (one term when y is an input), accumulated in fp32.
+// With single bf16 operands on the chain the max-abs error of o and of the
+// state settles near 2e-2 of their RMS on these workloads; with the split it
+// is ~1e-4.  The residual R is formed from the exact inputs, so the
+// cancellation in v - S^T k happens in fp32.  The output-only products, Q S
+// and P Ut, take one term each (S_hi, Y_hi, P'_hi): their rounding reaches o
+// once, at ~2^-9 of the term, and never the state.
 // ---------------------------------------------------------------------------
 struct ScanMaps {
     CUtensorMap K, Q, V;  // 3-D over k, q (box 64 x 1 x 64, swizzled) and v (box 128 x 1 x 64, plain)
+    CUtensorMap O;        // 3-D over o (box 128 x 1 x 64, plain): full output chunks leave by TMA stores
 };
 
 template <int MODE>
@@ -554,28 +613,29 @@ struct ScanStage {
     static constexpr int kP = kA + kImg2;         // P' image, hi | lo (kFwd)
     static constexpr int kBytes = kP + (MODE == kFwd ? kImg2 : 0);
 };
-// One 64 KiB operand region, reused within a chunk: S^T hi | lo (2 x 32 KiB,
-// [2 atoms][128][128 B]) while MMA1 reads it, then R^T hi | lo (2 x 16 KiB,
-// [128][128 B]) in its first half and Y^T hi | lo in its second half.
-constexpr int kOps = 65536;
 
-template <int MODE>
+constexpr int kEpiWarps = 16;                     // epilogue warps of the scan kernel
+constexpr int kScanThreads = 32 * (kEpiWarps + 2); // + the TMA producer and the MMA issuer
+
+// Output staging of the forward: one [64 tokens][128] tile of the output type.
+template <int MODE, typename TO>
+__host__ __device__ constexpr int scan_out_bytes() {
+    return MODE == kFwd ? 64 * 128 * (int)sizeof(TO) : 0;
+}
+template <int MODE, typename TO>
 __host__ __device__ constexpr int scan_smem() {
-    return 1024 + 2 * ScanStage<MODE>::kBytes + kOps + 2 * kAux + 256;
+    return 1024 + 2 * ScanStage<MODE>::kBytes + scan_out_bytes<MODE, TO>() + 2 * kAux + 256;
 }
 
 template <int MODE, typename TO>
-__global__ void __launch_bounds__(320, 1) k_scan_tc(Params p, const __grid_constant__ ScanMaps maps) {
+__global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __grid_constant__ ScanMaps maps) {
     extern __shared__ __align__(1024) char smraw[];
     char *sm = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
     using SL = ScanStage<MODE>;
-    static_assert(scan_smem<MODE>() <= 227 * 1024, "shared memory budget");
+    static_assert(scan_smem<MODE, TO>() <= 227 * 1024, "shared memory budget");
     char *stage0 = sm;
-    char *SBh = sm + 2 * SL::kBytes;
-    char *SBl = SBh + 32768;
-    char *RTh = SBh, *RTl = SBh + 16384;
-    char *YTh = SBh + 32768, *YTl = SBh + 49152;
-    char *aux0 = SBh + kOps;  // 2 x kAux, one per stage
+    char *ostage = sm + 2 * SL::kBytes;                        // output staging (kFwd)
+    char *aux0 = ostage + scan_out_bytes<MODE, TO>();         // 2 x kAux, one per stage
     uint64_t *bars = reinterpret_cast<uint64_t *>(aux0 + 2 * kAux);
     uint64_t *full = bars;        // [2]
     uint64_t *empty = bars + 2;   // [2]
@@ -586,8 +646,10 @@ __global__ void __launch_bounds__(320, 1) k_scan_tc(Params p, const __grid_const
     uint64_t *bar_ut = bars + 8;
     uint64_t *bar_m3 = bars + 9;
     uint64_t *bar_drain = bars + 10;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 11);
-    volatile int *abort = reinterpret_cast<volatile int *>(bars + 12);
+    uint64_t *bar_ofull = bars + 11;  // output tile staged (kFwd)
+    uint64_t *bar_ofree = bars + 12;  // output tile read by its TMA store (kFwd)
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 13);
+    volatile int *abort = reinterpret_cast<volatile int *>(bars + 14);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int sidx = blockIdx.x, h = blockIdx.y;
@@ -601,19 +663,21 @@ __global__ void __launch_bounds__(320, 1) k_scan_tc(Params p, const __grid_const
     if (tid == 0) {
         mbar_init(&full[0], 1);
         mbar_init(&full[1], 1);
-        mbar_init(&empty[0], 257);
-        mbar_init(&empty[1], 257);
-        mbar_init(bar_sb, 256);
+        mbar_init(&empty[0], kEpiWarps + 1);
+        mbar_init(&empty[1], kEpiWarps + 1);
+        mbar_init(bar_sb, kEpiWarps);
         mbar_init(bar_m1, 1);
-        mbar_init(bar_rt, 256);
+        mbar_init(bar_rt, MODE == kFwd ? kEpiWarps / 2 : kEpiWarps);  // the state warps
         mbar_init(bar_m1b, 1);
-        mbar_init(bar_ut, 256);
+        mbar_init(bar_ut, kEpiWarps);
         mbar_init(bar_m3, 1);
         mbar_init(bar_drain, 1);
+        mbar_init(bar_ofull, kEpiWarps / 2);
+        mbar_init(bar_ofree, 1);
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 9) {
+    if (warp == kEpiWarps + 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
                      "r"(512));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
@@ -622,13 +686,19 @@ __global__ void __launch_bounds__(320, 1) k_scan_tc(Params p, const __grid_const
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    // S^T [0,128); D1 = [(K S)^T | (Q S)^T] alternates between [128,256) and
-    // [384,512) so the output of chunk c is read while chunk c+1 runs;
-    // Ut^T [256,320); (P Ut)^T [320,384)
-    const uint32_t tS = tmem, tD1b = tmem + 256, tD2 = tmem + 320;
-    auto tD1 = [&](int cc) -> uint32_t { return tmem + ((cc & 1) ? 384u : 128u); };
+    // Tensor memory (lane v throughout):
+    //   [0,128)   S^T fp32                      (accumulator of MMA3)
+    //   [128,192) (K S)^T, [192,256) (Q S)^T    (MMA1)
+    //   [256,320) Ut^T                          (MMA1b)
+    //   [320,384) (P Ut)^T                      (MMA2)
+    //   [384,512) A operands as packed bf16 pairs: S^T hi | lo (64 + 64
+    //             columns) for MMA1, then R^T hi | lo at [384,448) for MMA1b
+    //             and Y^T hi | lo at [448,512) for MMA2 and MMA3
+    const uint32_t tS = tmem, tD1 = tmem + 128, tQS = tmem + 192, tD1b = tmem + 256, tD2 = tmem + 320;
+    const uint32_t tSh = tmem + 384, tSl = tmem + 448, tRh = tmem + 384, tRl = tmem + 416, tYh = tmem + 448,
+                   tYl = tmem + 480;
 
-    if (warp == 8) {
+    if (warp == kEpiWarps) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
             int issued = 0;
@@ -658,11 +728,8 @@ __global__ void __launch_bounds__(320, 1) k_scan_tc(Params p, const __grid_const
             for (int cc = issued - 2 < 0 ? 0 : issued - 2; cc < issued; ++cc)
                 drain_wait(&full[cc & 1], (cc >> 1) & 1);
         }
-    } else if (warp == 9) {
-        // ---------------- MMA issuer ----------------
-        // MMA2 is issued before MMA3: both read the Y^T images, which share
-        // the operand region with the next chunk's S^T images, so bar_m3 must
-        // cover both.
+    } else if (warp == kEpiWarps + 1) {
+        // ---------------- MMA issuer: A operands from tensor memory ----------------
         if (lane == 0) {
             const uint32_t id1 = idesc_bf16(128, MODE == kFwd ? 128 : 64);
             const uint32_t id64 = idesc_bf16(128, 64);
@@ -673,48 +740,47 @@ __global__ void __launch_bounds__(320, 1) k_scan_tc(Params p, const __grid_const
                 if (!bwait(&full[s], (cc >> 1) & 1, cap, abort)) break;
                 if (!bwait(bar_sb, cc & 1, cap, abort)) break;
                 tc_fence_after();
-                const uint32_t b1 = su32(st + SL::kB1), d1 = tD1(cc);
+                const uint32_t b1 = su32(st + SL::kB1);
+                // MMA1: D1 = S^T [K ; Q]^T over k, 16 k per step (8 packed columns)
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
-                    const uint32_t a0 = su32(half ? SBl : SBh);
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         const uint32_t ko = (kk & 3) * 32;
-                        mma(d1, sdesc(a0 + (kk >> 2) * 16384 + ko), sdesc(b1 + (kk >> 2) * SL::kAtom + ko), id1,
-                            (half | kk) != 0);
+                        mma_ts(tD1, (half ? tSl : tSh) + 8 * kk, sdesc(b1 + (kk >> 2) * SL::kAtom + ko), id1,
+                               (half | kk) != 0);
                     }
                 }
                 mma_commit(bar_m1);
                 if (!bwait(bar_rt, cc & 1, cap, abort)) break;
                 tc_fence_after();
                 {
-                    const uint32_t rh = su32(RTh), rl = su32(RTl), ah = su32(st + SL::kA), al = ah + kImg;
+                    const uint32_t ah = su32(st + SL::kA), al = ah + kImg;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint32_t o = kk * 32;
-                        mma(tD1b, sdesc(rh + o), sdesc(ah + o), id64, kk > 0);
-                        mma(tD1b, sdesc(rl + o), sdesc(ah + o), id64, 1);
-                        mma(tD1b, sdesc(rh + o), sdesc(al + o), id64, 1);
+                        mma_ts(tD1b, tRh + 8 * kk, sdesc(ah + o), id64, kk > 0);
+                        mma_ts(tD1b, tRl + 8 * kk, sdesc(ah + o), id64, 1);
+                        mma_ts(tD1b, tRh + 8 * kk, sdesc(al + o), id64, 1);
                     }
                 }
                 mma_commit(bar_m1b);
                 if (!bwait(bar_ut, cc & 1, cap, abort)) break;
                 tc_fence_after();
-                const uint32_t yh = su32(YTh), yl = su32(YTl);
                 if (MODE == kFwd) {
                     const uint32_t ph = su32(st + SL::kP), pl = ph + kImg;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint32_t o = kk * 32;
-                        mma(tD2, sdesc(yh + o), sdesc(ph + o), id64, kk > 0);
-                        mma(tD2, sdesc(yl + o), sdesc(ph + o), id64, 1);
-                        mma(tD2, sdesc(yh + o), sdesc(pl + o), id64, 1);
+                        mma_ts(tD2, tYh + 8 * kk, sdesc(ph + o), id64, kk > 0);
+                        mma_ts(tD2, tYl + 8 * kk, sdesc(ph + o), id64, 1);
+                        mma_ts(tD2, tYh + 8 * kk, sdesc(pl + o), id64, 1);
                     }
                 }
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
-                    mma(tS, sdesc(yh + kk * 32), sdesc(b1 + kk * 2048, SL::kAtom), id3, 1);
-                    mma(tS, sdesc(yl + kk * 32), sdesc(b1 + kk * 2048, SL::kAtom), id3, 1);
+                    mma_ts(tS, tYh + 8 * kk, sdesc(b1 + kk * 2048, SL::kAtom), id3, 1);
+                    mma_ts(tS, tYl + 8 * kk, sdesc(b1 + kk * 2048, SL::kAtom), id3, 1);
                 }
                 mma_commit(bar_m3);
                 mma_commit(&empty[s]);
@@ -722,17 +788,114 @@ __global__ void __launch_bounds__(320, 1) k_scan_tc(Params p, const __grid_const
             mma_commit(bar_drain);
             drain_wait(bar_drain, 0);
         }
-    } else {
-        // ---------------- epilogue: warps 0-7, two warpgroups splitting the columns;
-        // thread t of a warpgroup <-> TMEM lane t ----------------
-        const int wg = warp >> 2;  // two epilogue warpgroups split the columns
+    } else if (MODE == kFwd && warp >= kEpiWarps / 2) {
+        // ---------------- output warps 8-15 (kFwd): off the state chain.
+        // Warp w reads TMEM lanes 32 (w % 4) .. + 31 and writes tokens
+        // [32 th, 32 th + 32), th = w / 4 - 2, of O = scale diag(e^gamma) Q S
+        // + P Ut: (Q S)^T as soon as MMA1 lands (then MMA1 of the next chunk
+        // may overwrite it), (P Ut)^T once MMA2 lands (then MMA2 of the next
+        // chunk may).  A full chunk is staged as one [64][128] tile and
+        // leaves by a TMA store; a partial one (a sequence's last, so a CTA's
+        // last) is stored row by row. ----------------
         const int t = tid & 127;
         const uint32_t lo = (uint32_t)((warp & 3) * 32) << 16;
-        uint32_t r[32];
-        for (int j = 2 * wg; j < 2 * wg + 2; ++j) {
+        const int r0 = 32 * ((warp >> 2) - 2);
+        const bool e0 = warp == kEpiWarps / 2 && lane == 0;
+        TO *stg = reinterpret_cast<TO *>(ostage) + t;
+        const size_t pitch = (size_t)p.Hv * 128;
+        warp_arrive(bar_sb, lane);  // nothing of a previous chunk to read
+        warp_arrive(bar_ut, lane);
+        for (int cc = 0; cc < nch; ++cc) {
+            const int s = cc & 1;
+            const int c = sg.chunk0 + cc;
+            const int ctok0 = sq.tok0 + kChunk * (c - sq.chunk0);
+            const int clen = min(kChunk, sq.len - kChunk * (c - sq.chunk0));
+            if (!wbwait(&full[s], (cc >> 1) & 1, cap, abort)) break;
+            const float *eg = reinterpret_cast<const float *>(aux0 + s * kAux) + 64;
+            float o[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = p.scale * eg[r0 + i];
+            warp_arrive(&empty[s], lane);  // done with the stage
+            if (!wbwait(bar_m1, cc & 1, cap, abort)) break;
+            tc_fence_after();
+            {
+                uint32_t a[16], b[16];
+                tmem_ld16_issue(tQS + r0 + lo, a);
+                tmem_ld16_issue(tQS + r0 + 16 + lo, b);
+                tmem_wait_ld16(a);
+                tmem_hold16(b);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    o[i] *= __uint_as_float(a[i]);
+                    o[16 + i] *= __uint_as_float(b[i]);
+                }
+            }
+            tc_fence_before();
+            warp_arrive(bar_sb, lane);  // (Q S)^T of cc read
+            if (!wbwait(bar_m3, cc & 1, cap, abort)) break;
+            tc_fence_after();
+            {
+                uint32_t a[16], b[16];
+                tmem_ld16_issue(tD2 + r0 + lo, a);
+                tmem_ld16_issue(tD2 + r0 + 16 + lo, b);
+                tmem_wait_ld16(a);
+                tmem_hold16(b);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    o[i] += __uint_as_float(a[i]);
+                    o[16 + i] += __uint_as_float(b[i]);
+                }
+            }
+            tc_fence_before();
+            warp_arrive(bar_ut, lane);  // (P Ut)^T of cc read
+            if (clen == kChunk) {
+                if (cc > 0 && !wbwait(bar_ofree, (cc - 1) & 1, cap, abort)) break;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    if constexpr (sizeof(TO) == 4)
+                        stg[(r0 + i) * 128] = o[i];
+                    else
+                        stg[(r0 + i) * 128] = __float2bfloat16_rn(o[i]);
+                }
+                fence_async_smem();
+                warp_arrive(bar_ofull, lane);
+                if (e0) {
+                    if (!bwait(bar_ofull, cc & 1, cap, abort)) break;
+                    tma_store3d(&maps.O, ostage, 0, h, ctok0);
+                    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                    mbar_arrive(bar_ofree);
+                }
+            } else {
+                TO *orow = reinterpret_cast<TO *>(p.o) + ((size_t)ctok0 * p.Hv + h) * 128 + t;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    if (r0 + i < clen) {
+                        if constexpr (sizeof(TO) == 4)
+                            orow[(r0 + i) * pitch] = o[i];
+                        else
+                            orow[(r0 + i) * pitch] = __float2bfloat16_rn(o[i]);
+                    }
+                }
+            }
+        }
+        if (e0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // every output store complete
+    } else {
+        // ---------------- state warps: 0-7 in kFwd, 0-15 otherwise.  Warp w
+        // reads TMEM lanes 32 (w % 4) .. + 31 (thread t <-> lane t = v) and
+        // has column group cg = w / 4: state columns [kSC cg, + kSC) in (a),
+        // token columns [kTC cg, + kTC) in (c) and (c2). ----------------
+        const int cg = warp >> 2;
+        const int t = tid & 127;
+        const uint32_t lo = (uint32_t)((warp & 3) * 32) << 16;
+        constexpr int kSC = MODE == kFwd ? 64 : 32;  // state columns per warp
+        constexpr int kTC = MODE == kFwd ? 32 : 16;  // token columns per warp
+        const int sc0 = kSC * cg, tc0 = kTC * cg;
+#pragma unroll 1
+        for (int j = 0; j < kSC / 32; ++j) {
+            uint32_t r[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-                const int k = 32 * j + i;
+                const int k = sc0 + 32 * j + i;
                 float v0;
                 if (MODE == kSum)
                     v0 = (isM && k == t) ? 1.f : 0.f;
@@ -742,41 +905,10 @@ __global__ void __launch_bounds__(320, 1) k_scan_tc(Params p, const __grid_const
                     v0 = p.Sstart[(((size_t)sidx * p.Hv + h) * 128 + k) * 128 + t];
                 r[i] = __float_as_uint(v0);
             }
-            tmem_st32(tS + 32 * j + lo, r);
+            tmem_st32(tS + sc0 + 32 * j + lo, r);
         }
         tmem_wait_st();
         float *hdst = MODE == kFwd ? p.h_out : (MODE == kStates ? p.hbuf : nullptr);
-        // (e) O = scale diag(e^gamma) Q S + P Ut of chunk cc, run while chunk
-        // cc+1 is on the chain (after its (a), which waited for bar_m3 of cc)
-        auto out_phase = [&](int cc) {
-            const int s = cc & 1;
-            const float *eg = reinterpret_cast<const float *>(aux0 + s * kAux) + 64;
-            const int c = sg.chunk0 + cc;
-            const int ctok0 = sq.tok0 + kChunk * (c - sq.chunk0);
-            const int clen = min(kChunk, sq.len - kChunk * (c - sq.chunk0));
-            TO *o = reinterpret_cast<TO *>(p.o);
-            uint32_t r2[32];
-            const int j = wg;
-            tmem_ld32_issue(tD1(cc) + 64 + 32 * j + lo, r);
-            tmem_ld32_issue(tD2 + 32 * j + lo, r2);
-            tmem_wait_ld32(r);
-            tmem_hold32(r2);
-            TO *orow = o + ((size_t)ctok0 * p.Hv + h) * 128 + t;
-            const size_t pitch = (size_t)p.Hv * 128;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int rr = 32 * j + i;
-                const float val = p.scale * eg[rr] * __uint_as_float(r[i]) + __uint_as_float(r2[i]);
-                if (rr < clen) {
-                    if constexpr (sizeof(TO) == 4)
-                        orow[rr * pitch] = val;
-                    else
-                        orow[rr * pitch] = __float2bfloat16_rn(val);
-                }
-            }
-            tc_fence_before();
-            mbar_arrive(&empty[s]);
-        };
         bool live = true;
         for (int cc = 0; cc < nch; ++cc) {
             const int s = cc & 1;
@@ -784,95 +916,87 @@ __global__ void __launch_bounds__(320, 1) k_scan_tc(Params p, const __grid_const
             const float *bet = reinterpret_cast<const float *>(aux0 + s * kAux);
             const float *eg = bet + 64, *eL = bet + 128;
             const int c = sg.chunk0 + cc;
-            if (cc > 0 && !bwait(bar_m3, (cc - 1) & 1, cap, abort)) { live = false; break; }
+            if (cc > 0 && !wbwait(bar_m3, (cc - 1) & 1, cap, abort)) { live = false; break; }
             tc_fence_after();
-            if (!bwait(&full[s], (cc >> 1) & 1, cap, abort)) { live = false; break; }
-            const float dec = eg[63];
-            // (a)
+            if (!wbwait(&full[s], (cc >> 1) & 1, cap, abort)) { live = false; break; }
             {
-                uint32_t r2[32];
-                tmem_ld32_issue(tS + 64 * wg + lo, r);
-                tmem_ld32_issue(tS + 64 * wg + 32 + lo, r2);
-                tmem_wait_ld32(r);
-                tmem_hold32(r2);
+                // (a) S^T -> packed bf16 hi | lo A operands; S^T *= e^{gamma_n}
+                const float dec = eg[63];
+#pragma unroll 1
+                for (int j = 0; j < kSC / 32; ++j) {
+                    const int k0 = sc0 + 32 * j;
+                    uint32_t r[32];
+                    tmem_ld32(tS + k0 + lo, r);
+                    float f[32];
 #pragma unroll
-                for (int jj = 0; jj < 2; ++jj) {
-                    uint32_t(&rv)[32] = jj ? r2 : r;
-                    const int j = 2 * wg + jj;
-                    float f[32], hi[32], lw[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        f[i] = __uint_as_float(rv[i]);
-                        hi[i] = bf16_round(f[i]);
-                        lw[i] = f[i] - hi[i];
-                    }
-                    st_row32(SBh, 128, t, 32 * j, hi);
-                    st_row32(SBl, 128, t, 32 * j, lw);
+                    for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(r[i]);
+                    uint32_t hv[16], lv[16];
+                    split_pairs<16>(f, hv, lv);
+                    tmem_st16(tSh + k0 / 2 + lo, hv);
+                    tmem_st16(tSl + k0 / 2 + lo, lv);
                     if (hdst)
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            hdst[(((size_t)c * p.Hv + h) * 128 + 32 * j + i) * 128 + t] = f[i];
+                        for (int i = 0; i < 32; ++i) hdst[(((size_t)c * p.Hv + h) * 128 + k0 + i) * 128 + t] = f[i];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) rv[i] = __float_as_uint(f[i] * dec);
-                    tmem_st32(tS + 32 * j + lo, rv);
+                    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(f[i] * dec);
+                    tmem_st32(tS + k0 + lo, r);
                 }
+                tmem_wait_st();
             }
-            tmem_wait_st();
-            fence_async_smem();
             tc_fence_before();
-            mbar_arrive(bar_sb);
-            if (MODE == kFwd && cc > 0) out_phase(cc - 1);
+            warp_arrive(bar_sb, lane);
             // (c) R^T[t][s] = b_s (V[s][t] - e^{gamma_s} (K S)^T[t][s])
-            if (!bwait(bar_m1, cc & 1, cap, abort)) { live = false; break; }
+            if (!wbwait(bar_m1, cc & 1, cap, abort)) { live = false; break; }
             tc_fence_after();
-            const __nv_bfloat16 *Vs = reinterpret_cast<const __nv_bfloat16 *>(st + SL::kV);
             {
-                const int j = wg;
-                tmem_ld32(tD1(cc) + 32 * j + lo, r);
-                float f[32], lw[32];
+                const __nv_bfloat16 *Vs = reinterpret_cast<const __nv_bfloat16 *>(st + SL::kV);
+#pragma unroll 1
+                for (int j = 0; j < kTC / 16; ++j) {
+                    const int c0 = tc0 + 16 * j;
+                    float vv[16];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int s2 = 32 * j + i;
-                    const float vv = isM ? 0.f : __bfloat162float(Vs[s2 * 128 + t]);
-                    const float x = bet[s2] * (vv - eg[s2] * __uint_as_float(r[i]));
-                    f[i] = bf16_round(x);
-                    lw[i] = x - f[i];
+                    for (int i = 0; i < 16; ++i) vv[i] = isM ? 0.f : __bfloat162float(Vs[(c0 + i) * 128 + t]);
+                    uint32_t r[16];
+                    tmem_ld16_issue(tD1 + c0 + lo, r);
+                    tmem_wait_ld16(r);
+                    float x[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) x[i] = bet[c0 + i] * (vv[i] - eg[c0 + i] * __uint_as_float(r[i]));
+                    uint32_t hv[8], lv[8];
+                    split_pairs<8>(x, hv, lv);
+                    tmem_st8(tRh + c0 / 2 + lo, hv);
+                    tmem_st8(tRl + c0 / 2 + lo, lv);
                 }
-                st_row32(RTh, 128, t, 32 * j, f);
-                st_row32(RTl, 128, t, 32 * j, lw);
+                tmem_wait_st();
             }
-            fence_async_smem();
             tc_fence_before();
-            mbar_arrive(bar_rt);
+            warp_arrive(bar_rt, lane);
             // (c2) Y^T[t][r] = e^{gamma_n - gamma_r} Ut^T[t][r]
-            if (!bwait(bar_m1b, cc & 1, cap, abort)) { live = false; break; }
+            if (!wbwait(bar_m1b, cc & 1, cap, abort)) { live = false; break; }
             tc_fence_after();
             {
-                const int j = wg;
-                tmem_ld32(tD1b + 32 * j + lo, r);
-                float f[32], lw[32];
+#pragma unroll 1
+                for (int j = 0; j < kTC / 16; ++j) {
+                    const int c0 = tc0 + 16 * j;
+                    uint32_t r[16];
+                    tmem_ld16_issue(tD1b + c0 + lo, r);
+                    tmem_wait_ld16(r);
+                    float x[16];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float x = eL[32 * j + i] * __uint_as_float(r[i]);
-                    f[i] = bf16_round(x);
-                    lw[i] = x - f[i];
+                    for (int i = 0; i < 16; ++i) x[i] = eL[c0 + i] * __uint_as_float(r[i]);
+                    uint32_t hv[8], lv[8];
+                    split_pairs<8>(x, hv, lv);
+                    tmem_st8(tYh + c0 / 2 + lo, hv);
+                    tmem_st8(tYl + c0 / 2 + lo, lv);
                 }
-                st_row32(YTh, 128, t, 32 * j, f);
-                st_row32(YTl, 128, t, 32 * j, lw);
+                tmem_wait_st();
             }
-            fence_async_smem();
             tc_fence_before();
-            mbar_arrive(bar_ut);
-            if (MODE != kFwd) {
-                tc_fence_before();
-                mbar_arrive(&empty[s]);
-            }
+            warp_arrive(bar_ut, lane);
+            warp_arrive(&empty[s], lane);
         }
-        if (live && !*abort && nch > 0 && bwait(bar_m3, (nch - 1) & 1, cap, abort)) {
+        if (__all_sync(0xffffffffu, live && !*abort) && nch > 0 && wbwait(bar_m3, (nch - 1) & 1, cap, abort)) {
             tc_fence_after();
-            if (MODE == kFwd) out_phase(nch - 1);
-        }
-        if (!*abort) {
             float *dst = nullptr;
             size_t base = 0;
             if (MODE == kSum) {
@@ -885,16 +1009,19 @@ __global__ void __launch_bounds__(320, 1) k_scan_tc(Params p, const __grid_const
                 base = ((size_t)sg.seq * p.Hv + h) * 128 * 128;
             }
             if (dst)
-                for (int j = 2 * wg; j < 2 * wg + 2; ++j) {
-                    tmem_ld32(tS + 32 * j + lo, r);
+#pragma unroll 1
+                for (int j = 0; j < kSC / 32; ++j) {
+                    uint32_t r[32];
+                    tmem_ld32(tS + sc0 + 32 * j + lo, r);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) dst[base + (size_t)(32 * j + i) * 128 + t] = __uint_as_float(r[i]);
+                    for (int i = 0; i < 32; ++i)
+                        dst[base + (size_t)(sc0 + 32 * j + i) * 128 + t] = __uint_as_float(r[i]);
                 }
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 9) {
+    if (warp == kEpiWarps + 1) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512));
     }
@@ -923,6 +1050,7 @@ __global__ void __launch_bounds__(320, 1) k_scan_tc(Params p, const __grid_const
 // from it and stores dS1 and dUt of every chunk, and dh0 for the first.
 // ---------------------------------------------------------------------------
 constexpr int kDhFull = 0, kDhSum = 1;
+constexpr int kOps = 65536;  // operand region of the reverse scan (see DhStage)
 struct DhMaps {
     CUtensorMap K, Q, dO;  // 3-D, box (64, 1, 64), 128-byte swizzle
 };
@@ -1248,14 +1376,16 @@ EncodeFn encoder() {
 }
 
 // 3-D bf16 map over a [Ttot, H, 128] tensor, box (bx, 1, 64).
-bool map3(CUtensorMap *m, const void *base, int H, int Ttot, int bx, bool swizzle) {
+bool map3(CUtensorMap *m, const void *base, int H, int Ttot, int bx, bool swizzle, bool f32 = false) {
     EncodeFn fn = encoder();
     if (!fn) return false;
+    const cuuint64_t es_bytes = f32 ? 4 : 2;
     cuuint64_t d[3] = {128, (cuuint64_t)H, (cuuint64_t)Ttot};
-    cuuint64_t s[2] = {256, (cuuint64_t)H * 256};
+    cuuint64_t s[2] = {128 * es_bytes, (cuuint64_t)H * 128 * es_bytes};
     cuuint32_t b[3] = {(cuuint32_t)bx, 1, 64};
     cuuint32_t es[3] = {1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), d, s, b, es,
+    return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base),
+              d, s, b, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -1279,11 +1409,12 @@ int launch_scan(const char *name, const Params &p, cudaStream_t st) {
     if (!map3(&maps.K, p.k, p.Hq, p.Ttot, 64, true) || !map3(&maps.Q, p.q, p.Hq, p.Ttot, 64, true) ||
         !map3(&maps.V, p.v, p.Hv, p.Ttot, 128, false))
         return 1;
+    if (MODE == kFwd && !map3(&maps.O, p.o, p.Hv, p.Ttot, 128, false, sizeof(TO) == 4)) return 1;
     auto kern = k_scan_tc<MODE, TO>;
-    const int smem = scan_smem<MODE>();
+    const int smem = scan_smem<MODE, TO>();
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 1;
     tm_begin(p.tm, name, st);
-    kern<<<dim3(p.NSEG, p.Hv, MODE == kSum ? 2 : 1), 320, smem, st>>>(p, maps);
+    kern<<<dim3(p.NSEG, p.Hv, MODE == kSum ? 2 : 1), kScanThreads, smem, st>>>(p, maps);
     tm_end(p.tm, st);
     return cudaGetLastError() != cudaSuccess;
 }

@@ -234,22 +234,6 @@ __device__ __forceinline__ void split_pairs(const float *x, uint32_t *hv, uint32
 }
 
 
-// Row `row` of a K-major, 128-byte-swizzled bf16 tile of `rows` rows: writes
-// 32 consecutive elements starting at column `col0` (a multiple of 32).
-__device__ __forceinline__ void st_row32(char *tile, int rows, int row, int col0, const float *x) {
-    const int atom = col0 >> 6;
-    char *base = tile + atom * rows * 128 + row * 128;
-    const int c0 = (col0 & 63) >> 3;  // first 16-byte chunk
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        uint4 v;
-        v.x = pack_bf16(x[8 * j + 0], x[8 * j + 1]);
-        v.y = pack_bf16(x[8 * j + 2], x[8 * j + 3]);
-        v.z = pack_bf16(x[8 * j + 4], x[8 * j + 5]);
-        v.w = pack_bf16(x[8 * j + 6], x[8 * j + 7]);
-        *reinterpret_cast<uint4 *>(base + (((c0 + j) ^ (row & 7)) << 4)) = v;
-    }
-}
 
 
 // ---------------------------------------------------------------------------
@@ -995,7 +979,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
             warp_arrive(bar_ut, lane);
             warp_arrive(&empty[s], lane);
         }
-        if (__all_sync(0xffffffffu, live && !*abort) && nch > 0 && wbwait(bar_m3, (nch - 1) & 1, cap, abort)) {
+        // (a segment of an empty sequence has no chunk: its end state is its start state)
+        if (__all_sync(0xffffffffu, live && !*abort) && (nch == 0 || wbwait(bar_m3, (nch - 1) & 1, cap, abort))) {
             tc_fence_after();
             float *dst = nullptr;
             size_t base = 0;
@@ -1050,7 +1035,6 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
 // from it and stores dS1 and dUt of every chunk, and dh0 for the first.
 // ---------------------------------------------------------------------------
 constexpr int kDhFull = 0, kDhSum = 1;
-constexpr int kOps = 65536;  // operand region of the reverse scan (see DhStage)
 struct DhMaps {
     CUtensorMap K, Q, dO;  // 3-D, box (64, 1, 64), 128-byte swizzle
 };
@@ -1061,20 +1045,16 @@ struct DhStage {
     static constexpr int kP = 65536;      // P' image, hi | lo
     static constexpr int kBytes = 81920;
 };
-constexpr int kDhSmem = 1024 + 2 * DhStage::kBytes + kOps + 2 * kAux + 256;
+constexpr int kDhSmem = 1024 + 2 * DhStage::kBytes + 2 * kAux + 256;
 
 template <int DM>
-__global__ void __launch_bounds__(320, 1) k_dh_tc(Params p, const __grid_constant__ DhMaps maps) {
+__global__ void __launch_bounds__(kScanThreads, 1) k_dh_tc(Params p, const __grid_constant__ DhMaps maps) {
     extern __shared__ __align__(1024) char smraw[];
     char *sm = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
     static_assert(kDhSmem <= 227 * 1024, "shared memory budget");
     using SL = DhStage;
     char *stage0 = sm;
-    char *SBh = sm + 2 * SL::kBytes;    // dS1^T hi | lo, then dUt^T hi | lo, then X^T hi | lo
-    char *SBl = SBh + 32768;
-    char *UTh = SBh, *UTl = SBh + 16384;
-    char *XTh = SBh, *XTl = SBh + 32768;
-    char *aux0 = SBh + kOps;
+    char *aux0 = sm + 2 * SL::kBytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(aux0 + 2 * kAux);
     uint64_t *full = bars;
     uint64_t *empty = bars + 2;
@@ -1102,30 +1082,38 @@ __global__ void __launch_bounds__(320, 1) k_dh_tc(Params p, const __grid_constan
     if (tid == 0) {
         mbar_init(&full[0], 1);
         mbar_init(&full[1], 1);
-        mbar_init(&empty[0], 257);
-        mbar_init(&empty[1], 257);
-        mbar_init(bar_sb, 256);
+        mbar_init(&empty[0], kEpiWarps + 1);
+        mbar_init(&empty[1], kEpiWarps + 1);
+        mbar_init(bar_sb, kEpiWarps);
         mbar_init(bar_m1, 1);
-        mbar_init(bar_ut, 256);
+        mbar_init(bar_ut, kEpiWarps);
         mbar_init(bar_m2, 1);
-        mbar_init(bar_x, 256);
+        mbar_init(bar_x, kEpiWarps);
         mbar_init(bar_m3, 1);
         mbar_init(bar_drain, 1);
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 9) {
+    if (warp == kEpiWarps + 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
-                     "r"(256));
+                     "r"(512));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // Tensor memory (lane v throughout):
+    //   [0,128) dS^T fp32;  [128,192) dY^T (MMA-a);  [192,256) dR^T (MMA-b)
+    //   [256,384) dS1^T hi | lo as packed bf16 pairs (A of MMA-a), then dUt^T
+    //             hi | lo at [256,320) (A of MMA-b)
+    //   [384,512) X^T hi | lo (A of MMA-c; 64 columns each: the dO part for
+    //             K rows 0-63 of [Q ; K], then the dR part)
     const uint32_t tS = tmem, tD1 = tmem + 128, tD2 = tmem + 192;
+    const uint32_t tSh = tmem + 256, tSl = tmem + 320, tUh = tmem + 256, tUl = tmem + 288, tXh = tmem + 384,
+                   tXl = tmem + 448;
 
-    if (warp == 8) {
+    if (warp == kEpiWarps) {
         if (lane == 0) {
             int issued = 0;
             for (int cc = 0; cc < nch; ++cc) {
@@ -1150,7 +1138,7 @@ __global__ void __launch_bounds__(320, 1) k_dh_tc(Params p, const __grid_constan
             for (int cc = issued - 2 < 0 ? 0 : issued - 2; cc < issued; ++cc)
                 drain_wait(&full[cc & 1], (cc >> 1) & 1);
         }
-    } else if (warp == 9) {
+    } else if (warp == kEpiWarps + 1) {
         if (lane == 0) {
             const uint32_t idK = idesc_bf16(128, 64);           // dS1^T K^T
             const uint32_t idOP = idesc_bf16(128, 64, 1, 1);    // dO^T P'
@@ -1160,37 +1148,37 @@ __global__ void __launch_bounds__(320, 1) k_dh_tc(Params p, const __grid_constan
                 const int s = cc & 1;
                 char *st = stage0 + s * SL::kBytes;
                 if (!bwait(&full[s], (cc >> 1) & 1, cap, abort)) break;
-                if (!bwait(bar_sb, cc & 1, cap, abort)) break;
-                tc_fence_after();
                 const uint32_t qk = su32(st + SL::kQK), kr = qk + 8192;
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    const uint32_t a0 = su32(half ? SBl : SBh);
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t o = (kk >> 2) * 16384 + (kk & 3) * 32;
-                        mma(tD1, sdesc(a0 + o), sdesc(kr + o), idK, (half | kk) != 0);
-                    }
-                }
                 if (!isN) {
+                    // the dO term needs no state: issued as soon as the stage lands
                     const uint32_t dO = su32(st + SL::kdO), ph = su32(st + SL::kP), pl = ph + kImg;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        mma(tD1, sdesc(dO + kk * 2048, 8192), sdesc(ph + kk * 2048, 8192), idOP, 1);
+                        mma(tD1, sdesc(dO + kk * 2048, 8192), sdesc(ph + kk * 2048, 8192), idOP, kk > 0);
                         mma(tD1, sdesc(dO + kk * 2048, 8192), sdesc(pl + kk * 2048, 8192), idOP, 1);
+                    }
+                }
+                if (!bwait(bar_sb, cc & 1, cap, abort)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t o = (kk >> 2) * 16384 + (kk & 3) * 32;
+                        mma_ts(tD1, (half ? tSl : tSh) + 8 * kk, sdesc(kr + o), idK, isN ? (half | kk) != 0 : 1);
                     }
                 }
                 mma_commit(bar_m1);
                 if (!bwait(bar_ut, cc & 1, cap, abort)) break;
                 tc_fence_after();
                 {
-                    const uint32_t uh = su32(UTh), ul = su32(UTl), ah = su32(st + SL::kA), al = ah + kImg;
+                    const uint32_t ah = su32(st + SL::kA), al = ah + kImg;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        const uint32_t o = kk * 32, ob = kk * 2048;
-                        mma(tD2, sdesc(uh + o), sdesc(ah + ob, 8192), idA, kk > 0);
-                        mma(tD2, sdesc(ul + o), sdesc(ah + ob, 8192), idA, 1);
-                        mma(tD2, sdesc(uh + o), sdesc(al + ob, 8192), idA, 1);
+                        const uint32_t ob = kk * 2048;
+                        mma_ts(tD2, tUh + 8 * kk, sdesc(ah + ob, 8192), idA, kk > 0);
+                        mma_ts(tD2, tUl + 8 * kk, sdesc(ah + ob, 8192), idA, 1);
+                        mma_ts(tD2, tUh + 8 * kk, sdesc(al + ob, 8192), idA, 1);
                     }
                 }
                 mma_commit(bar_m2);
@@ -1198,10 +1186,9 @@ __global__ void __launch_bounds__(320, 1) k_dh_tc(Params p, const __grid_constan
                 tc_fence_after();
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
-                    const uint32_t a0 = su32(half ? XTl : XTh);
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
-                        mma(tS, sdesc(a0 + (kk >> 2) * 16384 + (kk & 3) * 32), sdesc(qk + kk * 2048, 16384), idQK, 1);
+                        mma_ts(tS, (half ? tXl : tXh) + 8 * kk, sdesc(qk + kk * 2048, 16384), idQK, 1);
                 }
                 mma_commit(bar_m3);
                 mma_commit(&empty[s]);
@@ -1210,14 +1197,19 @@ __global__ void __launch_bounds__(320, 1) k_dh_tc(Params p, const __grid_constan
             drain_wait(bar_drain, 0);
         }
     } else {
-        const int wg = warp >> 2;  // two epilogue warpgroups split the columns
+        // ---------------- epilogue: warps 0-15.  Warp w reads TMEM lanes
+        // 32 (w % 4) .. + 31 (thread t <-> lane t = v) and has column group
+        // cg = w / 4: state columns [32 cg, + 32) in (a), token columns
+        // [16 cg, + 16) in (c) and (c2). ----------------
+        const int cg = warp >> 2;
         const int t = tid & 127;
         const uint32_t lo = (uint32_t)((warp & 3) * 32) << 16;
-        uint32_t r[32];
-        for (int j = 2 * wg; j < 2 * wg + 2; ++j) {
+        const int sc0 = 32 * cg, tc0 = 16 * cg;
+        {
+            uint32_t r[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-                const int k = 32 * j + i;
+                const int k = sc0 + i;
                 float v0;
                 if (DM == kDhSum)
                     v0 = (isN && k == t) ? 1.f : 0.f;
@@ -1227,9 +1219,10 @@ __global__ void __launch_bounds__(320, 1) k_dh_tc(Params p, const __grid_constan
                     v0 = p.Sstart[(((size_t)sidx * p.Hv + h) * 128 + k) * 128 + t];
                 r[i] = __float_as_uint(v0);
             }
-            tmem_st32(tS + 32 * j + lo, r);
+            tmem_st32(tS + sc0 + lo, r);
+            tmem_wait_st();
         }
-        tmem_wait_st();
+        bool live = true;
         for (int cc = 0; cc < nch; ++cc) {
             const int s = cc & 1;
             char *st = stage0 + s * SL::kBytes;
@@ -1238,98 +1231,92 @@ __global__ void __launch_bounds__(320, 1) k_dh_tc(Params p, const __grid_constan
             const int c = cend - 1 - cc;
             const int len = min(kChunk, sq.len - kChunk * (c - sq.chunk0));
             const size_t ch = (size_t)c * p.Hv + h;
-            if (cc > 0 && !bwait(bar_m3, (cc - 1) & 1, cap, abort)) break;
+            if (cc > 0 && !wbwait(bar_m3, (cc - 1) & 1, cap, abort)) { live = false; break; }
             tc_fence_after();
-            if (!bwait(&full[s], (cc >> 1) & 1, cap, abort)) break;
-            const float dec = eg[63];
-            // (a)
-            for (int j = 2 * wg; j < 2 * wg + 2; ++j) {
-                tmem_ld32(tS + 32 * j + lo, r);
-                float f[32], hi[32], lw[32];
+            if (!wbwait(&full[s], (cc >> 1) & 1, cap, abort)) { live = false; break; }
+            // (a) dS1 = dS (stored for the chunk gradients) -> packed hi | lo; dS *= e^{gamma_n}
+            {
+                const float dec = eg[63];
+                uint32_t r[32];
+                tmem_ld32(tS + sc0 + lo, r);
+                float f[32];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    f[i] = __uint_as_float(r[i]);
-                    hi[i] = bf16_round(f[i]);
-                    lw[i] = f[i] - hi[i];
-                }
-                st_row32(SBh, 128, t, 32 * j, hi);
-                st_row32(SBl, 128, t, 32 * j, lw);
+                for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(r[i]);
+                uint32_t hv[16], lv[16];
+                split_pairs<16>(f, hv, lv);
+                tmem_st16(tSh + sc0 / 2 + lo, hv);
+                tmem_st16(tSl + sc0 / 2 + lo, lv);
                 if (DM == kDhFull)
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) p.dhbuf[(ch * 128 + 32 * j + i) * 128 + t] = f[i];
+                    for (int i = 0; i < 32; ++i) p.dhbuf[(ch * 128 + sc0 + i) * 128 + t] = f[i];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(f[i] * dec);
-                tmem_st32(tS + 32 * j + lo, r);
+                tmem_st32(tS + sc0 + lo, r);
+                tmem_wait_st();
             }
-            tmem_wait_st();
-            fence_async_smem();
             tc_fence_before();
-            mbar_arrive(bar_sb);
-            // (c) dUt^T[t][r] = e^{gamma_n - gamma_r} dY^T[t][r]
-            if (!bwait(bar_m1, cc & 1, cap, abort)) break;
+            warp_arrive(bar_sb, lane);
+            // (c) dUt^T[t][r] = e^{gamma_n - gamma_r} dY^T[t][r] (rows past the chunk end: 0)
+            if (!wbwait(bar_m1, cc & 1, cap, abort)) { live = false; break; }
             tc_fence_after();
-            for (int j = wg; j < wg + 1; ++j) {
-                tmem_ld32(tD1 + 32 * j + lo, r);
-                float f[32], lw[32];
+            {
+                float fe[16];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int rr = 32 * j + i;
-                    const float x = rr < len ? eL[rr] * __uint_as_float(r[i]) : 0.f;
-                    if (DM == kDhFull) p.dubuf[(ch * 64 + rr) * 128 + t] = x;
-                    f[i] = bf16_round(x);
-                    lw[i] = x - f[i];
-                }
-                st_row32(UTh, 128, t, 32 * j, f);
-                st_row32(UTl, 128, t, 32 * j, lw);
+                for (int i = 0; i < 16; ++i) fe[i] = tc0 + i < len ? eL[tc0 + i] : 0.f;
+                uint32_t r[16];
+                tmem_ld16_issue(tD1 + tc0 + lo, r);
+                tmem_wait_ld16(r);
+                float x[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) x[i] = fe[i] * __uint_as_float(r[i]);
+                uint32_t hv[8], lv[8];
+                split_pairs<8>(x, hv, lv);
+                tmem_st8(tUh + tc0 / 2 + lo, hv);
+                tmem_st8(tUl + tc0 / 2 + lo, lv);
+                if (DM == kDhFull)
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) p.dubuf[(ch * 64 + tc0 + i) * 128 + t] = x[i];
+                tmem_wait_st();
             }
-            fence_async_smem();
             tc_fence_before();
-            mbar_arrive(bar_ut);
+            warp_arrive(bar_ut, lane);
             // (c2) X^T = [scale e^{gamma_s} dO[s][t] | -b_s e^{gamma_s} dR^T[t][s]]
-            if (!bwait(bar_m2, cc & 1, cap, abort)) break;
-            tc_fence_after();
             {
                 const char *dO = st + SL::kdO + (t >> 6) * 8192;
                 const int cv = t & 63;
-                for (int j = wg; j < wg + 1; ++j) {
-                    float f[32], lw[32];
+                float xo[16], fr[16];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int s2 = 32 * j + i;
-                        const __nv_bfloat16 dv = *reinterpret_cast<const __nv_bfloat16 *>(
-                            dO + s2 * 128 + ((((cv >> 3) ^ (s2 & 7)) << 4) | ((cv & 7) << 1)));
-                        const float x = (s2 < len && !isN) ? p.scale * eg[s2] * __bfloat162float(dv) : 0.f;
-                        f[i] = bf16_round(x);
-                        lw[i] = x - f[i];
-                    }
-                    st_row32(XTh, 128, t, 32 * j, f);
-                    st_row32(XTl, 128, t, 32 * j, lw);
+                for (int i = 0; i < 16; ++i) {
+                    const int s2 = tc0 + i;
+                    const __nv_bfloat16 dv = *reinterpret_cast<const __nv_bfloat16 *>(
+                        dO + s2 * 128 + ((((cv >> 3) ^ (s2 & 7)) << 4) | ((cv & 7) << 1)));
+                    xo[i] = (s2 < len && !isN) ? p.scale * eg[s2] * __bfloat162float(dv) : 0.f;
+                    fr[i] = -bet[s2] * eg[s2];
                 }
-                for (int j = wg; j < wg + 1; ++j) {
-                    tmem_ld32(tD2 + 32 * j + lo, r);
-                    float f[32], lw[32];
+                uint32_t hv[8], lv[8];
+                split_pairs<8>(xo, hv, lv);
+                tmem_st8(tXh + tc0 / 2 + lo, hv);
+                tmem_st8(tXl + tc0 / 2 + lo, lv);
+                if (!wbwait(bar_m2, cc & 1, cap, abort)) { live = false; break; }
+                tc_fence_after();
+                uint32_t r[16];
+                tmem_ld16_issue(tD2 + tc0 + lo, r);
+                tmem_wait_ld16(r);
+                float x[16];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int s2 = 32 * j + i;
-                        const float x = -bet[s2] * eg[s2] * __uint_as_float(r[i]);
-                        f[i] = bf16_round(x);
-                        lw[i] = x - f[i];
-                    }
-                    st_row32(XTh, 128, t, 64 + 32 * j, f);
-                    st_row32(XTl, 128, t, 64 + 32 * j, lw);
-                }
+                for (int i = 0; i < 16; ++i) x[i] = fr[i] * __uint_as_float(r[i]);
+                split_pairs<8>(x, hv, lv);
+                tmem_st8(tXh + 32 + tc0 / 2 + lo, hv);
+                tmem_st8(tXl + 32 + tc0 / 2 + lo, lv);
+                tmem_wait_st();
             }
-            fence_async_smem();
             tc_fence_before();
-            mbar_arrive(bar_x);
-            tc_fence_before();
-            mbar_arrive(&empty[s]);
+            warp_arrive(bar_x, lane);
+            warp_arrive(&empty[s], lane);
         }
-        if (!*abort) {
-            if (nch > 0) bwait(bar_m3, (nch - 1) & 1, cap, abort);
+        // (a segment of an empty sequence has no chunk: its end state is its start state)
+        if (__all_sync(0xffffffffu, live && !*abort) && (nch == 0 || wbwait(bar_m3, (nch - 1) & 1, cap, abort))) {
             tc_fence_after();
-        }
-        if (!*abort) {
             float *dst = nullptr;
             size_t base = 0;
             if (DM == kDhFull && sg.idx == 0 && p.dh0) {
@@ -1339,19 +1326,19 @@ __global__ void __launch_bounds__(320, 1) k_dh_tc(Params p, const __grid_constan
                 dst = isN ? p.Mseg : p.Hseg;
                 base = ((size_t)sidx * p.Hv + h) * 128 * 128;
             }
-            if (dst)
-                for (int j = 2 * wg; j < 2 * wg + 2; ++j) {
-                    tmem_ld32(tS + 32 * j + lo, r);
+            if (dst) {
+                uint32_t r[32];
+                tmem_ld32(tS + sc0 + lo, r);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) dst[base + (size_t)(32 * j + i) * 128 + t] = __uint_as_float(r[i]);
-                }
+                for (int i = 0; i < 32; ++i) dst[base + (size_t)(sc0 + i) * 128 + t] = __uint_as_float(r[i]);
+            }
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 9) {
+    if (warp == kEpiWarps + 1) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(256));
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512));
     }
 }
 
@@ -1429,7 +1416,7 @@ int launch_dh(const char *name, const Params &p, cudaStream_t st) {
     auto kern = k_dh_tc<DM>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kDhSmem) != cudaSuccess) return 1;
     tm_begin(p.tm, name, st);
-    kern<<<dim3(p.NSEG, p.Hv, DM == kDhSum ? 2 : 1), 320, kDhSmem, st>>>(p, maps);
+    kern<<<dim3(p.NSEG, p.Hv, DM == kDhSum ? 2 : 1), kScanThreads, kDhSmem, st>>>(p, maps);
     tm_end(p.tm, st);
     return cudaGetLastError() != cudaSuccess;
 }

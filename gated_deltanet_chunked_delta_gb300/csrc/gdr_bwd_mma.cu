@@ -133,6 +133,7 @@ struct Smem {
     float gam[64], bet[64];
     float rUdU[64], rRV[64], rRKS[64], rQdq[64], rP[64], rLK[64], cL[64];
     float red[4];
+    int ticket;
 };
 // After the half loop these tiles overlay the dead half-loop buffers.
 struct Tail {
@@ -486,17 +487,57 @@ __global__ void __launch_bounds__(256, 1) k_bwd_chunk_mma(Params p) {
     wmma<8, false, false>(dk, Tl.Dl, L64, m0, S.K, L128, 64 * cb, 64);
     wmma<8, true, false>(dk, Tl.Dh, L64, m0, S.K, L128, 64 * cb, 64);
     wmma<8, true, false>(dk, Tl.Dl, L64, m0, S.K, L128, 64 * cb, 64);
+    // dq, dk summed over the G v-heads of the qk-head: every CTA of the group
+    // but the last to arrive leaves its partial (fp32) in the workspace; the
+    // last adds them in head order (so the sum does not depend on the order
+    // of arrival) and writes the bf16 result.
+    const int G = p.Hv / p.Hq;
+    if (G > 1)
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
+        for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int r = frow(m0, e), kk = fcol(64 * cb, nt, e);
-            if (r < len) {
-                const size_t off = ((size_t)(tok0 + r) * p.Hv + h) * 128 + kk;
-                p.dqp[off] = dq[nt][e];
-                p.dkp[off] = dk[nt][e];
+            for (int e = 0; e < 4; e += 2) {
+                const int r = frow(m0, e), kk = fcol(64 * cb, nt, e);
+                if (r < len) {
+                    const size_t off = ((size_t)(tok0 + r) * p.Hv + h) * 128 + kk;
+                    *reinterpret_cast<float2 *>(p.dqp + off) = make_float2(dq[nt][e], dq[nt][e + 1]);
+                    *reinterpret_cast<float2 *>(p.dkp + off) = make_float2(dk[nt][e], dk[nt][e + 1]);
+                }
             }
-        }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) S.ticket = G > 1 ? atomicAdd(&p.gcnt[(size_t)c * p.Hq + hq], 1) : 0;
+    __syncthreads();
+    if (S.ticket == G - 1) {
+        __threadfence();
+        bf16 *dqo = reinterpret_cast<bf16 *>(p.dq), *dko = reinterpret_cast<bf16 *>(p.dk);
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; e += 2) {
+                const int r = frow(m0, e), kk = fcol(64 * cb, nt, e);
+                if (r < len) {
+                    float2 sq = make_float2(0.f, 0.f), sk = make_float2(0.f, 0.f);
+                    for (int hh = hq * G; hh < hq * G + G; ++hh) {
+                        float2 a, b;
+                        if (hh == h) {
+                            a = make_float2(dq[nt][e], dq[nt][e + 1]);
+                            b = make_float2(dk[nt][e], dk[nt][e + 1]);
+                        } else {
+                            const size_t off = ((size_t)(tok0 + r) * p.Hv + hh) * 128 + kk;
+                            a = __ldcg(reinterpret_cast<const float2 *>(p.dqp + off));
+                            b = __ldcg(reinterpret_cast<const float2 *>(p.dkp + off));
+                        }
+                        sq.x += a.x; sq.y += a.y;
+                        sk.x += b.x; sk.y += b.y;
+                    }
+                    const size_t o = ((size_t)(tok0 + r) * p.Hq + hq) * 128 + kk;
+                    *reinterpret_cast<__nv_bfloat162 *>(dqo + o) = __floats2bfloat162_rn(sq.x, sq.y);
+                    *reinterpret_cast<__nv_bfloat162 *>(dko + o) = __floats2bfloat162_rn(sk.x, sk.y);
+                }
+            }
+        if (tid == 0 && G > 1) p.gcnt[(size_t)c * p.Hq + hq] = 0;  // ready for the next call
+    }
     // ---- per-row gate and beta gradients ----
     if (tid < 64) {
         const int r = tid;

@@ -40,6 +40,10 @@ constexpr int kFwd = 0, kStates = 1, kSum = 2;
 __device__ __forceinline__ uint32_t su32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
+// The first 1024-byte boundary inside the dynamic shared memory, reached by
+// pointer arithmetic on the shared array itself so that the compiler keeps
+// treating every access through it as a shared-memory access.
+__device__ __forceinline__ char *smem_align1024(char *raw) { return raw + ((1024u - (su32(raw) & 1023u)) & 1023u); }
 
 __device__ __forceinline__ void mbar_init(uint64_t *b, uint32_t n) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(n) : "memory");
@@ -294,7 +298,8 @@ __device__ __forceinline__ void st_img_half2(char *img, int row, int col0, const
 constexpr int kLd = 68;                            // fp32 row pitch of L and A (16-byte aligned rows)
 constexpr int kTLd = 52;                           // row pitch of the 16 x 48 product scratch
 constexpr int kChunkScratch = 2 * 64 * kLd * 4;    // L and A, laid over the K/Q tile once the MMA is done
-constexpr int kChunkSmem = 1024 + (kChunkScratch > 32768 ? kChunkScratch : 32768) + 16 * kTLd * 4 + 2 * 64 * 4 + 64;
+constexpr int kChunkSmem = 1024 + (kChunkScratch > 32768 ? kChunkScratch : 32768) + 16 * kTLd * 4 + 2 * 64 * 4 +
+                           4 * 64 * 4 + 64;
 
 // A[16i + r][c] for the thread's columns c = cg n .. cg n + n - 1, n = 2i:
 // T = L[16i:16i+16, 0:16i] A[0:16i, 0:16i], then A[16i:, 0:16i] = -A_ii T.
@@ -348,9 +353,9 @@ __device__ __forceinline__ void inv_row_block(float *Ls, float *As, float *Tt, i
     __syncthreads();
 }
 
-__global__ void __launch_bounds__(128, 4) k_chunk_tc(Params p, const __grid_constant__ ChunkMaps maps, int from_A) {
+__global__ void __launch_bounds__(128, 5) k_chunk_tc(Params p, const __grid_constant__ ChunkMaps maps, int from_A) {
     extern __shared__ __align__(1024) char smraw[];
-    char *sm = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+    char *sm = smem_align1024(smraw);
     constexpr int kTileRegion = kChunkScratch > 32768 ? kChunkScratch : 32768;
     char *tile = sm;                                              // [2 atoms][128 rows][128 B]: K rows 0-63, Q 64-127
     float *Ls = reinterpret_cast<float *>(sm);                    // [64][kLd], over the tile after the MMA
@@ -358,7 +363,8 @@ __global__ void __launch_bounds__(128, 4) k_chunk_tc(Params p, const __grid_cons
     float *Tt = reinterpret_cast<float *>(sm + kTileRegion);      // [16][kTLd]
     float *gam = Tt + 16 * kTLd;                                  // [64]
     float *bet = gam + 64;                                        // [64]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(bet + 64);      // tma, mma
+    float *Eb = bet + 64;                                         // [4][64] e^{gamma_16b - gamma_s}, s < 16 b
+    uint64_t *bars = reinterpret_cast<uint64_t *>(Eb + 4 * 64);   // tma, mma
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2);
     volatile int *abort = reinterpret_cast<volatile int *>(bars + 3);
 
@@ -429,10 +435,19 @@ __global__ void __launch_bounds__(128, 4) k_chunk_tc(Params p, const __grid_cons
     const float gC = gam[63];
     if (tid < 64) {
         float *aux = reinterpret_cast<float *>(reinterpret_cast<char *>(p.Aux) + ch * kAux);
-        aux[tid] = bet[tid];
-        aux[64 + tid] = __expf(gam[tid]);
-        aux[128 + tid] = __expf(gC - gam[tid]);
+        const float gt = gam[tid], bt = bet[tid];
+        aux[tid] = bt;
+        aux[64 + tid] = __expf(gt);
+        aux[128 + tid] = __expf(gC - gt);
+    } else if (!from_A) {
+        // decay factors of L against earlier 16-row blocks, factored through the
+        // block's first row: e^{gamma_r - gamma_s} = e^{gamma_r - gamma_16b}
+        // e^{gamma_16b - gamma_s}, both factors <= 1 (the gates are <= 0)
+        const int sc = tid - 64;
+#pragma unroll
+        for (int b = 1; b < 4; ++b) Eb[b * 64 + sc] = sc < 16 * b ? __expf(gam[16 * b] - gam[sc]) : 0.f;
     }
+    __syncthreads();  // the decay table
     const bool ok = bwait(&bars[1], 0, cap, abort);
     tc_fence_after();
     // rows of [K K^T ; Q K^T]: warps 0-1 -> L (unless from_A), warps 2-3 -> P'
@@ -440,22 +455,35 @@ __global__ void __launch_bounds__(128, 4) k_chunk_tc(Params p, const __grid_cons
         const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16);
         if (tid < 64) {
             if (!from_A) {
-                const int rr = tid;
+                const int rr = tid, b0 = rr & ~15;
                 const float br = bet[rr], gr = gam[rr];
-                uint32_t r0[32], r1[32];
-                tmem_ld32(ta, r0);
-                tmem_ld32(ta + 32, r1);
+                const float ar = br * __expf(gr - gam[b0]);  // b_r e^{gamma_r - gamma_16b}
+                const float *eb = Eb + (rr >> 4) * 64;
                 float *lrow = Ls + rr * kLd;
-                // each half computed in registers before its stores (a store
-                // into Ls may not pass a load of gam)
-#pragma unroll
+#pragma unroll 1
                 for (int hb = 0; hb < 2; ++hb) {
-                    const uint32_t *rv = hb ? r1 : r0;
+                    uint32_t rv[32];
+                    tmem_ld32(ta + 32 * hb, rv);
                     float x[32];
 #pragma unroll
                     for (int s = 0; s < 32; ++s) {
                         const int sc = 32 * hb + s;
-                        x[s] = sc < rr ? br * __expf(gr - gam[sc]) * __uint_as_float(rv[s]) : 0.f;
+                        x[s] = sc < b0 ? ar * eb[sc] * __uint_as_float(rv[s]) : 0.f;
+                    }
+                    if (hb == (rr >> 5)) {  // the row's own 16-column block: direct exponentials
+                        if (rr & 16) {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                const int sc = 32 * hb + 16 + j;
+                                if (sc < rr) x[16 + j] = br * __expf(gr - gam[sc]) * __uint_as_float(rv[16 + j]);
+                            }
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                const int sc = 32 * hb + j;
+                                if (sc < rr) x[j] = br * __expf(gr - gam[sc]) * __uint_as_float(rv[j]);
+                            }
+                        }
                     }
 #pragma unroll
                     for (int s = 0; s < 32; s += 4)
@@ -614,7 +642,7 @@ __host__ __device__ constexpr int scan_smem() {
 template <int MODE, typename TO>
 __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __grid_constant__ ScanMaps maps) {
     extern __shared__ __align__(1024) char smraw[];
-    char *sm = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+    char *sm = smem_align1024(smraw);
     using SL = ScanStage<MODE>;
     static_assert(scan_smem<MODE, TO>() <= 227 * 1024, "shared memory budget");
     char *stage0 = sm;
@@ -993,14 +1021,24 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
                 dst = p.final_state;
                 base = ((size_t)sg.seq * p.Hv + h) * 128 * 128;
             }
+            // the state row-major; the composed transition M transposed (row v
+            // of M^T is column v of M), the layout the tensor-core combine reads
             if (dst)
 #pragma unroll 1
                 for (int j = 0; j < kSC / 32; ++j) {
                     uint32_t r[32];
                     tmem_ld32(tS + sc0 + 32 * j + lo, r);
+                    if (isM) {
+                        float4 *d4 = reinterpret_cast<float4 *>(dst + base + (size_t)t * 128 + sc0 + 32 * j);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        dst[base + (size_t)(sc0 + 32 * j + i) * 128 + t] = __uint_as_float(r[i]);
+                        for (int i = 0; i < 8; ++i)
+                            d4[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                                __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            dst[base + (size_t)(sc0 + 32 * j + i) * 128 + t] = __uint_as_float(r[i]);
+                    }
                 }
         }
     }
@@ -1050,7 +1088,7 @@ constexpr int kDhSmem = 1024 + 2 * DhStage::kBytes + 2 * kAux + 256;
 template <int DM>
 __global__ void __launch_bounds__(kScanThreads, 1) k_dh_tc(Params p, const __grid_constant__ DhMaps maps) {
     extern __shared__ __align__(1024) char smraw[];
-    char *sm = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+    char *sm = smem_align1024(smraw);
     static_assert(kDhSmem <= 227 * 1024, "shared memory budget");
     using SL = DhStage;
     char *stage0 = sm;
@@ -1329,8 +1367,16 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_dh_tc(Params p, const __gri
             if (dst) {
                 uint32_t r[32];
                 tmem_ld32(tS + sc0 + lo, r);
+                if (isN) {  // the composed transition transposed, as in the forward summary
+                    float4 *d4 = reinterpret_cast<float4 *>(dst + base + (size_t)t * 128 + sc0);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) dst[base + (size_t)(sc0 + i) * 128 + t] = __uint_as_float(r[i]);
+                    for (int i = 0; i < 8; ++i)
+                        d4[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                            __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) dst[base + (size_t)(sc0 + i) * 128 + t] = __uint_as_float(r[i]);
+                }
             }
         }
     }
@@ -1340,6 +1386,100 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_dh_tc(Params p, const __gri
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512));
     }
+}
+
+// ---------------------------------------------------------------------------
+// Context-parallel combine of the tensor-core path (K = V = 128): one CTA per
+// (sequence, v-head, 8 state columns), sequential over the segments:
+//   forward  S_start(j+1) = M_j S_start(j) + H_j
+//   reverse  dS_end(j)    = N_{j+1} dS_end(j+1) + G_{j+1}
+// written to Sstart.  The summaries store each M (N) transposed, so the
+// step's matrix arrives as one contiguous 64 KiB bulk copy, issued one step
+// ahead into the other of two buffers; thread (row i, columns c0..c0+3)
+// then reads column i of M^T conflict-free and the state columns broadcast.
+// fp32 throughout (the combine is on the exact path of every later segment).
+// ---------------------------------------------------------------------------
+constexpr int kCombW = 8;
+constexpr int kCombSmem = 1024 + 2 * 65536 + 128 * kCombW * 4 + 256 * 16 + 64;
+
+template <bool kRev>
+__global__ void __launch_bounds__(512) k_combine_tc(Params p) {
+    extern __shared__ __align__(1024) char smraw[];
+    char *sm = smem_align1024(smraw);
+    float *Mt = reinterpret_cast<float *>(sm);          // [2][128][128]
+    float *S = Mt + 2 * 16384;                           // [128][kCombW]
+    float4 *part = reinterpret_cast<float4 *>(S + 128 * kCombW);  // [256] second-half partial sums
+    uint64_t *bars = reinterpret_cast<uint64_t *>(part + 256);
+    volatile int *abort = reinterpret_cast<volatile int *>(bars + 2);
+    const int n = blockIdx.x, h = blockIdx.y, v0 = blockIdx.z * kCombW, tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const SeqInfo sq = p.seq[n];
+    if (sq.nseg <= 1) return;
+    // thread (row i, columns c0..c0+3) of the product over l in [64 kh, 64 kh + 64)
+    const int u = tid & 255, kh = tid >> 8;
+    const int i = 32 * ((warp & 7) & 3) + lane, c0 = 4 * ((warp & 7) >> 2);
+    const long long cap = p.timeout_spins;
+    const int nsteps = sq.nseg - 1;
+    auto seg_of = [&](int step) -> size_t { return (size_t)sq.seg0 + (kRev ? (sq.nseg - 1 - step) : step); };
+    auto fetch = [&](int step) {
+        uint64_t *b = &bars[step & 1];
+        mbar_expect_tx(b, 65536);
+        bulk_g2s(Mt + (step & 1) * 16384, p.Mseg + (seg_of(step) * p.Hv + h) * 16384, 65536, b);
+    };
+    auto hrow = [&](int step) {
+        return *reinterpret_cast<const float4 *>(p.Hseg + (seg_of(step) * p.Hv + h) * 16384 + (size_t)i * 128 + v0 + c0);
+    };
+    if (kh == 0) {
+        const float *init = kRev ? p.dht : p.h0;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (init) v = *reinterpret_cast<const float4 *>(init + (((size_t)n * p.Hv + h) * 128 + i) * 128 + v0 + c0);
+        *reinterpret_cast<float4 *>(S + i * kCombW + c0) = v;
+    }
+    if (tid == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        *abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        fetch(0);
+    }
+    __syncthreads();
+    float4 hnext = kh == 0 ? hrow(0) : make_float4(0.f, 0.f, 0.f, 0.f);
+    int issued = 1, waited = 0;
+    for (int step = 0; step < nsteps; ++step) {
+        const size_t sgi = seg_of(step);
+        if (tid == 0 && step + 1 < nsteps) {  // its buffer was last read in step - 1
+            fetch(step + 1);
+            issued = step + 2;
+        }
+        float4 acc = hnext;
+        if (kh == 0 && step + 1 < nsteps) hnext = hrow(step + 1);  // in flight during this step
+        const bool ok = bwait(&bars[step & 1], (step >> 1) & 1, cap, abort);
+        if (__syncthreads_or(!ok)) break;
+        waited = step + 1;
+        const float *mt = Mt + (step & 1) * 16384 + 64 * kh * 128 + i;
+        const float *sv0 = S + 64 * kh * kCombW + c0;
+#pragma unroll 16
+        for (int l = 0; l < 64; ++l) {
+            const float m = mt[l * 128];
+            const float4 sv = *reinterpret_cast<const float4 *>(sv0 + l * kCombW);
+            acc.x = fmaf(m, sv.x, acc.x);
+            acc.y = fmaf(m, sv.y, acc.y);
+            acc.z = fmaf(m, sv.z, acc.z);
+            acc.w = fmaf(m, sv.w, acc.w);
+        }
+        if (kh == 1) part[u] = acc;
+        __syncthreads();
+        if (kh == 0) {
+            const float4 q = part[u];
+            acc.x += q.x; acc.y += q.y; acc.z += q.z; acc.w += q.w;
+            *reinterpret_cast<float4 *>(S + i * kCombW + c0) = acc;
+            float *dst = p.Sstart + ((kRev ? sgi - 1 : sgi + 1) * p.Hv + h) * 16384;
+            *reinterpret_cast<float4 *>(dst + (size_t)i * 128 + v0 + c0) = acc;
+        }
+        __syncthreads();
+    }
+    if (tid == 0)  // copies still in flight (after an abort) land before the CTA leaves
+        for (int step = waited; step < issued; ++step) drain_wait(&bars[step & 1], (step >> 1) & 1);
 }
 
 // ---------------------------------------------------------------------------
@@ -1421,6 +1561,17 @@ int launch_dh(const char *name, const Params &p, cudaStream_t st) {
     return cudaGetLastError() != cudaSuccess;
 }
 
+template <bool kRev>
+int launch_combine(const char *name, const Params &p, cudaStream_t st) {
+    if (p.N == 0) return 0;
+    auto kern = k_combine_tc<kRev>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kCombSmem) != cudaSuccess) return 1;
+    tm_begin(p.tm, name, st);
+    kern<<<dim3(p.N, p.Hv, 128 / kCombW), 512, kCombSmem, st>>>(p);
+    tm_end(p.tm, st);
+    return cudaGetLastError() != cudaSuccess;
+}
+
 }  // namespace
 
 int tc_supported(int K, int V) { return K == 128 && V == 128; }
@@ -1429,7 +1580,7 @@ int tc_fwd(const Params &p, int o_f32, int use_cp, cudaStream_t st) {
     if (launch_chunk("tc_chunk", p, 0, st)) return 1;
     if (use_cp) {
         if (launch_scan<kSum, float>("tc_cp_summary", p, st)) return 1;
-        if (simt_cp_combine(p, st)) return 1;
+        if (launch_combine<false>("tc_cp_combine", p, st)) return 1;
     }
     return o_f32 ? launch_scan<kFwd, float>("tc_scan", p, st) : launch_scan<kFwd, __nv_bfloat16>("tc_scan", p, st);
 }
@@ -1439,7 +1590,7 @@ int tc_bwd(const Params &p, int use_cp, cudaStream_t st) {
     if (launch_chunk("tc_chunk_from_A", p, 1, st)) return 1;
     if (use_cp) {
         if (launch_scan<kSum, float>("tc_cp_summary", p, st)) return 1;
-        if (simt_cp_combine(p, st)) return 1;
+        if (launch_combine<false>("tc_cp_combine", p, st)) return 1;
     }
     Params ps = p;
     ps.final_state = nullptr;
@@ -1447,12 +1598,13 @@ int tc_bwd(const Params &p, int use_cp, cudaStream_t st) {
     // a9: reverse state scan (segmented like the forward when the plan splits)
     if (use_cp) {
         if (launch_dh<kDhSum>("tc_dh_summary", p, st)) return 1;
-        if (simt_cp_combine_rev(p, st)) return 1;
+        if (launch_combine<true>("tc_cp_combine_rev", p, st)) return 1;
     }
     if (launch_dh<kDhFull>("tc_dh", p, st)) return 1;
     // a10, a11: chunk-local gradients
-    if (mma_bwd_chunk(p, st)) return 1;
-    return simt_group_sum(p, st);
+    // the qk-head sums of dq and dk happen inside the chunk kernel
+    if (cudaMemsetAsync(p.gcnt, 0, sizeof(int) * (size_t)p.NT * p.Hq, st) != cudaSuccess) return 1;
+    return mma_bwd_chunk(p, st);
 }
 
 unsigned tc_take_status(cudaStream_t st) {

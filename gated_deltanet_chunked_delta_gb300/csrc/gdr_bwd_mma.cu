@@ -143,7 +143,7 @@ struct Tail {
 };
 static_assert(sizeof(Tail) <= 2 * 128 * L64 * 2 + 8 * 64 * L64 * 2, "tail overlay");
 
-__global__ void __launch_bounds__(256, 1) k_bwd_chunk_mma(Params p) {
+__global__ void __launch_bounds__(512, 1) k_bwd_chunk_mma(Params p) {
     extern __shared__ __align__(16) char smraw[];
     Smem &S = *reinterpret_cast<Smem *>(smraw);
     Tail &Tl = *reinterpret_cast<Tail *>(&S.S0h[0]);
@@ -160,11 +160,11 @@ __global__ void __launch_bounds__(256, 1) k_bwd_chunk_mma(Params p) {
     // ---- setup: K, A, gates ----
     {
         // K: 64 rows x 16 vectors of 8; A: 64 rows x 16 float4 (identity rows past the chunk end)
-        uint4 kv[4];
-        float4 av[4];
+        uint4 kv[2];
+        float4 av[2];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int e = tid + 256 * u, r = e >> 4, c8 = (e & 15) * 8;
+        for (int u = 0; u < 2; ++u) {
+            const int e = tid + 512 * u, r = e >> 4, c8 = (e & 15) * 8;
             kv[u] = ld8(kin + ((size_t)(tok0 + r) * p.Hq + hq) * 128 + c8, r < len);
             const int c4 = (e & 15) * 4;
             if (r < len)
@@ -173,8 +173,8 @@ __global__ void __launch_bounds__(256, 1) k_bwd_chunk_mma(Params p) {
                 av[u] = make_float4(r == c4, r == c4 + 1, r == c4 + 2, r == c4 + 3);
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int e = tid + 256 * u, r = e >> 4;
+        for (int u = 0; u < 2; ++u) {
+            const int e = tid + 512 * u, r = e >> 4;
             *reinterpret_cast<uint4 *>(&S.K[r * L128 + (e & 15) * 8]) = kv[u];
             split4(av[u], &S.Ah[r * L64 + (e & 15) * 4], &S.Al[r * L64 + (e & 15) * 4]);
         }
@@ -202,10 +202,10 @@ __global__ void __launch_bounds__(256, 1) k_bwd_chunk_mma(Params p) {
     __syncthreads();
     const float gC = S.gam[63];
 
-    // warp tiling: 64 rows = 4 row blocks of 16; columns split in two
+    // warp tiling: 64 rows = 4 row blocks of 16; columns split in four
     const int m0 = 16 * (warp & 3);
     const int cb = warp >> 2;
-    float dq[8][4], dk[8][4], dP[4][4], dA[4][4];
+    float dq[4][4], dk[4][4], dP[2][4], dA[2][4];
     zero(dq);
     zero(dk);
     zero(dP);
@@ -220,70 +220,70 @@ __global__ void __launch_bounds__(256, 1) k_bwd_chunk_mma(Params p) {
         __syncthreads();
         {
             // S0 half: 128 rows x 16 float4; V, dO halves: 64 rows x 8 vectors; dUt half: 64 x 16 float4
-            float4 sv[8], uv[4];
-            uint4 vv8[2], dv8[2];
+            float4 sv[4], uv[2];
+            uint4 vv8[1], dv8[1];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int e = tid + 256 * u, kk = e >> 4, c4 = (e & 15) * 4;
+            for (int u = 0; u < 4; ++u) {
+                const int e = tid + 512 * u, kk = e >> 4, c4 = (e & 15) * 4;
                 sv[u] = *reinterpret_cast<const float4 *>(S0g + kk * 128 + v0 + c4);
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int e = tid + 256 * u, r = e >> 4, c4 = (e & 15) * 4;
+            for (int u = 0; u < 2; ++u) {
+                const int e = tid + 512 * u, r = e >> 4, c4 = (e & 15) * 4;
                 uv[u] = *reinterpret_cast<const float4 *>(dUg + r * 128 + v0 + c4);
             }
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int e = tid + 256 * u, r = e >> 3, c8 = (e & 7) * 8;
+            for (int u = 0; u < 1; ++u) {
+                const int e = tid + 512 * u, r = e >> 3, c8 = (e & 7) * 8;
                 const size_t off = ((size_t)(tok0 + r) * p.Hv + h) * 128 + v0 + c8;
                 vv8[u] = ld8(vin + off, r < len);
                 dv8[u] = ld8(din + off, r < len);
             }
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int e = tid + 256 * u, kk = e >> 4, c4 = (e & 15) * 4;
+            for (int u = 0; u < 4; ++u) {
+                const int e = tid + 512 * u, kk = e >> 4, c4 = (e & 15) * 4;
                 split4(sv[u], &S.S0h[kk * L64 + c4], &S.S0l[kk * L64 + c4]);
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int e = tid + 256 * u, r = e >> 4, c4 = (e & 15) * 4;
+            for (int u = 0; u < 2; ++u) {
+                const int e = tid + 512 * u, r = e >> 4, c4 = (e & 15) * 4;
                 split4(uv[u], &S.dUh[r * L64 + c4], &S.dUl[r * L64 + c4]);
             }
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int e = tid + 256 * u, r = e >> 3, c8 = (e & 7) * 8;
+            for (int u = 0; u < 1; ++u) {
+                const int e = tid + 512 * u, r = e >> 3, c8 = (e & 7) * 8;
                 *reinterpret_cast<uint4 *>(&S.V[r * L64 + c8]) = vv8[u];
                 *reinterpret_cast<uint4 *>(&S.dO[r * L64 + c8]) = dv8[u];
             }
         }
         __syncthreads();
         // (1) KS = K S0 (this half), kept in registers; R = b (V - e^gamma KS)
-        float ks[4][4];
+        float ks[2][4];
         zero(ks);
-        wmma<4, false, false>(ks, S.K, L128, m0, S.S0h, L64, 32 * cb, 128);
-        wmma<4, false, false>(ks, S.K, L128, m0, S.S0l, L64, 32 * cb, 128);
+        wmma<2, false, false>(ks, S.K, L128, m0, S.S0h, L64, 16 * cb, 128);
+        wmma<2, false, false>(ks, S.K, L128, m0, S.S0l, L64, 16 * cb, 128);
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
+        for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int r = frow(m0, e), vv = fcol(32 * cb, nt, e);
+                const int r = frow(m0, e), vv = fcol(16 * cb, nt, e);
                 const float x = S.bet[r] * (__bfloat162float(S.V[r * L64 + vv]) - __expf(S.gam[r]) * ks[nt][e]);
                 split(x, S.Rh[r * L64 + vv], S.Rl[r * L64 + vv]);
             }
         __syncthreads();
         // (2) Ut = A R;  rowdot(dUt, Ut);  Y = e^{gamma_n - gamma} Ut
         {
-            float u[4][4];
+            float u[2][4];
             zero(u);
-            wmma<4, false, false>(u, S.Ah, L64, m0, S.Rh, L64, 32 * cb, 64);
-            wmma<4, false, false>(u, S.Al, L64, m0, S.Rh, L64, 32 * cb, 64);
-            wmma<4, false, false>(u, S.Ah, L64, m0, S.Rl, L64, 32 * cb, 64);
+            wmma<2, false, false>(u, S.Ah, L64, m0, S.Rh, L64, 16 * cb, 64);
+            wmma<2, false, false>(u, S.Al, L64, m0, S.Rh, L64, 16 * cb, 64);
+            wmma<2, false, false>(u, S.Ah, L64, m0, S.Rl, L64, 16 * cb, 64);
             float rs[2] = {0.f, 0.f};
 #pragma unroll
-            for (int nt = 0; nt < 4; ++nt)
+            for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const int r = frow(m0, e), vv = fcol(32 * cb, nt, e);
+                    const int r = frow(m0, e), vv = fcol(16 * cb, nt, e);
                     const float du = __bfloat162float(S.dUh[r * L64 + vv]) + __bfloat162float(S.dUl[r * L64 + vv]);
                     rs[e >> 1] += du * u[nt][e];
                     split(__expf(gC - S.gam[r]) * u[nt][e], S.Yh[r * L64 + vv], S.Yl[r * L64 + vv]);
@@ -297,27 +297,27 @@ __global__ void __launch_bounds__(256, 1) k_bwd_chunk_mma(Params p) {
         }
         __syncthreads();
         // (3) dA += dUt R^T;  (4) dP' += dO Y^T;  (5) dQraw += dO S0^T
-        wmma<4, false, true>(dA, S.dUh, L64, m0, S.Rh, L64, 32 * cb, 64);
-        wmma<4, false, true>(dA, S.dUl, L64, m0, S.Rh, L64, 32 * cb, 64);
-        wmma<4, false, true>(dA, S.dUh, L64, m0, S.Rl, L64, 32 * cb, 64);
-        wmma<4, false, true>(dP, S.dO, L64, m0, S.Yh, L64, 32 * cb, 64);
-        wmma<4, false, true>(dP, S.dO, L64, m0, S.Yl, L64, 32 * cb, 64);
-        wmma<8, false, true>(dq, S.dO, L64, m0, S.S0h, L64, 64 * cb, 64);
-        wmma<8, false, true>(dq, S.dO, L64, m0, S.S0l, L64, 64 * cb, 64);
+        wmma<2, false, true>(dA, S.dUh, L64, m0, S.Rh, L64, 16 * cb, 64);
+        wmma<2, false, true>(dA, S.dUl, L64, m0, S.Rh, L64, 16 * cb, 64);
+        wmma<2, false, true>(dA, S.dUh, L64, m0, S.Rl, L64, 16 * cb, 64);
+        wmma<2, false, true>(dP, S.dO, L64, m0, S.Yh, L64, 16 * cb, 64);
+        wmma<2, false, true>(dP, S.dO, L64, m0, S.Yl, L64, 16 * cb, 64);
+        wmma<4, false, true>(dq, S.dO, L64, m0, S.S0h, L64, 32 * cb, 64);
+        wmma<4, false, true>(dq, S.dO, L64, m0, S.S0l, L64, 32 * cb, 64);
         // (6) dR = A^T dUt;  dv = b dR;  rowdot(dR, V), rowdot(dR, KS); dKS into the R buffers
-        float dr[4][4];
+        float dr[2][4];
         zero(dr);
-        wmma<4, true, false>(dr, S.Ah, L64, m0, S.dUh, L64, 32 * cb, 64);
-        wmma<4, true, false>(dr, S.Al, L64, m0, S.dUh, L64, 32 * cb, 64);
-        wmma<4, true, false>(dr, S.Ah, L64, m0, S.dUl, L64, 32 * cb, 64);
+        wmma<2, true, false>(dr, S.Ah, L64, m0, S.dUh, L64, 16 * cb, 64);
+        wmma<2, true, false>(dr, S.Al, L64, m0, S.dUh, L64, 16 * cb, 64);
+        wmma<2, true, false>(dr, S.Ah, L64, m0, S.dUl, L64, 16 * cb, 64);
         {
             float rv[2] = {0.f, 0.f}, rk[2] = {0.f, 0.f};
             bf16 *dv = reinterpret_cast<bf16 *>(p.dv);
 #pragma unroll
-            for (int nt = 0; nt < 4; ++nt)
+            for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const int r = frow(m0, e), vv = fcol(32 * cb, nt, e);
+                    const int r = frow(m0, e), vv = fcol(16 * cb, nt, e);
                     rv[e >> 1] += dr[nt][e] * __bfloat162float(S.V[r * L64 + vv]);
                     rk[e >> 1] += dr[nt][e] * ks[nt][e];
                     if (r < len) dv[((size_t)(tok0 + r) * p.Hv + h) * 128 + v0 + vv] = __float2bfloat16_rn(S.bet[r] * dr[nt][e]);
@@ -336,51 +336,51 @@ __global__ void __launch_bounds__(256, 1) k_bwd_chunk_mma(Params p) {
         }
         __syncthreads();  // every warp is done reading R
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
+        for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int r = frow(m0, e), vv = fcol(32 * cb, nt, e);
+                const int r = frow(m0, e), vv = fcol(16 * cb, nt, e);
                 split(-S.bet[r] * __expf(S.gam[r]) * dr[nt][e], S.Rh[r * L64 + vv], S.Rl[r * L64 + vv]);
             }
         __syncthreads();
         // (7) dK += dKS S0^T
-        wmma<8, false, true>(dk, S.Rh, L64, m0, S.S0h, L64, 64 * cb, 64);
-        wmma<8, false, true>(dk, S.Rl, L64, m0, S.S0h, L64, 64 * cb, 64);
-        wmma<8, false, true>(dk, S.Rh, L64, m0, S.S0l, L64, 64 * cb, 64);
+        wmma<4, false, true>(dk, S.Rh, L64, m0, S.S0h, L64, 32 * cb, 64);
+        wmma<4, false, true>(dk, S.Rl, L64, m0, S.S0h, L64, 32 * cb, 64);
+        wmma<4, false, true>(dk, S.Rh, L64, m0, S.S0l, L64, 32 * cb, 64);
         __syncthreads();  // S0 no longer needed: load dS1 into its buffers
         {
-            float4 dv[8], sv[8];
+            float4 dv[4], sv[4];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int e = tid + 256 * u, kk = e >> 4, c4 = (e & 15) * 4;
+            for (int u = 0; u < 4; ++u) {
+                const int e = tid + 512 * u, kk = e >> 4, c4 = (e & 15) * 4;
                 dv[u] = *reinterpret_cast<const float4 *>(dS1g + kk * 128 + v0 + c4);
                 sv[u] = *reinterpret_cast<const float4 *>(S0g + kk * 128 + v0 + c4);
             }
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int e = tid + 256 * u, kk = e >> 4, c4 = (e & 15) * 4;
+            for (int u = 0; u < 4; ++u) {
+                const int e = tid + 512 * u, kk = e >> 4, c4 = (e & 15) * 4;
                 s0ds1 += dv[u].x * sv[u].x + dv[u].y * sv[u].y + dv[u].z * sv[u].z + dv[u].w * sv[u].w;
                 split4(dv[u], &S.S0h[kk * L64 + c4], &S.S0l[kk * L64 + c4]);
             }
         }
         __syncthreads();
         // (8) dK += Y dS1^T
-        wmma<8, false, true>(dk, S.Yh, L64, m0, S.S0h, L64, 64 * cb, 64);
-        wmma<8, false, true>(dk, S.Yl, L64, m0, S.S0h, L64, 64 * cb, 64);
-        wmma<8, false, true>(dk, S.Yh, L64, m0, S.S0l, L64, 64 * cb, 64);
+        wmma<4, false, true>(dk, S.Yh, L64, m0, S.S0h, L64, 32 * cb, 64);
+        wmma<4, false, true>(dk, S.Yl, L64, m0, S.S0h, L64, 32 * cb, 64);
+        wmma<4, false, true>(dk, S.Yh, L64, m0, S.S0l, L64, 32 * cb, 64);
     }
     __syncthreads();
     // ---- after the halves: Q, QK, KK, dP'', dA -> X -> dL, assembly ----
     {
-        uint4 qv[4];
+        uint4 qv[2];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int e = tid + 256 * u, r = e >> 4, c8 = (e & 15) * 8;
+        for (int u = 0; u < 2; ++u) {
+            const int e = tid + 512 * u, r = e >> 4, c8 = (e & 15) * 8;
             qv[u] = ld8(qin + ((size_t)(tok0 + r) * p.Hq + hq) * 128 + c8, r < len);
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int e = tid + 256 * u, r = e >> 4;
+        for (int u = 0; u < 2; ++u) {
+            const int e = tid + 512 * u, r = e >> 4;
             *reinterpret_cast<uint4 *>(&S.Qb[r * L128 + (e & 15) * 8]) = qv[u];
         }
     }
@@ -390,20 +390,20 @@ __global__ void __launch_bounds__(256, 1) k_bwd_chunk_mma(Params p) {
         if ((tid & 31) == 0) atomicAdd(&S.red[0], w);
     }
     // QK, KK for this warp's tile (kept in registers for the row sums below)
-    float qk[4][4], kk2[4][4];
+    float qk[2][4], kk2[2][4];
     zero(qk);
     zero(kk2);
     __syncthreads();  // Q is in place
-    wmma<4, false, true>(qk, S.Qb, L128, m0, S.K, L128, 32 * cb, 128);
-    wmma<4, false, true>(kk2, S.K, L128, m0, S.K, L128, 32 * cb, 128);
+    wmma<2, false, true>(qk, S.Qb, L128, m0, S.K, L128, 16 * cb, 128);
+    wmma<2, false, true>(kk2, S.K, L128, m0, S.K, L128, 16 * cb, 128);
     {
         // dP'' = dP' o scale e^{gamma_r - gamma_n}, causal, inside the chunk; rowsum(dP'' o QK)
         float rp[2] = {0.f, 0.f};
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
+        for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int r = frow(m0, e), s2 = fcol(32 * cb, nt, e);
+                const int r = frow(m0, e), s2 = fcol(16 * cb, nt, e);
                 const float x = (s2 <= r && r < len) ? dP[nt][e] * p.scale * __expf(S.gam[r] - gC) : 0.f;
                 rp[e >> 1] += x * qk[nt][e];
                 split(x, Tl.Ph[r * L64 + s2], Tl.Pl[r * L64 + s2]);
@@ -412,10 +412,10 @@ __global__ void __launch_bounds__(256, 1) k_bwd_chunk_mma(Params p) {
         // rowdot(Q, dQraw)
         float rq[2] = {0.f, 0.f};
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
+        for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int r = frow(m0, e), kk = fcol(64 * cb, nt, e);
+                const int r = frow(m0, e), kk = fcol(32 * cb, nt, e);
                 rq[e >> 1] += dq[nt][e] * __bfloat162float(S.Qb[r * L128 + kk]);
             }
 #pragma unroll
@@ -432,34 +432,34 @@ __global__ void __launch_bounds__(256, 1) k_bwd_chunk_mma(Params p) {
     }
     __syncthreads();
     {
-        float x[4][4];  // X = A^T dA
+        float x[2][4];  // X = A^T dA
         zero(x);
-        wmma<4, true, false>(x, S.Ah, L64, m0, Tl.Dh, L64, 32 * cb, 64);
-        wmma<4, true, false>(x, S.Al, L64, m0, Tl.Dh, L64, 32 * cb, 64);
-        wmma<4, true, false>(x, S.Ah, L64, m0, Tl.Dl, L64, 32 * cb, 64);
+        wmma<2, true, false>(x, S.Ah, L64, m0, Tl.Dh, L64, 16 * cb, 64);
+        wmma<2, true, false>(x, S.Al, L64, m0, Tl.Dh, L64, 16 * cb, 64);
+        wmma<2, true, false>(x, S.Ah, L64, m0, Tl.Dl, L64, 16 * cb, 64);
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
+        for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int r = frow(m0, e), s2 = fcol(32 * cb, nt, e);
+                const int r = frow(m0, e), s2 = fcol(16 * cb, nt, e);
                 split(x[nt][e], Tl.Xh[r * L64 + s2], Tl.Xl[r * L64 + s2]);
             }
     }
     __syncthreads();
     {
         // dL = -strict_tril(X A^T) inside the chunk;  MM = dL o b_r e^{gamma_r - gamma_s}
-        float dl[4][4];
+        float dl[2][4];
         zero(dl);
-        wmma<4, false, true>(dl, Tl.Xh, L64, m0, S.Ah, L64, 32 * cb, 64);
-        wmma<4, false, true>(dl, Tl.Xl, L64, m0, S.Ah, L64, 32 * cb, 64);
-        wmma<4, false, true>(dl, Tl.Xh, L64, m0, S.Al, L64, 32 * cb, 64);
+        wmma<2, false, true>(dl, Tl.Xh, L64, m0, S.Ah, L64, 16 * cb, 64);
+        wmma<2, false, true>(dl, Tl.Xl, L64, m0, S.Ah, L64, 16 * cb, 64);
+        wmma<2, false, true>(dl, Tl.Xh, L64, m0, S.Al, L64, 16 * cb, 64);
         __syncthreads();  // every warp is done reading dA from Dh / Dl
         float rl[2] = {0.f, 0.f};
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
+        for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int r = frow(m0, e), s2 = fcol(32 * cb, nt, e);
+                const int r = frow(m0, e), s2 = fcol(16 * cb, nt, e);
                 const float v = (s2 < r && r < len) ? -dl[nt][e] : 0.f;
                 const float ek = __expf(S.gam[r] - S.gam[s2]) * kk2[nt][e];
                 rl[e >> 1] += v * ek;                       // sum_s dL e^{..} KK over the row
@@ -476,17 +476,17 @@ __global__ void __launch_bounds__(256, 1) k_bwd_chunk_mma(Params p) {
     __syncthreads();
     // dq = scale e^gamma dQraw + dP'' K;  dk += dP''^T Q + MM K + MM^T K
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
+    for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) dq[nt][e] *= p.scale * __expf(S.gam[frow(m0, e)]);
-    wmma<8, false, false>(dq, Tl.Ph, L64, m0, S.K, L128, 64 * cb, 64);
-    wmma<8, false, false>(dq, Tl.Pl, L64, m0, S.K, L128, 64 * cb, 64);
-    wmma<8, true, false>(dk, Tl.Ph, L64, m0, S.Qb, L128, 64 * cb, 64);
-    wmma<8, true, false>(dk, Tl.Pl, L64, m0, S.Qb, L128, 64 * cb, 64);
-    wmma<8, false, false>(dk, Tl.Dh, L64, m0, S.K, L128, 64 * cb, 64);
-    wmma<8, false, false>(dk, Tl.Dl, L64, m0, S.K, L128, 64 * cb, 64);
-    wmma<8, true, false>(dk, Tl.Dh, L64, m0, S.K, L128, 64 * cb, 64);
-    wmma<8, true, false>(dk, Tl.Dl, L64, m0, S.K, L128, 64 * cb, 64);
+    wmma<4, false, false>(dq, Tl.Ph, L64, m0, S.K, L128, 32 * cb, 64);
+    wmma<4, false, false>(dq, Tl.Pl, L64, m0, S.K, L128, 32 * cb, 64);
+    wmma<4, true, false>(dk, Tl.Ph, L64, m0, S.Qb, L128, 32 * cb, 64);
+    wmma<4, true, false>(dk, Tl.Pl, L64, m0, S.Qb, L128, 32 * cb, 64);
+    wmma<4, false, false>(dk, Tl.Dh, L64, m0, S.K, L128, 32 * cb, 64);
+    wmma<4, false, false>(dk, Tl.Dl, L64, m0, S.K, L128, 32 * cb, 64);
+    wmma<4, true, false>(dk, Tl.Dh, L64, m0, S.K, L128, 32 * cb, 64);
+    wmma<4, true, false>(dk, Tl.Dl, L64, m0, S.K, L128, 32 * cb, 64);
     // dq, dk summed over the G v-heads of the qk-head: every CTA of the group
     // but the last to arrive leaves its partial (fp32) in the workspace; the
     // last adds them in head order (so the sum does not depend on the order
@@ -494,10 +494,10 @@ __global__ void __launch_bounds__(256, 1) k_bwd_chunk_mma(Params p) {
     const int G = p.Hv / p.Hq;
     if (G > 1)
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
+        for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; e += 2) {
-                const int r = frow(m0, e), kk = fcol(64 * cb, nt, e);
+                const int r = frow(m0, e), kk = fcol(32 * cb, nt, e);
                 if (r < len) {
                     const size_t off = ((size_t)(tok0 + r) * p.Hv + h) * 128 + kk;
                     *reinterpret_cast<float2 *>(p.dqp + off) = make_float2(dq[nt][e], dq[nt][e + 1]);
@@ -512,10 +512,10 @@ __global__ void __launch_bounds__(256, 1) k_bwd_chunk_mma(Params p) {
         __threadfence();
         bf16 *dqo = reinterpret_cast<bf16 *>(p.dq), *dko = reinterpret_cast<bf16 *>(p.dk);
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
+        for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; e += 2) {
-                const int r = frow(m0, e), kk = fcol(64 * cb, nt, e);
+                const int r = frow(m0, e), kk = fcol(32 * cb, nt, e);
                 if (r < len) {
                     float2 sq = make_float2(0.f, 0.f), sk = make_float2(0.f, 0.f);
                     for (int hh = hq * G; hh < hq * G + G; ++hh) {
@@ -570,7 +570,7 @@ int mma_bwd_chunk(const Params &p, cudaStream_t st) {
     if (cudaFuncSetAttribute(k_bwd_chunk_mma, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return 1;
     tm_begin(p.tm, "mma_bwd_chunk", st);
-    k_bwd_chunk_mma<<<dim3(p.NT, p.Hv), 256, smem, st>>>(p);
+    k_bwd_chunk_mma<<<dim3(p.NT, p.Hv), 512, smem, st>>>(p);
     tm_end(p.tm, st);
     return cudaGetLastError() != cudaSuccess;
 }

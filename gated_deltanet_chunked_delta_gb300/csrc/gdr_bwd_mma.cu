@@ -349,17 +349,22 @@ __global__ void __launch_bounds__(512, 1) k_bwd_chunk_mma(Params p) {
         wmma<4, false, true>(dk, S.Rh, L64, m0, S.S0l, L64, 32 * cb, 64);
         __syncthreads();  // S0 no longer needed: load dS1 into its buffers
         {
-            float4 dv[4], sv[4];
+            // <dS1, S0> for dg from the S0 terms in shared memory (hi + lo), each
+            // thread reading the elements it then overwrites with dS1
+            float4 dv[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int e = tid + 512 * u, kk = e >> 4, c4 = (e & 15) * 4;
                 dv[u] = *reinterpret_cast<const float4 *>(dS1g + kk * 128 + v0 + c4);
-                sv[u] = *reinterpret_cast<const float4 *>(S0g + kk * 128 + v0 + c4);
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int e = tid + 512 * u, kk = e >> 4, c4 = (e & 15) * 4;
-                s0ds1 += dv[u].x * sv[u].x + dv[u].y * sv[u].y + dv[u].z * sv[u].z + dv[u].w * sv[u].w;
+                const bf16 *hh = &S.S0h[kk * L64 + c4], *ll = &S.S0l[kk * L64 + c4];
+                float sv[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) sv[q] = __bfloat162float(hh[q]) + __bfloat162float(ll[q]);
+                s0ds1 += dv[u].x * sv[0] + dv[u].y * sv[1] + dv[u].z * sv[2] + dv[u].w * sv[3];
                 split4(dv[u], &S.S0h[kk * L64 + c4], &S.S0l[kk * L64 + c4]);
             }
         }

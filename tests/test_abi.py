@@ -113,3 +113,11 @@ def test_binding_refuses_cpu_tensors(lib):
     q = torch.zeros(1, 64, 1, 64)
     with pytest.raises(gdr.GdrError):
         gdr.gdr_fwd(q, q, q, torch.zeros(1, 64, 1), torch.zeros(1, 64, 1))
+
+
+def test_high_level_call_refuses_cpu_tensors(lib):
+    # no CPU fallback behind the differentiable call either
+    import torch
+    q = torch.zeros(1, 64, 1, 64, requires_grad=True)
+    with pytest.raises(gdr.GdrError):
+        gdr.chunk_gated_delta_rule(q, q, q, torch.zeros(1, 64, 1), torch.zeros(1, 64, 1), output_final_state=True)

@@ -43,7 +43,7 @@ class gdr_opts(ctypes.Structure):
     _fields_ = [("cp_segments", ctypes.c_int), ("path", ctypes.c_int), ("debug_checks", ctypes.c_int),
                 ("timeout_spins", ctypes.c_longlong), ("events", ctypes.POINTER(ctypes.c_void_p)),
                 ("names", ctypes.POINTER(ctypes.c_char_p)), ("max_events", ctypes.c_int),
-                ("n_launched", ctypes.POINTER(ctypes.c_int))]
+                ("n_launched", ctypes.POINTER(ctypes.c_int)), ("cp_warmup", ctypes.c_int)]
 
 
 class KernelTimer:
@@ -171,8 +171,10 @@ class Problem:
         return int(n)
 
 
-def make_opts(cp_segments=0, path=GDR_PATH_AUTO, debug_checks=0, timeout_spins=0, timer=None) -> gdr_opts:
-    o = gdr_opts(int(cp_segments), int(path), int(debug_checks), int(timeout_spins), None, None, 0, None)
+def make_opts(cp_segments=0, path=GDR_PATH_AUTO, debug_checks=0, timeout_spins=0, timer=None,
+              cp_warmup=0) -> gdr_opts:
+    o = gdr_opts(int(cp_segments), int(path), int(debug_checks), int(timeout_spins), None, None, 0, None,
+                 int(cp_warmup))
     return timer.attach(o) if timer is not None else o
 
 
@@ -209,7 +211,7 @@ def _stream(stream):
 
 def gdr_fwd(q, k, v, g, beta, scale=None, h0=None, cu_seqlens=None, cu_seqlens_host=None, *, o_dtype=None,
             output_final_state=True, want_A=True, want_h=False, cp_segments=0, path=GDR_PATH_AUTO,
-            debug_checks=0, timeout_spins=0, workspace=None, out=None, stream=None, timer=None):
+            debug_checks=0, timeout_spins=0, workspace=None, out=None, stream=None, timer=None, cp_warmup=0):
     """Forward.  Returns dict(o, final_state, A, h) (entries None when not requested).
 
     ``out`` may hold preallocated output tensors under the same keys."""
@@ -218,7 +220,7 @@ def gdr_fwd(q, k, v, g, beta, scale=None, h0=None, cu_seqlens=None, cu_seqlens_h
     prob = Problem(q, v, cu_seqlens, cu_seqlens_host)
     if scale is None:
         scale = prob.K ** -0.5
-    opts = make_opts(cp_segments, path, debug_checks, timeout_spins, timer=timer)
+    opts = make_opts(cp_segments, path, debug_checks, timeout_spins, timer=timer, cp_warmup=cp_warmup)
     out = dict(out or {})
     dev = q.device
     if out.get("o") is None:
@@ -244,14 +246,14 @@ def gdr_fwd(q, k, v, g, beta, scale=None, h0=None, cu_seqlens=None, cu_seqlens_h
 
 def gdr_bwd(q, k, v, g, beta, A, do, dht=None, scale=None, h0=None, cu_seqlens=None, cu_seqlens_host=None, *,
             want_dh0=True, cp_segments=0, path=GDR_PATH_AUTO, debug_checks=0, timeout_spins=0, workspace=None,
-            out=None, stream=None, timer=None):
+            out=None, stream=None, timer=None, cp_warmup=0):
     """Backward.  Returns dict(dq, dk, dv, dbeta, dg, dh0)."""
     _check_dev(q, k, v, g, beta, A, do, dht, h0, cu_seqlens)
     lib = load()
     prob = Problem(q, v, cu_seqlens, cu_seqlens_host)
     if scale is None:
         scale = prob.K ** -0.5
-    opts = make_opts(cp_segments, path, debug_checks, timeout_spins, timer=timer)
+    opts = make_opts(cp_segments, path, debug_checks, timeout_spins, timer=timer, cp_warmup=cp_warmup)
     out = dict(out or {})
     dev = q.device
     for key, like in (("dq", q), ("dk", k), ("dv", v)):

@@ -156,7 +156,7 @@ int make_plan(const gdr_shape *s, const gdr_opts *o, int want_path, int in_f32, 
 size_t al(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Layout {
-    size_t seq, chunk, seg, gam, W, U, P, Hseg, Mseg, Sstart, hbuf, dhbuf, dubuf, dqp, dkp, gcnt;
+    size_t seq, chunk, seg, gam, W, U, P, Hseg, Mseg, Sstart, hbuf, dhbuf, dubuf, dqp, dkp, gcnt, warm;
     size_t Aimg, Pimg, Aux;
     bool f32_tiles, bf16_tiles;
     size_t total;
@@ -185,8 +185,9 @@ Layout layout(const gdr_shape *s, const Plan &pl, bool bwd) {
         L.Hseg = take(4 * NS * Hv * K * V);
         L.Mseg = take(4 * NS * Hv * K * K);
         L.Sstart = take(4 * NS * Hv * K * V);
+        L.warm = L.bf16_tiles ? take(4 * (size_t)NS * Hv) : 0;
     } else {
-        L.Hseg = L.Mseg = L.Sstart = 0;
+        L.Hseg = L.Mseg = L.Sstart = L.warm = 0;
     }
     if (bwd) {
         L.hbuf = take(4 * NT * Hv * K * V);
@@ -279,6 +280,12 @@ int fill_params(const gdr_shape *s, const Plan &pl, const Layout &L, void *ws, P
     p->dqp = F(L.dqp, L.dqp != 0);
     p->dkp = F(L.dkp, L.dkp != 0);
     p->gcnt = L.gcnt ? reinterpret_cast<int *>(w + L.gcnt) : nullptr;
+    p->warm = L.warm ? reinterpret_cast<int *>(w + L.warm) : nullptr;
+    // warm-up starts of CP segments: 0 -> 8 chunks when segments are at least
+    // four windows long (shorter ones would scan a large share of extra
+    // chunks), -1 -> off, n -> n
+    const int req = !o ? 0 : o->cp_warmup;
+    p->cp_warmup = !p->warm ? 0 : req < 0 ? 0 : req > 0 ? req : (pl.seg_len >= 4 * 8 ? 8 : 0);
     p->debug = o ? o->debug_checks : 0;
     p->timeout_spins = (o && o->timeout_spins > 0) ? o->timeout_spins : (1LL << 22);
     return GDR_OK;

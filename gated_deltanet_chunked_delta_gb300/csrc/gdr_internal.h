@@ -85,6 +85,8 @@ struct Params {
     float *dubuf;   // [NT,Hv,64,V]  (backward: gradient of the chunk pseudo-values)
     float *dqp, *dkp;  // [Ttot,Hv,K] per-v-head partial dq, dk
     int *gcnt;         // [NT,Hq] arrivals of the v-heads of a qk-head at their chunk (tensor-core backward)
+    int cp_warmup;     // warm-up chunks of a segment start (0: the exact split only)
+    int *warm;         // [NSEG,Hv] 1: the segment's warm-up start passes its bound (set on the device)
     // tensor-core path chunk tiles (bf16 shared-memory images, hi and lo terms, 16 KiB each)
     void *Aimg;     // [NT,Hv] x A
     void *Pimg;     // [NT,Hv] x P' = scale diag(e^{gamma - gamma_n}) (Q K^T o tril_incl)

@@ -240,6 +240,14 @@ __device__ __forceinline__ void split_pairs(const float *x, uint32_t *hv, uint32
 
 
 
+// The v-head takes warm-up starts only if every segment of the sequence passes.
+__device__ __forceinline__ bool head_warm(const Params &p, const SeqInfo &sq, int h) {
+    if (!p.warm || p.cp_warmup <= 0) return false;
+    for (int j = 0; j < sq.nseg; ++j)
+        if (!p.warm[(size_t)(sq.seg0 + j) * p.Hv + h]) return false;
+    return true;
+}
+
 // ---------------------------------------------------------------------------
 // chunk-tile images kept in the workspace (bf16, byte-for-byte the shared-
 // memory image the scan's MMAs read, so the scan fetches them with plain bulk
@@ -669,7 +677,14 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
     const SegInfo sg = p.seg[sidx];
     const SeqInfo sq = p.seq[sg.seq];
     const int hq = h / (p.Hv / p.Hq);
-    const int nch = (MODE == kSum && sg.idx >= sq.nseg - 1) ? 0 : sg.nch;  // last segment: no summary
+    // a v-head whose segments start by warm-up has no summary; its segments
+    // after the first begin Wc chunks early (from h0 when that reaches the
+    // sequence start, else from zero) and write nothing for those chunks
+    const bool warm = head_warm(p, sq, h) && (MODE == kSum || sg.idx > 0);
+    const int nch = (MODE == kSum && (sg.idx >= sq.nseg - 1 || warm)) ? 0 : sg.nch;  // last segment: no summary
+    const int Wc = (MODE != kSum && warm) ? min(p.cp_warmup, sg.chunk0 - sq.chunk0) : 0;
+    const int cfirst = sg.chunk0 - Wc;  // the first chunk this CTA scans
+    const int ntot = Wc + nch;
     const long long cap = p.timeout_spins;
 
     if (tid == 0) {
@@ -714,10 +729,10 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
         // ---------------- TMA producer ----------------
         if (lane == 0) {
             int issued = 0;
-            for (int cc = 0; cc < nch; ++cc) {
+            for (int cc = 0; cc < ntot; ++cc) {
                 const int s = cc & 1;
                 if (cc >= 2 && !bwait(&empty[s], ((cc >> 1) & 1) ^ 1, cap, abort)) break;
-                const int c = sg.chunk0 + cc;
+                const int c = cfirst + cc;
                 const int tok0 = sq.tok0 + kChunk * (c - sq.chunk0);
                 const size_t ch = (size_t)c * p.Hv + h;
                 char *st = stage0 + s * SL::kBytes;
@@ -746,7 +761,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
             const uint32_t id1 = idesc_bf16(128, MODE == kFwd ? 128 : 64);
             const uint32_t id64 = idesc_bf16(128, 64);
             const uint32_t id3 = idesc_bf16(128, 128, 0, 1);
-            for (int cc = 0; cc < nch; ++cc) {
+            for (int cc = 0; cc < ntot; ++cc) {
                 const int s = cc & 1;
                 char *st = stage0 + s * SL::kBytes;
                 if (!bwait(&full[s], (cc >> 1) & 1, cap, abort)) break;
@@ -817,9 +832,10 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
         const size_t pitch = (size_t)p.Hv * 128;
         warp_arrive(bar_sb, lane);  // nothing of a previous chunk to read
         warp_arrive(bar_ut, lane);
-        for (int cc = 0; cc < nch; ++cc) {
+        int ntile = 0;  // output tiles staged so far
+        for (int cc = 0; cc < ntot; ++cc) {
             const int s = cc & 1;
-            const int c = sg.chunk0 + cc;
+            const int c = cfirst + cc;
             const int ctok0 = sq.tok0 + kChunk * (c - sq.chunk0);
             const int clen = min(kChunk, sq.len - kChunk * (c - sq.chunk0));
             if (!wbwait(&full[s], (cc >> 1) & 1, cap, abort)) break;
@@ -860,8 +876,10 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
             }
             tc_fence_before();
             warp_arrive(bar_ut, lane);  // (P Ut)^T of cc read
-            if (clen == kChunk) {
-                if (cc > 0 && !wbwait(bar_ofree, (cc - 1) & 1, cap, abort)) break;
+            if (cc < Wc) {
+                // a warm-up chunk: no output
+            } else if (clen == kChunk) {
+                if (ntile > 0 && !wbwait(bar_ofree, (ntile - 1) & 1, cap, abort)) break;
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     if constexpr (sizeof(TO) == 4)
@@ -872,11 +890,12 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
                 fence_async_smem();
                 warp_arrive(bar_ofull, lane);
                 if (e0) {
-                    if (!bwait(bar_ofull, cc & 1, cap, abort)) break;
+                    if (!bwait(bar_ofull, ntile & 1, cap, abort)) break;
                     tma_store3d(&maps.O, ostage, 0, h, ctok0);
                     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
                     mbar_arrive(bar_ofree);
                 }
+                ++ntile;
             } else {
                 TO *orow = reinterpret_cast<TO *>(p.o) + ((size_t)ctok0 * p.Hv + h) * 128 + t;
 #pragma unroll
@@ -911,8 +930,10 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
                 float v0;
                 if (MODE == kSum)
                     v0 = (isM && k == t) ? 1.f : 0.f;
-                else if (sg.idx == 0)
+                else if (sg.idx == 0 || (warm && cfirst == sq.chunk0))
                     v0 = p.h0 ? p.h0[(((size_t)sg.seq * p.Hv + h) * 128 + k) * 128 + t] : 0.f;
+                else if (warm)
+                    v0 = 0.f;
                 else
                     v0 = p.Sstart[(((size_t)sidx * p.Hv + h) * 128 + k) * 128 + t];
                 r[i] = __float_as_uint(v0);
@@ -922,12 +943,12 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
         tmem_wait_st();
         float *hdst = MODE == kFwd ? p.h_out : (MODE == kStates ? p.hbuf : nullptr);
         bool live = true;
-        for (int cc = 0; cc < nch; ++cc) {
+        for (int cc = 0; cc < ntot; ++cc) {
             const int s = cc & 1;
             char *st = stage0 + s * SL::kBytes;
             const float *bet = reinterpret_cast<const float *>(aux0 + s * kAux);
             const float *eg = bet + 64, *eL = bet + 128;
-            const int c = sg.chunk0 + cc;
+            const int c = cfirst + cc;
             if (cc > 0 && !wbwait(bar_m3, (cc - 1) & 1, cap, abort)) { live = false; break; }
             tc_fence_after();
             if (!wbwait(&full[s], (cc >> 1) & 1, cap, abort)) { live = false; break; }
@@ -946,7 +967,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
                     split_pairs<16>(f, hv, lv);
                     tmem_st16(tSh + k0 / 2 + lo, hv);
                     tmem_st16(tSl + k0 / 2 + lo, lv);
-                    if (hdst)
+                    if (hdst && cc >= Wc)
 #pragma unroll
                         for (int i = 0; i < 32; ++i) hdst[(((size_t)c * p.Hv + h) * 128 + k0 + i) * 128 + t] = f[i];
 #pragma unroll
@@ -1008,12 +1029,12 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
             warp_arrive(&empty[s], lane);
         }
         // (a segment of an empty sequence has no chunk: its end state is its start state)
-        if (__all_sync(0xffffffffu, live && !*abort) && (nch == 0 || wbwait(bar_m3, (nch - 1) & 1, cap, abort))) {
+        if (__all_sync(0xffffffffu, live && !*abort) && (ntot == 0 || wbwait(bar_m3, (ntot - 1) & 1, cap, abort))) {
             tc_fence_after();
             float *dst = nullptr;
             size_t base = 0;
             if (MODE == kSum) {
-                if (sg.idx < sq.nseg - 1) {
+                if (sg.idx < sq.nseg - 1 && !warm) {
                     dst = isM ? p.Mseg : p.Hseg;
                     base = ((size_t)sidx * p.Hv + h) * 128 * 128;
                 }
@@ -1389,6 +1410,66 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_dh_tc(Params p, const __gri
 }
 
 // ---------------------------------------------------------------------------
+// Warm-up gate, before the CP summary: one CTA of 128 threads per (sequence,
+// v-head).  Segment j >= 1 may start from a scan of the W chunks before it
+// begun from zero: the difference between that state and the true one
+// evolves by E <- a (I - b k k^T) E, so its norm at the segment start is at
+// most prod_t a_t max(1, |1 - b_t |k_t|^2|) over the window times the norm of
+// the true state where the window begins.  A segment passes when that factor
+// is below 1e-6 (FlashQLA pages, page 3 "sliding-window warmup", makes the
+// approximation; the bound here keeps it far below the bf16 rounding of the
+// inputs), or when its window reaches the sequence start (the warm-up then
+// begins at h0 and is exact).  The v-head takes warm-up starts only if every
+// segment passes; the exact summary and combine then skip it.  The gate
+// runs one CTA per (segment, v-head); the kernels that follow take the AND
+// over a head's segments.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(128) k_warm_gate(Params p) {
+    // one CTA per (segment, v-head): its pass flag in warm[sidx * Hv + h]
+    const int sidx = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const SegInfo sg = p.seg[sidx];
+    const SeqInfo sq = p.seq[sg.seq];
+    const int hq = h / (p.Hv / p.Hq);
+    const int W = p.cp_warmup, c0 = sg.chunk0;
+    __shared__ float red[4];
+    int pass;
+    if (W <= 0) {
+        pass = 0;
+    } else if (sg.idx == 0 || c0 - W <= sq.chunk0) {
+        pass = 1;  // no start to approximate, or the window begins at the sequence start
+    } else {
+        const int t0 = sq.tok0 + kChunk * (c0 - W - sq.chunk0), t1 = sq.tok0 + kChunk * (c0 - sq.chunk0);
+        float acc = 0.f;
+        for (int t = t0 + tid; t < t1; t += 128) {
+            const uint4 *kr = reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(p.k) +
+                                                             ((size_t)t * p.Hq + hq) * 128);
+            uint4 u[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) u[i] = kr[i];
+            const float b = p.beta[(size_t)t * p.Hv + h], gt = p.g[(size_t)t * p.Hv + h];
+            float kk = 0.f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const uint32_t w[4] = {u[i].x, u[i].y, u[i].z, u[i].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float a = __uint_as_float(w[e] << 16), c = __uint_as_float(w[e] & 0xffff0000u);
+                    kk = fmaf(a, a, fmaf(c, c, kk));
+                }
+            }
+            acc += gt + logf(fmaxf(1.f, fabsf(1.f - b * kk)));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0) red[warp] = acc;
+        __syncthreads();
+        pass = red[0] + red[1] + red[2] + red[3] <= logf(1e-6f);  // NaN fails
+    }
+    if (tid == 0) p.warm[(size_t)sidx * p.Hv + h] = pass;
+}
+
+
+// ---------------------------------------------------------------------------
 // Context-parallel combine of the tensor-core path (K = V = 128): one CTA per
 // (sequence, v-head, 8 state columns), sequential over the segments:
 //   forward  S_start(j+1) = M_j S_start(j) + H_j
@@ -1415,6 +1496,7 @@ __global__ void __launch_bounds__(512) k_combine_tc(Params p) {
     const int warp = tid >> 5, lane = tid & 31;
     const SeqInfo sq = p.seq[n];
     if (sq.nseg <= 1) return;
+    if (!kRev && head_warm(p, sq, h)) return;  // its segments start by warm-up
     // thread (row i, columns c0..c0+3) of the product over l in [64 kh, 64 kh + 64)
     const int u = tid & 255, kh = tid >> 8;
     const int i = 32 * ((warp & 7) & 3) + lane, c0 = 4 * ((warp & 7) >> 2);
@@ -1576,9 +1658,18 @@ int launch_combine(const char *name, const Params &p, cudaStream_t st) {
 
 int tc_supported(int K, int V) { return K == 128 && V == 128; }
 
+static int launch_gate(const Params &p, cudaStream_t st) {
+    if (!p.warm || p.cp_warmup <= 0) return 0;
+    tm_begin(p.tm, "tc_warm_gate", st);
+    k_warm_gate<<<dim3(p.NSEG, p.Hv), 128, 0, st>>>(p);
+    tm_end(p.tm, st);
+    return cudaGetLastError() != cudaSuccess;
+}
+
 int tc_fwd(const Params &p, int o_f32, int use_cp, cudaStream_t st) {
     if (launch_chunk("tc_chunk", p, 0, st)) return 1;
     if (use_cp) {
+        if (launch_gate(p, st)) return 1;
         if (launch_scan<kSum, float>("tc_cp_summary", p, st)) return 1;
         if (launch_combine<false>("tc_cp_combine", p, st)) return 1;
     }
@@ -1589,6 +1680,7 @@ int tc_bwd(const Params &p, int use_cp, cudaStream_t st) {
     // a8: A image, P' image and gates from the forward's A; states before every chunk
     if (launch_chunk("tc_chunk_from_A", p, 1, st)) return 1;
     if (use_cp) {
+        if (launch_gate(p, st)) return 1;
         if (launch_scan<kSum, float>("tc_cp_summary", p, st)) return 1;
         if (launch_combine<false>("tc_cp_combine", p, st)) return 1;
     }

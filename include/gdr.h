@@ -117,6 +117,17 @@ typedef struct {
     const char **names;
     int max_events;
     int *n_launched;
+    /* Warm-up starts of context-parallel segments (FlashQLA pages: page 1,
+     * "balanced solution", and page 3, "sliding-window warmup": a segment's
+     * start state is approximated by scanning the few chunks before it from
+     * zero).  Here it replaces the exact summary and combine for a v-head only
+     * when, for every segment of every sequence, the bound on the start
+     * state's error, prod_t a_t max(1, |1 - b_t |k_t|^2|) over the warm-up
+     * window, is below 1e-6 (or the window reaches the sequence start, where
+     * the warm-up is exact).  0: 8 warm-up chunks (default); -1: always the
+     * exact split; n > 0: n warm-up chunks.  Tensor-core path, forward and the
+     * backward's state recompute; the reverse scan is always exact. */
+    int cp_warmup;
 } gdr_opts;
 
 /* Number of 64-token chunks over all sequences (the NT of h).  -1 on bad shape. */

@@ -668,8 +668,10 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
     uint64_t *bar_drain = bars + 10;
     uint64_t *bar_ofull = bars + 11;  // output tile staged (kFwd)
     uint64_t *bar_ofree = bars + 12;  // output tile read by its TMA store (kFwd)
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 13);
-    volatile int *abort = reinterpret_cast<volatile int *>(bars + 14);
+    uint64_t *bar_m2 = bars + 13;     // MMA2 done (kFwd)
+    uint64_t *bar_yr = bars + 14;     // every state warp has read its Ut^T columns
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 15);
+    volatile int *abort = reinterpret_cast<volatile int *>(bars + 16);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int sidx = blockIdx.x, h = blockIdx.y;
@@ -701,6 +703,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
         mbar_init(bar_drain, 1);
         mbar_init(bar_ofull, kEpiWarps / 2);
         mbar_init(bar_ofree, 1);
+        mbar_init(bar_m2, 1);
+        mbar_init(bar_yr, MODE == kFwd ? kEpiWarps / 2 : kEpiWarps);
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -720,10 +724,12 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
     //   [320,384) (P Ut)^T                      (MMA2)
     //   [384,512) A operands as packed bf16 pairs: S^T hi | lo (64 + 64
     //             columns) for MMA1, then R^T hi | lo at [384,448) for MMA1b
-    //             and Y^T hi | lo at [448,512) for MMA2 and MMA3
+    //   [256,320) Y^T hi | lo, in place of Ut^T once (c2) has read it, for
+    //             MMA3 and MMA2: the next chunk's (a) does not touch it, so
+    //             MMA2 (the output's term) runs after MMA3, off the chain
     const uint32_t tS = tmem, tD1 = tmem + 128, tQS = tmem + 192, tD1b = tmem + 256, tD2 = tmem + 320;
-    const uint32_t tSh = tmem + 384, tSl = tmem + 448, tRh = tmem + 384, tRl = tmem + 416, tYh = tmem + 448,
-                   tYl = tmem + 480;
+    const uint32_t tSh = tmem + 384, tSl = tmem + 448, tRh = tmem + 384, tRl = tmem + 416, tYh = tmem + 256,
+                   tYl = tmem + 288;
 
     if (warp == kEpiWarps) {
         // ---------------- TMA producer ----------------
@@ -794,7 +800,13 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
                 mma_commit(bar_m1b);
                 if (!bwait(bar_ut, cc & 1, cap, abort)) break;
                 tc_fence_after();
-                if (MODE == kFwd) {
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    mma_ts(tS, tYh + 8 * kk, sdesc(b1 + kk * 2048, SL::kAtom), id3, 1);
+                    mma_ts(tS, tYl + 8 * kk, sdesc(b1 + kk * 2048, SL::kAtom), id3, 1);
+                }
+                mma_commit(bar_m3);
+                if (MODE == kFwd) {  // in issue order before MMA1b of the next chunk overwrites Y
                     const uint32_t ph = su32(st + SL::kP), pl = ph + kImg;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
@@ -803,13 +815,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
                         mma_ts(tD2, tYl + 8 * kk, sdesc(ph + o), id64, 1);
                         mma_ts(tD2, tYh + 8 * kk, sdesc(pl + o), id64, 1);
                     }
+                    mma_commit(bar_m2);
                 }
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    mma_ts(tS, tYh + 8 * kk, sdesc(b1 + kk * 2048, SL::kAtom), id3, 1);
-                    mma_ts(tS, tYl + 8 * kk, sdesc(b1 + kk * 2048, SL::kAtom), id3, 1);
-                }
-                mma_commit(bar_m3);
                 mma_commit(&empty[s]);
             }
             mma_commit(bar_drain);
@@ -860,7 +867,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
             }
             tc_fence_before();
             warp_arrive(bar_sb, lane);  // (Q S)^T of cc read
-            if (!wbwait(bar_m3, cc & 1, cap, abort)) break;
+            if (!wbwait(bar_m2, cc & 1, cap, abort)) break;
             tc_fence_after();
             {
                 uint32_t a[16], b[16];
@@ -1008,7 +1015,10 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
             if (!wbwait(bar_m1b, cc & 1, cap, abort)) { live = false; break; }
             tc_fence_after();
             {
-#pragma unroll 1
+                // every state warp reads its Ut^T columns before any writes Y^T
+                // over them (bar_yr, one arrival per state warp)
+                uint32_t hv[kTC / 2], lv[kTC / 2];
+#pragma unroll
                 for (int j = 0; j < kTC / 16; ++j) {
                     const int c0 = tc0 + 16 * j;
                     uint32_t r[16];
@@ -1017,10 +1027,16 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
                     float x[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) x[i] = eL[c0 + i] * __uint_as_float(r[i]);
-                    uint32_t hv[8], lv[8];
-                    split_pairs<8>(x, hv, lv);
-                    tmem_st8(tYh + c0 / 2 + lo, hv);
-                    tmem_st8(tYl + c0 / 2 + lo, lv);
+                    split_pairs<8>(x, hv + 8 * j, lv + 8 * j);
+                }
+                tc_fence_before();
+                warp_arrive(bar_yr, lane);
+                if (!wbwait(bar_yr, cc & 1, cap, abort)) { live = false; break; }
+                tc_fence_after();
+#pragma unroll
+                for (int j = 0; j < kTC / 16; ++j) {
+                    tmem_st8(tYh + (tc0 + 16 * j) / 2 + lo, hv + 8 * j);
+                    tmem_st8(tYl + (tc0 + 16 * j) / 2 + lo, lv + 8 * j);
                 }
                 tmem_wait_st();
             }
@@ -1481,7 +1497,7 @@ __global__ void __launch_bounds__(128) k_warm_gate(Params p) {
 // fp32 throughout (the combine is on the exact path of every later segment).
 // ---------------------------------------------------------------------------
 constexpr int kCombW = 8;
-constexpr int kCombSmem = 1024 + 2 * 65536 + 128 * kCombW * 4 + 256 * 16 + 64;
+constexpr int kCombSmem = 1024 + 2 * 65536 + 128 * kCombW * 4 + 3 * 128 * 32 + 64;
 
 template <bool kRev>
 __global__ void __launch_bounds__(512) k_combine_tc(Params p) {
@@ -1489,17 +1505,16 @@ __global__ void __launch_bounds__(512) k_combine_tc(Params p) {
     char *sm = smem_align1024(smraw);
     float *Mt = reinterpret_cast<float *>(sm);          // [2][128][128]
     float *S = Mt + 2 * 16384;                           // [128][kCombW]
-    float4 *part = reinterpret_cast<float4 *>(S + 128 * kCombW);  // [256] second-half partial sums
-    uint64_t *bars = reinterpret_cast<uint64_t *>(part + 256);
+    float4 *part = reinterpret_cast<float4 *>(S + 128 * kCombW);  // [3][128][2] partial sums of quarters 1-3
+    uint64_t *bars = reinterpret_cast<uint64_t *>(part + 3 * 256);
     volatile int *abort = reinterpret_cast<volatile int *>(bars + 2);
     const int n = blockIdx.x, h = blockIdx.y, v0 = blockIdx.z * kCombW, tid = threadIdx.x;
-    const int warp = tid >> 5, lane = tid & 31;
     const SeqInfo sq = p.seq[n];
     if (sq.nseg <= 1) return;
     if (!kRev && head_warm(p, sq, h)) return;  // its segments start by warm-up
-    // thread (row i, columns c0..c0+3) of the product over l in [64 kh, 64 kh + 64)
-    const int u = tid & 255, kh = tid >> 8;
-    const int i = 32 * ((warp & 7) & 3) + lane, c0 = 4 * ((warp & 7) >> 2);
+    // thread (rows i, i+1; columns c0..c0+3) of the product over l in [32 kq, 32 kq + 32)
+    const int u = tid & 127, kq = tid >> 7;
+    const int i = 2 * (u & 63), c0 = 4 * (u >> 6);
     const long long cap = p.timeout_spins;
     const int nsteps = sq.nseg - 1;
     auto seg_of = [&](int step) -> size_t { return (size_t)sq.seg0 + (kRev ? (sq.nseg - 1 - step) : step); };
@@ -1508,14 +1523,18 @@ __global__ void __launch_bounds__(512) k_combine_tc(Params p) {
         mbar_expect_tx(b, 65536);
         bulk_g2s(Mt + (step & 1) * 16384, p.Mseg + (seg_of(step) * p.Hv + h) * 16384, 65536, b);
     };
-    auto hrow = [&](int step) {
-        return *reinterpret_cast<const float4 *>(p.Hseg + (seg_of(step) * p.Hv + h) * 16384 + (size_t)i * 128 + v0 + c0);
+    auto hrow = [&](int step, int r) {
+        return *reinterpret_cast<const float4 *>(p.Hseg + (seg_of(step) * p.Hv + h) * 16384 + (size_t)r * 128 + v0 + c0);
     };
-    if (kh == 0) {
+    if (kq == 0) {
         const float *init = kRev ? p.dht : p.h0;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (init) v = *reinterpret_cast<const float4 *>(init + (((size_t)n * p.Hv + h) * 128 + i) * 128 + v0 + c0);
-        *reinterpret_cast<float4 *>(S + i * kCombW + c0) = v;
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (init)
+                v = *reinterpret_cast<const float4 *>(init + (((size_t)n * p.Hv + h) * 128 + i + rr) * 128 + v0 + c0);
+            *reinterpret_cast<float4 *>(S + (i + rr) * kCombW + c0) = v;
+        }
     }
     if (tid == 0) {
         mbar_init(&bars[0], 1);
@@ -1525,7 +1544,11 @@ __global__ void __launch_bounds__(512) k_combine_tc(Params p) {
         fetch(0);
     }
     __syncthreads();
-    float4 hnext = kh == 0 ? hrow(0) : make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 hn0 = make_float4(0.f, 0.f, 0.f, 0.f), hn1 = hn0;
+    if (kq == 0) {
+        hn0 = hrow(0, i);
+        hn1 = hrow(0, i + 1);
+    }
     int issued = 1, waited = 0;
     for (int step = 0; step < nsteps; ++step) {
         const size_t sgi = seg_of(step);
@@ -1533,30 +1556,42 @@ __global__ void __launch_bounds__(512) k_combine_tc(Params p) {
             fetch(step + 1);
             issued = step + 2;
         }
-        float4 acc = hnext;
-        if (kh == 0 && step + 1 < nsteps) hnext = hrow(step + 1);  // in flight during this step
+        float4 a0 = hn0, a1 = hn1;
+        if (kq == 0 && step + 1 < nsteps) {  // in flight during this step
+            hn0 = hrow(step + 1, i);
+            hn1 = hrow(step + 1, i + 1);
+        }
         const bool ok = bwait(&bars[step & 1], (step >> 1) & 1, cap, abort);
         if (__syncthreads_or(!ok)) break;
         waited = step + 1;
-        const float *mt = Mt + (step & 1) * 16384 + 64 * kh * 128 + i;
-        const float *sv0 = S + 64 * kh * kCombW + c0;
-#pragma unroll 16
-        for (int l = 0; l < 64; ++l) {
-            const float m = mt[l * 128];
+        const float *mt = Mt + (step & 1) * 16384 + 32 * kq * 128 + i;
+        const float *sv0 = S + 32 * kq * kCombW + c0;
+#pragma unroll 8
+        for (int l = 0; l < 32; ++l) {
+            const float2 m = *reinterpret_cast<const float2 *>(mt + l * 128);
             const float4 sv = *reinterpret_cast<const float4 *>(sv0 + l * kCombW);
-            acc.x = fmaf(m, sv.x, acc.x);
-            acc.y = fmaf(m, sv.y, acc.y);
-            acc.z = fmaf(m, sv.z, acc.z);
-            acc.w = fmaf(m, sv.w, acc.w);
+            a0.x = fmaf(m.x, sv.x, a0.x); a0.y = fmaf(m.x, sv.y, a0.y);
+            a0.z = fmaf(m.x, sv.z, a0.z); a0.w = fmaf(m.x, sv.w, a0.w);
+            a1.x = fmaf(m.y, sv.x, a1.x); a1.y = fmaf(m.y, sv.y, a1.y);
+            a1.z = fmaf(m.y, sv.z, a1.z); a1.w = fmaf(m.y, sv.w, a1.w);
         }
-        if (kh == 1) part[u] = acc;
+        if (kq > 0) {
+            part[((kq - 1) * 128 + u) * 2] = a0;
+            part[((kq - 1) * 128 + u) * 2 + 1] = a1;
+        }
         __syncthreads();
-        if (kh == 0) {
-            const float4 q = part[u];
-            acc.x += q.x; acc.y += q.y; acc.z += q.z; acc.w += q.w;
-            *reinterpret_cast<float4 *>(S + i * kCombW + c0) = acc;
+        if (kq == 0) {
+#pragma unroll
+            for (int q = 0; q < 3; ++q) {
+                const float4 b0 = part[(q * 128 + u) * 2], b1 = part[(q * 128 + u) * 2 + 1];
+                a0.x += b0.x; a0.y += b0.y; a0.z += b0.z; a0.w += b0.w;
+                a1.x += b1.x; a1.y += b1.y; a1.z += b1.z; a1.w += b1.w;
+            }
+            *reinterpret_cast<float4 *>(S + i * kCombW + c0) = a0;
+            *reinterpret_cast<float4 *>(S + (i + 1) * kCombW + c0) = a1;
             float *dst = p.Sstart + ((kRev ? sgi - 1 : sgi + 1) * p.Hv + h) * 16384;
-            *reinterpret_cast<float4 *>(dst + (size_t)i * 128 + v0 + c0) = acc;
+            *reinterpret_cast<float4 *>(dst + (size_t)i * 128 + v0 + c0) = a0;
+            *reinterpret_cast<float4 *>(dst + (size_t)(i + 1) * 128 + v0 + c0) = a1;
         }
         __syncthreads();
     }

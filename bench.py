@@ -10,10 +10,12 @@ and dht ~ N(0, 0.1) drawn for the backward.
 Timing: W untimed warm-up steps, then K steps bracketed by a barrier and
 torch.cuda.synchronize() on both sides; each step is timed with CUDA events on
 the launching stream after an L2 flush (a 256 MiB write), and the value is the
-tokens of all ranks divided by the slowest rank's summed step time.  Each
-kernel is also bracketed by caller-owned events (gdr_opts.events); the
-dominant kernel's algorithmic work over its measured duration gives the
-roofline fraction.
+tokens of all ranks divided by the slowest rank's summed step time.  K more
+steps follow with every kernel bracketed by caller-owned events
+(gdr_opts.events; kept out of the timed steps, whose time the extra event
+records would inflate): the dominant kernel's algorithmic work over its
+measured duration gives the roofline fraction, and their launch count (the
+same calls as the timed steps) is gpu_launches.
 
 ``--impl reference`` times the fp64 CPU oracle (the reference arm of this
 build) on a bounded sample of the same workload.
@@ -346,19 +348,25 @@ def main():
     for i in range(args.steps):
         flush.zero_()
         e0[i].record(stream)
-        step(tf, tb)
+        step()
         e1[i].record(stream)
         torch.cuda.synchronize()
-        for timer in (tf, tb):
-            launches += timer.count.value
-            for nm, ms in timer.elapsed():
-                per_kernel.setdefault(nm, []).append(ms)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     t_wall1 = time.time()
     clk = clocks.stop(t_wall0, t_wall1)
     step_ms = [a.elapsed_time(b) for a, b in zip(e0, e1)]
+    # per-kernel durations from separate steps with caller-owned events around
+    # every launch (kept out of the timed steps, whose time they would inflate)
+    for i in range(args.steps):
+        flush.zero_()
+        step(tf, tb)
+        torch.cuda.synchronize()
+        for timer in (tf, tb):
+            launches += timer.count.value
+            for nm, ms in timer.elapsed():
+                per_kernel.setdefault(nm, []).append(ms)
     tokens = spec.tokens
     value, total_ms = aggregate(sum(step_ms), tokens, args.steps, dev)
     gdr.check_status()

@@ -159,6 +159,14 @@ def test_bwd_varlen(gdr, path, lengths):
 
 
 @pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("Hq,Hv", [(4, 4), (1, 4)])
+def test_bwd_grouped_heads(gdr, path, Hq, Hv):
+    # G = 1 (no qk-head sum) and G = 4 (the last of four v-heads adds the group)
+    spec = inputs.small(B=1, T=130, Hq=Hq, Hv=Hv, K=128, V=128, bwd=True)
+    _check_bwd(gdr, spec, _path(gdr, path, spec))
+
+
+@pytest.mark.parametrize("path", PATHS)
 def test_bwd_context_parallel_and_no_initial_state(gdr, path):
     spec = inputs.small(B=1, T=700, Hq=1, Hv=4, K=128, V=128, h0=False, bwd=True)
     p = _path(gdr, path, spec)

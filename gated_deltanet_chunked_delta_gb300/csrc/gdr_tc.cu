@@ -22,6 +22,7 @@
 // The state lives in tensor memory, transposed: TMEM lane v holds row v of
 // S^T, 128 fp32 columns of k.
 #include <cuda.h>
+#include <cstdlib>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -270,26 +271,31 @@ struct ChunkMaps {
     CUtensorMap K, Q;  // 3-D over k and q: (K, Hq, Ttot), box (64, 1, 64), 128-byte swizzle
 };
 
-// Row `row`, columns [col0, col0 + 32) of a [hi | lo] pair of 128-byte-swizzled
-// 64-column bf16 images (col0 = 0 or 32).
-__device__ __forceinline__ void st_img_half2(char *img, int row, int col0, const float *x /* 32 */) {
+// Row `row`, columns [col0, col0 + 32) (col0 a multiple of 8, inside one
+// 64-column atom) of a pair of 128-byte-swizzled bf16 images: hi = bf16(x) at
+// `hi`, lo = bf16(x - hi) at `lo` (both atom bases 1024-byte aligned).
+__device__ __forceinline__ void st_img_hl(char *hi, char *lo, int row, int col0, const float *x /* 32 */) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        float hi[8], lw[8];
+        float hv[8], lw[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            hi[e] = bf16_round(x[8 * j + e]);
-            lw[e] = x[8 * j + e] - hi[e];
+            hv[e] = bf16_round(x[8 * j + e]);
+            lw[e] = x[8 * j + e] - hv[e];
         }
         uint4 vh, vl;
-        vh.x = pack_bf16(hi[0], hi[1]); vh.y = pack_bf16(hi[2], hi[3]);
-        vh.z = pack_bf16(hi[4], hi[5]); vh.w = pack_bf16(hi[6], hi[7]);
+        vh.x = pack_bf16(hv[0], hv[1]); vh.y = pack_bf16(hv[2], hv[3]);
+        vh.z = pack_bf16(hv[4], hv[5]); vh.w = pack_bf16(hv[6], hv[7]);
         vl.x = pack_bf16(lw[0], lw[1]); vl.y = pack_bf16(lw[2], lw[3]);
         vl.z = pack_bf16(lw[4], lw[5]); vl.w = pack_bf16(lw[6], lw[7]);
         const int off = row * 128 + ((((col0 >> 3) + j) ^ (row & 7)) << 4);
-        *reinterpret_cast<uint4 *>(img + off) = vh;
-        *reinterpret_cast<uint4 *>(img + kImg + off) = vl;
+        *reinterpret_cast<uint4 *>(hi + off) = vh;
+        *reinterpret_cast<uint4 *>(lo + off) = vl;
     }
+}
+// The same for a [hi | lo] pair of 64-row images kImg bytes apart (col0 = 0 or 32).
+__device__ __forceinline__ void st_img_half2(char *img, int row, int col0, const float *x /* 32 */) {
+    st_img_hl(img, img + kImg, row, col0, x);
 }
 
 // ---------------------------------------------------------------------------
@@ -1600,6 +1606,599 @@ __global__ void __launch_bounds__(512) k_combine_tc(Params p) {
 }
 
 // ---------------------------------------------------------------------------
+// Chunk-local gradients of the backward on tcgen05 (K = V = 128).  One CTA of
+// 256 threads per (chunk, v-head); thread 0 issues every MMA, all eight warps
+// run the epilogues (warp w reads TMEM lanes 32 (w % 4) .. + 31 and columns
+// [32 (w / 4), + 32)).  The same reverse mode as the warp-MMA kernel, with
+// every product laid out so that its M side is 128 (a value, key or stacked
+// token index in the TMEM lanes):
+//   group 1  KS^T   = S0^T K^T          (S0 image read MN-major)
+//            dQr^T  = S0 dO^T
+//            dR^T   = dUt^T A           (dUt^T from TMEM, A read MN-major)
+//   epilogue R^T = (diag(b)(V - diag(e^gamma) KS))^T -> TMEM; dv = b dR;
+//            dKS^T = -(diag(b e^gamma) dR)^T -> image; dR -> image rows 64-127
+//            of the [dO ; dR] operand; row sums dR.V, dR.KS, dQr.Q
+//   group 2  Ut^T   = R^T A^T
+//            dK^T   = S0 dKS^T
+//   epilogue Ut^T -> image; row sums dUt.Ut; the dS1 image over S0 (<dS1, S0>)
+//   group 3  [dO ; dR] Ut^T             = [dO Ut^T ; X A^T]  (X = A^T dA, dA = dUt R^T)
+//            dK2^T  = dS1 Ut^T          (the decay e^{gamma_n - gamma} applied after)
+//            [Q ; K] K^T                = [Q K^T ; K K^T]
+//   epilogue dP'' = scale e^{gamma_r - gamma_s} (dO Ut^T) (causal), dL =
+//            -strict_tril(X A^T), MM = dL o b_r e^{gamma_r - gamma_s} -> images;
+//            row sums dP''.QK, dL.e KK and column sums of dL b e KK
+//   group 4  dq2^T  = K^T dP''^T,  dK^T += Q^T dP'' + K^T MM^T + K^T MM
+//   epilogue dq = scale e^gamma dQr + dq2, dk = dK + e^{gamma_n - gamma} dK2;
+//            the qk-head group sum; dbeta, dg.
+// X A^T = A^T dUt R^T A^T = dR Ut^T, so the 64 x 64 products X = A^T dA and
+// dL = X A^T need no separate pass.  Operands that are not exact bf16 inputs
+// enter as hi + lo bf16 pairs with three products (hi hi, lo hi, hi lo).
+// ---------------------------------------------------------------------------
+struct BcMaps {
+    CUtensorMap Q, K, dO;  // 3-D (x, head, token), box 64 x 1 x 64, 128-byte swizzle
+};
+constexpr int kBcThreads = 256;
+// shared memory (bytes from the 1024-aligned base)
+constexpr int kBcKQ = 0;        // [Q ; K]: 2 atoms (k halves) x [128 rows][128 B]: Q rows 0-63, K rows 64-127
+constexpr int kBcOR = 32768;    // [dO ; dR_hi]: 2 atoms (v halves) x [128 rows][128 B]
+constexpr int kBcRL = 65536;    // dR_lo: 2 atoms x [64 rows][128 B]; each atom's operand starts 8 KiB before it
+constexpr int kBcA = 81920;     // A image hi | lo, [64 rows t][64 s]
+constexpr int kBcS = 98304;     // S0, then dS1: hi | lo, each 2 atoms (v halves) x [128 rows k][128 B]
+constexpr int kBcW = 163840;    // dKS^T hi | lo [128 v][64 t] -> Ut^T hi | lo -> dP'' hi | lo, MM hi | lo [64][64]
+constexpr int kBcScr = 196608;  // fp32 scratch: 12 x 64 row arrays, 16 reduction slots, barriers
+constexpr int kBcSmem = 1024 + kBcScr + 4096;
+// tensor memory columns
+constexpr uint32_t kTbKS = 0;     // KS^T -> Ut^T -> dq2^T
+constexpr uint32_t kTbP1 = 64;    // [dO Ut^T ; dR_hi Ut^T + ...]
+constexpr uint32_t kTbDQ = 128;   // dQr^T
+constexpr uint32_t kTbDR = 192;   // dR^T -> [Q K^T ; K K^T]
+constexpr uint32_t kTbDK = 256;   // dK^T
+constexpr uint32_t kTbU = 320;    // dUt^T hi | lo (packed A operand) -> dK2^T
+constexpr uint32_t kTbR = 384;    // R^T hi | lo (packed A operand)
+constexpr uint32_t kTbP1B = 448;  // [. ; dR_lo Ut_hi^T]
+
+// Byte offset of element (row, col), col < 64, in a 128-byte-swizzled bf16 atom.
+__device__ __forceinline__ int swz_at(int row, int col) {
+    return row * 128 + ((((col >> 3)) ^ (row & 7)) << 4) + (col & 7) * 2;
+}
+// Per lane x[0..31] -> the sum over the warp's lanes of x[lane] (reduce-scatter; x is consumed).
+__device__ __forceinline__ float warp_rs32(float (&x)[32], int lane) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < o; ++i) {
+            const float send = up ? x[i] : x[i + o];
+            const float keep = up ? x[i + o] : x[i];
+            x[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    return x[0];
+}
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const __grid_constant__ BcMaps maps) {
+    extern __shared__ __align__(1024) char smraw[];
+    char *sm = smem_align1024(smraw);
+    char *KQ = sm + kBcKQ, *OR = sm + kBcOR, *RL = sm + kBcRL, *Aim = sm + kBcA, *Sim = sm + kBcS, *Wim = sm + kBcW;
+    float *scr = reinterpret_cast<float *>(sm + kBcScr);
+    float *gam = scr, *bet = scr + 64, *egv = scr + 128;
+    float *rRV = scr + 192, *rRKS = scr + 256, *rUdU = scr + 320, *rQdq = scr + 384, *rP = scr + 448,
+          *rLK = scr + 512, *cL = scr + 576, *dgm = scr + 640, *tnp = scr + 704;
+    float *red = scr + 768;  // [16]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(scr + 784);  // tma, mma
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2);
+    volatile int *abort = reinterpret_cast<volatile int *>(bars + 3);
+    int *ticket = reinterpret_cast<int *>(bars + 4);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int q4 = warp & 3, hc = warp >> 2;
+    const uint32_t lq = (uint32_t)(q4 * 32) << 16;
+    const int c = blockIdx.x, h = blockIdx.y;
+    const ChunkInfo ci = p.chunk[c];
+    const int len = ci.len, tok0 = ci.tok0;
+    const int hq = h / (p.Hv / p.Hq);
+    const size_t ch = (size_t)c * p.Hv + h;
+    const long long cap = p.timeout_spins;
+    const int row_v = 32 * q4 + lane;  // this thread's TMEM lane (a value, key or stacked token index)
+    const int t0 = 32 * hc;            // this thread's first TMEM column of a 64-column block
+
+    if (tid == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        *abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
+                     "r"(512));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    if (tid < 64) {
+        gam[tid] = tid < len ? p.g[(size_t)(tok0 + tid) * p.Hv + h] : 0.f;
+        bet[tid] = tid < len ? p.beta[(size_t)(tok0 + tid) * p.Hv + h] : 0.f;
+        rRV[tid] = rRKS[tid] = rUdU[tid] = rQdq[tid] = rP[tid] = rLK[tid] = cL[tid] = 0.f;
+    }
+    if (tid < 16) red[tid] = 0.f;
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    int ncommit = 0;  // MMA groups committed (thread 0)
+    bool tma_issued = false;
+    if (tid == 0) {
+        mbar_expect_tx(&bars[0], 49152);
+#pragma unroll
+        for (int a = 0; a < 2; ++a) {
+            tma3d(KQ + a * 16384, &maps.Q, 64 * a, hq, tok0, &bars[0]);
+            tma3d(KQ + a * 16384 + 8192, &maps.K, 64 * a, hq, tok0, &bars[0]);
+            tma3d(OR + a * 16384, &maps.dO, 64 * a, h, tok0, &bars[0]);
+        }
+        tma_issued = true;
+    }
+    if (tid < 32) {  // inclusive cumsum of the gates, two per lane
+        const float a = gam[2 * lane], b = gam[2 * lane + 1];
+        float s = a + b;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float n = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o) s += n;
+        }
+        gam[2 * lane] = s - b;
+        gam[2 * lane + 1] = s;
+    }
+    // A image (rows past the chunk end: identity rows)
+    if (tid < 128) {
+        const int rr = tid >> 1, c0 = 32 * (tid & 1);
+        float x[32];
+        if (rr < len) {
+            const float4 *src = reinterpret_cast<const float4 *>(p.A_in + ((size_t)(tok0 + rr) * p.Hv + h) * 64 + c0);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 v = src[i];
+                x[4 * i] = v.x; x[4 * i + 1] = v.y; x[4 * i + 2] = v.z; x[4 * i + 3] = v.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) x[i] = (c0 + i == rr) ? 1.f : 0.f;
+        }
+        st_img_hl(Aim, Aim + 8192, rr, c0, x);
+    }
+    // S0 image: row k, 32 columns per item
+    {
+        const float *S0g = p.hbuf + ch * 128 * 128;
+#pragma unroll 1
+        for (int u = 0; u < 2; ++u) {
+            const int it = tid + kBcThreads * u, k = it >> 2, cq = it & 3;
+            const float4 *src = reinterpret_cast<const float4 *>(S0g + (size_t)k * 128 + 32 * cq);
+            float x[32];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 v = src[i];
+                x[4 * i] = v.x; x[4 * i + 1] = v.y; x[4 * i + 2] = v.z; x[4 * i + 3] = v.w;
+            }
+            st_img_hl(Sim + (cq >> 1) * 16384, Sim + 32768 + (cq >> 1) * 16384, k, 32 * (cq & 1), x);
+        }
+    }
+    // dUt^T (lane v, tokens t0..t0+31; rows past the chunk end zero) -> packed hi | lo A operand
+    {
+        const float *dUg = p.dubuf + ch * 64 * 128 + row_v;
+        float x[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] = t0 + j < len ? dUg[(size_t)(t0 + j) * 128] : 0.f;
+        uint32_t hv[16], lv[16];
+        split_pairs<16>(x, hv, lv);
+        tmem_st16(tmem + kTbU + t0 / 2 + lq, hv);
+        tmem_st16(tmem + kTbU + 32 + t0 / 2 + lq, lv);
+        tmem_wait_st();
+    }
+    __syncthreads();  // gates
+    if (tid < 64) egv[tid] = __expf(gam[tid]);
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+
+    const uint32_t sKQ = su32(KQ), sOR = su32(OR), sRL = su32(RL), sA = su32(Aim), sS = su32(Sim), sW = su32(Wim);
+    bool ok = true;
+    // ---------------- group 1 ----------------
+    if (tid == 0) {
+        if (bwait(&bars[0], 0, cap, abort)) {
+            tc_fence_after();
+            {  // KS^T = S0^T K^T: A = S0 image MN-major (M = v in two 64-blocks 16 KiB apart), B = K rows
+                const uint32_t id = idesc_bf16(128, 64, 1, 0);
+#pragma unroll
+                for (int tm = 0; tm < 2; ++tm)
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma(tmem + kTbKS, sdesc(sS + tm * 32768 + kk * 2048, 16384),
+                            sdesc(sKQ + (kk >> 2) * 16384 + 8192 + (kk & 3) * 32), id, (tm | kk) != 0);
+            }
+            {  // dQr^T = S0 dO^T: A = S0 image K-major (M = k), B = dO rows
+                const uint32_t id = idesc_bf16(128, 64, 0, 0);
+#pragma unroll
+                for (int tm = 0; tm < 2; ++tm)
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma(tmem + kTbDQ, sdesc(sS + tm * 32768 + (kk >> 2) * 16384 + (kk & 3) * 32),
+                            sdesc(sOR + (kk >> 2) * 16384 + (kk & 3) * 32), id, (tm | kk) != 0);
+            }
+            {  // dR^T = dUt^T A: A operand dUt^T from TMEM, B = A image MN-major (K = s rows)
+                const uint32_t id = idesc_bf16(128, 64, 0, 1);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    mma_ts(tmem + kTbDR, tmem + kTbU + 8 * kk, sdesc(sA + kk * 2048), id, kk > 0);
+                    mma_ts(tmem + kTbDR, tmem + kTbU + 32 + 8 * kk, sdesc(sA + kk * 2048), id, 1);
+                    mma_ts(tmem + kTbDR, tmem + kTbU + 8 * kk, sdesc(sA + 8192 + kk * 2048), id, 1);
+                }
+            }
+            mma_commit(&bars[1]);
+            ncommit = 1;
+        }
+    }
+    ok = bwait(&bars[1], 0, cap, abort);
+    if (__syncthreads_or(!ok)) goto out;
+    tc_fence_after();
+    // ---------------- epilogue 1 ----------------
+    {
+        // lane v: R^T, dv, dKS^T, dR (as rows of the [dO ; dR] operand), row sums dR.V, dR.KS
+        const int v = row_v;
+        uint32_t ksu[32], dru[32];
+        tmem_ld32(tmem + kTbKS + t0 + lq, ksu);
+        tmem_ld32(tmem + kTbDR + t0 + lq, dru);
+        const __nv_bfloat16 *vin = reinterpret_cast<const __nv_bfloat16 *>(p.v) + ((size_t)tok0 * p.Hv + h) * 128 + v;
+        const size_t tstride = (size_t)p.Hv * 128;
+        float vv[32], x[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) vv[j] = t0 + j < len ? __bfloat162float(vin[(size_t)(t0 + j) * tstride]) : 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] = bet[t0 + j] * (vv[j] - egv[t0 + j] * __uint_as_float(ksu[j]));
+        {
+            uint32_t hv[16], lv[16];
+            split_pairs<16>(x, hv, lv);
+            tmem_st16(tmem + kTbR + t0 / 2 + lq, hv);
+            tmem_st16(tmem + kTbR + 32 + t0 / 2 + lq, lv);
+        }
+        float a1[32], a2[32];
+        __nv_bfloat16 *dvo = reinterpret_cast<__nv_bfloat16 *>(p.dv) + ((size_t)tok0 * p.Hv + h) * 128 + v;
+        char *orh = OR + (v >> 6) * 16384 + 8192;  // rows 64-127 of the v half's atom
+        char *orl = RL + (v >> 6) * 8192;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const int t = t0 + j;
+            const float dr = __uint_as_float(dru[j]);
+            a1[j] = dr * vv[j];
+            a2[j] = dr * __uint_as_float(ksu[j]);
+            if (t < len) dvo[(size_t)t * tstride] = __float2bfloat16_rn(bet[t] * dr);
+            x[j] = -bet[t] * egv[t] * dr;
+            const __nv_bfloat16 hb = __float2bfloat16_rn(dr);
+            const __nv_bfloat16 lb = __float2bfloat16_rn(dr - __bfloat162float(hb));
+            const int off = swz_at(t, v & 63);
+            *reinterpret_cast<__nv_bfloat16 *>(orh + off) = hb;
+            *reinterpret_cast<__nv_bfloat16 *>(orl + off) = lb;
+        }
+        st_img_hl(Wim, Wim + 16384, v, t0, x);  // dKS^T row v
+        const float s1 = warp_rs32(a1, lane);
+        const float s2 = warp_rs32(a2, lane);
+        atomicAdd(&rRV[t0 + lane], s1);
+        atomicAdd(&rRKS[t0 + lane], s2);
+    }
+    {
+        // lane k: row sums dQr.Q (Q from the [Q ; K] image)
+        const int k = row_v;
+        uint32_t dqu[32];
+        tmem_ld32(tmem + kTbDQ + t0 + lq, dqu);
+        const char *qa = KQ + (k >> 6) * 16384;
+        float a[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            a[j] = __uint_as_float(dqu[j]) *
+                   __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(qa + swz_at(t0 + j, k & 63)));
+        const float s = warp_rs32(a, lane);
+        atomicAdd(&rQdq[t0 + lane], s);
+    }
+    tmem_wait_st();
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    // ---------------- group 2 ----------------
+    if (tid == 0) {
+        tc_fence_after();
+        {  // Ut^T = R^T A^T: A operand R^T from TMEM, B = A image K-major (rows t)
+            const uint32_t id = idesc_bf16(128, 64, 0, 0);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                mma_ts(tmem + kTbKS, tmem + kTbR + 8 * kk, sdesc(sA + kk * 32), id, kk > 0);
+                mma_ts(tmem + kTbKS, tmem + kTbR + 32 + 8 * kk, sdesc(sA + kk * 32), id, 1);
+                mma_ts(tmem + kTbKS, tmem + kTbR + 8 * kk, sdesc(sA + 8192 + kk * 32), id, 1);
+            }
+        }
+        {  // dK^T = S0 dKS^T: B = dKS^T image MN-major (K = v rows)
+            const uint32_t id = idesc_bf16(128, 64, 0, 1);
+            const int ta[3] = {0, 1, 0}, tb[3] = {0, 0, 1};
+#pragma unroll
+            for (int m = 0; m < 3; ++m)
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma(tmem + kTbDK, sdesc(sS + ta[m] * 32768 + (kk >> 2) * 16384 + (kk & 3) * 32),
+                        sdesc(sW + tb[m] * 16384 + kk * 2048), id, (m | kk) != 0);
+        }
+        mma_commit(&bars[1]);
+        ncommit = 2;
+    }
+    ok = bwait(&bars[1], 1, cap, abort);
+    if (__syncthreads_or(!ok)) goto out;
+    tc_fence_after();
+    // ---------------- epilogue 2 ----------------
+    {
+        // lane v: Ut^T -> image (B operand of group 3), row sums dUt.Ut
+        const int v = row_v;
+        uint32_t uu[32], dh[16], dl[16];
+        tmem_ld32(tmem + kTbKS + t0 + lq, uu);
+        tmem_ld16_issue(tmem + kTbU + t0 / 2 + lq, dh);
+        tmem_ld16_issue(tmem + kTbU + 32 + t0 / 2 + lq, dl);
+        tmem_wait_ld16(dh);
+        tmem_hold16(dl);
+        float x[32], a[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(uu[j]);
+        st_img_hl(Wim, Wim + 16384, v, t0, x);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            a[2 * i] = (bf_lo(dh[i]) + bf_lo(dl[i])) * x[2 * i];
+            a[2 * i + 1] = (bf_hi(dh[i]) + bf_hi(dl[i])) * x[2 * i + 1];
+        }
+        const float s = warp_rs32(a, lane);
+        atomicAdd(&rUdU[t0 + lane], s);
+    }
+    {
+        // dS1 image over the S0 image, with <dS1, S0> from the S0 terms it replaces
+        const float *dS1g = p.dhbuf + ch * 128 * 128;
+        float part = 0.f;
+#pragma unroll 1
+        for (int u = 0; u < 2; ++u) {
+            const int it = tid + kBcThreads * u, k = it >> 2, cq = it & 3;
+            char *ih = Sim + (cq >> 1) * 16384, *il = ih + 32768;
+            const int c0 = 32 * (cq & 1);
+            const float4 *src = reinterpret_cast<const float4 *>(dS1g + (size_t)k * 128 + 32 * cq);
+            float x[32];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 v = src[i];
+                x[4 * i] = v.x; x[4 * i + 1] = v.y; x[4 * i + 2] = v.z; x[4 * i + 3] = v.w;
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int off = k * 128 + ((((c0 >> 3) + j) ^ (k & 7)) << 4);
+                const uint4 wh = *reinterpret_cast<const uint4 *>(ih + off);
+                const uint4 wl = *reinterpret_cast<const uint4 *>(il + off);
+                const uint32_t hh[4] = {wh.x, wh.y, wh.z, wh.w}, ll[4] = {wl.x, wl.y, wl.z, wl.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    part += x[8 * j + 2 * e] * (bf_lo(hh[e]) + bf_lo(ll[e])) +
+                            x[8 * j + 2 * e + 1] * (bf_hi(hh[e]) + bf_hi(ll[e]));
+            }
+            st_img_hl(ih, il, k, c0, x);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+        if (lane == 0) atomicAdd(&red[0], part);
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    // ---------------- group 3 ----------------
+    if (tid == 0) {
+        tc_fence_after();
+        const uint32_t id = idesc_bf16(128, 64, 0, 1);
+        // [dO ; dR_hi] (Ut_hi + Ut_lo)^T, and [. ; dR_lo] Ut_hi^T: B = Ut^T image MN-major
+#pragma unroll
+        for (int tb = 0; tb < 2; ++tb)
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                mma(tmem + kTbP1, sdesc(sOR + (kk >> 2) * 16384 + (kk & 3) * 32), sdesc(sW + tb * 16384 + kk * 2048),
+                    id, (tb | kk) != 0);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+            mma(tmem + kTbP1B, sdesc(sRL - 8192 + (kk >> 2) * 8192 + (kk & 3) * 32), sdesc(sW + kk * 2048), id,
+                kk > 0);
+        {  // dK2^T = dS1 Ut^T
+            const int ta[3] = {0, 1, 0}, tb[3] = {0, 0, 1};
+#pragma unroll
+            for (int m = 0; m < 3; ++m)
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma(tmem + kTbU, sdesc(sS + ta[m] * 32768 + (kk >> 2) * 16384 + (kk & 3) * 32),
+                        sdesc(sW + tb[m] * 16384 + kk * 2048), id, (m | kk) != 0);
+        }
+        {  // [Q ; K] K^T
+            const uint32_t id2 = idesc_bf16(128, 64, 0, 0);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                mma(tmem + kTbDR, sdesc(sKQ + (kk >> 2) * 16384 + (kk & 3) * 32),
+                    sdesc(sKQ + (kk >> 2) * 16384 + 8192 + (kk & 3) * 32), id2, kk > 0);
+        }
+        mma_commit(&bars[1]);
+        ncommit = 3;
+    }
+    ok = bwait(&bars[1], 0, cap, abort);
+    if (__syncthreads_or(!ok)) goto out;
+    tc_fence_after();
+    // ---------------- epilogue 3: token lanes ----------------
+    if (q4 < 2) {
+        // row t of dP'' = scale e^{gamma_t - gamma_s} (dO Ut^T)[t][s], s <= t < len; row sum dP''.QK
+        const int t = row_v;
+        uint32_t pu[32], qu[32];
+        tmem_ld32(tmem + kTbP1 + t0 + lq, pu);
+        tmem_ld32(tmem + kTbDR + t0 + lq, qu);
+        const float gt = gam[t];
+        float x[32], rp = 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const int s = t0 + j;
+            x[j] = (s <= t && t < len) ? p.scale * __expf(gt - gam[s]) * __uint_as_float(pu[j]) : 0.f;
+            rp += x[j] * __uint_as_float(qu[j]);
+        }
+        st_img_hl(Wim, Wim + 8192, t, t0, x);
+        atomicAdd(&rP[t], rp);
+    } else {
+        // row t of dL = -(X A^T)[t][s], s < t < len; MM = dL b_t e^{gamma_t - gamma_s};
+        // row sums dL e KK, column sums dL b e KK
+        const int t = row_v - 64;
+        uint32_t pu[32], pb[32], ku[32];
+        tmem_ld32(tmem + kTbP1 + t0 + lq, pu);
+        tmem_ld32(tmem + kTbP1B + t0 + lq, pb);
+        tmem_ld32(tmem + kTbDR + t0 + lq, ku);
+        const float gt = gam[t], bt = bet[t];
+        float mmx[32], col[32], rl = 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const int s = t0 + j;
+            const bool in = s < t && t < len;
+            const float e = in ? __expf(gt - gam[s]) : 0.f;
+            const float dl = in ? -(__uint_as_float(pu[j]) + __uint_as_float(pb[j])) : 0.f;
+            const float ek = e * __uint_as_float(ku[j]);
+            rl += dl * ek;
+            col[j] = dl * bt * ek;
+            mmx[j] = dl * bt * e;
+        }
+        st_img_hl(Wim + 16384, Wim + 24576, t, t0, mmx);
+        atomicAdd(&rLK[t], rl);
+        const float s = warp_rs32(col, lane);
+        atomicAdd(&cL[t0 + lane], s);
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    // ---------------- group 4 ----------------
+    if (tid == 0) {
+        tc_fence_after();
+        // A = K^T or Q^T: the K (Q) rows read MN-major (M = k in two 64-blocks 16 KiB apart)
+        const uint32_t aK = sKQ + 8192, aQ = sKQ;
+        const uint32_t idK = idesc_bf16(128, 64, 1, 0), idM = idesc_bf16(128, 64, 1, 1);
+#pragma unroll
+        for (int tb = 0; tb < 2; ++tb)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)  // dq2^T = K^T dP''^T (B = dP'' rows t, K-major)
+                mma(tmem + kTbKS, sdesc(aK + kk * 2048, 16384), sdesc(sW + tb * 8192 + kk * 32), idK, (tb | kk) != 0);
+#pragma unroll
+        for (int tb = 0; tb < 2; ++tb)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                // dK^T += Q^T dP'' (B MN-major), K^T MM^T (B K-major), K^T MM (B MN-major)
+                mma(tmem + kTbDK, sdesc(aQ + kk * 2048, 16384), sdesc(sW + tb * 8192 + kk * 2048), idM, 1);
+                mma(tmem + kTbDK, sdesc(aK + kk * 2048, 16384), sdesc(sW + 16384 + tb * 8192 + kk * 32), idK, 1);
+                mma(tmem + kTbDK, sdesc(aK + kk * 2048, 16384), sdesc(sW + 16384 + tb * 8192 + kk * 2048), idM, 1);
+            }
+        mma_commit(&bars[1]);
+        ncommit = 4;
+    }
+    ok = bwait(&bars[1], 1, cap, abort);
+    if (__syncthreads_or(!ok)) goto out;
+    tc_fence_after();
+    // ---------------- epilogue 4: lane k ----------------
+    {
+        const int k = row_v;
+        const float gC = gam[63];
+        uint32_t qr[32], q2[32], kd[32], k2[32];
+        tmem_ld32(tmem + kTbDQ + t0 + lq, qr);
+        tmem_ld32(tmem + kTbKS + t0 + lq, q2);
+        tmem_ld32(tmem + kTbDK + t0 + lq, kd);
+        tmem_ld32(tmem + kTbU + t0 + lq, k2);
+        float dqv[32], dkv[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const int t = t0 + j;
+            dqv[j] = p.scale * egv[t] * __uint_as_float(qr[j]) + __uint_as_float(q2[j]);
+            dkv[j] = __uint_as_float(kd[j]) + __expf(gC - gam[t]) * __uint_as_float(k2[j]);
+        }
+        // dq, dk summed over the G v-heads of the qk-head: every CTA of the group
+        // but the last to arrive leaves its partial (fp32) in the workspace; the
+        // last adds them in head order and writes the bf16 result
+        const int G = p.Hv / p.Hq;
+        if (G > 1) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (t0 + j < len) {
+                    const size_t off = ((size_t)(tok0 + t0 + j) * p.Hv + h) * 128 + k;
+                    p.dqp[off] = dqv[j];
+                    p.dkp[off] = dkv[j];
+                }
+            __threadfence();
+        }
+        __syncthreads();
+        if (tid == 0) *ticket = G > 1 ? atomicAdd(&p.gcnt[(size_t)c * p.Hq + hq], 1) : 0;
+        __syncthreads();
+        if (*ticket == G - 1) {
+            __threadfence();
+            __nv_bfloat16 *dqo = reinterpret_cast<__nv_bfloat16 *>(p.dq), *dko = reinterpret_cast<__nv_bfloat16 *>(p.dk);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int t = t0 + j;
+                if (t < len) {
+                    float sq = 0.f, sk = 0.f;
+                    for (int hh = hq * G; hh < hq * G + G; ++hh) {
+                        if (hh == h) {
+                            sq += dqv[j];
+                            sk += dkv[j];
+                        } else {
+                            const size_t off = ((size_t)(tok0 + t) * p.Hv + hh) * 128 + k;
+                            sq += __ldcg(p.dqp + off);
+                            sk += __ldcg(p.dkp + off);
+                        }
+                    }
+                    const size_t o = ((size_t)(tok0 + t) * p.Hq + hq) * 128 + k;
+                    dqo[o] = __float2bfloat16_rn(sq);
+                    dko[o] = __float2bfloat16_rn(sk);
+                }
+            }
+            if (tid == 0 && G > 1) p.gcnt[(size_t)c * p.Hq + hq] = 0;  // ready for the next call
+        }
+    }
+    // ---------------- gate and beta gradients ----------------
+    if (tid < 64) {
+        const int r = tid;
+        const float br = bet[r], egr = egv[r];
+        const float db = rRV[r] - egr * rRKS[r] + rLK[r];
+        const float dgam = -br * egr * rRKS[r] - rUdU[r] + p.scale * egr * rQdq[r] + rP[r] + br * rLK[r] - cL[r];
+        if (r < len) p.dbeta[(size_t)(tok0 + r) * p.Hv + h] = db;
+        dgm[r] = r < len ? dgam : 0.f;
+        tnp[r] = rUdU[r] - rP[r];
+    }
+    __syncthreads();
+    if (tid < 32) {
+        // dgamma_n collects e^{gamma_n} <dS1, S0> and the rows' shares; dg is the
+        // reverse cumulative sum of dgamma over the chunk
+        float tn = tnp[2 * lane] + tnp[2 * lane + 1];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) tn += __shfl_xor_sync(0xffffffffu, tn, o);
+        tn += __expf(gam[63]) * red[0];
+        float a = dgm[2 * lane], b = dgm[2 * lane + 1];
+        if (2 * lane == len - 1) a += tn;
+        if (2 * lane + 1 == len - 1) b += tn;
+        float s = a + b;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float n = __shfl_down_sync(0xffffffffu, s, o);
+            if (lane + o < 32) s += n;
+        }
+        if (2 * lane < len) p.dg[(size_t)(tok0 + 2 * lane) * p.Hv + h] = s;
+        if (2 * lane + 1 < len) p.dg[(size_t)(tok0 + 2 * lane + 1) * p.Hv + h] = s - a;
+    }
+out:
+    if (tid == 0) {  // no copy or MMA of this CTA may still be in flight when it leaves
+        if (tma_issued) drain_wait(&bars[0], 0);
+        if (ncommit > 0) drain_wait(&bars[1], (ncommit - 1) & 1);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512));
+    }
+}
+
+// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -1678,6 +2277,20 @@ int launch_dh(const char *name, const Params &p, cudaStream_t st) {
     return cudaGetLastError() != cudaSuccess;
 }
 
+int launch_bwd_chunk(const Params &p, cudaStream_t st) {
+    if (p.NT == 0) return 0;
+    BcMaps maps;
+    if (!map3(&maps.Q, p.q, p.Hq, p.Ttot, 64, true) || !map3(&maps.K, p.k, p.Hq, p.Ttot, 64, true) ||
+        !map3(&maps.dO, p.dout, p.Hv, p.Ttot, 64, true))
+        return 1;
+    if (cudaFuncSetAttribute(k_bwd_chunk_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kBcSmem) != cudaSuccess)
+        return 1;
+    tm_begin(p.tm, "tc_bwd_chunk", st);
+    k_bwd_chunk_tc<<<dim3(p.NT, p.Hv), kBcThreads, kBcSmem, st>>>(p, maps);
+    tm_end(p.tm, st);
+    return cudaGetLastError() != cudaSuccess;
+}
+
 template <bool kRev>
 int launch_combine(const char *name, const Params &p, cudaStream_t st) {
     if (p.N == 0) return 0;
@@ -1731,7 +2344,8 @@ int tc_bwd(const Params &p, int use_cp, cudaStream_t st) {
     // a10, a11: chunk-local gradients
     // the qk-head sums of dq and dk happen inside the chunk kernel
     if (cudaMemsetAsync(p.gcnt, 0, sizeof(int) * (size_t)p.NT * p.Hq, st) != cudaSuccess) return 1;
-    return mma_bwd_chunk(p, st);
+    static const bool warp_mma = getenv("GDR_BWD_WARP_MMA") != nullptr;
+    return warp_mma ? mma_bwd_chunk(p, st) : launch_bwd_chunk(p, st);
 }
 
 unsigned tc_take_status(cudaStream_t st) {

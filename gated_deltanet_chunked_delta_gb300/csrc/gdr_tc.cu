@@ -164,6 +164,17 @@ __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint3
         "r"(a), "l"(b), "r"(idesc), "r"(acc)
         : "memory");
 }
+// n MMAs into d, the operand descriptors advanced by da / db bytes per step
+// (the start-address field counts 16-byte units); the first accumulates iff acc.
+__device__ __forceinline__ void mma_seq(uint32_t d, uint64_t a, uint32_t da, uint64_t b, uint32_t db, uint32_t idesc,
+                                        int n, bool acc) {
+#pragma unroll 1
+    for (int i = 0; i < n; ++i) {
+        mma(d, a, b, idesc, (acc || i > 0) ? 1u : 0u);
+        a += da >> 4;
+        b += db >> 4;
+    }
+}
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(bar))
                  : "memory");
@@ -265,7 +276,6 @@ constexpr int kImg2 = 2 * kImg;  // hi and lo
 static_assert(kImg2 == kTileImgBytes, "tile image size");
 constexpr int kAux = kAuxBytes;
 
-__device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
 
 struct ChunkMaps {
     CUtensorMap K, Q;  // 3-D over k and q: (K, Hq, Ttot), box (64, 1, 64), 128-byte swizzle
@@ -277,20 +287,11 @@ struct ChunkMaps {
 __device__ __forceinline__ void st_img_hl(char *hi, char *lo, int row, int col0, const float *x /* 32 */) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        float hv[8], lw[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            hv[e] = bf16_round(x[8 * j + e]);
-            lw[e] = x[8 * j + e] - hv[e];
-        }
-        uint4 vh, vl;
-        vh.x = pack_bf16(hv[0], hv[1]); vh.y = pack_bf16(hv[2], hv[3]);
-        vh.z = pack_bf16(hv[4], hv[5]); vh.w = pack_bf16(hv[6], hv[7]);
-        vl.x = pack_bf16(lw[0], lw[1]); vl.y = pack_bf16(lw[2], lw[3]);
-        vl.z = pack_bf16(lw[4], lw[5]); vl.w = pack_bf16(lw[6], lw[7]);
+        uint32_t hv[4], lv[4];
+        split_pairs<4>(x + 8 * j, hv, lv);
         const int off = row * 128 + ((((col0 >> 3) + j) ^ (row & 7)) << 4);
-        *reinterpret_cast<uint4 *>(hi + off) = vh;
-        *reinterpret_cast<uint4 *>(lo + off) = vl;
+        *reinterpret_cast<uint4 *>(hi + off) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+        *reinterpret_cast<uint4 *>(lo + off) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
     }
 }
 // The same for a [hi | lo] pair of 64-row images kImg bytes apart (col0 = 0 or 32).
@@ -1607,9 +1608,9 @@ __global__ void __launch_bounds__(512) k_combine_tc(Params p) {
 
 // ---------------------------------------------------------------------------
 // Chunk-local gradients of the backward on tcgen05 (K = V = 128).  One CTA of
-// 256 threads per (chunk, v-head); thread 0 issues every MMA, all eight warps
-// run the epilogues (warp w reads TMEM lanes 32 (w % 4) .. + 31 and columns
-// [32 (w / 4), + 32)).  The same reverse mode as the warp-MMA kernel, with
+// 512 threads per (chunk, v-head); thread 0 issues every MMA, all sixteen
+// warps run the epilogues (warp w reads TMEM lanes 32 (w % 4) .. + 31 and
+// columns [16 (w / 4), + 16)).  The same reverse mode as the warp-MMA kernel, with
 // every product laid out so that its M side is 128 (a value, key or stacked
 // token index in the TMEM lanes):
 //   group 1  KS^T   = S0^T K^T          (S0 image read MN-major)
@@ -1637,7 +1638,7 @@ __global__ void __launch_bounds__(512) k_combine_tc(Params p) {
 struct BcMaps {
     CUtensorMap Q, K, dO;  // 3-D (x, head, token), box 64 x 1 x 64, 128-byte swizzle
 };
-constexpr int kBcThreads = 256;
+constexpr int kBcThreads = 512;
 // shared memory (bytes from the 1024-aligned base)
 constexpr int kBcKQ = 0;        // [Q ; K]: 2 atoms (k halves) x [128 rows][128 B]: Q rows 0-63, K rows 64-127
 constexpr int kBcOR = 32768;    // [dO ; dR_hi]: 2 atoms (v halves) x [128 rows][128 B]
@@ -1657,14 +1658,13 @@ constexpr uint32_t kTbU = 320;    // dUt^T hi | lo (packed A operand) -> dK2^T
 constexpr uint32_t kTbR = 384;    // R^T hi | lo (packed A operand)
 constexpr uint32_t kTbP1B = 448;  // [. ; dR_lo Ut_hi^T]
 
-// Byte offset of element (row, col), col < 64, in a 128-byte-swizzled bf16 atom.
-__device__ __forceinline__ int swz_at(int row, int col) {
-    return row * 128 + ((((col >> 3)) ^ (row & 7)) << 4) + (col & 7) * 2;
-}
-// Per lane x[0..31] -> the sum over the warp's lanes of x[lane] (reduce-scatter; x is consumed).
-__device__ __forceinline__ float warp_rs32(float (&x)[32], int lane) {
+// Per lane x[0..15] -> the sum over the warp's 32 lanes of x[lane % 16]
+// (an all-reduce over lane bit 4, then a reduce-scatter; x is consumed).
+__device__ __forceinline__ float warp_rs16(float (&x)[16], int lane) {
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
+    for (int i = 0; i < 16; ++i) x[i] += __shfl_xor_sync(0xffffffffu, x[i], 16);
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1) {
         const bool up = (lane & o) != 0;
 #pragma unroll
         for (int i = 0; i < o; ++i) {
@@ -1674,6 +1674,22 @@ __device__ __forceinline__ float warp_rs32(float (&x)[32], int lane) {
         }
     }
     return x[0];
+}
+// 16 columns [col0, col0 + 16) of row `row` (col0 a multiple of 8, inside one
+// 64-column atom) of a pair of 128-byte-swizzled bf16 images (hi, lo).
+__device__ __forceinline__ void st_img_hl16(char *hi, char *lo, int row, int col0, const float *x /* 16 */) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        uint32_t hv[4], lv[4];
+        split_pairs<4>(x + 8 * j, hv, lv);
+        const int off = row * 128 + ((((col0 >> 3) + j) ^ (row & 7)) << 4);
+        *reinterpret_cast<uint4 *>(hi + off) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+        *reinterpret_cast<uint4 *>(lo + off) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+    }
+}
+__device__ __forceinline__ void tmem_ld16w(uint32_t ta, uint32_t (&r)[16]) {
+    tmem_ld16_issue(ta, r);
+    tmem_wait_ld16(r);
 }
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
@@ -1690,10 +1706,9 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
     uint64_t *bars = reinterpret_cast<uint64_t *>(scr + 784);  // tma, mma
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2);
     volatile int *abort = reinterpret_cast<volatile int *>(bars + 3);
-    int *ticket = reinterpret_cast<int *>(bars + 4);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int q4 = warp & 3, hc = warp >> 2;
+    const int q4 = warp & 3, cq = warp >> 2;
     const uint32_t lq = (uint32_t)(q4 * 32) << 16;
     const int c = blockIdx.x, h = blockIdx.y;
     const ChunkInfo ci = p.chunk[c];
@@ -1702,7 +1717,7 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
     const size_t ch = (size_t)c * p.Hv + h;
     const long long cap = p.timeout_spins;
     const int row_v = 32 * q4 + lane;  // this thread's TMEM lane (a value, key or stacked token index)
-    const int t0 = 32 * hc;            // this thread's first TMEM column of a 64-column block
+    const int t0 = 16 * cq;            // this thread's 16 columns of a 64-column block
 
     if (tid == 0) {
         mbar_init(&bars[0], 1);
@@ -1748,49 +1763,52 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
         gam[2 * lane] = s - b;
         gam[2 * lane + 1] = s;
     }
-    // A image (rows past the chunk end: identity rows)
-    if (tid < 128) {
-        const int rr = tid >> 1, c0 = 32 * (tid & 1);
-        float x[32];
-        if (rr < len) {
-            const float4 *src = reinterpret_cast<const float4 *>(p.A_in + ((size_t)(tok0 + rr) * p.Hv + h) * 64 + c0);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float4 v = src[i];
-                x[4 * i] = v.x; x[4 * i + 1] = v.y; x[4 * i + 2] = v.z; x[4 * i + 3] = v.w;
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) x[i] = (c0 + i == rr) ? 1.f : 0.f;
-        }
-        st_img_hl(Aim, Aim + 8192, rr, c0, x);
-    }
-    // S0 image: row k, 32 columns per item
     {
-        const float *S0g = p.hbuf + ch * 128 * 128;
-#pragma unroll 1
-        for (int u = 0; u < 2; ++u) {
-            const int it = tid + kBcThreads * u, k = it >> 2, cq = it & 3;
-            const float4 *src = reinterpret_cast<const float4 *>(S0g + (size_t)k * 128 + 32 * cq);
-            float x[32];
+        // every load of this phase in flight before the conversions: one S0
+        // item (row k, 32 columns), the A rows (threads 0-127), the dUt^T column
+        const int k = tid >> 2, sq = tid & 3;
+        const float4 *s0 = reinterpret_cast<const float4 *>(p.hbuf + ch * 128 * 128 + (size_t)k * 128 + 32 * sq);
+        float4 sv[8], av[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float4 v = src[i];
-                x[4 * i] = v.x; x[4 * i + 1] = v.y; x[4 * i + 2] = v.z; x[4 * i + 3] = v.w;
+        for (int i = 0; i < 8; ++i) sv[i] = s0[i];
+        const int rr = (tid & 127) >> 1, ac0 = 32 * (tid & 1);
+        if (tid < 128) {
+            if (rr < len) {
+                const float4 *src =
+                    reinterpret_cast<const float4 *>(p.A_in + ((size_t)(tok0 + rr) * p.Hv + h) * 64 + ac0);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) av[i] = src[i];
+            } else {
+                // rows past the chunk end: identity rows
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int c4 = ac0 + 4 * i;
+                    av[i] = make_float4(c4 == rr, c4 + 1 == rr, c4 + 2 == rr, c4 + 3 == rr);
+                }
             }
-            st_img_hl(Sim + (cq >> 1) * 16384, Sim + 32768 + (cq >> 1) * 16384, k, 32 * (cq & 1), x);
         }
-    }
-    // dUt^T (lane v, tokens t0..t0+31; rows past the chunk end zero) -> packed hi | lo A operand
-    {
         const float *dUg = p.dubuf + ch * 64 * 128 + row_v;
-        float x[32];
+        float du[16];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] = t0 + j < len ? dUg[(size_t)(t0 + j) * 128] : 0.f;
-        uint32_t hv[16], lv[16];
-        split_pairs<16>(x, hv, lv);
-        tmem_st16(tmem + kTbU + t0 / 2 + lq, hv);
-        tmem_st16(tmem + kTbU + 32 + t0 / 2 + lq, lv);
+        for (int j = 0; j < 16; ++j) du[j] = t0 + j < len ? dUg[(size_t)(t0 + j) * 128] : 0.f;
+        float x[32];
+        if (tid < 128) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                x[4 * i] = av[i].x; x[4 * i + 1] = av[i].y; x[4 * i + 2] = av[i].z; x[4 * i + 3] = av[i].w;
+            }
+            st_img_hl(Aim, Aim + 8192, rr, ac0, x);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            x[4 * i] = sv[i].x; x[4 * i + 1] = sv[i].y; x[4 * i + 2] = sv[i].z; x[4 * i + 3] = sv[i].w;
+        }
+        st_img_hl(Sim + (sq >> 1) * 16384, Sim + 32768 + (sq >> 1) * 16384, k, 32 * (sq & 1), x);
+        // dUt^T (rows past the chunk end zero) -> packed hi | lo A operand
+        uint32_t hv[8], lv[8];
+        split_pairs<8>(du, hv, lv);
+        tmem_st8(tmem + kTbU + t0 / 2 + lq, hv);
+        tmem_st8(tmem + kTbU + 32 + t0 / 2 + lq, lv);
         tmem_wait_st();
     }
     __syncthreads();  // gates
@@ -1805,27 +1823,19 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
     if (tid == 0) {
         if (bwait(&bars[0], 0, cap, abort)) {
             tc_fence_after();
-            {  // KS^T = S0^T K^T: A = S0 image MN-major (M = v in two 64-blocks 16 KiB apart), B = K rows
-                const uint32_t id = idesc_bf16(128, 64, 1, 0);
-#pragma unroll
-                for (int tm = 0; tm < 2; ++tm)
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma(tmem + kTbKS, sdesc(sS + tm * 32768 + kk * 2048, 16384),
-                            sdesc(sKQ + (kk >> 2) * 16384 + 8192 + (kk & 3) * 32), id, (tm | kk) != 0);
-            }
-            {  // dQr^T = S0 dO^T: A = S0 image K-major (M = k), B = dO rows
-                const uint32_t id = idesc_bf16(128, 64, 0, 0);
-#pragma unroll
-                for (int tm = 0; tm < 2; ++tm)
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma(tmem + kTbDQ, sdesc(sS + tm * 32768 + (kk >> 2) * 16384 + (kk & 3) * 32),
-                            sdesc(sOR + (kk >> 2) * 16384 + (kk & 3) * 32), id, (tm | kk) != 0);
-            }
+            // KS^T = S0^T K^T: A = S0 image MN-major (M = v in two 64-blocks 16 KiB apart), B = K rows
+            for (int tm = 0; tm < 2; ++tm)
+                for (int at = 0; at < 2; ++at)
+                    mma_seq(tmem + kTbKS, sdesc(sS + tm * 32768 + at * 8192, 16384), 2048,
+                            sdesc(sKQ + at * 16384 + 8192), 32, idesc_bf16(128, 64, 1, 0), 4, (tm | at) != 0);
+            // dQr^T = S0 dO^T: A = S0 image K-major (M = k), B = dO rows
+            for (int tm = 0; tm < 2; ++tm)
+                for (int at = 0; at < 2; ++at)
+                    mma_seq(tmem + kTbDQ, sdesc(sS + tm * 32768 + at * 16384), 32, sdesc(sOR + at * 16384), 32,
+                            idesc_bf16(128, 64, 0, 0), 4, (tm | at) != 0);
             {  // dR^T = dUt^T A: A operand dUt^T from TMEM, B = A image MN-major (K = s rows)
                 const uint32_t id = idesc_bf16(128, 64, 0, 1);
-#pragma unroll
+#pragma unroll 1
                 for (int kk = 0; kk < 4; ++kk) {
                     mma_ts(tmem + kTbDR, tmem + kTbU + 8 * kk, sdesc(sA + kk * 2048), id, kk > 0);
                     mma_ts(tmem + kTbDR, tmem + kTbU + 32 + 8 * kk, sdesc(sA + kk * 2048), id, 1);
@@ -1836,6 +1846,14 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
             ncommit = 1;
         }
     }
+    // this thread's V column (lane v, tokens t0..) loads while the MMAs run
+    float vv[16];
+    {
+        const __nv_bfloat16 *vin = reinterpret_cast<const __nv_bfloat16 *>(p.v) + ((size_t)tok0 * p.Hv + h) * 128 + row_v;
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            vv[j] = t0 + j < len ? __bfloat162float(vin[(size_t)(t0 + j) * p.Hv * 128]) : 0.f;
+    }
     ok = bwait(&bars[1], 0, cap, abort);
     if (__syncthreads_or(!ok)) goto out;
     tc_fence_after();
@@ -1843,59 +1861,71 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
     {
         // lane v: R^T, dv, dKS^T, dR (as rows of the [dO ; dR] operand), row sums dR.V, dR.KS
         const int v = row_v;
-        uint32_t ksu[32], dru[32];
-        tmem_ld32(tmem + kTbKS + t0 + lq, ksu);
-        tmem_ld32(tmem + kTbDR + t0 + lq, dru);
-        const __nv_bfloat16 *vin = reinterpret_cast<const __nv_bfloat16 *>(p.v) + ((size_t)tok0 * p.Hv + h) * 128 + v;
+        uint32_t ksu[16], dru[16];
+        tmem_ld16_issue(tmem + kTbKS + t0 + lq, ksu);
+        tmem_ld16_issue(tmem + kTbDR + t0 + lq, dru);
+        tmem_wait_ld16(ksu);
+        tmem_hold16(dru);
         const size_t tstride = (size_t)p.Hv * 128;
-        float vv[32], x[32];
+        float x[16];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) vv[j] = t0 + j < len ? __bfloat162float(vin[(size_t)(t0 + j) * tstride]) : 0.f;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] = bet[t0 + j] * (vv[j] - egv[t0 + j] * __uint_as_float(ksu[j]));
+        for (int j = 0; j < 16; ++j) x[j] = bet[t0 + j] * (vv[j] - egv[t0 + j] * __uint_as_float(ksu[j]));
         {
-            uint32_t hv[16], lv[16];
-            split_pairs<16>(x, hv, lv);
-            tmem_st16(tmem + kTbR + t0 / 2 + lq, hv);
-            tmem_st16(tmem + kTbR + 32 + t0 / 2 + lq, lv);
+            uint32_t hv[8], lv[8];
+            split_pairs<8>(x, hv, lv);
+            tmem_st8(tmem + kTbR + t0 / 2 + lq, hv);
+            tmem_st8(tmem + kTbR + 32 + t0 / 2 + lq, lv);
         }
-        float a1[32], a2[32];
+        float a1[16], a2[16];
         __nv_bfloat16 *dvo = reinterpret_cast<__nv_bfloat16 *>(p.dv) + ((size_t)tok0 * p.Hv + h) * 128 + v;
-        char *orh = OR + (v >> 6) * 16384 + 8192;  // rows 64-127 of the v half's atom
-        char *orl = RL + (v >> 6) * 8192;
+        // rows 64 + t of the v half's [dO ; dR_hi] atom and row t of its dR_lo atom;
+        // t0 is a multiple of 8, so row t's 16-byte chunk is (v % 64) / 8 ^ (j % 8)
+        const int xc = ((v & 63) >> 3), xb = (v & 7) * 2;
+        char *orh = OR + (v >> 6) * 16384 + 8192 + t0 * 128 + xb;
+        char *orl = RL + (v >> 6) * 8192 + t0 * 128 + xb;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
+        for (int j = 0; j < 16; ++j) {
             const int t = t0 + j;
             const float dr = __uint_as_float(dru[j]);
             a1[j] = dr * vv[j];
             a2[j] = dr * __uint_as_float(ksu[j]);
             if (t < len) dvo[(size_t)t * tstride] = __float2bfloat16_rn(bet[t] * dr);
             x[j] = -bet[t] * egv[t] * dr;
-            const __nv_bfloat16 hb = __float2bfloat16_rn(dr);
-            const __nv_bfloat16 lb = __float2bfloat16_rn(dr - __bfloat162float(hb));
-            const int off = swz_at(t, v & 63);
-            *reinterpret_cast<__nv_bfloat16 *>(orh + off) = hb;
-            *reinterpret_cast<__nv_bfloat16 *>(orl + off) = lb;
+            const uint32_t hw = pack_bf16(dr, 0.f);
+            const int off = j * 128 + ((xc ^ (j & 7)) << 4);
+            *reinterpret_cast<uint16_t *>(orh + off) = (uint16_t)hw;
+            *reinterpret_cast<__nv_bfloat16 *>(orl + off) = __float2bfloat16_rn(dr - __uint_as_float(hw << 16));
         }
-        st_img_hl(Wim, Wim + 16384, v, t0, x);  // dKS^T row v
-        const float s1 = warp_rs32(a1, lane);
-        const float s2 = warp_rs32(a2, lane);
-        atomicAdd(&rRV[t0 + lane], s1);
-        atomicAdd(&rRKS[t0 + lane], s2);
+        st_img_hl16(Wim, Wim + 16384, v, t0, x);  // dKS^T row v
+        const float s1 = warp_rs16(a1, lane);
+        const float s2 = warp_rs16(a2, lane);
+        if (lane < 16) {
+            atomicAdd(&rRV[t0 + lane], s1);
+            atomicAdd(&rRKS[t0 + lane], s2);
+        }
     }
     {
         // lane k: row sums dQr.Q (Q from the [Q ; K] image)
         const int k = row_v;
-        uint32_t dqu[32];
-        tmem_ld32(tmem + kTbDQ + t0 + lq, dqu);
-        const char *qa = KQ + (k >> 6) * 16384;
-        float a[32];
+        uint32_t dqu[16];
+        tmem_ld16w(tmem + kTbDQ + t0 + lq, dqu);
+        const char *qa = KQ + (k >> 6) * 16384 + t0 * 128 + (k & 7) * 2;
+        const int xc = (k & 63) >> 3;
+        float a[16];
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
+        for (int j = 0; j < 16; ++j)
             a[j] = __uint_as_float(dqu[j]) *
-                   __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(qa + swz_at(t0 + j, k & 63)));
-        const float s = warp_rs32(a, lane);
-        atomicAdd(&rQdq[t0 + lane], s);
+                   __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(qa + j * 128 + ((xc ^ (j & 7)) << 4)));
+        const float s = warp_rs16(a, lane);
+        if (lane < 16) atomicAdd(&rQdq[t0 + lane], s);
+    }
+    // this thread's dS1 item loads while the next MMAs run
+    float4 d1v[8];
+    {
+        const int k = tid >> 2, sq = tid & 3;
+        const float4 *src = reinterpret_cast<const float4 *>(p.dhbuf + ch * 128 * 128 + (size_t)k * 128 + 32 * sq);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) d1v[i] = src[i];
     }
     tmem_wait_st();
     fence_async_smem();
@@ -1906,23 +1936,18 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
         tc_fence_after();
         {  // Ut^T = R^T A^T: A operand R^T from TMEM, B = A image K-major (rows t)
             const uint32_t id = idesc_bf16(128, 64, 0, 0);
-#pragma unroll
+#pragma unroll 1
             for (int kk = 0; kk < 4; ++kk) {
                 mma_ts(tmem + kTbKS, tmem + kTbR + 8 * kk, sdesc(sA + kk * 32), id, kk > 0);
                 mma_ts(tmem + kTbKS, tmem + kTbR + 32 + 8 * kk, sdesc(sA + kk * 32), id, 1);
                 mma_ts(tmem + kTbKS, tmem + kTbR + 8 * kk, sdesc(sA + 8192 + kk * 32), id, 1);
             }
         }
-        {  // dK^T = S0 dKS^T: B = dKS^T image MN-major (K = v rows)
-            const uint32_t id = idesc_bf16(128, 64, 0, 1);
-            const int ta[3] = {0, 1, 0}, tb[3] = {0, 0, 1};
-#pragma unroll
-            for (int m = 0; m < 3; ++m)
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma(tmem + kTbDK, sdesc(sS + ta[m] * 32768 + (kk >> 2) * 16384 + (kk & 3) * 32),
-                        sdesc(sW + tb[m] * 16384 + kk * 2048), id, (m | kk) != 0);
-        }
+        // dK^T = S0 dKS^T: B = dKS^T image MN-major (K = v rows); terms (hi, hi), (lo, hi), (hi, lo)
+        for (int m = 0; m < 3; ++m)
+            for (int at = 0; at < 2; ++at)
+                mma_seq(tmem + kTbDK, sdesc(sS + (m == 1) * 32768 + at * 16384), 32,
+                        sdesc(sW + (m == 2) * 16384 + at * 8192), 2048, idesc_bf16(128, 64, 0, 1), 4, (m | at) != 0);
         mma_commit(&bars[1]);
         ncommit = 2;
     }
@@ -1933,53 +1958,51 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
     {
         // lane v: Ut^T -> image (B operand of group 3), row sums dUt.Ut
         const int v = row_v;
-        uint32_t uu[32], dh[16], dl[16];
-        tmem_ld32(tmem + kTbKS + t0 + lq, uu);
-        tmem_ld16_issue(tmem + kTbU + t0 / 2 + lq, dh);
-        tmem_ld16_issue(tmem + kTbU + 32 + t0 / 2 + lq, dl);
-        tmem_wait_ld16(dh);
-        tmem_hold16(dl);
-        float x[32], a[32];
+        uint32_t uu[16], dh[8], dl[8];
+        tmem_ld16w(tmem + kTbKS + t0 + lq, uu);
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                     : "=r"(dh[0]), "=r"(dh[1]), "=r"(dh[2]), "=r"(dh[3]), "=r"(dh[4]), "=r"(dh[5]), "=r"(dh[6]),
+                       "=r"(dh[7])
+                     : "r"(tmem + kTbU + t0 / 2 + lq));
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                     : "=r"(dl[0]), "=r"(dl[1]), "=r"(dl[2]), "=r"(dl[3]), "=r"(dl[4]), "=r"(dl[5]), "=r"(dl[6]),
+                       "=r"(dl[7])
+                     : "r"(tmem + kTbU + 32 + t0 / 2 + lq));
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        float x[16], a[16];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(uu[j]);
-        st_img_hl(Wim, Wim + 16384, v, t0, x);
+        for (int j = 0; j < 16; ++j) x[j] = __uint_as_float(uu[j]);
+        st_img_hl16(Wim, Wim + 16384, v, t0, x);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < 8; ++i) {
             a[2 * i] = (bf_lo(dh[i]) + bf_lo(dl[i])) * x[2 * i];
             a[2 * i + 1] = (bf_hi(dh[i]) + bf_hi(dl[i])) * x[2 * i + 1];
         }
-        const float s = warp_rs32(a, lane);
-        atomicAdd(&rUdU[t0 + lane], s);
+        const float s = warp_rs16(a, lane);
+        if (lane < 16) atomicAdd(&rUdU[t0 + lane], s);
     }
     {
-        // dS1 image over the S0 image, with <dS1, S0> from the S0 terms it replaces
-        const float *dS1g = p.dhbuf + ch * 128 * 128;
-        float part = 0.f;
-#pragma unroll 1
-        for (int u = 0; u < 2; ++u) {
-            const int it = tid + kBcThreads * u, k = it >> 2, cq = it & 3;
-            char *ih = Sim + (cq >> 1) * 16384, *il = ih + 32768;
-            const int c0 = 32 * (cq & 1);
-            const float4 *src = reinterpret_cast<const float4 *>(dS1g + (size_t)k * 128 + 32 * cq);
-            float x[32];
+        // the dS1 image over the S0 image, with <dS1, S0> from the S0 terms it replaces
+        const int k = tid >> 2, sq = tid & 3;
+        char *ih = Sim + (sq >> 1) * 16384, *il = ih + 32768;
+        const int c0 = 32 * (sq & 1);
+        float x[32], part = 0.f;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float4 v = src[i];
-                x[4 * i] = v.x; x[4 * i + 1] = v.y; x[4 * i + 2] = v.z; x[4 * i + 3] = v.w;
-            }
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int off = k * 128 + ((((c0 >> 3) + j) ^ (k & 7)) << 4);
-                const uint4 wh = *reinterpret_cast<const uint4 *>(ih + off);
-                const uint4 wl = *reinterpret_cast<const uint4 *>(il + off);
-                const uint32_t hh[4] = {wh.x, wh.y, wh.z, wh.w}, ll[4] = {wl.x, wl.y, wl.z, wl.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    part += x[8 * j + 2 * e] * (bf_lo(hh[e]) + bf_lo(ll[e])) +
-                            x[8 * j + 2 * e + 1] * (bf_hi(hh[e]) + bf_hi(ll[e]));
-            }
-            st_img_hl(ih, il, k, c0, x);
+        for (int i = 0; i < 8; ++i) {
+            x[4 * i] = d1v[i].x; x[4 * i + 1] = d1v[i].y; x[4 * i + 2] = d1v[i].z; x[4 * i + 3] = d1v[i].w;
         }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int off = k * 128 + ((((c0 >> 3) + j) ^ (k & 7)) << 4);
+            const uint4 wh = *reinterpret_cast<const uint4 *>(ih + off);
+            const uint4 wl = *reinterpret_cast<const uint4 *>(il + off);
+            const uint32_t hh[4] = {wh.x, wh.y, wh.z, wh.w}, ll[4] = {wl.x, wl.y, wl.z, wl.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                part += x[8 * j + 2 * e] * (bf_lo(hh[e]) + bf_lo(ll[e])) +
+                        x[8 * j + 2 * e + 1] * (bf_hi(hh[e]) + bf_hi(ll[e]));
+        }
+        st_img_hl(ih, il, k, c0, x);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
         if (lane == 0) atomicAdd(&red[0], part);
@@ -1992,32 +2015,21 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
         tc_fence_after();
         const uint32_t id = idesc_bf16(128, 64, 0, 1);
         // [dO ; dR_hi] (Ut_hi + Ut_lo)^T, and [. ; dR_lo] Ut_hi^T: B = Ut^T image MN-major
-#pragma unroll
         for (int tb = 0; tb < 2; ++tb)
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-                mma(tmem + kTbP1, sdesc(sOR + (kk >> 2) * 16384 + (kk & 3) * 32), sdesc(sW + tb * 16384 + kk * 2048),
-                    id, (tb | kk) != 0);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-            mma(tmem + kTbP1B, sdesc(sRL - 8192 + (kk >> 2) * 8192 + (kk & 3) * 32), sdesc(sW + kk * 2048), id,
-                kk > 0);
-        {  // dK2^T = dS1 Ut^T
-            const int ta[3] = {0, 1, 0}, tb[3] = {0, 0, 1};
-#pragma unroll
-            for (int m = 0; m < 3; ++m)
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma(tmem + kTbU, sdesc(sS + ta[m] * 32768 + (kk >> 2) * 16384 + (kk & 3) * 32),
-                        sdesc(sW + tb[m] * 16384 + kk * 2048), id, (m | kk) != 0);
-        }
-        {  // [Q ; K] K^T
-            const uint32_t id2 = idesc_bf16(128, 64, 0, 0);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-                mma(tmem + kTbDR, sdesc(sKQ + (kk >> 2) * 16384 + (kk & 3) * 32),
-                    sdesc(sKQ + (kk >> 2) * 16384 + 8192 + (kk & 3) * 32), id2, kk > 0);
-        }
+            for (int at = 0; at < 2; ++at)
+                mma_seq(tmem + kTbP1, sdesc(sOR + at * 16384), 32, sdesc(sW + tb * 16384 + at * 8192), 2048, id, 4,
+                        (tb | at) != 0);
+        for (int at = 0; at < 2; ++at)
+            mma_seq(tmem + kTbP1B, sdesc(sRL - 8192 + at * 8192), 32, sdesc(sW + at * 8192), 2048, id, 4, at != 0);
+        // dK2^T = dS1 Ut^T
+        for (int m = 0; m < 3; ++m)
+            for (int at = 0; at < 2; ++at)
+                mma_seq(tmem + kTbU, sdesc(sS + (m == 1) * 32768 + at * 16384), 32,
+                        sdesc(sW + (m == 2) * 16384 + at * 8192), 2048, id, 4, (m | at) != 0);
+        // [Q ; K] K^T
+        for (int at = 0; at < 2; ++at)
+            mma_seq(tmem + kTbDR, sdesc(sKQ + at * 16384), 32, sdesc(sKQ + at * 16384 + 8192), 32,
+                    idesc_bf16(128, 64, 0, 0), 4, at != 0);
         mma_commit(&bars[1]);
         ncommit = 3;
     }
@@ -2028,31 +2040,36 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
     if (q4 < 2) {
         // row t of dP'' = scale e^{gamma_t - gamma_s} (dO Ut^T)[t][s], s <= t < len; row sum dP''.QK
         const int t = row_v;
-        uint32_t pu[32], qu[32];
-        tmem_ld32(tmem + kTbP1 + t0 + lq, pu);
-        tmem_ld32(tmem + kTbDR + t0 + lq, qu);
+        uint32_t pu[16], qu[16];
+        tmem_ld16_issue(tmem + kTbP1 + t0 + lq, pu);
+        tmem_ld16_issue(tmem + kTbDR + t0 + lq, qu);
+        tmem_wait_ld16(pu);
+        tmem_hold16(qu);
         const float gt = gam[t];
-        float x[32], rp = 0.f;
+        float x[16], rp = 0.f;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
+        for (int j = 0; j < 16; ++j) {
             const int s = t0 + j;
             x[j] = (s <= t && t < len) ? p.scale * __expf(gt - gam[s]) * __uint_as_float(pu[j]) : 0.f;
             rp += x[j] * __uint_as_float(qu[j]);
         }
-        st_img_hl(Wim, Wim + 8192, t, t0, x);
+        st_img_hl16(Wim, Wim + 8192, t, t0, x);
         atomicAdd(&rP[t], rp);
     } else {
         // row t of dL = -(X A^T)[t][s], s < t < len; MM = dL b_t e^{gamma_t - gamma_s};
         // row sums dL e KK, column sums dL b e KK
         const int t = row_v - 64;
-        uint32_t pu[32], pb[32], ku[32];
-        tmem_ld32(tmem + kTbP1 + t0 + lq, pu);
-        tmem_ld32(tmem + kTbP1B + t0 + lq, pb);
-        tmem_ld32(tmem + kTbDR + t0 + lq, ku);
+        uint32_t pu[16], pb[16], ku[16];
+        tmem_ld16_issue(tmem + kTbP1 + t0 + lq, pu);
+        tmem_ld16_issue(tmem + kTbP1B + t0 + lq, pb);
+        tmem_ld16_issue(tmem + kTbDR + t0 + lq, ku);
+        tmem_wait_ld16(pu);
+        tmem_hold16(pb);
+        tmem_hold16(ku);
         const float gt = gam[t], bt = bet[t];
-        float mmx[32], col[32], rl = 0.f;
+        float mmx[16], col[16], rl = 0.f;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
+        for (int j = 0; j < 16; ++j) {
             const int s = t0 + j;
             const bool in = s < t && t < len;
             const float e = in ? __expf(gt - gam[s]) : 0.f;
@@ -2062,10 +2079,10 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
             col[j] = dl * bt * ek;
             mmx[j] = dl * bt * e;
         }
-        st_img_hl(Wim + 16384, Wim + 24576, t, t0, mmx);
+        st_img_hl16(Wim + 16384, Wim + 24576, t, t0, mmx);
         atomicAdd(&rLK[t], rl);
-        const float s = warp_rs32(col, lane);
-        atomicAdd(&cL[t0 + lane], s);
+        const float s = warp_rs16(col, lane);
+        if (lane < 16) atomicAdd(&cL[t0 + lane], s);
     }
     fence_async_smem();
     tc_fence_before();
@@ -2074,22 +2091,16 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
     if (tid == 0) {
         tc_fence_after();
         // A = K^T or Q^T: the K (Q) rows read MN-major (M = k in two 64-blocks 16 KiB apart)
-        const uint32_t aK = sKQ + 8192, aQ = sKQ;
+        const uint64_t aK = sdesc(sKQ + 8192, 16384), aQ = sdesc(sKQ, 16384);
         const uint32_t idK = idesc_bf16(128, 64, 1, 0), idM = idesc_bf16(128, 64, 1, 1);
-#pragma unroll
-        for (int tb = 0; tb < 2; ++tb)
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)  // dq2^T = K^T dP''^T (B = dP'' rows t, K-major)
-                mma(tmem + kTbKS, sdesc(aK + kk * 2048, 16384), sdesc(sW + tb * 8192 + kk * 32), idK, (tb | kk) != 0);
-#pragma unroll
-        for (int tb = 0; tb < 2; ++tb)
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                // dK^T += Q^T dP'' (B MN-major), K^T MM^T (B K-major), K^T MM (B MN-major)
-                mma(tmem + kTbDK, sdesc(aQ + kk * 2048, 16384), sdesc(sW + tb * 8192 + kk * 2048), idM, 1);
-                mma(tmem + kTbDK, sdesc(aK + kk * 2048, 16384), sdesc(sW + 16384 + tb * 8192 + kk * 32), idK, 1);
-                mma(tmem + kTbDK, sdesc(aK + kk * 2048, 16384), sdesc(sW + 16384 + tb * 8192 + kk * 2048), idM, 1);
-            }
+        for (int tb = 0; tb < 2; ++tb) {
+            // dq2^T = K^T dP''^T (B = dP'' rows t, K-major)
+            mma_seq(tmem + kTbKS, aK, 2048, sdesc(sW + tb * 8192), 32, idK, 4, tb != 0);
+            // dK^T += Q^T dP'' (B MN-major), K^T MM^T (B K-major), K^T MM (B MN-major)
+            mma_seq(tmem + kTbDK, aQ, 2048, sdesc(sW + tb * 8192), 2048, idM, 4, true);
+            mma_seq(tmem + kTbDK, aK, 2048, sdesc(sW + 16384 + tb * 8192), 32, idK, 4, true);
+            mma_seq(tmem + kTbDK, aK, 2048, sdesc(sW + 16384 + tb * 8192), 2048, idM, 4, true);
+        }
         mma_commit(&bars[1]);
         ncommit = 4;
     }
@@ -2100,59 +2111,42 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
     {
         const int k = row_v;
         const float gC = gam[63];
-        uint32_t qr[32], q2[32], kd[32], k2[32];
-        tmem_ld32(tmem + kTbDQ + t0 + lq, qr);
-        tmem_ld32(tmem + kTbKS + t0 + lq, q2);
-        tmem_ld32(tmem + kTbDK + t0 + lq, kd);
-        tmem_ld32(tmem + kTbU + t0 + lq, k2);
-        float dqv[32], dkv[32];
+        uint32_t qr[16], q2[16], kd[16], k2[16];
+        tmem_ld16_issue(tmem + kTbDQ + t0 + lq, qr);
+        tmem_ld16_issue(tmem + kTbKS + t0 + lq, q2);
+        tmem_ld16_issue(tmem + kTbDK + t0 + lq, kd);
+        tmem_ld16_issue(tmem + kTbU + t0 + lq, k2);
+        tmem_wait_ld16(qr);
+        tmem_hold16(q2);
+        tmem_hold16(kd);
+        tmem_hold16(k2);
+        float dqv[16], dkv[16];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
+        for (int j = 0; j < 16; ++j) {
             const int t = t0 + j;
             dqv[j] = p.scale * egv[t] * __uint_as_float(qr[j]) + __uint_as_float(q2[j]);
             dkv[j] = __uint_as_float(kd[j]) + __expf(gC - gam[t]) * __uint_as_float(k2[j]);
         }
-        // dq, dk summed over the G v-heads of the qk-head: every CTA of the group
-        // but the last to arrive leaves its partial (fp32) in the workspace; the
-        // last adds them in head order and writes the bf16 result
+        // with G > 1 v-heads per qk-head the fp32 partials go to the workspace and
+        // a separate pass sums them in head order; with G = 1 dq, dk are final
         const int G = p.Hv / p.Hq;
         if (G > 1) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
+            for (int j = 0; j < 16; ++j)
                 if (t0 + j < len) {
                     const size_t off = ((size_t)(tok0 + t0 + j) * p.Hv + h) * 128 + k;
                     p.dqp[off] = dqv[j];
                     p.dkp[off] = dkv[j];
                 }
-            __threadfence();
-        }
-        __syncthreads();
-        if (tid == 0) *ticket = G > 1 ? atomicAdd(&p.gcnt[(size_t)c * p.Hq + hq], 1) : 0;
-        __syncthreads();
-        if (*ticket == G - 1) {
-            __threadfence();
+        } else {
             __nv_bfloat16 *dqo = reinterpret_cast<__nv_bfloat16 *>(p.dq), *dko = reinterpret_cast<__nv_bfloat16 *>(p.dk);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int t = t0 + j;
-                if (t < len) {
-                    float sq = 0.f, sk = 0.f;
-                    for (int hh = hq * G; hh < hq * G + G; ++hh) {
-                        if (hh == h) {
-                            sq += dqv[j];
-                            sk += dkv[j];
-                        } else {
-                            const size_t off = ((size_t)(tok0 + t) * p.Hv + hh) * 128 + k;
-                            sq += __ldcg(p.dqp + off);
-                            sk += __ldcg(p.dkp + off);
-                        }
-                    }
-                    const size_t o = ((size_t)(tok0 + t) * p.Hq + hq) * 128 + k;
-                    dqo[o] = __float2bfloat16_rn(sq);
-                    dko[o] = __float2bfloat16_rn(sk);
+            for (int j = 0; j < 16; ++j)
+                if (t0 + j < len) {
+                    const size_t o = ((size_t)(tok0 + t0 + j) * p.Hq + hq) * 128 + k;
+                    dqo[o] = __float2bfloat16_rn(dqv[j]);
+                    dko[o] = __float2bfloat16_rn(dkv[j]);
                 }
-            }
-            if (tid == 0 && G > 1) p.gcnt[(size_t)c * p.Hq + hq] = 0;  // ready for the next call
         }
     }
     // ---------------- gate and beta gradients ----------------
@@ -2343,9 +2337,13 @@ int tc_bwd(const Params &p, int use_cp, cudaStream_t st) {
     if (launch_dh<kDhFull>("tc_dh", p, st)) return 1;
     // a10, a11: chunk-local gradients
     // the qk-head sums of dq and dk happen inside the chunk kernel
-    if (cudaMemsetAsync(p.gcnt, 0, sizeof(int) * (size_t)p.NT * p.Hq, st) != cudaSuccess) return 1;
     static const bool warp_mma = getenv("GDR_BWD_WARP_MMA") != nullptr;
-    return warp_mma ? mma_bwd_chunk(p, st) : launch_bwd_chunk(p, st);
+    if (warp_mma) {
+        if (cudaMemsetAsync(p.gcnt, 0, sizeof(int) * (size_t)p.NT * p.Hq, st) != cudaSuccess) return 1;
+        return mma_bwd_chunk(p, st);
+    }
+    if (launch_bwd_chunk(p, st)) return 1;
+    return p.Hv > p.Hq ? simt_group_sum(p, st) : 0;
 }
 
 unsigned tc_take_status(cudaStream_t st) {

@@ -55,6 +55,10 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *b) {
 __device__ __forceinline__ void mbar_expect_tx(uint64_t *b, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(bytes) : "memory");
 }
+// Adds `bytes` to the current phase's expected transaction count without arriving.
+__device__ __forceinline__ void mbar_expect_tx_only(uint64_t *b, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ uint32_t mbar_try(uint64_t *b, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -211,6 +215,14 @@ __device__ __forceinline__ void tmem_wait_ld16(uint32_t (&r)[16]) {
 __device__ __forceinline__ void tmem_hold16(uint32_t (&r)[16]) {
     asm volatile("" : W4(0), W4(4), W4(8), W4(12)::"memory");
 }
+// 8 consecutive TMEM columns of this warp's lanes (issue only; tmem_wait_ld8
+// or a later wait plus tmem_hold8 before use).
+__device__ __forceinline__ void tmem_ld8_issue(uint32_t ta, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(ta));
+}
+__device__ __forceinline__ void tmem_hold8(uint32_t (&r)[8]) { asm volatile("" : W4(0), W4(4)::"memory"); }
 // Orders the use of a second load's registers after a wait already issued.
 __device__ __forceinline__ void tmem_st32(uint32_t ta, const uint32_t (&r)[32]) {
     asm volatile(
@@ -1637,7 +1649,10 @@ __global__ void __launch_bounds__(512) k_combine_tc(Params p) {
 // ---------------------------------------------------------------------------
 struct BcMaps {
     CUtensorMap Q, K, dO;  // 3-D (x, head, token), box 64 x 1 x 64, 128-byte swizzle
+    CUtensorMap S0, dU;    // fp32 3-D (v, k or t, unit), box 32 x 128 (64) x 1, 128-byte swizzle
+    CUtensorMap A;         // fp32 3-D (s, head, token), box 32 x 1 x 64, 128-byte swizzle
 };
+constexpr uint32_t kBcPrefetch = 16384 + 65536 + 16384 + 32768 + 32768;  // A, S0, dO, [Q ; K], dUt per unit
 constexpr int kBcThreads = 512;
 // shared memory (bytes from the 1024-aligned base)
 constexpr int kBcKQ = 0;        // [Q ; K]: 2 atoms (k halves) x [128 rows][128 B]: Q rows 0-63, K rows 64-127
@@ -1654,8 +1669,8 @@ constexpr uint32_t kTbP1 = 64;    // [dO Ut^T ; dR_hi Ut^T + ...]
 constexpr uint32_t kTbDQ = 128;   // dQr^T
 constexpr uint32_t kTbDR = 192;   // dR^T -> [Q K^T ; K K^T]
 constexpr uint32_t kTbDK = 256;   // dK^T
-constexpr uint32_t kTbU = 320;    // dUt^T hi | lo (packed A operand) -> dK2^T
-constexpr uint32_t kTbR = 384;    // R^T hi | lo (packed A operand)
+constexpr uint32_t kTbU = 320;    // dUt^T hi | lo (packed A operand)
+constexpr uint32_t kTbR = 384;    // R^T hi | lo (packed A operand) -> dK2^T
 constexpr uint32_t kTbP1B = 448;  // [. ; dR_lo Ut_hi^T]
 
 // Per lane x[0..15] -> the sum over the warp's 32 lanes of x[lane % 16]
@@ -1706,18 +1721,15 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
     uint64_t *bars = reinterpret_cast<uint64_t *>(scr + 784);  // tma, mma
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2);
     volatile int *abort = reinterpret_cast<volatile int *>(bars + 3);
+    int *nxt = reinterpret_cast<int *>(bars + 4);  // [3] the next unit's coordinates (thread 0)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int q4 = warp & 3, cq = warp >> 2;
     const uint32_t lq = (uint32_t)(q4 * 32) << 16;
-    const int c = blockIdx.x, h = blockIdx.y;
-    const ChunkInfo ci = p.chunk[c];
-    const int len = ci.len, tok0 = ci.tok0;
-    const int hq = h / (p.Hv / p.Hq);
-    const size_t ch = (size_t)c * p.Hv + h;
     const long long cap = p.timeout_spins;
     const int row_v = 32 * q4 + lane;  // this thread's TMEM lane (a value, key or stacked token index)
     const int t0 = 16 * cq;            // this thread's 16 columns of a 64-column block
+    const int NU = p.NT * p.Hv;        // units (chunk, v-head), u = chunk * Hv + v-head
 
     if (tid == 0) {
         mbar_init(&bars[0], 1);
@@ -1730,81 +1742,125 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
                      "r"(512));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t sKQ = su32(KQ), sOR = su32(OR), sRL = su32(RL), sA = su32(Aim), sS = su32(Sim), sW = su32(Wim);
+    // Thread 0's bookkeeping: MMA groups committed, and the copy phase of
+    // bars[0] still open (its arrival made or not) for the drain on an abort.
+    int ncommit = 0, pf_phase = -1;
+    bool pf_arrived = true;
+    // The copies of one unit's inputs, issued one unit ahead by thread 0 as
+    // their shared-memory regions free up: the A rows once group 2 is done
+    // with the A image, S0 and dO once group 3 is done with dS1 and [dO ; dR],
+    // [Q ; K] and dUt once group 4 is done with [Q ; K] and the dP'' / MM images.
+    auto unit_tok = [&](int un, int &hn, int &hqn) {
+        const int cn = un / p.Hv;
+        hn = un - cn * p.Hv;
+        hqn = hn / (p.Hv / p.Hq);
+        return p.chunk[cn].tok0;
+    };
+    auto copy_A = [&](int un, int hn, int hqn, int tk) {
+        tma3d(Aim, &maps.A, 0, hn, tk, &bars[0]);
+        tma3d(Aim + 8192, &maps.A, 32, hn, tk, &bars[0]);
+    };
+    auto copy_S0_dO = [&](int un, int hn, int hqn, int tk) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tma3d(Sim + q * 16384, &maps.S0, 32 * q, 0, un, &bars[0]);
+        tma3d(OR, &maps.dO, 0, hn, tk, &bars[0]);
+        tma3d(OR + 16384, &maps.dO, 64, hn, tk, &bars[0]);
+    };
+    auto copy_KQ_dU = [&](int un, int hn, int hqn, int tk) {
+#pragma unroll
+        for (int a = 0; a < 2; ++a) {
+            tma3d(KQ + a * 16384, &maps.Q, 64 * a, hqn, tk, &bars[0]);
+            tma3d(KQ + a * 16384 + 8192, &maps.K, 64 * a, hqn, tk, &bars[0]);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tma3d(Wim + q * 8192, &maps.dU, 32 * q, 0, un, &bars[0]);
+    };
+    if (tid == 0 && (int)blockIdx.x < NU) {
+        int hn, hqn;
+        const int tk = unit_tok(blockIdx.x, hn, hqn);
+        mbar_expect_tx(&bars[0], kBcPrefetch);
+        copy_A(blockIdx.x, hn, hqn, tk);
+        copy_S0_dO(blockIdx.x, hn, hqn, tk);
+        copy_KQ_dU(blockIdx.x, hn, hqn, tk);
+        pf_phase = 0;
+    }
+    bool ok = true;
+    int it = 0;
+    for (int u = blockIdx.x; u < NU; u += gridDim.x, ++it) {
+    const int c = u / p.Hv, h = u - c * p.Hv;
+    const ChunkInfo ci = p.chunk[c];
+    const int len = ci.len, tok0 = ci.tok0;
+    const int hq = h / (p.Hv / p.Hq);
+    const size_t ch = (size_t)u;
+    const int un = u + gridDim.x;  // this CTA's next unit
+    if (tid == 0 && un < NU) nxt[2] = unit_tok(un, nxt[0], nxt[1]);  // its head, qk-head, first token
+    __syncthreads();  // the previous unit's tail is done with the scratch rows
     if (tid < 64) {
         gam[tid] = tid < len ? p.g[(size_t)(tok0 + tid) * p.Hv + h] : 0.f;
         bet[tid] = tid < len ? p.beta[(size_t)(tok0 + tid) * p.Hv + h] : 0.f;
         rRV[tid] = rRKS[tid] = rUdU[tid] = rQdq[tid] = rP[tid] = rLK[tid] = cL[tid] = 0.f;
     }
     if (tid < 16) red[tid] = 0.f;
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    int ncommit = 0;  // MMA groups committed (thread 0)
-    bool tma_issued = false;
-    if (tid == 0) {
-        mbar_expect_tx(&bars[0], 49152);
-#pragma unroll
-        for (int a = 0; a < 2; ++a) {
-            tma3d(KQ + a * 16384, &maps.Q, 64 * a, hq, tok0, &bars[0]);
-            tma3d(KQ + a * 16384 + 8192, &maps.K, 64 * a, hq, tok0, &bars[0]);
-            tma3d(OR + a * 16384, &maps.dO, 64 * a, h, tok0, &bars[0]);
-        }
-        tma_issued = true;
-    }
-    if (tid < 32) {  // inclusive cumsum of the gates, two per lane
-        const float a = gam[2 * lane], b = gam[2 * lane + 1];
-        float s = a + b;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const float n = __shfl_up_sync(0xffffffffu, s, o);
-            if (lane >= o) s += n;
-        }
-        gam[2 * lane] = s - b;
-        gam[2 * lane + 1] = s;
-    }
+    ok = bwait(&bars[0], it & 1, cap, abort);
+    if (__syncthreads_or(!ok)) goto out;
+    if (tid == 0) pf_phase = -1;
     {
-        // every load of this phase in flight before the conversions: one S0
-        // item (row k, 32 columns), the A rows (threads 0-127), the dUt^T column
+        // This unit's copies have landed (128-byte-swizzled fp32 rows: 16-byte
+        // chunk j of row r at j ^ (r % 8)).  Every thread reads its share into
+        // registers, then, after a barrier, writes the bf16 hi | lo images over
+        // them: one S0 item (row k, 32 columns), the A row half (threads
+        // 0-127; rows past the chunk end become identity rows), the dUt^T column.
         const int k = tid >> 2, sq = tid & 3;
-        const float4 *s0 = reinterpret_cast<const float4 *>(p.hbuf + ch * 128 * 128 + (size_t)k * 128 + 32 * sq);
-        float4 sv[8], av[8];
+        float xs[32], xa[32], du[16];
+        {
+            const char *src = Sim + sq * 16384 + k * 128;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) sv[i] = s0[i];
-        const int rr = (tid & 127) >> 1, ac0 = 32 * (tid & 1);
-        if (tid < 128) {
-            if (rr < len) {
-                const float4 *src =
-                    reinterpret_cast<const float4 *>(p.A_in + ((size_t)(tok0 + rr) * p.Hv + h) * 64 + ac0);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) av[i] = src[i];
-            } else {
-                // rows past the chunk end: identity rows
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int c4 = ac0 + 4 * i;
-                    av[i] = make_float4(c4 == rr, c4 + 1 == rr, c4 + 2 == rr, c4 + 3 == rr);
-                }
+            for (int j = 0; j < 8; ++j) {
+                const float4 v = *reinterpret_cast<const float4 *>(src + ((j ^ (k & 7)) << 4));
+                xs[4 * j] = v.x; xs[4 * j + 1] = v.y; xs[4 * j + 2] = v.z; xs[4 * j + 3] = v.w;
             }
         }
-        const float *dUg = p.dubuf + ch * 64 * 128 + row_v;
-        float du[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) du[j] = t0 + j < len ? dUg[(size_t)(t0 + j) * 128] : 0.f;
-        float x[32];
+        const int rr = (tid & 127) >> 1, ah = tid & 1;
         if (tid < 128) {
+            const char *src = Aim + ah * 8192 + rr * 128;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                x[4 * i] = av[i].x; x[4 * i + 1] = av[i].y; x[4 * i + 2] = av[i].z; x[4 * i + 3] = av[i].w;
+            for (int j = 0; j < 8; ++j) {
+                const float4 v = *reinterpret_cast<const float4 *>(src + ((j ^ (rr & 7)) << 4));
+                xa[4 * j] = v.x; xa[4 * j + 1] = v.y; xa[4 * j + 2] = v.z; xa[4 * j + 3] = v.w;
             }
-            st_img_hl(Aim, Aim + 8192, rr, ac0, x);
-        }
+            if (rr >= len)
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            x[4 * i] = sv[i].x; x[4 * i + 1] = sv[i].y; x[4 * i + 2] = sv[i].z; x[4 * i + 3] = sv[i].w;
+                for (int j = 0; j < 32; ++j) xa[j] = (32 * ah + j == rr) ? 1.f : 0.f;
         }
-        st_img_hl(Sim + (sq >> 1) * 16384, Sim + 32768 + (sq >> 1) * 16384, k, 32 * (sq & 1), x);
-        // dUt^T (rows past the chunk end zero) -> packed hi | lo A operand
+        {
+            const int v = row_v;
+            const char *src = Wim + (v >> 5) * 8192 + (v & 3) * 4;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int t = t0 + j;
+                du[j] = t < len ? *reinterpret_cast<const float *>(src + t * 128 + ((((v & 31) >> 2) ^ (t & 7)) << 4))
+                                : 0.f;
+            }
+        }
+        __syncthreads();  // every raw row read
+        if (tid < 32) {  // inclusive cumsum of the gates, two per lane
+            const float a = gam[2 * lane], b = gam[2 * lane + 1];
+            float sc = a + b;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float n = __shfl_up_sync(0xffffffffu, sc, o);
+                if (lane >= o) sc += n;
+            }
+            gam[2 * lane] = sc - b;
+            gam[2 * lane + 1] = sc;
+        }
+        st_img_hl(Sim + (sq >> 1) * 16384, Sim + 32768 + (sq >> 1) * 16384, k, 32 * (sq & 1), xs);
+        if (tid < 128) st_img_hl(Aim, Aim + 8192, rr, 32 * ah, xa);
         uint32_t hv[8], lv[8];
         split_pairs<8>(du, hv, lv);
         tmem_st8(tmem + kTbU + t0 / 2 + lq, hv);
@@ -1817,11 +1873,9 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
     tc_fence_before();
     __syncthreads();
 
-    const uint32_t sKQ = su32(KQ), sOR = su32(OR), sRL = su32(RL), sA = su32(Aim), sS = su32(Sim), sW = su32(Wim);
-    bool ok = true;
     // ---------------- group 1 ----------------
     if (tid == 0) {
-        if (bwait(&bars[0], 0, cap, abort)) {
+        {
             tc_fence_after();
             // KS^T = S0^T K^T: A = S0 image MN-major (M = v in two 64-blocks 16 KiB apart), B = K rows
             for (int tm = 0; tm < 2; ++tm)
@@ -1843,7 +1897,7 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
                 }
             }
             mma_commit(&bars[1]);
-            ncommit = 1;
+            ++ncommit;
         }
     }
     // this thread's V column (lane v, tokens t0..) loads while the MMAs run
@@ -1904,21 +1958,6 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
             atomicAdd(&rRKS[t0 + lane], s2);
         }
     }
-    {
-        // lane k: row sums dQr.Q (Q from the [Q ; K] image)
-        const int k = row_v;
-        uint32_t dqu[16];
-        tmem_ld16w(tmem + kTbDQ + t0 + lq, dqu);
-        const char *qa = KQ + (k >> 6) * 16384 + t0 * 128 + (k & 7) * 2;
-        const int xc = (k & 63) >> 3;
-        float a[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-            a[j] = __uint_as_float(dqu[j]) *
-                   __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(qa + j * 128 + ((xc ^ (j & 7)) << 4)));
-        const float s = warp_rs16(a, lane);
-        if (lane < 16) atomicAdd(&rQdq[t0 + lane], s);
-    }
     // this thread's dS1 item loads while the next MMAs run
     float4 d1v[8];
     {
@@ -1949,37 +1988,42 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
                 mma_seq(tmem + kTbDK, sdesc(sS + (m == 1) * 32768 + at * 16384), 32,
                         sdesc(sW + (m == 2) * 16384 + at * 8192), 2048, idesc_bf16(128, 64, 0, 1), 4, (m | at) != 0);
         mma_commit(&bars[1]);
-        ncommit = 2;
+        ++ncommit;
+    }
+    // while group 2 runs: row sums dQr.Q (dQr^T stays in TMEM until the end)
+    {
+        // lane k: row sums dQr.Q (Q from the [Q ; K] image)
+        const int k = row_v;
+        uint32_t dqu[16];
+        tmem_ld16w(tmem + kTbDQ + t0 + lq, dqu);
+        const char *qa = KQ + (k >> 6) * 16384 + t0 * 128 + (k & 7) * 2;
+        const int xc = (k & 63) >> 3;
+        float a[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            a[j] = __uint_as_float(dqu[j]) *
+                   __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(qa + j * 128 + ((xc ^ (j & 7)) << 4)));
+        const float s = warp_rs16(a, lane);
+        if (lane < 16) atomicAdd(&rQdq[t0 + lane], s);
     }
     ok = bwait(&bars[1], 1, cap, abort);
     if (__syncthreads_or(!ok)) goto out;
     tc_fence_after();
+    if (tid == 0 && un < NU) {  // the next unit's A rows, over the A image groups 1-2 have read
+        mbar_expect_tx_only(&bars[0], 16384);
+        copy_A(un, nxt[0], nxt[1], nxt[2]);
+        pf_phase = (it + 1) & 1;
+        pf_arrived = false;
+    }
     // ---------------- epilogue 2 ----------------
     {
-        // lane v: Ut^T -> image (B operand of group 3), row sums dUt.Ut
-        const int v = row_v;
-        uint32_t uu[16], dh[8], dl[8];
+        // lane v: Ut^T -> image (B operand of group 3)
+        uint32_t uu[16];
         tmem_ld16w(tmem + kTbKS + t0 + lq, uu);
-        asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-                     : "=r"(dh[0]), "=r"(dh[1]), "=r"(dh[2]), "=r"(dh[3]), "=r"(dh[4]), "=r"(dh[5]), "=r"(dh[6]),
-                       "=r"(dh[7])
-                     : "r"(tmem + kTbU + t0 / 2 + lq));
-        asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-                     : "=r"(dl[0]), "=r"(dl[1]), "=r"(dl[2]), "=r"(dl[3]), "=r"(dl[4]), "=r"(dl[5]), "=r"(dl[6]),
-                       "=r"(dl[7])
-                     : "r"(tmem + kTbU + 32 + t0 / 2 + lq));
-        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-        float x[16], a[16];
+        float x[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) x[j] = __uint_as_float(uu[j]);
-        st_img_hl16(Wim, Wim + 16384, v, t0, x);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            a[2 * i] = (bf_lo(dh[i]) + bf_lo(dl[i])) * x[2 * i];
-            a[2 * i + 1] = (bf_hi(dh[i]) + bf_hi(dl[i])) * x[2 * i + 1];
-        }
-        const float s = warp_rs16(a, lane);
-        if (lane < 16) atomicAdd(&rUdU[t0 + lane], s);
+        st_img_hl16(Wim, Wim + 16384, row_v, t0, x);
     }
     {
         // the dS1 image over the S0 image, with <dS1, S0> from the S0 terms it replaces
@@ -2021,21 +2065,43 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
                         (tb | at) != 0);
         for (int at = 0; at < 2; ++at)
             mma_seq(tmem + kTbP1B, sdesc(sRL - 8192 + at * 8192), 32, sdesc(sW + at * 8192), 2048, id, 4, at != 0);
-        // dK2^T = dS1 Ut^T
+        // dK2^T = dS1 Ut^T (over the R^T operand, read by group 2)
         for (int m = 0; m < 3; ++m)
             for (int at = 0; at < 2; ++at)
-                mma_seq(tmem + kTbU, sdesc(sS + (m == 1) * 32768 + at * 16384), 32,
+                mma_seq(tmem + kTbR, sdesc(sS + (m == 1) * 32768 + at * 16384), 32,
                         sdesc(sW + (m == 2) * 16384 + at * 8192), 2048, id, 4, (m | at) != 0);
         // [Q ; K] K^T
         for (int at = 0; at < 2; ++at)
             mma_seq(tmem + kTbDR, sdesc(sKQ + at * 16384), 32, sdesc(sKQ + at * 16384 + 8192), 32,
                     idesc_bf16(128, 64, 0, 0), 4, at != 0);
         mma_commit(&bars[1]);
-        ncommit = 3;
+        ++ncommit;
+    }
+    {
+        // while group 3 runs: row sums dUt.Ut (lane v; dUt^T packed in TMEM, Ut^T in TMEM)
+        uint32_t uu[16], dh[8], dl[8];
+        tmem_ld16_issue(tmem + kTbKS + t0 + lq, uu);
+        tmem_ld8_issue(tmem + kTbU + t0 / 2 + lq, dh);
+        tmem_ld8_issue(tmem + kTbU + 32 + t0 / 2 + lq, dl);
+        tmem_wait_ld16(uu);
+        tmem_hold8(dh);
+        tmem_hold8(dl);
+        float a[16];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            a[2 * i] = (bf_lo(dh[i]) + bf_lo(dl[i])) * __uint_as_float(uu[2 * i]);
+            a[2 * i + 1] = (bf_hi(dh[i]) + bf_hi(dl[i])) * __uint_as_float(uu[2 * i + 1]);
+        }
+        const float rs = warp_rs16(a, lane);
+        if (lane < 16) atomicAdd(&rUdU[t0 + lane], rs);
     }
     ok = bwait(&bars[1], 0, cap, abort);
     if (__syncthreads_or(!ok)) goto out;
     tc_fence_after();
+    if (tid == 0 && un < NU) {  // the next S0 and dO, over dS1 and [dO ; dR] that group 3 has read
+        mbar_expect_tx_only(&bars[0], 65536 + 16384);
+        copy_S0_dO(un, nxt[0], nxt[1], nxt[2]);
+    }
     // ---------------- epilogue 3: token lanes ----------------
     if (q4 < 2) {
         // row t of dP'' = scale e^{gamma_t - gamma_s} (dO Ut^T)[t][s], s <= t < len; row sum dP''.QK
@@ -2102,11 +2168,16 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
             mma_seq(tmem + kTbDK, aK, 2048, sdesc(sW + 16384 + tb * 8192), 2048, idM, 4, true);
         }
         mma_commit(&bars[1]);
-        ncommit = 4;
+        ++ncommit;
     }
     ok = bwait(&bars[1], 1, cap, abort);
     if (__syncthreads_or(!ok)) goto out;
     tc_fence_after();
+    if (tid == 0 && un < NU) {  // the next [Q ; K] and dUt, over the tiles group 4 has read; the phase's arrival
+        mbar_expect_tx(&bars[0], 32768 + 32768);
+        copy_KQ_dU(un, nxt[0], nxt[1], nxt[2]);
+        pf_arrived = true;
+    }
     // ---------------- epilogue 4: lane k ----------------
     {
         const int k = row_v;
@@ -2115,7 +2186,7 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
         tmem_ld16_issue(tmem + kTbDQ + t0 + lq, qr);
         tmem_ld16_issue(tmem + kTbKS + t0 + lq, q2);
         tmem_ld16_issue(tmem + kTbDK + t0 + lq, kd);
-        tmem_ld16_issue(tmem + kTbU + t0 + lq, k2);
+        tmem_ld16_issue(tmem + kTbR + t0 + lq, k2);
         tmem_wait_ld16(qr);
         tmem_hold16(q2);
         tmem_hold16(kd);
@@ -2179,9 +2250,13 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
         if (2 * lane < len) p.dg[(size_t)(tok0 + 2 * lane) * p.Hv + h] = s;
         if (2 * lane + 1 < len) p.dg[(size_t)(tok0 + 2 * lane + 1) * p.Hv + h] = s - a;
     }
+    }  // units
 out:
     if (tid == 0) {  // no copy or MMA of this CTA may still be in flight when it leaves
-        if (tma_issued) drain_wait(&bars[0], 0);
+        if (pf_phase >= 0) {
+            if (!pf_arrived) mbar_arrive(&bars[0]);  // the copies issued so far complete the phase
+            drain_wait(&bars[0], pf_phase);
+        }
         if (ncommit > 0) drain_wait(&bars[1], (ncommit - 1) & 1);
     }
     tc_fence_before();
@@ -2189,6 +2264,37 @@ out:
     if (warp == 0) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512));
+    }
+}
+
+// dq, dk [t, hq] = the sum in head order of the G per-v-head fp32 partials
+// [t, hq G + j]; one thread per 8 consecutive k of one (token, qk-head).
+__global__ void __launch_bounds__(256) k_group_sum_tc(Params p) {
+    const int G = p.Hv / p.Hq;
+    const long long n = (long long)p.Ttot * p.Hq * 16;
+    __nv_bfloat16 *dqo = reinterpret_cast<__nv_bfloat16 *>(p.dq), *dko = reinterpret_cast<__nv_bfloat16 *>(p.dk);
+    for (long long it = blockIdx.x * (long long)blockDim.x + threadIdx.x; it < n; it += (long long)gridDim.x * blockDim.x) {
+        const long long th = it >> 4;  // t * Hq + hq
+        const int k8 = (int)(it & 15) * 8;
+        float aq[8], ak[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) aq[e] = ak[e] = 0.f;
+        for (int j = 0; j < G; ++j) {
+            const size_t off = (size_t)(th * G + j) * 128 + k8;
+            const float4 q0 = __ldcs(reinterpret_cast<const float4 *>(p.dqp + off));
+            const float4 q1 = __ldcs(reinterpret_cast<const float4 *>(p.dqp + off + 4));
+            const float4 k0 = __ldcs(reinterpret_cast<const float4 *>(p.dkp + off));
+            const float4 k1 = __ldcs(reinterpret_cast<const float4 *>(p.dkp + off + 4));
+            aq[0] += q0.x; aq[1] += q0.y; aq[2] += q0.z; aq[3] += q0.w;
+            aq[4] += q1.x; aq[5] += q1.y; aq[6] += q1.z; aq[7] += q1.w;
+            ak[0] += k0.x; ak[1] += k0.y; ak[2] += k0.z; ak[3] += k0.w;
+            ak[4] += k1.x; ak[5] += k1.y; ak[6] += k1.z; ak[7] += k1.w;
+        }
+        const size_t o = (size_t)th * 128 + k8;
+        *reinterpret_cast<uint4 *>(dqo + o) = make_uint4(pack_bf16(aq[0], aq[1]), pack_bf16(aq[2], aq[3]),
+                                                         pack_bf16(aq[4], aq[5]), pack_bf16(aq[6], aq[7]));
+        *reinterpret_cast<uint4 *>(dko + o) = make_uint4(pack_bf16(ak[0], ak[1]), pack_bf16(ak[2], ak[3]),
+                                                         pack_bf16(ak[4], ak[5]), pack_bf16(ak[6], ak[7]));
     }
 }
 
@@ -2225,6 +2331,20 @@ bool map3(CUtensorMap *m, const void *base, int H, int Ttot, int bx, bool swizzl
               d, s, b, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D fp32 map (d0 innermost), 128-byte swizzle, box (b0, b1, b2) with b0 * 4 = 128 bytes.
+bool mapf32(CUtensorMap *m, const void *base, cuuint64_t d0, cuuint64_t d1, cuuint64_t d2, cuuint64_t s1_bytes,
+            cuuint64_t s2_bytes, cuuint32_t b0, cuuint32_t b1, cuuint32_t b2) {
+    EncodeFn fn = encoder();
+    if (!fn) return false;
+    cuuint64_t d[3] = {d0, d1, d2};
+    cuuint64_t s[2] = {s1_bytes, s2_bytes};
+    cuuint32_t b[3] = {b0, b1, b2};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(base), d, s, b, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 int launch_chunk(const char *name, const Params &p, int from_A, cudaStream_t st) {
@@ -2273,14 +2393,27 @@ int launch_dh(const char *name, const Params &p, cudaStream_t st) {
 
 int launch_bwd_chunk(const Params &p, cudaStream_t st) {
     if (p.NT == 0) return 0;
+    const cuuint64_t NU = (cuuint64_t)p.NT * p.Hv;
     BcMaps maps;
     if (!map3(&maps.Q, p.q, p.Hq, p.Ttot, 64, true) || !map3(&maps.K, p.k, p.Hq, p.Ttot, 64, true) ||
-        !map3(&maps.dO, p.dout, p.Hv, p.Ttot, 64, true))
+        !map3(&maps.dO, p.dout, p.Hv, p.Ttot, 64, true) ||
+        !mapf32(&maps.S0, p.hbuf, 128, 128, NU, 512, 65536, 32, 128, 1) ||
+        !mapf32(&maps.dU, p.dubuf, 128, 64, NU, 512, 32768, 32, 64, 1) ||
+        !mapf32(&maps.A, p.A_in, 64, p.Hv, p.Ttot, 256, (cuuint64_t)p.Hv * 256, 32, 1, 64))
         return 1;
     if (cudaFuncSetAttribute(k_bwd_chunk_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kBcSmem) != cudaSuccess)
         return 1;
+    // persistent: one CTA per SM, each over units blockIdx.x, + gridDim.x, ...
+    static int nsm = 0;
+    if (!nsm) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || nsm <= 0)
+            nsm = 148;
+    }
+    const int grid = (int)(NU < (cuuint64_t)nsm ? NU : (cuuint64_t)nsm);
     tm_begin(p.tm, "tc_bwd_chunk", st);
-    k_bwd_chunk_tc<<<dim3(p.NT, p.Hv), kBcThreads, kBcSmem, st>>>(p, maps);
+    k_bwd_chunk_tc<<<grid, kBcThreads, kBcSmem, st>>>(p, maps);
     tm_end(p.tm, st);
     return cudaGetLastError() != cudaSuccess;
 }
@@ -2343,7 +2476,13 @@ int tc_bwd(const Params &p, int use_cp, cudaStream_t st) {
         return mma_bwd_chunk(p, st);
     }
     if (launch_bwd_chunk(p, st)) return 1;
-    return p.Hv > p.Hq ? simt_group_sum(p, st) : 0;
+    if (p.Hv > p.Hq && p.Ttot > 0) {
+        tm_begin(p.tm, "tc_group_sum", st);
+        k_group_sum_tc<<<152 * 8, 256, 0, st>>>(p);
+        tm_end(p.tm, st);
+        if (cudaGetLastError() != cudaSuccess) return 1;
+    }
+    return 0;
 }
 
 unsigned tc_take_status(cudaStream_t st) {

@@ -156,7 +156,7 @@ int make_plan(const gdr_shape *s, const gdr_opts *o, int want_path, int in_f32, 
 size_t al(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Layout {
-    size_t seq, chunk, seg, gam, W, U, P, Hseg, Mseg, Sstart, hbuf, dhbuf, dubuf, dqp, dkp, gcnt, warm;
+    size_t seq, chunk, seg, gam, W, U, P, Hseg, Mseg, Sstart, hbuf, dhbuf, dubuf, dqp, dkp, warm;
     size_t Aimg, Pimg, Aux;
     bool f32_tiles, bf16_tiles;
     size_t total;
@@ -195,9 +195,8 @@ Layout layout(const gdr_shape *s, const Plan &pl, bool bwd) {
         L.dubuf = take(4 * NT * Hv * 64 * V);
         L.dqp = take(4 * (size_t)pl.Ttot * Hv * K);
         L.dkp = take(4 * (size_t)pl.Ttot * Hv * K);
-        L.gcnt = L.bf16_tiles ? take(4 * NT * s->Hq) : 0;
     } else {
-        L.hbuf = L.dhbuf = L.dubuf = L.dqp = L.dkp = L.gcnt = 0;
+        L.hbuf = L.dhbuf = L.dubuf = L.dqp = L.dkp = 0;
     }
     L.total = off;
     return L;
@@ -279,7 +278,6 @@ int fill_params(const gdr_shape *s, const Plan &pl, const Layout &L, void *ws, P
     p->dubuf = F(L.dubuf, L.dubuf != 0);
     p->dqp = F(L.dqp, L.dqp != 0);
     p->dkp = F(L.dkp, L.dkp != 0);
-    p->gcnt = L.gcnt ? reinterpret_cast<int *>(w + L.gcnt) : nullptr;
     p->warm = L.warm ? reinterpret_cast<int *>(w + L.warm) : nullptr;
     // warm-up starts of CP segments: 0 -> 8 chunks when segments are at least
     // four windows long (shorter ones would scan a large share of extra

@@ -84,7 +84,6 @@ struct Params {
     float *dhbuf;   // [NT,Hv,K,V]   (backward: gradient of the state after each chunk)
     float *dubuf;   // [NT,Hv,64,V]  (backward: gradient of the chunk pseudo-values)
     float *dqp, *dkp;  // [Ttot,Hv,K] per-v-head partial dq, dk
-    int *gcnt;         // [NT,Hq] arrivals of the v-heads of a qk-head at their chunk (tensor-core backward)
     int cp_warmup;     // warm-up chunks of a segment start (0: the exact split only)
     int *warm;         // [NSEG,Hv] 1: the segment's warm-up start passes its bound (set on the device)
     // tensor-core path chunk tiles (bf16 shared-memory images, hi and lo terms, 16 KiB each)
@@ -106,7 +105,6 @@ unsigned simt_take_status(cudaStream_t st);
 int simt_cp_combine(const Params &p, cudaStream_t st);
 int simt_cp_combine_rev(const Params &p, cudaStream_t st);
 int simt_group_sum(const Params &p, cudaStream_t st);   // dq, dk from per-v-head partials (bf16)
-int mma_bwd_chunk(const Params &p, cudaStream_t st);    // chunk-local gradients, warp MMAs
 int prep_tables(const int32_t *cu_dev, int N, int T_fixed, int seg_len, SeqInfo *seq,
                 ChunkInfo *chunk, SegInfo *seg, cudaStream_t st);
 }  // namespace gdr

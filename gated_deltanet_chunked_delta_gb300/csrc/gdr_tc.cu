@@ -22,7 +22,6 @@
 // The state lives in tensor memory, transposed: TMEM lane v holds row v of
 // S^T, 128 fp32 columns of k.
 #include <cuda.h>
-#include <cstdlib>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -1815,7 +1814,7 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
         // registers, then, after a barrier, writes the bf16 hi | lo images over
         // them: one S0 item (row k, 32 columns), the A row half (threads
         // 0-127; rows past the chunk end become identity rows), the dUt^T column.
-        const int k = tid >> 2, sq = tid & 3;
+        const int k = tid & 127, sq = tid >> 7;  // a warp: 32 consecutive rows of one quarter
         float xs[32], xa[32], du[16];
         {
             const char *src = Sim + sq * 16384 + k * 128;
@@ -1825,7 +1824,7 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
                 xs[4 * j] = v.x; xs[4 * j + 1] = v.y; xs[4 * j + 2] = v.z; xs[4 * j + 3] = v.w;
             }
         }
-        const int rr = (tid & 127) >> 1, ah = tid & 1;
+        const int rr = tid & 63, ah = (tid >> 6) & 1;
         if (tid < 128) {
             const char *src = Aim + ah * 8192 + rr * 128;
 #pragma unroll
@@ -1961,7 +1960,7 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
     // this thread's dS1 item loads while the next MMAs run
     float4 d1v[8];
     {
-        const int k = tid >> 2, sq = tid & 3;
+        const int k = tid & 127, sq = tid >> 7;  // a warp: 32 consecutive rows of one quarter
         const float4 *src = reinterpret_cast<const float4 *>(p.dhbuf + ch * 128 * 128 + (size_t)k * 128 + 32 * sq);
 #pragma unroll
         for (int i = 0; i < 8; ++i) d1v[i] = src[i];
@@ -2027,7 +2026,7 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
     }
     {
         // the dS1 image over the S0 image, with <dS1, S0> from the S0 terms it replaces
-        const int k = tid >> 2, sq = tid & 3;
+        const int k = tid & 127, sq = tid >> 7;  // a warp: 32 consecutive rows of one quarter
         char *ih = Sim + (sq >> 1) * 16384, *il = ih + 32768;
         const int c0 = 32 * (sq & 1);
         float x[32], part = 0.f;
@@ -2470,11 +2469,6 @@ int tc_bwd(const Params &p, int use_cp, cudaStream_t st) {
     if (launch_dh<kDhFull>("tc_dh", p, st)) return 1;
     // a10, a11: chunk-local gradients
     // the qk-head sums of dq and dk happen inside the chunk kernel
-    static const bool warp_mma = getenv("GDR_BWD_WARP_MMA") != nullptr;
-    if (warp_mma) {
-        if (cudaMemsetAsync(p.gcnt, 0, sizeof(int) * (size_t)p.NT * p.Hq, st) != cudaSuccess) return 1;
-        return mma_bwd_chunk(p, st);
-    }
     if (launch_bwd_chunk(p, st)) return 1;
     if (p.Hv > p.Hq && p.Ttot > 0) {
         tm_begin(p.tm, "tc_group_sum", st);

@@ -324,8 +324,7 @@ __device__ __forceinline__ void st_img_half2(char *img, int row, int col0, const
 constexpr int kLd = 68;                            // fp32 row pitch of L and A (16-byte aligned rows)
 constexpr int kTLd = 52;                           // row pitch of the 16 x 48 product scratch
 constexpr int kChunkScratch = 2 * 64 * kLd * 4;    // L and A, laid over the K/Q tile once the MMA is done
-constexpr int kChunkSmem = 1024 + (kChunkScratch > 32768 ? kChunkScratch : 32768) + 16 * kTLd * 4 + 2 * 64 * 4 +
-                           4 * 64 * 4 + 64;
+constexpr int kChunkSmem = 1024 + (kChunkScratch > 32768 ? kChunkScratch : 32768) + 16 * kTLd * 4 + 2 * 64 * 4 + 64;
 
 // A[16i + r][c] for the thread's columns c = cg n .. cg n + n - 1, n = 2i:
 // T = L[16i:16i+16, 0:16i] A[0:16i, 0:16i], then A[16i:, 0:16i] = -A_ii T.
@@ -389,8 +388,7 @@ __global__ void __launch_bounds__(128, 5) k_chunk_tc(Params p, const __grid_cons
     float *Tt = reinterpret_cast<float *>(sm + kTileRegion);      // [16][kTLd]
     float *gam = Tt + 16 * kTLd;                                  // [64]
     float *bet = gam + 64;                                        // [64]
-    float *Eb = bet + 64;                                         // [4][64] e^{gamma_16b - gamma_s}, s < 16 b
-    uint64_t *bars = reinterpret_cast<uint64_t *>(Eb + 4 * 64);   // tma, mma
+    uint64_t *bars = reinterpret_cast<uint64_t *>(bet + 64);      // tma, mma
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2);
     volatile int *abort = reinterpret_cast<volatile int *>(bars + 3);
 
@@ -465,15 +463,7 @@ __global__ void __launch_bounds__(128, 5) k_chunk_tc(Params p, const __grid_cons
         aux[tid] = bt;
         aux[64 + tid] = __expf(gt);
         aux[128 + tid] = __expf(gC - gt);
-    } else if (!from_A) {
-        // decay factors of L against earlier 16-row blocks, factored through the
-        // block's first row: e^{gamma_r - gamma_s} = e^{gamma_r - gamma_16b}
-        // e^{gamma_16b - gamma_s}, both factors <= 1 (the gates are <= 0)
-        const int sc = tid - 64;
-#pragma unroll
-        for (int b = 1; b < 4; ++b) Eb[b * 64 + sc] = sc < 16 * b ? __expf(gam[16 * b] - gam[sc]) : 0.f;
     }
-    __syncthreads();  // the decay table
     const bool ok = bwait(&bars[1], 0, cap, abort);
     tc_fence_after();
     // rows of [K K^T ; Q K^T]: warps 0-1 -> L (unless from_A), warps 2-3 -> P'
@@ -481,10 +471,10 @@ __global__ void __launch_bounds__(128, 5) k_chunk_tc(Params p, const __grid_cons
         const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16);
         if (tid < 64) {
             if (!from_A) {
-                const int rr = tid, b0 = rr & ~15;
+                // L[r][s] = b_r e^{gamma_r - gamma_s} (k_r . k_s) for s < r: one
+                // exponential per entry, of a non-positive argument (the gates are <= 0)
+                const int rr = tid;
                 const float br = bet[rr], gr = gam[rr];
-                const float ar = br * __expf(gr - gam[b0]);  // b_r e^{gamma_r - gamma_16b}
-                const float *eb = Eb + (rr >> 4) * 64;
                 float *lrow = Ls + rr * kLd;
 #pragma unroll 1
                 for (int hb = 0; hb < 2; ++hb) {
@@ -494,22 +484,7 @@ __global__ void __launch_bounds__(128, 5) k_chunk_tc(Params p, const __grid_cons
 #pragma unroll
                     for (int s = 0; s < 32; ++s) {
                         const int sc = 32 * hb + s;
-                        x[s] = sc < b0 ? ar * eb[sc] * __uint_as_float(rv[s]) : 0.f;
-                    }
-                    if (hb == (rr >> 5)) {  // the row's own 16-column block: direct exponentials
-                        if (rr & 16) {
-#pragma unroll
-                            for (int j = 0; j < 16; ++j) {
-                                const int sc = 32 * hb + 16 + j;
-                                if (sc < rr) x[16 + j] = br * __expf(gr - gam[sc]) * __uint_as_float(rv[16 + j]);
-                            }
-                        } else {
-#pragma unroll
-                            for (int j = 0; j < 16; ++j) {
-                                const int sc = 32 * hb + j;
-                                if (sc < rr) x[j] = br * __expf(gr - gam[sc]) * __uint_as_float(rv[j]);
-                            }
-                        }
+                        x[s] = sc < rr ? br * __expf(gr - gam[sc]) * __uint_as_float(rv[s]) : 0.f;
                     }
 #pragma unroll
                     for (int s = 0; s < 32; s += 4)

@@ -482,9 +482,16 @@ __global__ void __launch_bounds__(128, 5) k_chunk_tc(Params p, const __grid_cons
                     tmem_ld32(ta + 32 * hb, rv);
                     float x[32];
 #pragma unroll
-                    for (int s = 0; s < 32; ++s) {
-                        const int sc = 32 * hb + s;
-                        x[s] = sc < rr ? br * __expf(gr - gam[sc]) * __uint_as_float(rv[s]) : 0.f;
+                    for (int s4 = 0; s4 < 32; s4 += 4) {
+                        const float4 g4 = *reinterpret_cast<const float4 *>(gam + 32 * hb + s4);
+                        const float gs[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            // branch-free: the exponent is clamped to <= 0 and the mask applied after
+                            const int sc = 32 * hb + s4 + e;
+                            const float v = br * __expf(fminf(gr - gs[e], 0.f)) * __uint_as_float(rv[s4 + e]);
+                            x[s4 + e] = sc < rr ? v : 0.f;
+                        }
                     }
 #pragma unroll
                     for (int s = 0; s < 32; s += 4)
@@ -557,7 +564,9 @@ __global__ void __launch_bounds__(128, 5) k_chunk_tc(Params p, const __grid_cons
         inv_row_block<3>(Ls, As, Tt, tid);
     }
     if (!*abort) {
-        // A image (hi | lo) and the fp32 A output: thread -> row tid/2, 32 columns
+        // the A image (hi | lo: thread -> row tid/2, 32 columns) staged over L,
+        // dead after the inverse, for one bulk store; the fp32 A output a row
+        // per warp at a time (coalesced)
         const int rr = tid >> 1, c0 = 32 * (tid & 1);
         float x[32];
 #pragma unroll
@@ -565,19 +574,27 @@ __global__ void __launch_bounds__(128, 5) k_chunk_tc(Params p, const __grid_cons
             const float4 v = *reinterpret_cast<const float4 *>(As + rr * kLd + c0 + s);
             x[s] = v.x; x[s + 1] = v.y; x[s + 2] = v.z; x[s + 3] = v.w;
         }
-        st_img_half2(reinterpret_cast<char *>(p.Aimg) + ch * kImg2, rr, c0, x);
-        if (p.A_out && !from_A && rr < len) {
-            float4 *dst = reinterpret_cast<float4 *>(p.A_out + ((size_t)(tok0 + rr) * p.Hv + h) * 64 + c0);
-#pragma unroll
-            for (int s = 0; s < 8; ++s) dst[s] = make_float4(x[4 * s], x[4 * s + 1], x[4 * s + 2], x[4 * s + 3]);
-        }
+        st_img_half2(reinterpret_cast<char *>(Ls), rr, c0, x);
+        if (p.A_out && !from_A)
+            for (int r = warp; r < len; r += 4)
+                *reinterpret_cast<float2 *>(p.A_out + ((size_t)(tok0 + r) * p.Hv + h) * 64 + 2 * lane) =
+                    *reinterpret_cast<const float2 *>(As + r * kLd + 2 * lane);
     }
+    fence_async_smem();
     if (tid == 0) {  // no copy or MMA of this CTA may still be in flight when it leaves
         drain_wait(&bars[0], 0);
         if (mma_issued) drain_wait(&bars[1], 0);
     }
     tc_fence_before();
     __syncthreads();
+    if (tid == 0 && !*abort) {
+        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                         reinterpret_cast<char *>(p.Aimg) + ch * kImg2),
+                     "r"(su32(Ls)), "r"(kImg2)
+                     : "memory");
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // written before the CTA leaves
+    }
     if (warp == 0) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(64));

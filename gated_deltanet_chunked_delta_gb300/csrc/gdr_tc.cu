@@ -502,7 +502,7 @@ __global__ void __launch_bounds__(128, 5) k_chunk_tc(Params p, const __grid_cons
             // rows past the chunk end are zero (the backward mixes rows through P'^T)
             const int rr = tid - 64;
             const float f = rr < len ? p.scale * __expf(gam[rr] - gC) : 0.f;
-            char *pimg = reinterpret_cast<char *>(p.Pimg) + ch * kImg2;
+            char *pimg = reinterpret_cast<char *>(As);  // staged for one bulk store
 #pragma unroll
             for (int hb = 0; hb < 2; ++hb) {
                 uint32_t r0[32];
@@ -514,7 +514,17 @@ __global__ void __launch_bounds__(128, 5) k_chunk_tc(Params p, const __grid_cons
             }
         }
     }
+    fence_async_smem();
     __syncthreads();  // L complete; the K/Q tile is dead (the MMA that read it has completed)
+    if (tid == 0 && ok) {  // the P' image, staged in A's buffer, leaves by one bulk store
+        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                         reinterpret_cast<char *>(p.Pimg) + ch * kImg2),
+                     "r"(su32(As)), "r"(kImg2)
+                     : "memory");
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+    }
+    __syncthreads();  // the staged P' image has been read
     if (from_A) {
         // 64 rows x 16 float4, eight per thread, all in flight before the stores
         float4 av[8];
@@ -587,13 +597,15 @@ __global__ void __launch_bounds__(128, 5) k_chunk_tc(Params p, const __grid_cons
     }
     tc_fence_before();
     __syncthreads();
-    if (tid == 0 && !*abort) {
-        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
-                         reinterpret_cast<char *>(p.Aimg) + ch * kImg2),
-                     "r"(su32(Ls)), "r"(kImg2)
-                     : "memory");
-        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // written before the CTA leaves
+    if (tid == 0) {
+        if (!*abort) {
+            asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                             reinterpret_cast<char *>(p.Aimg) + ch * kImg2),
+                         "r"(su32(Ls)), "r"(kImg2)
+                         : "memory");
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
+        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // every bulk store written before the CTA leaves
     }
     if (warp == 0) {
         tc_fence_after();

@@ -315,66 +315,99 @@ __device__ __forceinline__ void st_img_half2(char *img, int row, int col0, const
 // CTAs per SM.  [K ; Q] K^T on tcgen05 (warps 0-1 read the K K^T rows, warps
 // 2-3 the Q K^T rows), the gate cumsum, L = strict_tril(diag(b) (K K^T o D)),
 // P', and the unit-lower-triangular inverse A = (I + L)^-1 on the CUDA cores
-// by row blocks of 16: the four 16x16 diagonal inverses first (one column
-// per thread), then for i = 1..3
-//     A[i, <i] = -A_ii (L[i, <i] A[<i, <i])
+// by recursive doubling: the four 16x16 diagonal inverses first (one column
+// per thread), then the two 32x32 diagonal blocks and then the whole matrix,
+// each from its two diagonal halves as
+//     A[lo, hi] = -A[lo, lo] (L[lo, hi] A[hi, hi])     (lo the lower half)
 // with every product register-blocked over all 128 threads.  With from_A
 // (the backward) A is read back from the forward's output instead.
 // ---------------------------------------------------------------------------
 constexpr int kLd = 68;                            // fp32 row pitch of L and A (16-byte aligned rows)
-constexpr int kTLd = 52;                           // row pitch of the 16 x 48 product scratch
+constexpr int kTLd = 36;                           // row pitch of the 32 x 32 product scratch
 constexpr int kChunkScratch = 2 * 64 * kLd * 4;    // L and A, laid over the K/Q tile once the MMA is done
-constexpr int kChunkSmem = 1024 + (kChunkScratch > 32768 ? kChunkScratch : 32768) + 16 * kTLd * 4 + 2 * 64 * 4 + 64;
+constexpr int kChunkSmem = 1024 + (kChunkScratch > 32768 ? kChunkScratch : 32768) + 32 * kTLd * 4 + 2 * 64 * 4 + 64;
 
-// A[16i + r][c] for the thread's columns c = cg n .. cg n + n - 1, n = 2i:
-// T = L[16i:16i+16, 0:16i] A[0:16i, 0:16i], then A[16i:, 0:16i] = -A_ii T.
-template <int I>
-__device__ __forceinline__ void inv_row_block(float *Ls, float *As, float *Tt, int tid) {
-    constexpr int n = 2 * I, KD = 16 * I;
-    const int r = tid >> 3, cg = tid & 7, c0 = cg * n;
-    float acc[n];
+// The two 32x32 diagonal blocks b = 0, 1 of A from their 16x16 diagonal
+// blocks: T_b = L[32b+16:, 32b:32b+16] A[32b:32b+16, 32b:32b+16], then
+// A[32b+16:, 32b:32b+16] = -A[32b+16:, 32b+16:] T_b.  Thread: block tid / 64,
+// row (tid % 64) / 4, four columns 4 (tid % 4).
+__device__ __forceinline__ void inv_level16(const float *Ls, float *As, float *Tt, int tid) {
+    const int b = tid >> 6, r = (tid & 63) >> 2, c4 = (tid & 3) * 4, o = 32 * b;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    const float *lrow = Ls + (o + 16 + r) * kLd + o;
 #pragma unroll
-    for (int u = 0; u < n; ++u) acc[u] = 0.f;
-    const float *lrow = Ls + (16 * I + r) * kLd;
-#pragma unroll
-    for (int k = 0; k < KD; k += 4) {
+    for (int k = 0; k < 16; k += 4) {
         const float4 l4 = *reinterpret_cast<const float4 *>(lrow + k);
         const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const float *arow = As + (k + q) * kLd + c0;
-#pragma unroll
-            for (int u = 0; u < n; u += 2) {
-                const float2 a2 = *reinterpret_cast<const float2 *>(arow + u);
-                acc[u] = fmaf(lv[q], a2.x, acc[u]);
-                acc[u + 1] = fmaf(lv[q], a2.y, acc[u + 1]);
-            }
+            const float4 a4 = *reinterpret_cast<const float4 *>(As + (o + k + q) * kLd + o + c4);
+            acc[0] = fmaf(lv[q], a4.x, acc[0]); acc[1] = fmaf(lv[q], a4.y, acc[1]);
+            acc[2] = fmaf(lv[q], a4.z, acc[2]); acc[3] = fmaf(lv[q], a4.w, acc[3]);
         }
     }
-#pragma unroll
-    for (int u = 0; u < n; u += 2) *reinterpret_cast<float2 *>(Tt + r * kTLd + c0 + u) = make_float2(acc[u], acc[u + 1]);
+    float *t = Tt + (b * 16 + r) * kTLd + c4;
+    *reinterpret_cast<float4 *>(t) = make_float4(acc[0], acc[1], acc[2], acc[3]);
     __syncthreads();
-#pragma unroll
-    for (int u = 0; u < n; ++u) acc[u] = 0.f;
-    const float *drow = As + (16 * I + r) * kLd + 16 * I;
+    acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+    const float *drow = As + (o + 16 + r) * kLd + o + 16;
 #pragma unroll
     for (int m = 0; m < 16; m += 4) {
         const float4 d4 = *reinterpret_cast<const float4 *>(drow + m);
         const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const float *trow = Tt + (m + q) * kTLd + c0;
-#pragma unroll
-            for (int u = 0; u < n; u += 2) {
-                const float2 t2 = *reinterpret_cast<const float2 *>(trow + u);
-                acc[u] = fmaf(dv[q], t2.x, acc[u]);
-                acc[u + 1] = fmaf(dv[q], t2.y, acc[u + 1]);
-            }
+            const float4 t4 = *reinterpret_cast<const float4 *>(Tt + (b * 16 + m + q) * kTLd + c4);
+            acc[0] = fmaf(dv[q], t4.x, acc[0]); acc[1] = fmaf(dv[q], t4.y, acc[1]);
+            acc[2] = fmaf(dv[q], t4.z, acc[2]); acc[3] = fmaf(dv[q], t4.w, acc[3]);
         }
     }
+    *reinterpret_cast<float4 *>(As + (o + 16 + r) * kLd + o + c4) = make_float4(-acc[0], -acc[1], -acc[2], -acc[3]);
+    __syncthreads();
+}
+// The whole matrix from its two 32x32 diagonal blocks: T = L[32:, :32]
+// A[:32, :32], then A[32:, :32] = -A[32:, 32:] T.  Thread: rows 2 (tid / 8),
+// + 1, four columns 4 (tid % 8).
+__device__ __forceinline__ void inv_level32(const float *Ls, float *As, float *Tt, int tid) {
+    const int r = 2 * (tid >> 3), c4 = (tid & 7) * 4;
+    float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
+    const float *l0 = Ls + (32 + r) * kLd, *l1 = l0 + kLd;
+#pragma unroll 2
+    for (int k = 0; k < 32; k += 4) {
+        const float4 x4 = *reinterpret_cast<const float4 *>(l0 + k);
+        const float4 y4 = *reinterpret_cast<const float4 *>(l1 + k);
+        const float xv[4] = {x4.x, x4.y, x4.z, x4.w}, yv[4] = {y4.x, y4.y, y4.z, y4.w};
 #pragma unroll
-    for (int u = 0; u < n; u += 2)
-        *reinterpret_cast<float2 *>(As + (16 * I + r) * kLd + c0 + u) = make_float2(-acc[u], -acc[u + 1]);
+        for (int q = 0; q < 4; ++q) {
+            const float4 a4 = *reinterpret_cast<const float4 *>(As + (k + q) * kLd + c4);
+            a0[0] = fmaf(xv[q], a4.x, a0[0]); a0[1] = fmaf(xv[q], a4.y, a0[1]);
+            a0[2] = fmaf(xv[q], a4.z, a0[2]); a0[3] = fmaf(xv[q], a4.w, a0[3]);
+            a1[0] = fmaf(yv[q], a4.x, a1[0]); a1[1] = fmaf(yv[q], a4.y, a1[1]);
+            a1[2] = fmaf(yv[q], a4.z, a1[2]); a1[3] = fmaf(yv[q], a4.w, a1[3]);
+        }
+    }
+    *reinterpret_cast<float4 *>(Tt + r * kTLd + c4) = make_float4(a0[0], a0[1], a0[2], a0[3]);
+    *reinterpret_cast<float4 *>(Tt + (r + 1) * kTLd + c4) = make_float4(a1[0], a1[1], a1[2], a1[3]);
+    __syncthreads();
+#pragma unroll
+    for (int e = 0; e < 4; ++e) a0[e] = a1[e] = 0.f;
+    const float *d0 = As + (32 + r) * kLd + 32, *d1 = d0 + kLd;
+#pragma unroll 2
+    for (int m = 0; m < 32; m += 4) {
+        const float4 x4 = *reinterpret_cast<const float4 *>(d0 + m);
+        const float4 y4 = *reinterpret_cast<const float4 *>(d1 + m);
+        const float xv[4] = {x4.x, x4.y, x4.z, x4.w}, yv[4] = {y4.x, y4.y, y4.z, y4.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float4 t4 = *reinterpret_cast<const float4 *>(Tt + (m + q) * kTLd + c4);
+            a0[0] = fmaf(xv[q], t4.x, a0[0]); a0[1] = fmaf(xv[q], t4.y, a0[1]);
+            a0[2] = fmaf(xv[q], t4.z, a0[2]); a0[3] = fmaf(xv[q], t4.w, a0[3]);
+            a1[0] = fmaf(yv[q], t4.x, a1[0]); a1[1] = fmaf(yv[q], t4.y, a1[1]);
+            a1[2] = fmaf(yv[q], t4.z, a1[2]); a1[3] = fmaf(yv[q], t4.w, a1[3]);
+        }
+    }
+    *reinterpret_cast<float4 *>(As + (32 + r) * kLd + c4) = make_float4(-a0[0], -a0[1], -a0[2], -a0[3]);
+    *reinterpret_cast<float4 *>(As + (33 + r) * kLd + c4) = make_float4(-a1[0], -a1[1], -a1[2], -a1[3]);
     __syncthreads();
 }
 
@@ -385,8 +418,8 @@ __global__ void __launch_bounds__(128, 5) k_chunk_tc(Params p, const __grid_cons
     char *tile = sm;                                              // [2 atoms][128 rows][128 B]: K rows 0-63, Q 64-127
     float *Ls = reinterpret_cast<float *>(sm);                    // [64][kLd], over the tile after the MMA
     float *As = Ls + 64 * kLd;                                    // [64][kLd]
-    float *Tt = reinterpret_cast<float *>(sm + kTileRegion);      // [16][kTLd]
-    float *gam = Tt + 16 * kTLd;                                  // [64]
+    float *Tt = reinterpret_cast<float *>(sm + kTileRegion);      // [32][kTLd]
+    float *gam = Tt + 32 * kTLd;                                  // [64]
     float *bet = gam + 64;                                        // [64]
     uint64_t *bars = reinterpret_cast<uint64_t *>(bet + 64);      // tma, mma
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2);
@@ -569,9 +602,8 @@ __global__ void __launch_bounds__(128, 5) k_chunk_tc(Params p, const __grid_cons
             }
         }
         __syncthreads();
-        inv_row_block<1>(Ls, As, Tt, tid);
-        inv_row_block<2>(Ls, As, Tt, tid);
-        inv_row_block<3>(Ls, As, Tt, tid);
+        inv_level16(Ls, As, Tt, tid);
+        inv_level32(Ls, As, Tt, tid);
     }
     if (!*abort) {
         // the A image (hi | lo: thread -> row tid/2, 32 columns) staged over L,

@@ -462,20 +462,6 @@ __global__ void __launch_bounds__(128, 5) k_chunk_tc(Params p, const __grid_cons
         const float x = t < len ? (tid < 64 ? p.g : p.beta)[(size_t)(tok0 + t) * p.Hv + h] : 0.f;
         (tid < 64 ? gam : bet)[t] = x;
     }
-    if (tid == 0) {
-        if (bwait(&bars[0], 0, cap, abort)) {
-            tc_fence_after();
-            const uint32_t id = idesc_bf16(128, 64);
-            const uint32_t a0 = su32(tile);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                mma(tmem, sdesc(a0 + off), sdesc(a0 + off), id, kk > 0);
-            }
-            mma_commit(&bars[1]);
-            mma_issued = true;
-        }
-    }
     __syncthreads();
     if (tid < 32) {  // inclusive cumsum over 64 values, two per lane
         const float a = gam[2 * lane], b = gam[2 * lane + 1];
@@ -496,6 +482,20 @@ __global__ void __launch_bounds__(128, 5) k_chunk_tc(Params p, const __grid_cons
         aux[tid] = bt;
         aux[64 + tid] = __expf(gt);
         aux[128 + tid] = __expf(gC - gt);
+    }
+    if (tid == 0) {  // [K ; Q] K^T once the tiles have landed (the gates' work overlapped the copies)
+        if (bwait(&bars[0], 0, cap, abort)) {
+            tc_fence_after();
+            const uint32_t id = idesc_bf16(128, 64);
+            const uint32_t a0 = su32(tile);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                mma(tmem, sdesc(a0 + off), sdesc(a0 + off), id, kk > 0);
+            }
+            mma_commit(&bars[1]);
+            mma_issued = true;
+        }
     }
     const bool ok = bwait(&bars[1], 0, cap, abort);
     tc_fence_after();
@@ -577,15 +577,22 @@ __global__ void __launch_bounds__(128, 5) k_chunk_tc(Params p, const __grid_cons
         if (tid < 64) {
             // diagonal 16x16 blocks: thread (b, j) solves column j of block b in
             // registers, x[r] = [r == j] - sum_{s<r} L[b+r][b+s] x[s]
+            // (each row's sum in four partial sums, over vector reads of the row)
             const int b = 16 * (tid >> 4), jj = tid & 15;
             float x[16];
 #pragma unroll
             for (int rr = 0; rr < 16; ++rr) {
                 const float *lrow = Ls + (b + rr) * kLd + b;
-                float acc = rr == jj ? 1.f : 0.f;
+                float a[4] = {rr == jj ? 1.f : 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int s = 0; s < rr; ++s) acc = fmaf(-lrow[s], x[s], acc);
-                x[rr] = rr < jj ? 0.f : acc;
+                for (int s4 = 0; s4 < rr; s4 += 4) {
+                    const float4 l4 = *reinterpret_cast<const float4 *>(lrow + s4);
+                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (s4 + e < rr) a[e] = fmaf(-lv[e], x[s4 + e], a[e]);
+                }
+                x[rr] = rr < jj ? 0.f : (a[0] + a[1]) + (a[2] + a[3]);
             }
 #pragma unroll
             for (int rr = 0; rr < 16; ++rr) As[(b + rr) * kLd + b + jj] = x[rr];

@@ -330,9 +330,10 @@ constexpr int kChunkSmem = 1024 + (kChunkScratch > 32768 ? kChunkScratch : 32768
 // The two 32x32 diagonal blocks b = 0, 1 of A from their 16x16 diagonal
 // blocks: T_b = L[32b+16:, 32b:32b+16] A[32b:32b+16, 32b:32b+16], then
 // A[32b+16:, 32b:32b+16] = -A[32b+16:, 32b+16:] T_b.  Thread: block tid / 64,
-// row (tid % 64) / 4, four columns 4 (tid % 4).
+// row tid % 16, four columns 4 ((tid / 16) % 4) (eight consecutive lanes on
+// eight rows: conflict-free vector accesses).
 __device__ __forceinline__ void inv_level16(const float *Ls, float *As, float *Tt, int tid) {
-    const int b = tid >> 6, r = (tid & 63) >> 2, c4 = (tid & 3) * 4, o = 32 * b;
+    const int b = tid >> 6, r = tid & 15, c4 = ((tid >> 4) & 3) * 4, o = 32 * b;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     const float *lrow = Ls + (o + 16 + r) * kLd + o;
 #pragma unroll
@@ -613,10 +614,10 @@ __global__ void __launch_bounds__(128, 5) k_chunk_tc(Params p, const __grid_cons
         inv_level32(Ls, As, Tt, tid);
     }
     if (!*abort) {
-        // the A image (hi | lo: thread -> row tid/2, 32 columns) staged over L,
-        // dead after the inverse, for one bulk store; the fp32 A output a row
-        // per warp at a time (coalesced)
-        const int rr = tid >> 1, c0 = 32 * (tid & 1);
+        // the A image (hi | lo: thread -> row tid % 64, 32 columns from 32 (tid
+        // / 64)) staged over L, dead after the inverse, for one bulk store; the
+        // fp32 A output a row per warp at a time (coalesced)
+        const int rr = tid & 63, c0 = 32 * (tid >> 6);
         float x[32];
 #pragma unroll
         for (int s = 0; s < 32; s += 4) {

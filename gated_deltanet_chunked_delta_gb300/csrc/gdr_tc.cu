@@ -1694,8 +1694,9 @@ struct BcMaps {
     CUtensorMap Q, K, dO;  // 3-D (x, head, token), box 64 x 1 x 64, 128-byte swizzle
     CUtensorMap S0, dU;    // fp32 3-D (v, k or t, unit), box 32 x 128 (64) x 1, 128-byte swizzle
     CUtensorMap A;         // fp32 3-D (s, head, token), box 32 x 1 x 64, 128-byte swizzle
+    CUtensorMap V;         // 3-D (v, head, token), box 128 x 1 x 64, plain rows
 };
-constexpr uint32_t kBcPrefetch = 16384 + 65536 + 16384 + 32768 + 32768;  // A, S0, dO, [Q ; K], dUt per unit
+constexpr uint32_t kBcPrefetch = 16384 + 16384 + 65536 + 16384 + 32768 + 32768;  // A, V, S0, dO, [Q ; K], dUt
 constexpr int kBcThreads = 512;
 // shared memory (bytes from the 1024-aligned base)
 constexpr int kBcKQ = 0;        // [Q ; K]: 2 atoms (k halves) x [128 rows][128 B]: Q rows 0-63, K rows 64-127
@@ -1705,7 +1706,8 @@ constexpr int kBcA = 81920;     // A image hi | lo, [64 rows t][64 s]
 constexpr int kBcS = 98304;     // S0, then dS1: hi | lo, each 2 atoms (v halves) x [128 rows k][128 B]
 constexpr int kBcW = 163840;    // dKS^T hi | lo [128 v][64 t] -> Ut^T hi | lo -> dP'' hi | lo, MM hi | lo [64][64]
 constexpr int kBcScr = 196608;  // fp32 scratch: 12 x 64 row arrays, 16 reduction slots, barriers
-constexpr int kBcSmem = 1024 + kBcScr + 4096;
+constexpr int kBcV = kBcScr + 4096;  // V [64 t][128 v] bf16, plain rows
+constexpr int kBcSmem = 1024 + kBcV + 16384;
 // tensor memory columns
 constexpr uint32_t kTbKS = 0;     // KS^T -> Ut^T -> dq2^T
 constexpr uint32_t kTbP1 = 64;    // [dO Ut^T ; dR_hi Ut^T + ...]
@@ -1756,6 +1758,7 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
     extern __shared__ __align__(1024) char smraw[];
     char *sm = smem_align1024(smraw);
     char *KQ = sm + kBcKQ, *OR = sm + kBcOR, *RL = sm + kBcRL, *Aim = sm + kBcA, *Sim = sm + kBcS, *Wim = sm + kBcW;
+    const __nv_bfloat16 *Vsm = reinterpret_cast<const __nv_bfloat16 *>(sm + kBcV);
     float *scr = reinterpret_cast<float *>(sm + kBcScr);
     float *gam = scr, *bet = scr + 64, *egv = scr + 128;
     float *rRV = scr + 192, *rRKS = scr + 256, *rUdU = scr + 320, *rQdq = scr + 384, *rP = scr + 448,
@@ -1804,9 +1807,10 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
         hqn = hn / (p.Hv / p.Hq);
         return p.chunk[cn].tok0;
     };
-    auto copy_A = [&](int un, int hn, int hqn, int tk) {
+    auto copy_A = [&](int un, int hn, int hqn, int tk) {  // the A rows and the V tile
         tma3d(Aim, &maps.A, 0, hn, tk, &bars[0]);
         tma3d(Aim + 8192, &maps.A, 32, hn, tk, &bars[0]);
+        tma3d(sm + kBcV, &maps.V, 0, hn, tk, &bars[0]);
     };
     auto copy_S0_dO = [&](int un, int hn, int hqn, int tk) {
 #pragma unroll
@@ -1943,14 +1947,10 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
             ++ncommit;
         }
     }
-    // this thread's V column (lane v, tokens t0..) loads while the MMAs run
+    // this thread's V column (lane v, tokens t0..; the tile landed with the unit's copies)
     float vv[16];
-    {
-        const __nv_bfloat16 *vin = reinterpret_cast<const __nv_bfloat16 *>(p.v) + ((size_t)tok0 * p.Hv + h) * 128 + row_v;
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-            vv[j] = t0 + j < len ? __bfloat162float(vin[(size_t)(t0 + j) * p.Hv * 128]) : 0.f;
-    }
+    for (int j = 0; j < 16; ++j) vv[j] = t0 + j < len ? __bfloat162float(Vsm[(t0 + j) * 128 + row_v]) : 0.f;
     ok = bwait(&bars[1], 0, cap, abort);
     if (__syncthreads_or(!ok)) goto out;
     tc_fence_after();
@@ -2053,7 +2053,7 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
     if (__syncthreads_or(!ok)) goto out;
     tc_fence_after();
     if (tid == 0 && un < NU) {  // the next unit's A rows, over the A image groups 1-2 have read
-        mbar_expect_tx_only(&bars[0], 16384);
+        mbar_expect_tx_only(&bars[0], 16384 + 16384);
         copy_A(un, nxt[0], nxt[1], nxt[2]);
         pf_phase = (it + 1) & 1;
         pf_arrived = false;
@@ -2442,7 +2442,8 @@ int launch_bwd_chunk(const Params &p, cudaStream_t st) {
         !map3(&maps.dO, p.dout, p.Hv, p.Ttot, 64, true) ||
         !mapf32(&maps.S0, p.hbuf, 128, 128, NU, 512, 65536, 32, 128, 1) ||
         !mapf32(&maps.dU, p.dubuf, 128, 64, NU, 512, 32768, 32, 64, 1) ||
-        !mapf32(&maps.A, p.A_in, 64, p.Hv, p.Ttot, 256, (cuuint64_t)p.Hv * 256, 32, 1, 64))
+        !mapf32(&maps.A, p.A_in, 64, p.Hv, p.Ttot, 256, (cuuint64_t)p.Hv * 256, 32, 1, 64) ||
+        !map3(&maps.V, p.v, p.Hv, p.Ttot, 128, false))
         return 1;
     if (cudaFuncSetAttribute(k_bwd_chunk_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kBcSmem) != cudaSuccess)
         return 1;

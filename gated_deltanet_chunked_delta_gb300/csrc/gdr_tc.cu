@@ -1383,9 +1383,26 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_dh_tc(Params p, const __gri
                 split_pairs<16>(f, hv, lv);
                 tmem_st16(tSh + sc0 / 2 + lo, hv);
                 tmem_st16(tSl + sc0 / 2 + lo, lv);
-                if (DM == kDhFull)
+                if (DM == kDhFull) {
+                    // dS1 leaves as the chunk kernel's A operand: a bf16 hi | lo pair of
+                    // 128-byte-swizzled images [2 value halves][128 rows k][64 values],
+                    // 64 KiB per (chunk, v-head).  Lanes v, v^1 swap halves so that the
+                    // even lane writes the hi word of the pair, the odd lane the lo word.
+                    const int ve = t & ~1, term = t & 1;
+                    char *img = reinterpret_cast<char *>(p.dhbuf) + ch * 65536 + term * 32768 + (ve >> 6) * 16384 +
+                                (ve & 7) * 2;
+                    const int vc = (ve & 63) >> 3;
+                    // (the bf16 terms are the ones split_pairs packed along k above)
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) p.dhbuf[(ch * 128 + sc0 + i) * 128 + t] = f[i];
+                    for (int i = 0; i < 32; ++i) {
+                        const int k = sc0 + i;
+                        const uint32_t hb = (i & 1) ? (hv[i >> 1] >> 16) : (hv[i >> 1] & 0xffffu);
+                        const uint32_t lb = (i & 1) ? (lv[i >> 1] >> 16) : (lv[i >> 1] & 0xffffu);
+                        const uint32_t other = __shfl_xor_sync(0xffffffffu, term ? hb : lb, 1);
+                        const uint32_t w = term ? (other | (lb << 16)) : (hb | (other << 16));
+                        *reinterpret_cast<uint32_t *>(img + k * 128 + ((vc ^ (k & 7)) << 4)) = w;
+                    }
+                }
 #pragma unroll
                 for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(f[i] * dec);
                 tmem_st32(tS + sc0 + lo, r);
@@ -1780,6 +1797,7 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
     if (tid == 0) {
         mbar_init(&bars[0], 1);
         mbar_init(&bars[1], 1);
+        mbar_init(&bars[6], 1);  // the dS1 image copy
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -1792,6 +1810,7 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    int ds1_copies = 0, ds1_parity = 0;  // dS1 copies issued (thread 0), waits done (every thread)
     const uint32_t sKQ = su32(KQ), sOR = su32(OR), sRL = su32(RL), sA = su32(Aim), sS = su32(Sim), sW = su32(Wim);
     // Thread 0's bookkeeping: MMA groups committed, and the copy phase of
     // bars[0] still open (its arrival made or not) for the drain on an abort.
@@ -2001,14 +2020,6 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
             atomicAdd(&rRKS[t0 + lane], s2);
         }
     }
-    // this thread's dS1 item loads while the next MMAs run
-    float4 d1v[8];
-    {
-        const int k = tid & 127, sq = tid >> 7;  // a warp: 32 consecutive rows of one quarter
-        const float4 *src = reinterpret_cast<const float4 *>(p.dhbuf + ch * 128 * 128 + (size_t)k * 128 + 32 * sq);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) d1v[i] = src[i];
-    }
     tmem_wait_st();
     fence_async_smem();
     tc_fence_before();
@@ -2059,6 +2070,29 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
         pf_arrived = false;
     }
     // ---------------- epilogue 2 ----------------
+    // <dS1, S0>: this thread's S0 terms (row k, 32 values) are read before the
+    // dS1 image, which the reverse scan stored ready for the MMA, is copied
+    // over them
+    uint32_t s0w[32];
+    {
+        const int k = tid & 127, sq = tid >> 7;  // a warp: 32 consecutive rows of one quarter
+        const char *ih = Sim + (sq >> 1) * 16384 + k * 128, *il = ih + 32768;
+        const int c0 = 32 * (sq & 1);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int off = ((((c0 >> 3) + j) ^ (k & 7)) << 4);
+            const uint4 wh = *reinterpret_cast<const uint4 *>(ih + off);
+            const uint4 wl = *reinterpret_cast<const uint4 *>(il + off);
+            s0w[8 * j] = wh.x; s0w[8 * j + 1] = wh.y; s0w[8 * j + 2] = wh.z; s0w[8 * j + 3] = wh.w;
+            s0w[8 * j + 4] = wl.x; s0w[8 * j + 5] = wl.y; s0w[8 * j + 6] = wl.z; s0w[8 * j + 7] = wl.w;
+        }
+    }
+    __syncthreads();  // every S0 term read
+    if (tid == 0) {
+        mbar_expect_tx(&bars[6], 65536);
+        bulk_g2s(Sim, reinterpret_cast<const char *>(p.dhbuf) + ch * 65536, 65536, &bars[6]);
+        ++ds1_copies;
+    }
     {
         // lane v: Ut^T -> image (B operand of group 3)
         uint32_t uu[16];
@@ -2068,28 +2102,26 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
         for (int j = 0; j < 16; ++j) x[j] = __uint_as_float(uu[j]);
         st_img_hl16(Wim, Wim + 16384, row_v, t0, x);
     }
+    ok = bwait(&bars[6], (ds1_parity++) & 1, cap, abort);
+    if (__syncthreads_or(!ok)) goto out;
     {
-        // the dS1 image over the S0 image, with <dS1, S0> from the S0 terms it replaces
-        const int k = tid & 127, sq = tid >> 7;  // a warp: 32 consecutive rows of one quarter
-        char *ih = Sim + (sq >> 1) * 16384, *il = ih + 32768;
+        const int k = tid & 127, sq = tid >> 7;
+        const char *ih = Sim + (sq >> 1) * 16384 + k * 128, *il = ih + 32768;
         const int c0 = 32 * (sq & 1);
-        float x[32], part = 0.f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            x[4 * i] = d1v[i].x; x[4 * i + 1] = d1v[i].y; x[4 * i + 2] = d1v[i].z; x[4 * i + 3] = d1v[i].w;
-        }
+        float part = 0.f;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const int off = k * 128 + ((((c0 >> 3) + j) ^ (k & 7)) << 4);
+            const int off = ((((c0 >> 3) + j) ^ (k & 7)) << 4);
             const uint4 wh = *reinterpret_cast<const uint4 *>(ih + off);
             const uint4 wl = *reinterpret_cast<const uint4 *>(il + off);
-            const uint32_t hh[4] = {wh.x, wh.y, wh.z, wh.w}, ll[4] = {wl.x, wl.y, wl.z, wl.w};
+            const uint32_t dh[4] = {wh.x, wh.y, wh.z, wh.w}, dl[4] = {wl.x, wl.y, wl.z, wl.w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                part += x[8 * j + 2 * e] * (bf_lo(hh[e]) + bf_lo(ll[e])) +
-                        x[8 * j + 2 * e + 1] * (bf_hi(hh[e]) + bf_hi(ll[e]));
+            for (int e = 0; e < 4; ++e) {
+                const uint32_t sh = s0w[8 * j + e], sl = s0w[8 * j + 4 + e];
+                part += (bf_lo(dh[e]) + bf_lo(dl[e])) * (bf_lo(sh) + bf_lo(sl)) +
+                        (bf_hi(dh[e]) + bf_hi(dl[e])) * (bf_hi(sh) + bf_hi(sl));
+            }
         }
-        st_img_hl(ih, il, k, c0, x);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
         if (lane == 0) atomicAdd(&red[0], part);
@@ -2301,6 +2333,7 @@ out:
             drain_wait(&bars[0], pf_phase);
         }
         if (ncommit > 0) drain_wait(&bars[1], (ncommit - 1) & 1);
+        if (ds1_copies > 0) drain_wait(&bars[6], (ds1_copies - 1) & 1);
     }
     tc_fence_before();
     __syncthreads();

@@ -1771,7 +1771,11 @@ __device__ __forceinline__ void tmem_ld16w(uint32_t ta, uint32_t (&r)[16]) {
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-__global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const __grid_constant__ BcMaps maps) {
+// gsteps: G (the qk-head's v-heads taken one after another by one CTA, dq and
+// dk summed in place) or 1 (units one at a time, dq and dk partials for a
+// separate sum).
+__global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const __grid_constant__ BcMaps maps,
+                                                                int gsteps) {
     extern __shared__ __align__(1024) char smraw[];
     char *sm = smem_align1024(smraw);
     char *KQ = sm + kBcKQ, *OR = sm + kBcOR, *RL = sm + kBcRL, *Aim = sm + kBcA, *Sim = sm + kBcS, *Wim = sm + kBcW;
@@ -1793,6 +1797,8 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
     const int row_v = 32 * q4 + lane;  // this thread's TMEM lane (a value, key or stacked token index)
     const int t0 = 16 * cq;            // this thread's 16 columns of a 64-column block
     const int NU = p.NT * p.Hv;        // units (chunk, v-head), u = chunk * Hv + v-head
+    const int G = p.Hv / p.Hq;         // the v-heads of one qk-head: units hq G .. hq G + G - 1 of a chunk
+    const int NQ = NU / gsteps;        // groups of gsteps consecutive units, each taken whole by one CTA
 
     if (tid == 0) {
         mbar_init(&bars[0], 1);
@@ -1846,24 +1852,27 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
 #pragma unroll
         for (int q = 0; q < 4; ++q) tma3d(Wim + q * 8192, &maps.dU, 32 * q, 0, un, &bars[0]);
     };
-    if (tid == 0 && (int)blockIdx.x < NU) {
+    if (tid == 0 && (int)blockIdx.x < NQ) {
+        const int u0 = blockIdx.x * gsteps;
         int hn, hqn;
-        const int tk = unit_tok(blockIdx.x, hn, hqn);
+        const int tk = unit_tok(u0, hn, hqn);
         mbar_expect_tx(&bars[0], kBcPrefetch);
-        copy_A(blockIdx.x, hn, hqn, tk);
-        copy_S0_dO(blockIdx.x, hn, hqn, tk);
-        copy_KQ_dU(blockIdx.x, hn, hqn, tk);
+        copy_A(u0, hn, hqn, tk);
+        copy_S0_dO(u0, hn, hqn, tk);
+        copy_KQ_dU(u0, hn, hqn, tk);
         pf_phase = 0;
     }
     bool ok = true;
     int it = 0;
-    for (int u = blockIdx.x; u < NU; u += gridDim.x, ++it) {
+    for (int q = blockIdx.x, gj = 0; q < NQ;
+         ++it, q = (gj + 1 == gsteps) ? q + (int)gridDim.x : q, gj = (gj + 1 == gsteps) ? 0 : gj + 1) {
+    const int u = q * gsteps + gj;
     const int c = u / p.Hv, h = u - c * p.Hv;
     const ChunkInfo ci = p.chunk[c];
     const int len = ci.len, tok0 = ci.tok0;
-    const int hq = h / (p.Hv / p.Hq);
+    const int hq = h / G;
     const size_t ch = (size_t)u;
-    const int un = u + gridDim.x;  // this CTA's next unit
+    const int un = gj + 1 < gsteps ? u + 1 : (q + (int)gridDim.x < NQ ? (q + (int)gridDim.x) * gsteps : NU);  // next unit
     if (tid == 0 && un < NU) nxt[2] = unit_tok(un, nxt[0], nxt[1]);  // its head, qk-head, first token
     __syncthreads();  // the previous unit's tail is done with the scratch rows
     if (tid < 64) {
@@ -2273,10 +2282,13 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
             dqv[j] = p.scale * egv[t] * __uint_as_float(qr[j]) + __uint_as_float(q2[j]);
             dkv[j] = __uint_as_float(kd[j]) + __expf(gC - gam[t]) * __uint_as_float(k2[j]);
         }
-        // with G > 1 v-heads per qk-head the fp32 partials go to the workspace and
-        // a separate pass sums them in head order; with G = 1 dq, dk are final
-        const int G = p.Hv / p.Hq;
-        if (G > 1) {
+        // dq, dk summed over the G v-heads of the qk-head in head order: with
+        // gsteps = G this CTA takes the group's units one after another, and each
+        // thread keeps the running sum of its own (token, k) elements in the
+        // workspace between them (the first head's slot), written and read back
+        // by that thread only; with gsteps = 1 every unit leaves its partial in
+        // its own slot for a separate pass
+        if (G > 1 && gsteps == 1) {
 #pragma unroll
             for (int j = 0; j < 16; ++j)
                 if (t0 + j < len) {
@@ -2284,6 +2296,35 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
                     p.dqp[off] = dqv[j];
                     p.dkp[off] = dkv[j];
                 }
+        } else if (G > 1) {
+            float* accq = p.dqp + ((size_t)tok0 * p.Hv + hq * G) * 128 + k;
+            float* acck = p.dkp + ((size_t)tok0 * p.Hv + hq * G) * 128 + k;
+            const size_t ts = (size_t)p.Hv * 128;
+            if (gj > 0) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    if (t0 + j < len) {
+                        dqv[j] += accq[(t0 + j) * ts];
+                        dkv[j] += acck[(t0 + j) * ts];
+                    }
+            }
+            if (gj + 1 < G) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    if (t0 + j < len) {
+                        accq[(t0 + j) * ts] = dqv[j];
+                        acck[(t0 + j) * ts] = dkv[j];
+                    }
+            } else {
+                __nv_bfloat16 *dqo = reinterpret_cast<__nv_bfloat16 *>(p.dq), *dko = reinterpret_cast<__nv_bfloat16 *>(p.dk);
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    if (t0 + j < len) {
+                        const size_t o = ((size_t)(tok0 + t0 + j) * p.Hq + hq) * 128 + k;
+                        dqo[o] = __float2bfloat16_rn(dqv[j]);
+                        dko[o] = __float2bfloat16_rn(dkv[j]);
+                    }
+            }
         } else {
             __nv_bfloat16 *dqo = reinterpret_cast<__nv_bfloat16 *>(p.dq), *dko = reinterpret_cast<__nv_bfloat16 *>(p.dk);
 #pragma unroll
@@ -2373,6 +2414,7 @@ __global__ void __launch_bounds__(256) k_group_sum_tc(Params p) {
                                                          pack_bf16(ak[4], ak[5]), pack_bf16(ak[6], ak[7]));
     }
 }
+
 
 // ---------------------------------------------------------------------------
 // host side
@@ -2488,10 +2530,24 @@ int launch_bwd_chunk(const Params &p, cudaStream_t st) {
             cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || nsm <= 0)
             nsm = 148;
     }
-    const int grid = (int)(NU < (cuuint64_t)nsm ? NU : (cuuint64_t)nsm);
+    // whole qk-head groups per CTA (dq, dk summed in place) unless that makes
+    // the busiest CTA take more units than one at a time would; then the
+    // partials and a separate head-order sum
+    const int G = p.Hv / p.Hq;
+    const cuuint64_t NQ = (cuuint64_t)p.NT * p.Hq;
+    const bool whole = G > 1 && ((NQ + nsm - 1) / nsm) * G <= (NU + nsm - 1) / nsm;
+    const int gsteps = whole ? G : 1;
+    const cuuint64_t NG = NU / gsteps;
+    const int grid = (int)(NG < (cuuint64_t)nsm ? NG : (cuuint64_t)nsm);
     tm_begin(p.tm, "tc_bwd_chunk", st);
-    k_bwd_chunk_tc<<<grid, kBcThreads, kBcSmem, st>>>(p, maps);
+    k_bwd_chunk_tc<<<grid, kBcThreads, kBcSmem, st>>>(p, maps, gsteps);
     tm_end(p.tm, st);
+    if (cudaGetLastError() != cudaSuccess) return 1;
+    if (G > 1 && !whole && p.Ttot > 0) {
+        tm_begin(p.tm, "tc_group_sum", st);
+        k_group_sum_tc<<<152 * 8, 256, 0, st>>>(p);
+        tm_end(p.tm, st);
+    }
     return cudaGetLastError() != cudaSuccess;
 }
 
@@ -2547,14 +2603,7 @@ int tc_bwd(const Params &p, int use_cp, cudaStream_t st) {
     if (launch_dh<kDhFull>("tc_dh", p, st)) return 1;
     // a10, a11: chunk-local gradients
     // the qk-head sums of dq and dk happen inside the chunk kernel
-    if (launch_bwd_chunk(p, st)) return 1;
-    if (p.Hv > p.Hq && p.Ttot > 0) {
-        tm_begin(p.tm, "tc_group_sum", st);
-        k_group_sum_tc<<<152 * 8, 256, 0, st>>>(p);
-        tm_end(p.tm, st);
-        if (cudaGetLastError() != cudaSuccess) return 1;
-    }
-    return 0;
+    return launch_bwd_chunk(p, st);
 }
 
 unsigned tc_take_status(cudaStream_t st) {

@@ -200,3 +200,13 @@ def test_bounded_waits_report_timeout_and_leave_the_context_usable(gdr):
     gdr.check_status()  # the status word was cleared
     _check_fwd(gdr, spec, gdr.GDR_PATH_TC, cp=4)
     _check_bwd(gdr, spec, gdr.GDR_PATH_TC, cp=4)
+
+
+@pytest.mark.slow
+def test_bwd_qk_group_summed_in_place(gdr):
+    """152 chunks x one qk-head of G = 4 v-heads: every CTA of the backward's
+    chunk kernel takes whole qk-head groups and sums dq, dk over the group in
+    place (the path the large workloads take; the small cases above take the
+    separate head-order sum)."""
+    spec = inputs.small(B=1, T=64 * 152, Hq=1, Hv=4, K=128, V=128, bwd=True)
+    _check_bwd(gdr, spec, _path(gdr, "tc", spec))

@@ -193,7 +193,7 @@ def bwd_workspace_size(prob: Problem, opts: gdr_opts) -> int:
 
 
 def tc_available(K: int = 128, V: int = 128) -> bool:
-    """Whether this build carries the tensor-core path for these head sizes."""
+    """Whether the loaded library carries the tensor-core path for these head sizes."""
     shp = gdr_shape(1, 64, 1, 1, K, V, 0, None, None)
     opts = make_opts(path=GDR_PATH_TC)
     return load().gdr_fwd_workspace_size(ctypes.byref(shp), ctypes.byref(opts)) > 0

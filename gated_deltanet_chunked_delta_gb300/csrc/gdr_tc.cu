@@ -7,7 +7,7 @@
 // batch x heads blocks (page 1, "efficiency problem"), which the segment split
 // fixes.  The pages also claim an algebraic reformulation that cuts
 // tensor-core, CUDA-core and SFU work without losing precision, but give no
-// formula; the one used here is this build's own:
+// formula; the one used here:
 //   * the chunk's pseudo-values are formed as Ut = A R with the residual
 //     R = diag(b) (V - diag(e^gamma) K S0) built from the exact bf16 inputs and
 //     a two-term (hi + lo bf16) split of the fp32 state, so the cancellation in

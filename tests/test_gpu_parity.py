@@ -29,7 +29,7 @@ def _path(gdr, name, spec):
     if spec.in_dtype != "bf16" or spec.K != 128 or spec.V != 128:
         pytest.skip("tensor-core path covers bf16 with K = V = 128")
     if not gdr.tc_available(spec.K, spec.V):
-        pytest.skip("this build has no tensor-core path")
+        pytest.skip("the library has no tensor-core path")
     return gdr.GDR_PATH_TC
 
 
@@ -188,7 +188,7 @@ def test_bounded_waits_report_timeout_and_leave_the_context_usable(gdr):
     drain their own copies and MMAs, free tensor memory and return; the host
     reads GDR_ERR_TIMEOUT, and the next call on the same context is correct."""
     if not gdr.tc_available():
-        pytest.skip("this build has no tensor-core path")
+        pytest.skip("the library has no tensor-core path")
     spec = inputs.small(B=1, T=64 * 40, Hq=1, Hv=2, K=128, V=128, bwd=True)
     x = inputs.make(spec)
     d = to_dev(x)

@@ -156,7 +156,7 @@ int make_plan(const gdr_shape *s, const gdr_opts *o, int want_path, int in_f32, 
 size_t al(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Layout {
-    size_t seq, chunk, seg, gam, W, U, P, Hseg, Mseg, Sstart, hbuf, dhbuf, dubuf, dqp, dkp, warm;
+    size_t seq, chunk, seg, gam, W, U, P, Hseg, Mseg, Nseg, Sstart, hbuf, dhbuf, dubuf, dqp, dkp, warm;
     size_t Aimg, Pimg, Aux;
     bool f32_tiles, bf16_tiles;
     size_t total;
@@ -186,8 +186,9 @@ Layout layout(const gdr_shape *s, const Plan &pl, bool bwd) {
         L.Mseg = take(4 * NS * Hv * K * K);
         L.Sstart = take(4 * NS * Hv * K * V);
         L.warm = L.bf16_tiles ? take(4 * (size_t)NS * Hv) : 0;
+        L.Nseg = (bwd && L.bf16_tiles) ? take(4 * NS * Hv * K * K) : 0;
     } else {
-        L.Hseg = L.Mseg = L.Sstart = L.warm = 0;
+        L.Hseg = L.Mseg = L.Nseg = L.Sstart = L.warm = 0;
     }
     if (bwd) {
         L.hbuf = take(4 * NT * Hv * K * V);
@@ -272,6 +273,7 @@ int fill_params(const gdr_shape *s, const Plan &pl, const Layout &L, void *ws, P
     p->Aux = F(L.Aux, L.bf16_tiles);
     p->Hseg = F(L.Hseg, pl.use_cp);
     p->Mseg = F(L.Mseg, pl.use_cp);
+    p->Nseg = F(L.Nseg, L.Nseg != 0);
     p->Sstart = F(L.Sstart, pl.use_cp);
     p->hbuf = F(L.hbuf, L.hbuf != 0);
     p->dhbuf = F(L.dhbuf, L.dhbuf != 0);

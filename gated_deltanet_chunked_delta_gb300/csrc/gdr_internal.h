@@ -79,6 +79,8 @@ struct Params {
     float *P;       // [NT,Hv,64,64]
     float *Hseg;    // [NSEG,Hv,K,V]
     float *Mseg;    // [NSEG,Hv,K,K]
+    float *Nseg;    // [NSEG,Hv,K,K] (tensor-core backward): each segment's composed
+                    // transition untransposed, i.e. the reverse scan's transposed one
     float *Sstart;  // [NSEG,Hv,K,V]
     float *hbuf;    // [NT,Hv,K,V]   (backward: states before each chunk)
     float *dhbuf;   // [NT,Hv,K,V]   (backward: gradient of the state after each chunk)

@@ -745,7 +745,10 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
     // after the first begin Wc chunks early (from h0 when that reaches the
     // sequence start, else from zero) and write nothing for those chunks
     const bool warm = head_warm(p, sq, h) && (MODE == kSum || sg.idx > 0);
-    const int nch = (MODE == kSum && (sg.idx >= sq.nseg - 1 || warm)) ? 0 : sg.nch;  // last segment: no summary
+    // the last segment has no summary, except the composed transition that
+    // the backward's reverse combine reads (in Nseg, untransposed)
+    const bool wantN = isM && p.Nseg;
+    const int nch = (MODE == kSum && (warm || (sg.idx >= sq.nseg - 1 && !wantN))) ? 0 : sg.nch;
     const int Wc = (MODE != kSum && warm) ? min(p.cp_warmup, sg.chunk0 - sq.chunk0) : 0;
     const int cfirst = sg.chunk0 - Wc;  // the first chunk this CTA scans
     const int ntot = Wc + nch;
@@ -1109,30 +1112,38 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
         // (a segment of an empty sequence has no chunk: its end state is its start state)
         if (__all_sync(0xffffffffu, live && !*abort) && (ntot == 0 || wbwait(bar_m3, (ntot - 1) & 1, cap, abort))) {
             tc_fence_after();
-            float *dst = nullptr;
+            float *dst = nullptr, *dstN = nullptr;
             size_t base = 0;
             if (MODE == kSum) {
-                if (sg.idx < sq.nseg - 1 && !warm) {
-                    dst = isM ? p.Mseg : p.Hseg;
-                    base = ((size_t)sidx * p.Hv + h) * 128 * 128;
-                }
+                base = ((size_t)sidx * p.Hv + h) * 128 * 128;
+                if (sg.idx < sq.nseg - 1 && !warm) dst = isM ? p.Mseg : p.Hseg;
+                if (wantN && sg.idx > 0 && !warm) dstN = p.Nseg + base;
             } else if (sg.idx == sq.nseg - 1 && p.final_state) {
                 dst = p.final_state;
                 base = ((size_t)sg.seq * p.Hv + h) * 128 * 128;
             }
             // the state row-major; the composed transition M transposed (row v
-            // of M^T is column v of M), the layout the tensor-core combine reads
-            if (dst)
+            // of M^T is column v of M), the layout the tensor-core combine
+            // reads, and for the backward also row-major in Nseg: the reverse
+            // scan's composed transition is M^T, which the reverse combine
+            // reads in the same transposed layout
+            if (dst || dstN)
 #pragma unroll 1
                 for (int j = 0; j < kSC / 32; ++j) {
                     uint32_t r[32];
                     tmem_ld32(tS + sc0 + 32 * j + lo, r);
                     if (isM) {
-                        float4 *d4 = reinterpret_cast<float4 *>(dst + base + (size_t)t * 128 + sc0 + 32 * j);
+                        if (dst) {
+                            float4 *d4 = reinterpret_cast<float4 *>(dst + base + (size_t)t * 128 + sc0 + 32 * j);
 #pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            d4[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
-                                                __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+                            for (int i = 0; i < 8; ++i)
+                                d4[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                                    __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+                        }
+                        if (dstN)
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                dstN[(size_t)(sc0 + 32 * j + i) * 128 + t] = __uint_as_float(r[i]);
                     } else {
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
@@ -1165,10 +1176,12 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
 //
 // The map dS1 -> dS0 is affine, so the reverse scan splits into segments
 // exactly like the forward (the context-parallel backward): kDhSum summarises
-// every segment but the first from dS = 0 (G, with the dO terms) and, in a
-// second CTA, from dS = I without the dO terms (N, the composed transposed
-// transitions); a reverse combine gives every segment's true end gradient
-// (dS_end(j) = N_{j+1} dS_end(j+1) + G_{j+1}); kDhFull re-runs each segment
+// every segment but the first from dS = 0 (G, with the dO terms).  The
+// composed transposed transitions N are M^T, the composed transitions that the
+// summary of the backward's state recompute leaves in Nseg, so a second CTA
+// runs from dS = I without the dO terms only for v-heads whose segments start
+// by warm-up (they have no summary).  A reverse combine gives every segment's
+// true end gradient (dS_end(j) = N_{j+1} dS_end(j+1) + G_{j+1}); kDhFull re-runs each segment
 // from it and stores dS1 and dUt of every chunk, and dh0 for the first.
 // ---------------------------------------------------------------------------
 constexpr int kDhFull = 0, kDhSum = 1;
@@ -1213,6 +1226,9 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_dh_tc(Params p, const __gri
     const bool isN = DM == kDhSum && blockIdx.z == 1;  // the composed-transition state
     const int hq = h / (p.Hv / p.Hq);
     const int nch = (DM == kDhSum && sg.idx == 0) ? 0 : sg.nch;  // the first segment needs no summary
+    // N is M^T, the forward summary's composed transition: that summary leaves
+    // it in Nseg for every v-head that does not start its segments by warm-up
+    if (isN && p.Nseg && !head_warm(p, sq, h)) return;
     const int cend = sg.chunk0 + sg.nch;                        // chunks run cend-1 down to chunk0
     const long long cap = p.timeout_spins;
 
@@ -1477,7 +1493,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_dh_tc(Params p, const __gri
                 dst = p.dh0;
                 base = ((size_t)n * p.Hv + h) * 128 * 128;
             } else if (DM == kDhSum && sg.idx > 0) {
-                dst = isN ? p.Mseg : p.Hseg;
+                dst = isN ? p.Nseg : p.Hseg;
                 base = ((size_t)sidx * p.Hv + h) * 128 * 128;
             }
             if (dst) {
@@ -1576,17 +1592,18 @@ __global__ void __launch_bounds__(128) k_warm_gate(Params p) {
 // fp32 throughout (the combine is on the exact path of every later segment).
 // ---------------------------------------------------------------------------
 constexpr int kCombW = 8;
-constexpr int kCombSmem = 1024 + 2 * 65536 + 128 * kCombW * 4 + 3 * 128 * 32 + 64;
+constexpr int kCombBufs = 2;
+constexpr int kCombSmem = 1024 + kCombBufs * 65536 + 128 * kCombW * 4 + 3 * 128 * 32 + 64;
 
 template <bool kRev>
 __global__ void __launch_bounds__(512) k_combine_tc(Params p) {
     extern __shared__ __align__(1024) char smraw[];
     char *sm = smem_align1024(smraw);
-    float *Mt = reinterpret_cast<float *>(sm);          // [2][128][128]
-    float *S = Mt + 2 * 16384;                           // [128][kCombW]
+    float *Mt = reinterpret_cast<float *>(sm);          // [kCombBufs][128][128]
+    float *S = Mt + kCombBufs * 16384;                   // [128][kCombW]
     float4 *part = reinterpret_cast<float4 *>(S + 128 * kCombW);  // [3][128][2] partial sums of quarters 1-3
-    uint64_t *bars = reinterpret_cast<uint64_t *>(part + 3 * 256);
-    volatile int *abort = reinterpret_cast<volatile int *>(bars + 2);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(part + 3 * 256);  // [kCombBufs]
+    volatile int *abort = reinterpret_cast<volatile int *>(bars + kCombBufs);
     const int n = blockIdx.x, h = blockIdx.y, v0 = blockIdx.z * kCombW, tid = threadIdx.x;
     const SeqInfo sq = p.seq[n];
     if (sq.nseg <= 1) return;
@@ -1600,7 +1617,7 @@ __global__ void __launch_bounds__(512) k_combine_tc(Params p) {
     auto fetch = [&](int step) {
         uint64_t *b = &bars[step & 1];
         mbar_expect_tx(b, 65536);
-        bulk_g2s(Mt + (step & 1) * 16384, p.Mseg + (seg_of(step) * p.Hv + h) * 16384, 65536, b);
+        bulk_g2s(Mt + (step & 1) * 16384, (kRev ? p.Nseg : p.Mseg) + (seg_of(step) * p.Hv + h) * 16384, 65536, b);
     };
     auto hrow = [&](int step, int r) {
         return *reinterpret_cast<const float4 *>(p.Hseg + (seg_of(step) * p.Hv + h) * 16384 + (size_t)r * 128 + v0 + c0);
@@ -2504,7 +2521,9 @@ int launch_dh(const char *name, const Params &p, cudaStream_t st) {
     auto kern = k_dh_tc<DM>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kDhSmem) != cudaSuccess) return 1;
     tm_begin(p.tm, name, st);
-    kern<<<dim3(p.NSEG, p.Hv, DM == kDhSum ? 2 : 1), kScanThreads, kDhSmem, st>>>(p, maps);
+    // the second z-plane (N) only where a v-head may start by warm-up
+    const int nz = (DM == kDhSum && (p.cp_warmup > 0 || !p.Nseg)) ? 2 : 1;
+    kern<<<dim3(p.NSEG, p.Hv, nz), kScanThreads, kDhSmem, st>>>(p, maps);
     tm_end(p.tm, st);
     return cudaGetLastError() != cudaSuccess;
 }

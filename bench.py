@@ -17,8 +17,9 @@ records would inflate): the dominant kernel's algorithmic work over its
 measured duration gives the roofline fraction, and their launch count (the
 same calls as the timed steps) is gpu_launches.
 
-``--impl reference`` times the fp64 CPU oracle (the reference arm of this
-build) on a bounded sample of the same workload.
+``--impl reference`` times the fp64 CPU oracle (the pages ship no code to
+run, so the oracle is the reference arm) on a bounded sample of the same
+workload.
 """
 from __future__ import annotations
 

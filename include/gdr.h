@@ -124,9 +124,10 @@ typedef struct {
      * when, for every segment of every sequence, the bound on the start
      * state's error, prod_t a_t max(1, |1 - b_t |k_t|^2|) over the warm-up
      * window, is below 1e-6 (or the window reaches the sequence start, where
-     * the warm-up is exact).  0: 8 warm-up chunks (default); -1: always the
-     * exact split; n > 0: n warm-up chunks.  Tensor-core path, forward and the
-     * backward's state recompute; the reverse scan is always exact. */
+     * the warm-up is exact).  0 (default): 8 warm-up chunks where the plan's
+     * segments are at least 32 chunks long, else the exact split; -1: always
+     * the exact split; n > 0: n warm-up chunks.  Tensor-core path, forward and
+     * the backward's state recompute; the reverse scan is always exact. */
     int cp_warmup;
 } gdr_opts;
 

@@ -19,8 +19,8 @@ GDR_BF16, GDR_F32 = 0, 1
 GDR_PATH_AUTO, GDR_PATH_SIMT, GDR_PATH_TC = 0, 1, 2
 ERRORS = {1: "GDR_ERR_ARG", 2: "GDR_ERR_SHAPE", 3: "GDR_ERR_DTYPE", 4: "GDR_ERR_ALIGN",
           5: "GDR_ERR_WORKSPACE", 6: "GDR_ERR_CUDA", 7: "GDR_ERR_TIMEOUT", 8: "GDR_ERR_DEVICE"}
-EXPORTS = ("gdr_num_chunks", "gdr_fwd_workspace_size", "gdr_bwd_workspace_size", "gdr_fwd", "gdr_bwd",
-           "gdr_check_status", "gdr_last_error", "gdr_version")
+EXPORTS = ("gdr_num_chunks", "gdr_get_plan", "gdr_fwd_workspace_size", "gdr_bwd_workspace_size", "gdr_fwd",
+           "gdr_bwd", "gdr_check_status", "gdr_last_error", "gdr_version")
 
 
 class GdrError(RuntimeError):
@@ -44,6 +44,11 @@ class gdr_opts(ctypes.Structure):
                 ("timeout_spins", ctypes.c_longlong), ("events", ctypes.POINTER(ctypes.c_void_p)),
                 ("names", ctypes.POINTER(ctypes.c_char_p)), ("max_events", ctypes.c_int),
                 ("n_launched", ctypes.POINTER(ctypes.c_int)), ("cp_warmup", ctypes.c_int)]
+
+
+class gdr_plan(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int), ("n_chunks", ctypes.c_longlong), ("n_segments", ctypes.c_int),
+                ("seg_len", ctypes.c_int), ("cp_warmup", ctypes.c_int)]
 
 
 class KernelTimer:
@@ -95,6 +100,8 @@ def load(build_if_missing: bool = False):
     P, vp, sz = ctypes.POINTER, ctypes.c_void_p, ctypes.c_size_t
     lib.gdr_num_chunks.argtypes = [P(gdr_shape)]
     lib.gdr_num_chunks.restype = ctypes.c_longlong
+    lib.gdr_get_plan.argtypes = [P(gdr_shape), ctypes.c_int, P(gdr_opts), P(gdr_plan)]
+    lib.gdr_get_plan.restype = ctypes.c_int
     for f in (lib.gdr_fwd_workspace_size, lib.gdr_bwd_workspace_size):
         f.argtypes = [P(gdr_shape), P(gdr_opts)]
         f.restype = sz
@@ -176,6 +183,18 @@ def make_opts(cp_segments=0, path=GDR_PATH_AUTO, debug_checks=0, timeout_spins=0
     o = gdr_opts(int(cp_segments), int(path), int(debug_checks), int(timeout_spins), None, None, 0, None,
                  int(cp_warmup))
     return timer.attach(o) if timer is not None else o
+
+
+def get_plan(prob: Problem, in_dtype: int = GDR_BF16, opts: Optional[gdr_opts] = None) -> dict:
+    """The plan a call with these sizes, input dtype and options would take
+    (host-side query: path, chunks, context-parallel segments, warm-up)."""
+    out = gdr_plan()
+    rc = load().gdr_get_plan(ctypes.byref(prob.shape), int(in_dtype), ctypes.byref(opts or make_opts()),
+                             ctypes.byref(out))
+    if rc:
+        raise GdrError(rc, load().gdr_last_error().decode())
+    return {"path": out.path, "n_chunks": out.n_chunks, "n_segments": out.n_segments, "seg_len": out.seg_len,
+            "cp_warmup": out.cp_warmup}
 
 
 def fwd_workspace_size(prob: Problem, opts: gdr_opts) -> int:

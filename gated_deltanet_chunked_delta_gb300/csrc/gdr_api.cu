@@ -153,6 +153,15 @@ int make_plan(const gdr_shape *s, const gdr_opts *o, int want_path, int in_f32, 
     return GDR_OK;
 }
 
+// Warm-up starts of CP segments (tensor-core path with a split only): option
+// 0 -> 8 chunks when segments are at least four windows long (shorter ones
+// would scan a large share of extra chunks), -1 -> off, n -> n.
+int warmup_chunks(const Plan &pl, const gdr_opts *o) {
+    if (!pl.use_cp || pl.path != GDR_PATH_TC) return 0;
+    const int req = !o ? 0 : o->cp_warmup;
+    return req < 0 ? 0 : req > 0 ? req : (pl.seg_len >= 4 * 8 ? 8 : 0);
+}
+
 size_t al(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Layout {
@@ -281,11 +290,7 @@ int fill_params(const gdr_shape *s, const Plan &pl, const Layout &L, void *ws, P
     p->dqp = F(L.dqp, L.dqp != 0);
     p->dkp = F(L.dkp, L.dkp != 0);
     p->warm = L.warm ? reinterpret_cast<int *>(w + L.warm) : nullptr;
-    // warm-up starts of CP segments: 0 -> 8 chunks when segments are at least
-    // four windows long (shorter ones would scan a large share of extra
-    // chunks), -1 -> off, n -> n
-    const int req = !o ? 0 : o->cp_warmup;
-    p->cp_warmup = !p->warm ? 0 : req < 0 ? 0 : req > 0 ? req : (pl.seg_len >= 4 * 8 ? 8 : 0);
+    p->cp_warmup = p->warm ? warmup_chunks(pl, o) : 0;
     p->debug = o ? o->debug_checks : 0;
     p->timeout_spins = (o && o->timeout_spins > 0) ? o->timeout_spins : (1LL << 22);
     return GDR_OK;
@@ -331,6 +336,21 @@ static size_t ws_size(const gdr_shape *shape, const gdr_opts *opts, bool bwd) {
     }
     if (any) g_err[0] = 0;
     return best;
+}
+
+int gdr_get_plan(const gdr_shape *shape, int in_dtype, const gdr_opts *opts, gdr_plan *out) {
+    g_err[0] = 0;
+    if (!out) return fail(GDR_ERR_ARG, "out is null");
+    if (in_dtype != GDR_BF16 && in_dtype != GDR_F32) return fail(GDR_ERR_DTYPE, "unknown dtype %d", in_dtype);
+    Plan pl;
+    const int rc = make_plan(shape, opts, 0, in_dtype == GDR_F32, &pl);
+    if (rc) return rc;
+    out->path = pl.path;
+    out->n_chunks = pl.NT;
+    out->n_segments = pl.NSEG;
+    out->seg_len = pl.seg_len;
+    out->cp_warmup = warmup_chunks(pl, opts);
+    return GDR_OK;
 }
 
 size_t gdr_fwd_workspace_size(const gdr_shape *shape, const gdr_opts *opts) { return ws_size(shape, opts, false); }

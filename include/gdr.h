@@ -134,6 +134,26 @@ typedef struct {
 /* Number of 64-token chunks over all sequences (the NT of h).  -1 on bad shape. */
 GDR_API long long gdr_num_chunks(const gdr_shape *shape);
 
+/* How a call with these sizes, input dtype and options would run.  The
+ * intra-card context-parallel split follows the pages' cost reasoning (page 1,
+ * "two fused kernels and automatic CP": the per-segment steps cost about the
+ * segment length, the combine about the number of segments), re-fitted to the
+ * SM count of the current device (152 when no device is visible). */
+typedef struct {
+    int path;             /* GDR_PATH_SIMT or GDR_PATH_TC */
+    long long n_chunks;   /* as gdr_num_chunks */
+    int n_segments;       /* segments over all sequences; equal to the number of
+                             sequences when no sequence is split */
+    int seg_len;          /* chunks per segment (a sequence's last may be shorter) */
+    int cp_warmup;        /* warm-up chunks at segment starts (0: exact split only) */
+} gdr_plan;
+
+/* Fills *out for a forward or backward call with inputs of element type
+ * `in_dtype` (GDR_BF16 or GDR_F32).  Host-side only: touches no device memory
+ * and launches nothing.  Returns GDR_OK or the error gdr_fwd would return for
+ * these sizes, dtype and options. */
+GDR_API int gdr_get_plan(const gdr_shape *shape, int in_dtype, const gdr_opts *opts, gdr_plan *out);
+
 /* Workspace bytes needed by gdr_fwd / gdr_bwd for this shape and options.
  * Returns 0 and sets the last error on an invalid shape. */
 GDR_API size_t gdr_fwd_workspace_size(const gdr_shape *shape, const gdr_opts *opts);

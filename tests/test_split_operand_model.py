@@ -31,8 +31,8 @@ def bf16(x):
 
 def mm(a, b, split):
     """a @ b as the tensor cores take it: bf16 operands, fp32 accumulation.
-    `split` lists which operands are computed (not exact bf16 inputs) and so
-    enter as hi + lo."""
+    split == "none": each operand rounded to bf16 once; otherwise each enters
+    as hi + lo with three products (for an exact bf16 input lo is zero)."""
     a = np.asarray(a, np.float32)
     b = np.asarray(b, np.float32)
     if split == "none":
@@ -88,7 +88,7 @@ def test_split_operands_keep_the_state_accurate_over_a_long_sequence():
     single_s, single_o = run(48, "none")
     split_s, split_o = run(48, "split")
     assert split_s < 1e-3 and split_o < 1e-3
-    # single bf16 operands lose about two orders of magnitude against the split
+    # single bf16 operands lose two to three orders of magnitude against the split
     assert single_s > 20 * split_s
     assert single_o > 10 * split_o
 

@@ -10,6 +10,7 @@ runs the CUDA library.
   backward reads the forward summary's M instead of running its own chain.
 * Zero-padded rows (k = q = v = 0, b = 0, g = 0) of a partial chunk change
   nothing.
+* The tensor-core reformulation: Ut = A R, P' Y = P Ut, K^T Y = Kt^T Ut.
 * The backward's stacked product: with Ut = A R, dA = dUt R^T, X = A^T dA and
   dR = A^T dUt, X A^T = dR Ut^T; and dL = -strict_tril(A^T dA A^T) is the
   gradient through A = (I + L)^-1 for a strictly lower L.
@@ -125,3 +126,23 @@ def test_backward_stacked_product_and_the_inverse_gradient():
         E[i, j] = h
         fd = (f(L + E) - f(L - E)) / (2 * h)
         assert abs(fd - dL[i, j]) <= 1e-6 * max(1.0, abs(dL[i, j]))
+
+
+def test_tensor_core_reformulation():
+    """Ut = A R with R = diag(b)(V - diag(e^gamma) K S0) is U - W S0; with
+    Y = diag(e^{gamma_n - gamma}) Ut and P' = scale diag(e^{gamma - gamma_n})
+    (Q K^T o tril_incl), P' Y = P Ut and K^T Y = Kt^T Ut."""
+    q, k, v, g, b = chunk_inputs(6, n=50)
+    gam, A, W, Kt, T = chunk_terms(k, g, b)
+    rng = np.random.default_rng(7)
+    S0 = rng.standard_normal((6, 5))
+    scale = 0.41
+    U = A @ (b[:, None] * v)
+    Ut = U - W @ S0
+    R = b[:, None] * (v - np.exp(gam)[:, None] * (k @ S0))
+    np.testing.assert_allclose(A @ R, Ut, rtol=0, atol=1e-12)
+    Y = np.exp(gam[-1] - gam)[:, None] * Ut
+    P = scale * np.tril(q @ k.T) * np.exp(gam[:, None] - gam[None, :])
+    Pp = scale * np.exp(gam - gam[-1])[:, None] * np.tril(q @ k.T)
+    np.testing.assert_allclose(Pp @ Y, P @ Ut, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(k.T @ Y, Kt.T @ Ut, rtol=0, atol=1e-12)

@@ -121,3 +121,20 @@ def test_high_level_call_refuses_cpu_tensors(lib):
     q = torch.zeros(1, 64, 1, 64, requires_grad=True)
     with pytest.raises(gdr.GdrError):
         gdr.chunk_gated_delta_rule(q, q, q, torch.zeros(1, 64, 1), torch.zeros(1, 64, 1), output_final_state=True)
+
+
+def test_plain_c_client_compiles_links_and_runs(lib, tmp_path):
+    """include/gdr.h compiles as C11 and libgdr links with C linkage: a plain-C
+    program calls the host-side entry points (no device needed)."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    libdir = os.path.dirname(B.library_path())
+    exe = str(tmp_path / "abi_smoke")
+    src = os.path.join(ROOT, "tests", "c_abi", "abi_smoke.c")
+    subprocess.run([gcc, "-std=c11", "-Wall", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"), src,
+                    "-o", exe, "-L", libdir, "-lgdr", f"-Wl,-rpath,{libdir}"], check=True)
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout + r.stderr

@@ -48,3 +48,26 @@ def test_single_process_aggregation_is_local():
     import bench
     value, total_ms = bench.aggregate(4.0, 1000, 2, "cpu")
     assert total_ms == 4.0 and value == pytest.approx(1000 * 2 / 0.004 / 1e6)
+
+
+def test_reference_arm_prints_once_on_rank_zero():
+    """Under a multi-rank launch the reference arm (the oracle on the host
+    cores) runs on rank 0 alone and prints one JSON line; other ranks exit 0
+    without work or output."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    outs = []
+    for rank in (0, 1):
+        env = dict(os.environ, RANK=str(rank), LOCAL_RANK=str(rank), WORLD_SIZE="2")
+        r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--gpus", "2",
+                            "--steps", "1", "--warmup", "0", "--ref-tokens", "64"],
+                           capture_output=True, text=True, env=env, cwd=root, timeout=300)
+        assert r.returncode == 0, r.stderr[-2000:]
+        outs.append([ln for ln in r.stdout.splitlines() if ln.strip()])
+    assert outs[1] == []
+    assert len(outs[0]) == 1
+    line = json.loads(outs[0][0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"

@@ -3,9 +3,13 @@
 
 One step = gdr_fwd (o, final_state, A) followed by gdr_bwd (dq, dk, dv, dbeta,
 dg, dh0) over one synthetic batch: every step of the hot path.  The default
-workload is the context-parallel forward case B=1, T=8192, Hq=4, Hv=8,
-K=V=128 (bf16 q/k/v, fp32 g/beta, 30% of v-heads with g == 0) with do ~ N(0,1)
-and dht ~ N(0, 0.1) drawn for the backward.
+workload is the largest one, the training case B=2, T=16384, Hq=32, Hv=64,
+K=V=128 (bf16 q/k/v, fp32 g/beta, 30% of v-heads with g == 0, h0 ~ N(0, 0.1),
+do ~ N(0, 1), dht ~ N(0, 0.1)).  The same line carries, under
+``fwd_workloads``, the forward alone on the long-context case (B=1, T=262144,
+Hq=8, Hv=16, o fp32) and the 4-sequence varlen case (Hq=16, Hv=32), each with
+the context-parallel warm-up starts the planner chose and, beside it, with the
+exact split only (cp_warmup = -1).
 
 Timing: W untimed warm-up steps, then K steps bracketed by a barrier and
 torch.cuda.synchronize() on both sides; each step is timed with CUDA events on
@@ -38,7 +42,8 @@ sys.path.insert(0, ROOT)
 import torch  # noqa: E402
 
 METRIC = "GDN chunked-prefill fwd/bwd Mtokens/s at 1 GB300; % of bf16 roofline"
-DEFAULT_WORKLOAD = "fwd_bf16_T8192_hq4_hv8_d128"
+DEFAULT_WORKLOAD = "bwd_bf16_B2_T16384_hq32_hv64_d128"
+FWD_EXTRAS = ("fwd_bf16_T262144_hq8_hv16_d128", "fwd_bf16_varlen4_hq16_hv32_d128")
 FLUSH_BYTES = 256 << 20
 
 
@@ -81,10 +86,10 @@ def kernel_work(name, spec, in_bytes, o_bytes, nchunk_heads):
     mac = {
         # [K;Q] K^T (shared by the group), the triangular inverse
         "chunk": n * (2 * C * C * K / G + C ** 3 / 3),
-        # K S0, Q S0, K^T Y; A R; P' Y (causal)
+        # K S0, Q S0, K^T Y; A R; P Ut (causal)
         "scan": n * (3 * C * K * V + C * C * V + C * C * V / 2),
         "scan_states": n * (2 * C * K * V + C * C * V),
-        # dS1 K^T, X [Q ; K]; dO^T P' (causal); dUt A
+        # dS1 K^T, X [Q ; K]; dO^T P (causal); dUt A
         "dh": n * (3 * C * K * V + C * C * V / 2 + C * C * V),
         # K S0, dO S0^T, dKS S0^T, Y dS1^T; A R, A^T dUt, dUt R^T, dO Y^T;
         # Q K^T, K K^T, dP'' K, dP''^T Q, MM K, MM^T K; A^T dA A^T
@@ -169,9 +174,10 @@ class Clocks:
 # ---------------------------------------------------------------------------
 # the CPU oracle arm
 # ---------------------------------------------------------------------------
-def oracle_sample(x, spec, t_sample, heads_sample):
-    """Run the fp64 oracle forward+backward on the first t_sample tokens of every
-    sequence's first batch element, over the first `heads_sample` qk-heads."""
+def oracle_sample(x, spec, t_sample, heads_sample, nthreads=None):
+    """Run the fp64 oracle forward+backward on the first t_sample tokens of the
+    first sequence, over the first `heads_sample` qk-heads and their v-heads.
+    Returns (full-workload Mtokens/s, seconds, tokens, threads)."""
     import oracle
     G = spec.Hv // spec.Hq
     hq = slice(0, heads_sample)
@@ -185,7 +191,7 @@ def oracle_sample(x, spec, t_sample, heads_sample):
     h0 = None if x["h0"] is None else x["h0"][:1, hv]
     do = x["do"][:1, :T, hv]
     dht = x["dht"][:1, hv]
-    nthreads = os.cpu_count() or 1
+    nthreads = nthreads or os.cpu_count() or 1
     t0 = time.perf_counter()
     oracle.fwd(q, k, v, g, beta, x["scale"], h0=h0, nthreads=nthreads, vblock=16)
     oracle.bwd(q, k, v, g, beta, x["scale"], do, dht=dht, h0=h0, nthreads=nthreads)
@@ -196,6 +202,8 @@ def oracle_sample(x, spec, t_sample, heads_sample):
 
 
 def run_reference(args, spec, rank, world):
+    """The oracle as it stands on the host cores: each step one bounded sample
+    (the first --ref-tokens tokens of sequence 0, every v-head) of the workload."""
     from gated_deltanet_chunked_delta_gb300 import inputs
     if rank != 0:
         return
@@ -203,21 +211,22 @@ def run_reference(args, spec, rank, world):
     import oracle
     oracle.build()
     t_sample, heads = args.ref_tokens, spec.Hq
-    vals = []
+    vals, secs = [], []
     for i in range(args.warmup + args.steps):
         v, dt, T, nth = oracle_sample(x, spec, t_sample, heads)
         if i >= args.warmup:
             vals.append(v)
+            secs.append(dt)
     value = statistics.mean(vals)
-    # time the oracle needs for one whole step of the workload at this throughput
-    ms_full = spec.tokens / (value * 1e6) * 1e3
     line = {"metric": METRIC, "impl": "reference", "value": value, "unit": "Mtokens/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_full, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(secs),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": _config(spec, args),
+            "ms_per_full_step_extrapolated": spec.tokens / (value * 1e6) * 1e3,
             "cpu_baseline": {"value": value, "unit": "Mtokens/s", "cores": nth, "kind": "oracle",
-                             "sample": f"oracle fwd+bwd on tokens [0,{T}) of sequence 0, all {spec.Hv} v-heads; "
-                                       f"throughput in full-workload tokens"},
+                             "sample": f"each step: oracle fwd+bwd on tokens [0,{T}) of sequence 0, all {spec.Hv} "
+                                       f"v-heads; ms_per_step is that sample's time, value its throughput in "
+                                       f"full-workload tokens"},
             "e2e": {"value": value, "unit": "Mtokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -235,13 +244,16 @@ def aggregate(total_ms, tokens, steps, device):
     return tokens * steps / (total_ms / 1e3) / 1e6, total_ms
 
 
-def _config(spec, args):
+STEP_DESC = {"both": "gdr_fwd(o, final_state, A) + gdr_bwd(dq, dk, dv, dbeta, dg, dh0)",
+             "fwd": "gdr_fwd(o, final_state, A)",
+             "bwd": "gdr_bwd(dq, dk, dv, dbeta, dg, dh0)"}
+
+
+def _config(spec, args, mode=None):
     return {"workload": spec.name, "B": spec.B, "T": spec.T, "Hq": spec.Hq, "Hv": spec.Hv, "K": spec.K,
             "V": spec.V, "lengths": list(spec.lengths) if spec.lengths else None,
             "in_dtype": spec.in_dtype, "o_dtype": spec.out_dtype,
-            "step": {"both": "gdr_fwd(o, final_state, A) + gdr_bwd(dq, dk, dv, dbeta, dg, dh0)",
-                     "fwd": "gdr_fwd(o, final_state, A)",
-                     "bwd": "gdr_bwd(dq, dk, dv, dbeta, dg, dh0)"}[getattr(args, "mode", "both")],
+            "step": STEP_DESC[mode or getattr(args, "mode", "both")],
             "l2": f"flushed before every timed step ({FLUSH_BYTES >> 20} MiB write)",
             "parallelism": f"independent replicas x{args.gpus} (no collective)"}
 
@@ -249,6 +261,186 @@ def _config(spec, args):
 # ---------------------------------------------------------------------------
 # the GPU arm
 # ---------------------------------------------------------------------------
+class Workload:
+    """Device inputs, outputs and workspaces of one workload, and its step."""
+
+    def __init__(self, gdr, spec, mode, dev, path, cp, cp_warmup=0):
+        self.gdr, self.spec, self.mode, self.path, self.cp, self.cp_warmup = gdr, spec, mode, path, cp, cp_warmup
+        x = inputs_make(spec)
+        self.x = x
+        keys = ("q", "k", "v", "g", "beta", "h0", "do", "dht", "cu_seqlens")
+        self.d = d = {k: (x[k].to(dev) if torch.is_tensor(x.get(k)) else None) for k in keys}
+        self.cu_host = x["cu_seqlens"]
+        o_dtype = torch.float32 if spec.out_dtype == "f32" else torch.bfloat16
+        self.prob = prob = gdr.Problem(d["q"], d["v"], d["cu_seqlens"], self.cu_host)
+        self.opts = opts = gdr.make_opts(cp, path, cp_warmup=cp_warmup)
+        self.plan = gdr.get_plan(prob, gdr.GDR_BF16 if spec.in_dtype == "bf16" else gdr.GDR_F32, opts)
+        self.ws_f = gdr.alloc_workspace(gdr.fwd_workspace_size(prob, opts), dev)
+        self.ws_b = gdr.alloc_workspace(gdr.bwd_workspace_size(prob, opts), dev) if mode != "fwd" else None
+        N, B, T, Hv, K, V = prob.N, spec.B, spec.T, spec.Hv, spec.K, spec.V
+        self.out_f = {"o": torch.empty(B, T, Hv, V, device=dev, dtype=o_dtype),
+                      "final_state": torch.empty(N, Hv, K, V, device=dev),
+                      "A": torch.empty(B, T, Hv, 64, device=dev)}
+        self.out_b = None
+        if mode != "fwd":
+            self.out_b = {"dq": torch.empty_like(d["q"]), "dk": torch.empty_like(d["k"]),
+                          "dv": torch.empty_like(d["v"]), "dbeta": torch.empty_like(d["g"]),
+                          "dg": torch.empty_like(d["g"]), "dh0": torch.empty(N, Hv, K, V, device=dev)}
+        if mode == "bwd":
+            self.run_fwd()  # A for the backward, untimed
+
+    def run_fwd(self, timer=None):
+        d = self.d
+        self.gdr.gdr_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], self.x["scale"], h0=d["h0"],
+                         cu_seqlens=d["cu_seqlens"], cu_seqlens_host=self.cu_host, out=self.out_f,
+                         workspace=self.ws_f, cp_segments=self.cp, path=self.path, timer=timer,
+                         cp_warmup=self.cp_warmup)
+
+    def run_bwd(self, timer=None):
+        d = self.d
+        self.gdr.gdr_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], self.out_f["A"], d["do"], dht=d["dht"],
+                         scale=self.x["scale"], h0=d["h0"], cu_seqlens=d["cu_seqlens"],
+                         cu_seqlens_host=self.cu_host, out=self.out_b, workspace=self.ws_b, cp_segments=self.cp,
+                         path=self.path, timer=timer, cp_warmup=self.cp_warmup)
+
+    def step(self, timer_f=None, timer_b=None):
+        if self.mode in ("both", "fwd"):
+            self.run_fwd(timer_f)
+        if self.mode in ("both", "bwd"):
+            self.run_bwd(timer_b)
+
+
+def inputs_make(spec):
+    from gated_deltanet_chunked_delta_gb300 import inputs
+    return inputs.make(spec, seed=0)
+
+
+def timed_steps(w, steps, warmup, flush, stream, world, clocks=None):
+    """W warm-up steps, then `steps` timed ones (barrier + synchronize on both
+    sides, an L2 flush before each, CUDA events on the launching stream); then
+    as many steps again with every kernel bracketed by caller-owned events.
+    Returns (per-step ms, per-kernel ms lists, launches, wall seconds, clocks)."""
+    gdr = w.gdr
+    for _ in range(warmup):
+        flush.zero_()
+        w.step()
+    torch.cuda.synchronize()
+    gdr.check_status()
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(steps):
+        flush.zero_()
+        e0[i].record(stream)
+        w.step()
+        e1[i].record(stream)
+        torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t1 = time.time()
+    clk = clocks.stop(t0, t1) if clocks else None
+    step_ms = [a.elapsed_time(b) for a, b in zip(e0, e1)]
+    # per-kernel durations from separate steps with caller-owned events around
+    # every launch (kept out of the timed steps, whose time they would inflate)
+    tf, tb = gdr.KernelTimer(32), gdr.KernelTimer(32)
+    per_kernel, launches = {}, 0
+    for i in range(steps):
+        flush.zero_()
+        w.step(tf, tb)
+        torch.cuda.synchronize()
+        for timer in (tf, tb):
+            launches += timer.count.value
+            for nm, ms in timer.elapsed():
+                per_kernel.setdefault(nm, []).append(ms)
+    gdr.check_status()
+    return step_ms, per_kernel, launches // steps, t1 - t0, clk
+
+
+def rooflines(spec, mode, per_kernel, peaks, nch_heads, step_ms_mean):
+    """The dominant kernel's roofline object and the whole step's fraction of
+    max(flops / bf16 peak, bytes / HBM peak)."""
+    K, V, Hv = spec.K, spec.V, spec.Hv
+    tokens = spec.tokens
+    in_b = 2 if spec.in_dtype == "bf16" else 4
+    o_b = 4 if spec.out_dtype == "f32" else 2
+    agg = {nm: (sum(v), len(v)) for nm, v in per_kernel.items()}
+    dom = max(agg, key=lambda n: agg[n][0])
+    dom_ms = agg[dom][0] / agg[dom][1]
+    fl, by = kernel_work(dom, spec, in_b, o_b, nch_heads)
+    tc_peak = peaks["bf16_tflops"]
+    alu_peak = 152 * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12  # fp32 FFMA, TFLOP/s
+    if dom.startswith("simt"):
+        t_c, t_m = fl / (alu_peak * 1e12), by / (peaks["hbm_gbs"] * 1e9)
+        if t_c >= t_m:
+            roof = {"bound": "alu", "achieved": fl / (dom_ms / 1e3) / 1e12, "peak": alu_peak, "unit": "TFLOP/s"}
+        else:
+            roof = {"bound": "hbm", "achieved": by / (dom_ms / 1e3) / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    else:
+        t_c, t_m = fl / (tc_peak * 1e12), by / (peaks["hbm_gbs"] * 1e9)
+        if t_c >= t_m:
+            roof = {"bound": "tensor", "achieved": fl / (dom_ms / 1e3) / 1e12, "peak": tc_peak, "unit": "TFLOP/s"}
+        else:
+            roof = {"bound": "hbm", "achieved": by / (dom_ms / 1e3) / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = TRAFFIC.get((dom, spec.name))
+    roof["algorithmic_bytes"] = by
+    roof["algorithmic_flops"] = fl
+    roof["kernel"] = dom
+    roof["kernel_ms"] = dom_ms
+    roof["peak_source"] = peaks["source"]
+
+    # whole-step roofline (the metric's "% of bf16 roofline"): algorithmic flops
+    # (forward 166.6 kflop and backward 491.5 kflop per token-head at K = V = 128,
+    # G = 2) and bytes (inputs read once, outputs written once)
+    N = spec.n_seqs
+    th = tokens * Hv
+    qk_b, v_b, gb_b = tokens * spec.Hq * K * in_b, tokens * Hv * V * in_b, tokens * Hv * 4
+    A_b, st_b = tokens * Hv * 64 * 4, N * Hv * K * V * 4
+    f_fl, b_fl = th * 166.6e3, th * 491.5e3
+    f_by = 2 * qk_b + v_b + 2 * gb_b + (st_b if spec.h0 else 0) + tokens * Hv * V * o_b + st_b + A_b
+    b_by = (2 * qk_b + 2 * v_b + 2 * gb_b + A_b + (2 * st_b if spec.h0 else st_b)
+            + 2 * qk_b + v_b + 2 * gb_b + st_b)
+    step_flops = (f_fl if mode != "bwd" else 0) + (b_fl if mode != "fwd" else 0)
+    step_bytes = (f_by if mode != "bwd" else 0) + (b_by if mode != "fwd" else 0)
+    step_roof_ms = max(step_flops / (tc_peak * 1e12), step_bytes / (peaks["hbm_gbs"] * 1e9)) * 1e3
+    total = sum(a for a, _ in agg.values())
+    kernels = {nm: {"launches": n, "ms_total": round(t, 4), "share": round(t / total, 4)}
+               for nm, (t, n) in sorted(agg.items(), key=lambda kv: -kv[1][0])}
+    step = {"flops": step_flops, "bytes": step_bytes, "ms": step_roof_ms,
+            "bound": "tensor" if step_flops / (tc_peak * 1e12) * 1e3 >= step_roof_ms else "hbm"}
+    return roof, step_roof_ms / step_ms_mean, step, kernels
+
+
+def fwd_extra(gdr, name, args, dev, path, flush, stream, peaks):
+    """Forward-only figures of one workload: with the planner's warm-up starts
+    and with the exact context-parallel split only."""
+    from gated_deltanet_chunked_delta_gb300 import inputs
+    spec = inputs.resolve(name)
+    res = {"workload": name, "mode": "fwd", "step": STEP_DESC["fwd"]}
+    steps, warmup = max(3, args.steps // 2), max(3, min(args.warmup, 5))
+    for key, cw in (("planned", 0), ("exact_cp", -1)):
+        w = Workload(gdr, spec, "fwd", dev, path, args.cp, cw)
+        step_ms, per_kernel, launches, _, _ = timed_steps(w, steps, warmup, flush, stream, 1)
+        ms = statistics.mean(step_ms)
+        roof, frac, sroof, kernels = rooflines(spec, "fwd", per_kernel, peaks, w.prob.num_chunks() * spec.Hv, ms)
+        r = {"value": spec.tokens / (ms / 1e3) / 1e6, "unit": "Mtokens/s", "ms_per_step": ms,
+             "step_roofline_frac": frac, "cp_warmup": w.plan["cp_warmup"], "cp_segments": w.plan["n_segments"],
+             "seg_len": w.plan["seg_len"], "gpu_launches": launches, "kernels": kernels}
+        if key == "planned":
+            r.update({"roofline": roof, "step_roofline": sroof})
+        res[key] = r
+        del w
+        torch.cuda.empty_cache()
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -258,12 +450,16 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--path", default="auto", choices=["auto", "simt", "tc"])
     ap.add_argument("--cp", type=int, default=0, help="cp_segments (0 auto, 1 off, n forced)")
+    ap.add_argument("--cp-warmup", type=int, default=0, help="cp_warmup (0 planner's choice, -1 off, n chunks)")
     ap.add_argument("--mode", default="both", choices=["both", "fwd", "bwd"],
                     help="step = forward + backward (default), forward only, or backward only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip the forward-only workloads")
     ap.add_argument("--ref-tokens", type=int, default=1024, help="tokens per oracle step (reference arm)")
-    ap.add_argument("--cpu-tokens", type=int, default=0,
-                    help="tokens of the cpu_baseline sample (0: the whole first sequence)")
+    ap.add_argument("--cpu-tokens", type=int, default=4096,
+                    help="tokens of the all-cores cpu_baseline sample (0: the whole first sequence)")
+    ap.add_argument("--cpu-tokens-1core", type=int, default=1024,
+                    help="tokens of the one-core cpu_baseline sample (over 8 v-heads at most)")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -288,88 +484,15 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
     path = {"auto": gdr.GDR_PATH_AUTO, "simt": gdr.GDR_PATH_SIMT, "tc": gdr.GDR_PATH_TC}[args.path]
     peaks = _peaks()
-
-    x = inputs.make(spec, seed=0)
-    keys = ("q", "k", "v", "g", "beta", "h0", "do", "dht", "cu_seqlens")
-    d = {k: (x[k].to(dev) if torch.is_tensor(x[k]) else None) for k in keys}
-    cu_host = x["cu_seqlens"]
-    o_dtype = torch.float32 if spec.out_dtype == "f32" else torch.bfloat16
-    prob = gdr.Problem(d["q"], d["v"], d["cu_seqlens"], cu_host)
-    opts = gdr.make_opts(args.cp, path)
-    ws_f = gdr.alloc_workspace(gdr.fwd_workspace_size(prob, opts), dev)
-    ws_b = gdr.alloc_workspace(gdr.bwd_workspace_size(prob, opts), dev)
-    N, B, T, Hv, K, V = prob.N, spec.B, spec.T, spec.Hv, spec.K, spec.V
-    out_f = {"o": torch.empty(B, T, Hv, V, device=dev, dtype=o_dtype),
-             "final_state": torch.empty(N, Hv, K, V, device=dev),
-             "A": torch.empty(B, T, Hv, 64, device=dev)}
-    out_b = {"dq": torch.empty_like(d["q"]), "dk": torch.empty_like(d["k"]), "dv": torch.empty_like(d["v"]),
-             "dbeta": torch.empty_like(d["g"]), "dg": torch.empty_like(d["g"]),
-             "dh0": torch.empty(N, Hv, K, V, device=dev)}
-    tf = gdr.KernelTimer(32)
-    tb = gdr.KernelTimer(32)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def run_fwd(timer=None):
-        gdr.gdr_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], x["scale"], h0=d["h0"], cu_seqlens=d["cu_seqlens"],
-                    cu_seqlens_host=cu_host, out=out_f, workspace=ws_f, cp_segments=args.cp, path=path, timer=timer)
-
-    def run_bwd(timer=None):
-        gdr.gdr_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], out_f["A"], d["do"], dht=d["dht"],
-                    scale=x["scale"], h0=d["h0"], cu_seqlens=d["cu_seqlens"], cu_seqlens_host=cu_host,
-                    out=out_b, workspace=ws_b, cp_segments=args.cp, path=path, timer=timer)
-
-    def step(timer_f=None, timer_b=None):
-        if args.mode in ("both", "fwd"):
-            run_fwd(timer_f)
-        if args.mode in ("both", "bwd"):
-            run_bwd(timer_b)
-
-    if args.mode == "bwd":
-        run_fwd()  # A for the backward, untimed
-
-    for _ in range(args.warmup):
-        flush.zero_()
-        step()
-    torch.cuda.synchronize()
-    gdr.check_status()
-
+    w = Workload(gdr, spec, args.mode, dev, path, args.cp, args.cp_warmup)
+    x, d, out_f, out_b = w.x, w.d, w.out_f, w.out_b
     clocks = Clocks(local)
-    clocks.start()
-    time.sleep(0.3)
-    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    per_kernel = {}
-    launches = 0
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    t_wall0 = time.time()
-    for i in range(args.steps):
-        flush.zero_()
-        e0[i].record(stream)
-        step()
-        e1[i].record(stream)
-        torch.cuda.synchronize()
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    t_wall1 = time.time()
-    clk = clocks.stop(t_wall0, t_wall1)
-    step_ms = [a.elapsed_time(b) for a, b in zip(e0, e1)]
-    # per-kernel durations from separate steps with caller-owned events around
-    # every launch (kept out of the timed steps, whose time they would inflate)
-    for i in range(args.steps):
-        flush.zero_()
-        step(tf, tb)
-        torch.cuda.synchronize()
-        for timer in (tf, tb):
-            launches += timer.count.value
-            for nm, ms in timer.elapsed():
-                per_kernel.setdefault(nm, []).append(ms)
+    step_ms, per_kernel, launches, _, clk = timed_steps(w, args.steps, args.warmup, flush, stream, world, clocks)
     tokens = spec.tokens
     value, total_ms = aggregate(sum(step_ms), tokens, args.steps, dev)
-    gdr.check_status()
 
     # e2e: pinned host buffers, copies inside the timed region (every input of
     # the timed calls in, every output out)
@@ -396,7 +519,7 @@ def main():
         if not overlap:
             for k, t in hin.items():
                 dst_of[k].copy_(t, non_blocking=True)
-            step()
+            w.step()
             for k, t in dev_out.items():
                 hout[k].copy_(t, non_blocking=True)
         else:
@@ -409,7 +532,7 @@ def main():
                     dst_of[k].copy_(hin[k], non_blocking=True)
             ev_in = torch.cuda.Event()
             ev_in.record(cs)
-            run_fwd()
+            w.run_fwd()
             ev_f = torch.cuda.Event()
             ev_f.record(stream)
             cs.wait_event(ev_f)
@@ -419,7 +542,7 @@ def main():
             ev_o = torch.cuda.Event()
             ev_o.record(cs)
             stream.wait_event(ev_in)
-            run_bwd()
+            w.run_bwd()
             for k, t in out_b.items():
                 hout[k].copy_(t, non_blocking=True)
             stream.wait_event(ev_o)
@@ -427,72 +550,43 @@ def main():
         torch.cuda.synchronize()
         e2e_ms.append(ee0.elapsed_time(ee1))
     e2e_val = tokens * world / (statistics.mean(e2e_ms) / 1e3) / 1e6
+    gdr.check_status()
 
-    # roofline of the dominant kernel
-    nch_heads = prob.num_chunks() * Hv
-    in_b = 2 if spec.in_dtype == "bf16" else 4
-    o_b = 4 if spec.out_dtype == "f32" else 2
-    agg = {nm: (sum(v), len(v)) for nm, v in per_kernel.items()}
-    dom = max(agg, key=lambda n: agg[n][0])
-    dom_ms = agg[dom][0] / agg[dom][1]
-    fl, by = kernel_work(dom, spec, in_b, o_b, nch_heads)
-    tc_peak = peaks["bf16_tflops"]
-    alu_peak = 152 * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12  # fp32 FFMA, TFLOP/s
-    if dom.startswith("simt"):
-        t_c, t_m = fl / (alu_peak * 1e12), by / (peaks["hbm_gbs"] * 1e9)
-        if t_c >= t_m:
-            roof = {"bound": "alu", "achieved": fl / (dom_ms / 1e3) / 1e12, "peak": alu_peak, "unit": "TFLOP/s"}
-        else:
-            roof = {"bound": "hbm", "achieved": by / (dom_ms / 1e3) / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
-    else:
-        t_c, t_m = fl / (tc_peak * 1e12), by / (peaks["hbm_gbs"] * 1e9)
-        if t_c >= t_m:
-            roof = {"bound": "tensor", "achieved": fl / (dom_ms / 1e3) / 1e12, "peak": tc_peak, "unit": "TFLOP/s"}
-        else:
-            roof = {"bound": "hbm", "achieved": by / (dom_ms / 1e3) / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = TRAFFIC.get((dom, spec.name))
-    roof["algorithmic_bytes"] = by
-    roof["algorithmic_flops"] = fl
-    roof["kernel"] = dom
-    roof["peak_source"] = peaks["source"]
-
-    # whole-step roofline (the metric's "% of bf16 roofline"): algorithmic flops
-    # (forward 166.6 kflop and backward 491.5 kflop per token-head at K = V = 128,
-    # G = 2) and bytes (inputs read once, outputs written once)
-    th = tokens * Hv
-    qk_b, v_b, gb_b = tokens * spec.Hq * K * in_b, tokens * Hv * V * in_b, tokens * Hv * 4
-    A_b, st_b = tokens * Hv * 64 * 4, N * Hv * K * V * 4
-    f_fl, b_fl = th * 166.6e3, th * 491.5e3
-    f_by = 2 * qk_b + v_b + 2 * gb_b + (st_b if spec.h0 else 0) + tokens * Hv * V * o_b + st_b + A_b
-    b_by = (2 * qk_b + 2 * v_b + 2 * gb_b + A_b + (2 * st_b if spec.h0 else st_b)
-            + 2 * qk_b + v_b + 2 * gb_b + st_b)
-    step_flops = (f_fl if args.mode != "bwd" else 0) + (b_fl if args.mode != "fwd" else 0)
-    step_bytes = (f_by if args.mode != "bwd" else 0) + (b_by if args.mode != "fwd" else 0)
-    step_roof_ms = max(step_flops / (tc_peak * 1e12), step_bytes / (peaks["hbm_gbs"] * 1e9)) * 1e3
-
-    kernels = {nm: {"launches": n, "ms_total": round(t, 4), "share": round(t / sum(a for a, _ in agg.values()), 4)}
-               for nm, (t, n) in sorted(agg.items(), key=lambda kv: -kv[1][0])}
+    roof, step_frac, sroof, kernels = rooflines(spec, args.mode, per_kernel, peaks,
+                                                w.prob.num_chunks() * spec.Hv, total_ms / args.steps)
+    cfg = _config(spec, args)
+    cfg["cp_warmup"] = w.plan["cp_warmup"]
+    cfg["cp_segments"] = w.plan["n_segments"]
     line = {"metric": METRIC, "value": value, "unit": "Mtokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if spec.in_dtype == "bf16" else "f32",
-            "data": "synthetic", "config": _config(spec, args),
+            "data": "synthetic", "config": cfg,
             "roofline": roof,
-            "step_roofline_frac": step_roof_ms / (total_ms / args.steps),
-            "step_roofline": {"flops": step_flops, "bytes": step_bytes, "ms": step_roof_ms,
-                              "bound": "tensor" if step_flops / (tc_peak * 1e12) * 1e3 >= step_roof_ms else "hbm"},
+            "step_roofline_frac": step_frac,
+            "step_roofline": sroof,
             "kernels": kernels,
             "e2e": {"value": e2e_val, "unit": "Mtokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "copies": ("do, dht in during the forward and the forward's outputs out during the backward, "
                                "on a second stream; the rest in line" if overlap else "in line")},
             "gpu_launches": launches, "clocks": clk}
+    del hin, hout, dst_of, dev_out, out_f, out_b, d
+    if rank == 0 and world == 1 and not args.no_extras and args.workload == DEFAULT_WORKLOAD:
+        del w
+        torch.cuda.empty_cache()
+        line["fwd_workloads"] = [fwd_extra(gdr, nm, args, dev, path, flush, stream, peaks) for nm in FWD_EXTRAS]
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
         oracle.build()
         v, dt, Ts, nth = oracle_sample(x, spec, args.cpu_tokens or (1 << 30), spec.Hq)
+        h1 = max(1, min(spec.Hq, 8 // max(1, spec.Hv // spec.Hq)))
+        v1, dt1, T1, _ = oracle_sample(x, spec, args.cpu_tokens_1core, h1, nthreads=1)
         line["cpu_baseline"] = {"value": v, "unit": "Mtokens/s", "cores": nth, "kind": "oracle",
                                 "sample": f"oracle fwd+bwd on tokens [0,{Ts}) of sequence 0, all {spec.Hv} "
-                                          f"v-heads ({dt:.1f} s); throughput in full-workload tokens"}
+                                          f"v-heads ({dt:.1f} s); throughput in full-workload tokens",
+                                "one_core": {"value": v1, "unit": "Mtokens/s", "cores": 1,
+                                             "sample": f"oracle fwd+bwd on tokens [0,{T1}) of sequence 0, "
+                                                       f"{h1 * (spec.Hv // spec.Hq)} v-heads ({dt1:.1f} s); "
+                                                       f"throughput in full-workload tokens"}}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -310,6 +310,27 @@ int launch_prep(const gdr_shape *s, const Plan &pl, const Params &p, cudaStream_
 namespace gdr {
 // Records a message for gdr_last_error() on behalf of another translation unit.
 int set_last_error(int code, const char *msg) { return fail(code, "%s", msg); }
+
+// The argument checks of gdr_fwd and the workspace that call would need, for
+// the plan of the given inputs' own dtype (the path, and so the layout,
+// follows the dtype).  Returns gdr_fwd's error code for arguments it would
+// reject, with the same message.
+int fwd_check_and_size(const gdr_shape *shape, gdr_buf q, gdr_buf k, gdr_buf v, const float *g, const float *beta,
+                       const float *h0, gdr_buf o, const float *final_state, const float *A, const float *h,
+                       const gdr_opts *opts, size_t *need) {
+    g_err[0] = 0;
+    int rc;
+    if ((rc = check_buf("q", q, true)) || (rc = check_buf("k", k, true)) || (rc = check_buf("v", v, true)) ||
+        (rc = check_buf("o", o, true)) || (rc = check_ptr("g", g, true)) || (rc = check_ptr("beta", beta, true)) ||
+        (rc = check_ptr("h0", h0, false)) || (rc = check_ptr("final_state", final_state, false)) ||
+        (rc = check_ptr("A", A, false)) || (rc = check_ptr("h", h, false)))
+        return rc;
+    if (q.dtype != k.dtype || q.dtype != v.dtype) return fail(GDR_ERR_DTYPE, "q, k, v must share one dtype");
+    Plan pl;
+    if ((rc = make_plan(shape, opts, 0, q.dtype == GDR_F32, &pl))) return rc;
+    *need = layout(shape, pl, false).total;
+    return GDR_OK;
+}
 }  // namespace gdr
 
 extern "C" {

@@ -8,7 +8,7 @@ namespace gdr {
 
 constexpr int kChunk = 64;  // tokens per chunk
 // Tensor-core path per-(chunk, v-head) workspace records (bytes).
-constexpr int kTileImgBytes = 16384;  // one bf16 hi | lo pair of 64x64 images (A, P')
+constexpr int kTileImgBytes = 16384;  // one bf16 hi | lo pair of 64x64 images (A, P)
 constexpr int kAuxBytes = 768;        // beta, e^gamma, e^{gamma_n - gamma}: 3 x 64 fp32
 
 // Per sequence: token range, chunk range and segment range (context-parallel split).
@@ -90,8 +90,8 @@ struct Params {
     int *warm;         // [NSEG,Hv] 1: the segment's warm-up start passes its bound (set on the device)
     // tensor-core path chunk tiles (bf16 shared-memory images, hi and lo terms, 16 KiB each)
     void *Aimg;     // [NT,Hv] x A
-    void *Pimg;     // [NT,Hv] x P' = scale diag(e^{gamma - gamma_n}) (Q K^T o tril_incl)
-    void *Aux;      // [NT,Hv] x (gamma[64], beta[64]) fp32
+    void *Pimg;     // [NT,Hv] x P = scale (Q K^T o D o tril_incl), D_rs = e^{gamma_r - gamma_s}
+    void *Aux;      // [NT,Hv] x (beta[64], e^gamma[64], e^{gamma_n - gamma}[64]) fp32
     int debug;
     long long timeout_spins;
     Timing *tm;  // host-side only: launch timing (may be null)

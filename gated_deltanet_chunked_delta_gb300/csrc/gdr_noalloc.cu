@@ -17,6 +17,9 @@
 
 namespace gdr {
 int set_last_error(int code, const char *msg);
+int fwd_check_and_size(const gdr_shape *shape, gdr_buf q, gdr_buf k, gdr_buf v, const float *g, const float *beta,
+                       const float *h0, gdr_buf o, const float *final_state, const float *A, const float *h,
+                       const gdr_opts *opts, size_t *need);
 }
 
 namespace {
@@ -29,7 +32,11 @@ constexpr int kMaxDevices = 64;
 void *g_ws_addr[kMaxDevices];  // device address of g_noalloc_ws, per device
 std::mutex g_ws_mu;
 
-// Device address of the array on the current device, looked up once per device.
+// Device address of the array on the current device, looked up once per
+// device and kept for the life of the process.  A cudaDeviceReset() destroys
+// the device's context and this library's device image with it; the address
+// kept here is then stale, so the caller must not call gdr_fwd_noalloc on a
+// device after resetting it.
 int workspace_address(void **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {
@@ -59,8 +66,12 @@ int workspace_address(void **out) {
 extern "C" GDR_API int gdr_fwd_noalloc(const gdr_shape *shape, gdr_buf q, gdr_buf k, gdr_buf v, const float *g,
                                        const float *beta, float scale, const float *h0, gdr_buf o,
                                        float *final_state, float *A, float *h, const gdr_opts *opts, void *stream) {
-    const size_t need = gdr_fwd_workspace_size(shape, opts);
-    if (need == 0) return GDR_ERR_SHAPE;  // the message is already set
+    // gdr_fwd's own checks, and the workspace of the plan this call takes (the
+    // plan follows the input dtype: the tensor-core plan for bf16, the
+    // CUDA-core plan with its fp32 tiles for fp32)
+    size_t need = 0;
+    const int bad = gdr::fwd_check_and_size(shape, q, k, v, g, beta, h0, o, final_state, A, h, opts, &need);
+    if (bad) return bad;  // the message is already set
     if (need > kNoallocBytes) {
         char msg[256];
         snprintf(msg, sizeof(msg),

@@ -15,10 +15,14 @@
 //     never need to be formed;
 //   * the state update uses K itself (read as an MN-major operand) with the
 //     decay e^{gamma_n - gamma_r} folded into the left operand, so no decayed
-//     copy of K is stored;
-//   * the intra-chunk attention P = scale (Q K^T o D o tril) is stored as
-//     P' = scale diag(e^{gamma - gamma_n}) (Q K^T o tril), which needs one
-//     exponential per row instead of one per entry.
+//     copy of K is stored.
+// The intra-chunk attention P = scale (Q K^T o D o tril) keeps the pairwise
+// decay D_rs = e^{gamma_r - gamma_s} (s <= r, a non-positive exponent) in
+// every entry.  Splitting it into a row factor e^{gamma_r - gamma_n} and a
+// column factor e^{gamma_n - gamma_s} would save exponentials but leaves fp32
+// once a chunk's log-decay passes about -88 (the row factor overflows while
+// the column factor underflows), and strongly decaying gates are inside the
+// method's domain.
 // The state lives in tensor memory, transposed: TMEM lane v holds row v of
 // S^T, 128 fp32 columns of k.
 #include <cuda.h>
@@ -277,7 +281,7 @@ __device__ __forceinline__ bool head_warm(const Params &p, const SeqInfo &sq, in
 // copies).  Each fp32 matrix is stored as two bf16 terms, hi = bf16(x) and
 // lo = bf16(x - hi), which together carry ~16 significant bits:
 //   A image   [hi | lo], each [64 rows r][128 B], 128-byte swizzled: A[r][s] over s
-//   P' image  same layout: P'[r][s] = scale e^{gamma_r - gamma_n} (q_r . k_s), s <= r
+//   P image   same layout: P[r][s] = scale e^{gamma_r - gamma_s} (q_r . k_s), s <= r
 //   aux       beta[64], e^gamma[64], e^{gamma_n - gamma}[64] (fp32; rows past
 //             the chunk end: beta 0, gamma = gamma_n), the row factors every
 //             scan epilogue needs, computed once per chunk
@@ -314,7 +318,7 @@ __device__ __forceinline__ void st_img_half2(char *img, int row, int col0, const
 // Chunk-parallel kernel: one CTA of 128 threads per (chunk, v-head), several
 // CTAs per SM.  [K ; Q] K^T on tcgen05 (warps 0-1 read the K K^T rows, warps
 // 2-3 the Q K^T rows), the gate cumsum, L = strict_tril(diag(b) (K K^T o D)),
-// P', and the unit-lower-triangular inverse A = (I + L)^-1 on the CUDA cores
+// P, and the unit-lower-triangular inverse A = (I + L)^-1 on the CUDA cores
 // by recursive doubling: the four 16x16 diagonal inverses first (one column
 // per thread), then the two 32x32 diagonal blocks and then the whole matrix,
 // each from its two diagonal halves as
@@ -500,7 +504,7 @@ __global__ void __launch_bounds__(128, 5) k_chunk_tc(Params p, const __grid_cons
     }
     const bool ok = bwait(&bars[1], 0, cap, abort);
     tc_fence_after();
-    // rows of [K K^T ; Q K^T]: warps 0-1 -> L (unless from_A), warps 2-3 -> P'
+    // rows of [K K^T ; Q K^T]: warps 0-1 -> L (unless from_A), warps 2-3 -> P
     if (ok) {
         const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16);
         if (tid < 64) {
@@ -533,9 +537,12 @@ __global__ void __launch_bounds__(128, 5) k_chunk_tc(Params p, const __grid_cons
                 }
             }
         } else {
-            // rows past the chunk end are zero (the backward mixes rows through P'^T)
+            // P[r][s] = scale e^{gamma_r - gamma_s} (q_r . k_s) for s <= r: one
+            // exponential per entry, of a non-positive argument, so the entry
+            // stays in range however strongly the gates decay.  Rows past the
+            // chunk end are zero (the backward mixes rows through P^T).
             const int rr = tid - 64;
-            const float f = rr < len ? p.scale * __expf(gam[rr] - gC) : 0.f;
+            const float gr = gam[rr], sc = rr < len ? p.scale : 0.f;
             char *pimg = reinterpret_cast<char *>(As);  // staged for one bulk store
 #pragma unroll
             for (int hb = 0; hb < 2; ++hb) {
@@ -543,14 +550,23 @@ __global__ void __launch_bounds__(128, 5) k_chunk_tc(Params p, const __grid_cons
                 tmem_ld32(ta + 32 * hb, r0);
                 float x[32];
 #pragma unroll
-                for (int s = 0; s < 32; ++s) x[s] = 32 * hb + s <= rr ? f * __uint_as_float(r0[s]) : 0.f;
+                for (int s4 = 0; s4 < 32; s4 += 4) {
+                    const float4 g4 = *reinterpret_cast<const float4 *>(gam + 32 * hb + s4);
+                    const float gs[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int s = 32 * hb + s4 + e;
+                        const float v = sc * __expf(fminf(gr - gs[e], 0.f)) * __uint_as_float(r0[s4 + e]);
+                        x[s4 + e] = s <= rr ? v : 0.f;
+                    }
+                }
                 st_img_half2(pimg, rr, 32 * hb, x);
             }
         }
     }
     fence_async_smem();
     __syncthreads();  // L complete; the K/Q tile is dead (the MMA that read it has completed)
-    if (tid == 0 && ok) {  // the P' image, staged in A's buffer, leaves by one bulk store
+    if (tid == 0 && ok) {  // the P image, staged in A's buffer, leaves by one bulk store
         asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
                          reinterpret_cast<char *>(p.Pimg) + ch * kImg2),
                      "r"(su32(As)), "r"(kImg2)
@@ -558,7 +574,7 @@ __global__ void __launch_bounds__(128, 5) k_chunk_tc(Params p, const __grid_cons
         asm volatile("cp.async.bulk.commit_group;" ::: "memory");
         asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
     }
-    __syncthreads();  // the staged P' image has been read
+    __syncthreads();  // the staged P image has been read
     if (from_A) {
         // 64 rows x 16 float4, eight per thread, all in flight before the stores
         float4 av[8];
@@ -667,8 +683,9 @@ __global__ void __launch_bounds__(128, 5) k_chunk_tc(Params p, const __grid_cons
 //   (c)  R^T = (diag(b) (V - diag(e^gamma) K S))^T        -> bf16 hi + lo
 //   MMA1b D1b = R^T A^T = Ut^T
 //   (c2) Y^T = (diag(e^{gamma_n - gamma}) Ut)^T           -> bf16 hi + lo
+//        (kFwd: Ut^T itself too, over the dead (K S)^T columns)
 //   MMA3 S^T += Y^T K     (K tile read MN-major)          = (e^{gamma_n} S + Kt^T Ut)^T
-//   MMA2 D2 = Y^T P'^T = (P Ut)^T                         (kFwd)
+//   MMA2 D2 = Ut^T P^T = (P Ut)^T                         (kFwd)
 //   (e)  O = scale diag(e^gamma) Q S + P Ut               (kFwd, one chunk behind)
 // The state chain (S -> K S -> R -> Ut -> Y -> S) keeps every operand that
 // is not an exact bf16 input (S, R, A, Y) as two bf16 terms: x y ~ x_hi y_hi
@@ -676,9 +693,9 @@ __global__ void __launch_bounds__(128, 5) k_chunk_tc(Params p, const __grid_cons
 // With single bf16 operands on the chain the max-abs error of o and of the
 // state settles near 2e-2 of their RMS on these workloads; with the split it
 // is ~1e-4.  The residual R is formed from the exact inputs, so the
-// cancellation in v - S^T k happens in fp32.  The output-only products, Q S
-// and P Ut, take one term each (S_hi, Y_hi, P'_hi): their rounding reaches o
-// once, at ~2^-9 of the term, and never the state.
+// cancellation in v - S^T k happens in fp32.  Of the output-only products,
+// Q S takes one term (S_hi) and P Ut three (Ut and P as hi + lo pairs): their
+// rounding reaches o once and never the state.
 // ---------------------------------------------------------------------------
 struct ScanMaps {
     CUtensorMap K, Q, V;  // 3-D over k, q (box 64 x 1 x 64, swizzled) and v (box 128 x 1 x 64, plain)
@@ -692,7 +709,7 @@ struct ScanStage {
     static constexpr int kB1 = 0;
     static constexpr int kV = 2 * kAtom;          // [64][128] bf16 plain row-major
     static constexpr int kA = kV + 16384;         // A image, hi | lo
-    static constexpr int kP = kA + kImg2;         // P' image, hi | lo (kFwd)
+    static constexpr int kP = kA + kImg2;         // P image, hi | lo (kFwd)
     static constexpr int kBytes = kP + (MODE == kFwd ? kImg2 : 0);
 };
 
@@ -790,11 +807,14 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
     //   [384,512) A operands as packed bf16 pairs: S^T hi | lo (64 + 64
     //             columns) for MMA1, then R^T hi | lo at [384,448) for MMA1b
     //   [256,320) Y^T hi | lo, in place of Ut^T once (c2) has read it, for
-    //             MMA3 and MMA2: the next chunk's (a) does not touch it, so
-    //             MMA2 (the output's term) runs after MMA3, off the chain
+    //             MMA3
+    //   [128,192) Ut^T hi | lo (kFwd), over (K S)^T once (c) has read it, for
+    //             MMA2: the next chunk's (a) touches neither, so MMA2 (the
+    //             output's term) runs after MMA3, off the chain, and MMA1 of
+    //             the next chunk, issued after it, overwrites them in order
     const uint32_t tS = tmem, tD1 = tmem + 128, tQS = tmem + 192, tD1b = tmem + 256, tD2 = tmem + 320;
     const uint32_t tSh = tmem + 384, tSl = tmem + 448, tRh = tmem + 384, tRl = tmem + 416, tYh = tmem + 256,
-                   tYl = tmem + 288;
+                   tYl = tmem + 288, tUh = tmem + 128, tUl = tmem + 160;
 
     if (warp == kEpiWarps) {
         // ---------------- TMA producer ----------------
@@ -871,14 +891,14 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
                     mma_ts(tS, tYl + 8 * kk, sdesc(b1 + kk * 2048, SL::kAtom), id3, 1);
                 }
                 mma_commit(bar_m3);
-                if (MODE == kFwd) {  // in issue order before MMA1b of the next chunk overwrites Y
+                if (MODE == kFwd) {  // in issue order before MMA1 of the next chunk overwrites Ut^T
                     const uint32_t ph = su32(st + SL::kP), pl = ph + kImg;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint32_t o = kk * 32;
-                        mma_ts(tD2, tYh + 8 * kk, sdesc(ph + o), id64, kk > 0);
-                        mma_ts(tD2, tYl + 8 * kk, sdesc(ph + o), id64, 1);
-                        mma_ts(tD2, tYh + 8 * kk, sdesc(pl + o), id64, 1);
+                        mma_ts(tD2, tUh + 8 * kk, sdesc(ph + o), id64, kk > 0);
+                        mma_ts(tD2, tUl + 8 * kk, sdesc(ph + o), id64, 1);
+                        mma_ts(tD2, tUh + 8 * kk, sdesc(pl + o), id64, 1);
                     }
                     mma_commit(bar_m2);
                 }
@@ -1076,7 +1096,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
             }
             tc_fence_before();
             warp_arrive(bar_rt, lane);
-            // (c2) Y^T[t][r] = e^{gamma_n - gamma_r} Ut^T[t][r]
+            // (c2) Y^T[t][r] = e^{gamma_n - gamma_r} Ut^T[t][r] (and, in kFwd, Ut^T
+            // itself as the A operand of MMA2)
             if (!wbwait(bar_m1b, cc & 1, cap, abort)) { live = false; break; }
             tc_fence_after();
             {
@@ -1090,6 +1111,14 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
                     tmem_ld16_issue(tD1b + c0 + lo, r);
                     tmem_wait_ld16(r);
                     float x[16];
+                    if (MODE == kFwd) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) x[i] = __uint_as_float(r[i]);
+                        uint32_t uh[8], ul[8];
+                        split_pairs<8>(x, uh, ul);
+                        tmem_st8(tUh + c0 / 2 + lo, uh);
+                        tmem_st8(tUl + c0 / 2 + lo, ul);
+                    }
 #pragma unroll
                     for (int i = 0; i < 16; ++i) x[i] = eL[c0 + i] * __uint_as_float(r[i]);
                     split_pairs<8>(x, hv + 8 * j, lv + 8 * j);
@@ -1163,12 +1192,13 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
 // ---------------------------------------------------------------------------
 // Reverse state scan of the backward: one CTA per (sequence, v-head), over the
 // chunks from last to first, with dS^T (the gradient of the state after the
-// chunk, transposed: lane v) in TMEM.  With dY = P'^T dO + K dS1 (the
-// gradient of Y = diag(e^{gamma_n - gamma}) Ut), dUt = diag(e^{gamma_n -
-// gamma}) dY and dR = A^T dUt:
+// chunk, transposed: lane v) in TMEM.  With dUt = P^T dO + diag(e^{gamma_n -
+// gamma}) K dS1 and dR = A^T dUt:
+//   MMA-o D1 = dO^T P                      (dO and P read MN-major; no state:
+//                                           issued as soon as the stage lands)
 //   (a)  store dS1; dS1^T -> bf16 hi + lo; dS^T *= e^{gamma_n} in place
-//   MMA-a D1 = dS1^T K^T + dO^T P'         = dY^T  (dO and P' read MN-major)
-//   (c)  store dUt; dUt^T -> bf16 hi + lo
+//   MMA-a E  = dS1^T K^T
+//   (c)  dUt^T = D1 + E diag(e^{gamma_n - gamma}); store dUt; -> bf16 hi + lo
 //   MMA-b D2 = dUt^T A                     = dR^T  (A read MN-major)
 //   (c2) X^T = [ (diag(scale e^gamma) dO)^T | -(diag(b e^gamma) dR)^T ] -> hi + lo
 //   MMA-c dS^T += X^T [Q ; K]              (the stacked Q, K tile read MN-major)
@@ -1192,7 +1222,7 @@ struct DhStage {
     static constexpr int kQK = 0;         // [2 atoms][128 rows][128 B]: Q rows 0-63, K rows 64-127
     static constexpr int kdO = 32768;     // [2 atoms (v halves)][64 rows][128 B]
     static constexpr int kA = 49152;      // A image, hi | lo
-    static constexpr int kP = 65536;      // P' image, hi | lo
+    static constexpr int kP = 65536;      // P image, hi | lo
     static constexpr int kBytes = 81920;
 };
 constexpr int kDhSmem = 1024 + 2 * DhStage::kBytes + 2 * kAux + 256;
@@ -1257,7 +1287,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_dh_tc(Params p, const __gri
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     // Tensor memory (lane v throughout):
-    //   [0,128) dS^T fp32;  [128,192) dY^T (MMA-a);  [192,256) dR^T (MMA-b)
+    //   [0,128) dS^T fp32;  [128,192) (dO^T P) (MMA-o);  [192,256) (dS1^T K^T)
+    //   (MMA-a), then dR^T (MMA-b, issued once (c) has read MMA-a's result)
     //   [256,384) dS1^T hi | lo as packed bf16 pairs (A of MMA-a), then dUt^T
     //             hi | lo at [256,320) (A of MMA-b)
     //   [384,512) X^T hi | lo (A of MMA-c; 64 columns each: the dO part for
@@ -1294,7 +1325,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_dh_tc(Params p, const __gri
     } else if (warp == kEpiWarps + 1) {
         if (lane == 0) {
             const uint32_t idK = idesc_bf16(128, 64);           // dS1^T K^T
-            const uint32_t idOP = idesc_bf16(128, 64, 1, 1);    // dO^T P'
+            const uint32_t idOP = idesc_bf16(128, 64, 1, 1);    // dO^T P
             const uint32_t idA = idesc_bf16(128, 64, 0, 1);     // dUt^T A
             const uint32_t idQK = idesc_bf16(128, 128, 0, 1);   // X^T [Q ; K]
             for (int cc = 0; cc < nch; ++cc) {
@@ -1318,7 +1349,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_dh_tc(Params p, const __gri
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         const uint32_t o = (kk >> 2) * 16384 + (kk & 3) * 32;
-                        mma_ts(tD1, (half ? tSl : tSh) + 8 * kk, sdesc(kr + o), idK, isN ? (half | kk) != 0 : 1);
+                        mma_ts(tD2, (half ? tSl : tSh) + 8 * kk, sdesc(kr + o), idK, (half | kk) != 0);
                     }
                 }
                 mma_commit(bar_m1);
@@ -1426,19 +1457,23 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_dh_tc(Params p, const __gri
             }
             tc_fence_before();
             warp_arrive(bar_sb, lane);
-            // (c) dUt^T[t][r] = e^{gamma_n - gamma_r} dY^T[t][r] (rows past the chunk end: 0)
+            // (c) dUt^T[t][r] = (dO^T P)[t][r] + e^{gamma_n - gamma_r} (dS1^T K^T)[t][r]
+            // (rows past the chunk end: 0; P has no entry there)
             if (!wbwait(bar_m1, cc & 1, cap, abort)) { live = false; break; }
             tc_fence_after();
             {
                 float fe[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) fe[i] = tc0 + i < len ? eL[tc0 + i] : 0.f;
-                uint32_t r[16];
-                tmem_ld16_issue(tD1 + tc0 + lo, r);
+                uint32_t r[16], ro[16];
+                tmem_ld16_issue(tD2 + tc0 + lo, r);
+                if (!isN) tmem_ld16_issue(tD1 + tc0 + lo, ro);
                 tmem_wait_ld16(r);
+                if (!isN) tmem_hold16(ro);
                 float x[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) x[i] = fe[i] * __uint_as_float(r[i]);
+                for (int i = 0; i < 16; ++i)
+                    x[i] = fe[i] * __uint_as_float(r[i]) + (isN ? 0.f : __uint_as_float(ro[i]));
                 uint32_t hv[8], lv[8];
                 split_pairs<8>(x, hv, lv);
                 tmem_st8(tUh + tc0 / 2 + lo, hv);
@@ -2604,7 +2639,7 @@ int tc_fwd(const Params &p, int o_f32, int use_cp, cudaStream_t st) {
 }
 
 int tc_bwd(const Params &p, int use_cp, cudaStream_t st) {
-    // a8: A image, P' image and gates from the forward's A; states before every chunk
+    // a8: A image, P image and gates from the forward's A; states before every chunk
     if (launch_chunk("tc_chunk_from_A", p, 1, st)) return 1;
     if (use_cp) {
         if (launch_gate(p, st)) return 1;

@@ -11,6 +11,11 @@ q, k, v, g-noise, beta-noise, zero-gate heads, h0, do, dht):
 * v ~ N(0, 1);  beta = sigmoid(N(0, 1));  g = logsigmoid(N(4, 1.5));
 * ``round(zero_frac * Hv)`` v-heads, picked by a seeded permutation, get
   g == 0 in every batch element (a gate of exactly 1);
+* strong-decay variants (not used by the five workloads): the logsigmoid's
+  mean ``gate_mu`` (4 by default) can be moved, e.g. to -4, and ``const_heads``
+  further v-heads of the same permutation can take the constant log-gate
+  ``const_g`` in every token, so that a 64-token chunk's log-decay reaches
+  64 const_g;
 * h0 ~ N(0, 0.1) (std 0.1) when requested;  do ~ N(0, 1);  dht ~ N(0, 0.1).
 
 Varlen lengths are integers drawn uniformly from ``[lo, hi]`` with a separate
@@ -43,6 +48,9 @@ class Spec:
     lengths: Optional[Tuple[int, ...]] = None  # varlen: B == 1, T == sum(lengths)
     bwd: bool = False              # also draw do and dht
     varlen_draw: Optional[Tuple[int, int, int, int]] = field(default=None)  # (n, lo, hi, max_total)
+    gate_mu: float = 4.0           # g = logsigmoid(N(gate_mu, 1.5))
+    const_heads: int = 0           # v-heads after the g == 0 ones with g == const_g in every token
+    const_g: float = -3.0
 
     @property
     def out_dtype(self) -> str:
@@ -107,17 +115,22 @@ def make(spec, seed: int = 0) -> dict:
     q = F.normalize(torch.randn(B, T, Hq, K, generator=gen), p=2.0, dim=-1).to(dt)
     k = F.normalize(torch.randn(B, T, Hq, K, generator=gen), p=2.0, dim=-1).to(dt)
     v = torch.randn(B, T, Hv, V, generator=gen).to(dt)
-    g = F.logsigmoid(4.0 + 1.5 * torch.randn(B, T, Hv, generator=gen))
+    g = F.logsigmoid(spec.gate_mu + 1.5 * torch.randn(B, T, Hv, generator=gen))
     beta = torch.sigmoid(torch.randn(B, T, Hv, generator=gen))
     nz = int(round(spec.zero_frac * Hv))
-    zero_heads = torch.randperm(Hv, generator=gen)[:nz]
+    perm = torch.randperm(Hv, generator=gen)
+    zero_heads = perm[:nz]
     if nz:
         g[:, :, zero_heads] = 0.0
+    const_heads = perm[nz:nz + spec.const_heads]
+    if spec.const_heads:
+        g[:, :, const_heads] = float(spec.const_g)
     N = spec.n_seqs
     h0 = 0.1 * torch.randn(N, Hv, K, V, generator=gen) if spec.h0 else None
     out = {
         "spec": spec, "q": q, "k": k, "v": v, "g": g.contiguous(), "beta": beta.contiguous(),
         "h0": h0, "scale": K ** -0.5, "zero_heads": sorted(int(x) for x in zero_heads),
+        "const_heads": sorted(int(x) for x in const_heads),
         "cu_seqlens": None,
     }
     if spec.lengths is not None:
@@ -132,10 +145,12 @@ def make(spec, seed: int = 0) -> dict:
 
 
 def small(B=1, T=200, Hq=2, Hv=4, K=64, V=64, in_dtype="bf16", lengths=None, zero_frac=0.25,
-          h0=True, bwd=False, o_dtype=None, name="small") -> Spec:
+          h0=True, bwd=False, o_dtype=None, name="small", gate_mu=4.0, const_heads=0,
+          const_g=-3.0) -> Spec:
     """A reduced spec with the same distributions, for parity at oracle-friendly sizes."""
     if lengths is not None:
         B, T = 1, sum(lengths)
         lengths = tuple(lengths)
     return Spec(name, B=B, T=T, Hq=Hq, Hv=Hv, K=K, V=V, in_dtype=in_dtype, o_dtype=o_dtype,
-                zero_frac=zero_frac, h0=h0, lengths=lengths, bwd=bwd)
+                zero_frac=zero_frac, h0=h0, lengths=lengths, bwd=bwd, gate_mu=gate_mu,
+                const_heads=const_heads, const_g=const_g)

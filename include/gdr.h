@@ -193,10 +193,13 @@ GDR_API int gdr_bwd(const gdr_shape *shape, gdr_buf q, gdr_buf k, gdr_buf v, con
  * convenience.  Arguments and results are those of gdr_fwd, minus the
  * workspace: the call uses a fixed 64 MiB array compiled into the library,
  * which every GPU that loads the library keeps until the process exits.
- * Problems whose gdr_fwd_workspace_size() exceeds 64 MiB are rejected with
- * GDR_ERR_WORKSPACE before anything is launched.  The first call on each
- * device looks the array's device address up (cudaGetSymbolAddress); make that
- * first call before any stream capture.  All calls share the one array: calls
+ * Problems whose forward workspace, for the plan of the inputs' own dtype,
+ * exceeds 64 MiB are rejected with GDR_ERR_WORKSPACE before anything is
+ * launched; invalid arguments get gdr_fwd's error codes.  The first call on
+ * each device looks the array's device address up (cudaGetSymbolAddress) and
+ * keeps it for the life of the process; make that first call before any
+ * stream capture, and make no call on a device after a cudaDeviceReset() of
+ * it (the kept address is then stale).  All calls share the one array: calls
  * whose work overlaps on the GPU (different streams, or another thread) race
  * and corrupt each other's results, so serialise them.  Nothing carried over
  * from an earlier call is read.  The call itself allocates nothing.

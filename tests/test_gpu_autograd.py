@@ -43,12 +43,12 @@ def test_autograd_matches_oracle(gdr, spec, use_final):
     gdr.check_status()
     tol = TOL[spec.in_dtype]
     ref = oracle_fwd(x)
-    assert err(o.detach(), ref["o"]) <= tol
-    assert err(fs.detach(), ref["final_state"]) <= tol
+    assert err(o.detach(), ref["o"], "o") <= tol
+    assert err(fs.detach(), ref["final_state"], "final_state") <= tol
     y = dict(x)
     y["dht"] = x["dht"] if use_final else None
     rg = oracle_bwd(y)
     got = {"dq": leaves["q"].grad, "dk": leaves["k"].grad, "dv": leaves["v"].grad, "dbeta": leaves["beta"].grad,
            "dg": leaves["g"].grad, "dh0": leaves["h0"].grad}
-    e = {key: err(got[key], rg[key]) for key in got}
+    e = {key: err(got[key], rg[key], key) for key in got}
     assert all(v <= tol for v in e.values()), e

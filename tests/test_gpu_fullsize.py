@@ -2,7 +2,8 @@
 benchmark times (automatic path and context-parallel plan).  The oracle checks
 whole qk-head groups (every output of the selected heads over the whole
 sequence) where a full check would take too long on the host: one group with a
-unit-gate head and one gated group per workload."""
+unit-gate head and one group whose heads all decay, per workload, forward and
+backward."""
 import numpy as np
 import pytest
 import torch
@@ -54,9 +55,9 @@ def _fwd_case(gdr, name, full_oracle=False):
         ref = oracle.fwd(y["q"], y["k"], y["v"], y["g"], y["beta"], x["scale"], h0=y["h0"],
                          cu_seqlens=x["cu_seqlens"], vblock=16)
         A_ref = oracle.A_matrix(y["k"], y["g"], y["beta"], cu_seqlens=x["cu_seqlens"])
-        e = {"o": err(out["o"][:, :, hv], ref["o"]),
-             "final_state": err(out["final_state"][:, hv], ref["final_state"]),
-             "A": err(out["A"][:, :, hv], A_ref)}
+        e = {"o": err(out["o"][:, :, hv], ref["o"], f"o hq{hq}"),
+             "final_state": err(out["final_state"][:, hv], ref["final_state"], f"final_state hq{hq}"),
+             "A": err(out["A"][:, :, hv], A_ref, f"A hq{hq}")}
         assert all(v <= tol for v in e.values()), (name, hq, e)
 
 
@@ -83,11 +84,13 @@ def test_bwd_workload(gdr):
     torch.cuda.synchronize()
     gdr.check_status()
     tol = TOL[spec.in_dtype]
-    for hq in _groups(x)[:1]:
+    groups = _groups(x)
+    assert len(groups) == 2  # one group holding a g == 0 head, one whose heads all decay
+    for hq in groups:
         y, hv = select_heads(x, hq)
         ref = oracle.bwd(y["q"], y["k"], y["v"], y["g"], y["beta"], x["scale"], y["do"], dht=y["dht"],
                          h0=y["h0"])
-        e = {"dq": err(gr["dq"][:, :, hq:hq + 1], ref["dq"]), "dk": err(gr["dk"][:, :, hq:hq + 1], ref["dk"]),
-             "dv": err(gr["dv"][:, :, hv], ref["dv"]), "dbeta": err(gr["dbeta"][:, :, hv], ref["dbeta"]),
-             "dg": err(gr["dg"][:, :, hv], ref["dg"]), "dh0": err(gr["dh0"][:, hv], ref["dh0"])}
+        e = {key: err(gr[key][:, :, hq:hq + 1], ref[key], f"{key} hq{hq}") for key in ("dq", "dk")}
+        e.update({key: err(gr[key][:, :, hv], ref[key], f"{key} hq{hq}") for key in ("dv", "dbeta", "dg")})
+        e["dh0"] = err(gr["dh0"][:, hv], ref["dh0"], f"dh0 hq{hq}")
         assert all(v <= tol for v in e.values()), (name, hq, e)

@@ -42,10 +42,10 @@ def _check_fwd(gdr, spec, path, cp=0, want_h=True, seed=0):
     gdr.check_status()
     ref = oracle_fwd(x, want_h=want_h)
     tol = TOL[spec.in_dtype]
-    e = {"o": err(out["o"], ref["o"]), "final_state": err(out["final_state"], ref["final_state"]),
-         "A": err(out["A"], oracle_A(x))}
+    e = {"o": err(out["o"], ref["o"], "o"), "final_state": err(out["final_state"], ref["final_state"], "final_state"),
+         "A": err(out["A"], oracle_A(x), "A")}
     if want_h:
-        e["h"] = err(out["h"], ref["h"].reshape(out["h"].shape))
+        e["h"] = err(out["h"], ref["h"].reshape(out["h"].shape), "h")
     assert all(v <= tol for v in e.values()), e
     return out
 
@@ -59,7 +59,7 @@ def _check_bwd(gdr, spec, path, cp=0, seed=0):
     gdr.check_status()
     ref = oracle_bwd(x)
     tol = TOL[spec.in_dtype]
-    e = {key: err(gr[key], ref[key]) for key in ("dq", "dk", "dv", "dbeta", "dg", "dh0")}
+    e = {key: err(gr[key], ref[key], key) for key in ("dq", "dk", "dv", "dbeta", "dg", "dh0")}
     assert all(v <= tol for v in e.values()), e
 
 
@@ -103,7 +103,7 @@ def test_fwd_context_parallel_segmentations(gdr, path):
     outs = [_check_fwd(gdr, spec, p, cp=cp, want_h=True) for cp in (1, 2, 3, 5, 11)]
     # each segmentation is exact up to rounding: all agree with each other
     for o in outs[1:]:
-        assert err(o["o"], outs[0]["o"].double().cpu().numpy()) <= 2e-2
+        assert err(o["o"], outs[0]["o"].double().cpu().numpy(), "o vs cp=1") <= 2e-2
     # and a repeated run is bit-identical
     again = _check_fwd(gdr, spec, p, cp=3, want_h=True)
     assert torch.equal(again["o"], outs[2]["o"]) and torch.equal(again["final_state"], outs[2]["final_state"])
@@ -128,9 +128,9 @@ def test_fwd_beta_zero_is_pure_decay(gdr, path):
     G = x["g"].double().cumsum(dim=1)
     q = x["q"].double().repeat_interleave(2, dim=2)
     o_ref = x["scale"] * torch.exp(G)[..., None] * torch.einsum("bthk,bhkv->bthv", q, x["h0"].double())
-    assert err(out["o"], o_ref.numpy()) <= TOL["bf16"]
+    assert err(out["o"], o_ref.numpy(), "o") <= TOL["bf16"]
     fs_ref = torch.exp(G[:, -1])[:, :, None, None] * x["h0"].double()
-    assert err(out["final_state"], fs_ref.numpy()) <= 1e-5
+    assert err(out["final_state"], fs_ref.numpy(), "final_state") <= 1e-5
 
 
 @pytest.mark.parametrize("path", PATHS)

@@ -38,8 +38,8 @@ def test_warmup_starts(gdr, lengths):
     ref = oracle_fwd(x)
     tol = TOL[spec.in_dtype]
     for out in (warm, exact):
-        assert err(out["o"], ref["o"]) <= tol
-        assert err(out["final_state"], ref["final_state"]) <= tol
+        assert err(out["o"], ref["o"], "o") <= tol
+        assert err(out["final_state"], ref["final_state"], "final_state") <= tol
     zero = x["zero_heads"]
     decaying = [h for h in range(spec.Hv) if h not in zero]
     assert zero and decaying
@@ -56,7 +56,7 @@ def test_warmup_starts(gdr, lengths):
     torch.cuda.synchronize()
     gdr.check_status()
     rg = oracle_bwd(x)
-    e = {key: err(gr[key], rg[key]) for key in ("dq", "dk", "dv", "dbeta", "dg", "dh0")}
+    e = {key: err(gr[key], rg[key], key) for key in ("dq", "dk", "dv", "dbeta", "dg", "dh0")}
     assert all(v <= tol for v in e.values()), e
 
 
@@ -83,8 +83,8 @@ def test_warmup_start_is_taken(gdr):
     gdr.check_status()
     ref = oracle_fwd(x, want_h=True)
     for out in (warm, exact):
-        assert err(out["o"], ref["o"]) <= TOL["bf16"]
-        assert err(out["h"], ref["h"].reshape(out["h"].shape)) <= TOL["bf16"]
+        assert err(out["o"], ref["o"], "o") <= TOL["bf16"]
+        assert err(out["h"], ref["h"].reshape(out["h"].shape), "h") <= TOL["bf16"]
     hw, he = warm["h"][10], exact["h"][10]  # before chunk 10, the first of segment 1
     assert torch.count_nonzero(hw[0, 1:]) == 0          # head 0 started from zero 8 chunks back
     assert torch.count_nonzero(he[0, 1:]) > 0           # the exact start carries the decayed h0

@@ -78,3 +78,80 @@ def write_report(path):
         lines.append(f"| {t} | {k} | {dt} | {c} | {me:.2e} | {mr:.2e} |")
     with open(path, "w") as f:
         f.write("\n".join(lines) + "\n")
+
+
+def to_dev(x, dev="cuda"):
+    return {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in x.items()}
+
+
+def _nans(shape, dtype, like):
+    return torch.full(shape, float("nan"), dtype=dtype, device=like.device)
+
+
+def _n_seqs(d):
+    return d["cu_seqlens"].numel() - 1 if d["cu_seqlens"] is not None else d["v"].shape[0]
+
+
+def gpu_fwd(gdr, d, **kw):
+    """The forward into NaN-filled outputs, so that an element the kernels never
+    write shows up as a parity failure."""
+    if "out" not in kw:
+        B, T, Hv, V = d["v"].shape
+        K = d["q"].shape[-1]
+        kw["out"] = {"o": _nans((B, T, Hv, V), kw.get("o_dtype") or d["q"].dtype, d["v"]),
+                     "final_state": _nans((_n_seqs(d), Hv, K, V), torch.float32, d["v"]),
+                     "A": _nans((B, T, Hv, 64), torch.float32, d["v"])}
+        if kw.get("want_h"):
+            if d["cu_seqlens"] is not None:
+                lens = (d["cu_seqlens"][1:] - d["cu_seqlens"][:-1]).cpu()
+                nt = int(((lens + 63) // 64).sum())
+            else:
+                nt = B * ((T + 63) // 64)
+            kw["out"]["h"] = _nans((nt, Hv, K, V), torch.float32, d["v"])
+    return gdr.gdr_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["scale"], h0=d["h0"],
+                       cu_seqlens=d["cu_seqlens"], **kw)
+
+
+def gpu_bwd(gdr, d, A, **kw):
+    """The backward into NaN-filled outputs (see gpu_fwd)."""
+    if "out" not in kw:
+        Hv, V = d["v"].shape[2:]
+        K = d["q"].shape[-1]
+        kw["out"] = {"dq": torch.full_like(d["q"], float("nan")), "dk": torch.full_like(d["k"], float("nan")),
+                     "dv": torch.full_like(d["v"], float("nan")),
+                     "dbeta": _nans(d["g"].shape, torch.float32, d["g"]),
+                     "dg": _nans(d["g"].shape, torch.float32, d["g"]),
+                     "dh0": _nans((_n_seqs(d), Hv, K, V), torch.float32, d["g"])}
+    return gdr.gdr_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], A, d["do"], dht=d.get("dht"),
+                       scale=d["scale"], h0=d["h0"], cu_seqlens=d["cu_seqlens"], **kw)
+
+
+def oracle_fwd(x, want_h=False):
+    return oracle.fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], h0=x["h0"],
+                      cu_seqlens=x["cu_seqlens"], want_h=want_h)
+
+
+def oracle_bwd(x):
+    return oracle.bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], x["do"], dht=x.get("dht"),
+                      h0=x["h0"], cu_seqlens=x["cu_seqlens"])
+
+
+def oracle_A(x):
+    return oracle.A_matrix(x["k"], x["g"], x["beta"], cu_seqlens=x["cu_seqlens"])
+
+
+def select_heads(x, hq):
+    """Inputs restricted to qk-head hq and the v-heads of its group."""
+    spec = x["spec"]
+    G = spec.Hv // spec.Hq
+    hv = slice(hq * G, (hq + 1) * G)
+    y = dict(x)
+    y["q"] = x["q"][:, :, hq:hq + 1].contiguous()
+    y["k"] = x["k"][:, :, hq:hq + 1].contiguous()
+    for key in ("v", "g", "beta", "do"):
+        if key in x and x[key] is not None:
+            y[key] = x[key][:, :, hv].contiguous()
+    for key in ("h0", "dht"):
+        if key in x and x[key] is not None:
+            y[key] = x[key][:, hv].contiguous()
+    return y, hv

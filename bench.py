@@ -460,6 +460,8 @@ def main():
                     help="tokens of the all-cores cpu_baseline sample (0: the whole first sequence)")
     ap.add_argument("--cpu-tokens-1core", type=int, default=1024,
                     help="tokens of the one-core cpu_baseline sample (over 8 v-heads at most)")
+    ap.add_argument("--T", type=int, default=0,
+                    help="shorter sequences of the same fixed-length workload (profiling captures)")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -470,6 +472,10 @@ def main():
     base = inputs.resolve(args.workload)
     from dataclasses import replace
     spec = replace(base, bwd=True)
+    if args.T:
+        if spec.lengths is not None:
+            raise SystemExit("--T applies to fixed-length workloads")
+        spec = replace(spec, T=args.T, name=f"{spec.name}@T{args.T}")
 
     if args.impl == "reference":
         run_reference(args, spec, rank, world)

@@ -182,6 +182,43 @@ __device__ __forceinline__ void mma_seq(uint32_t d, uint64_t a, uint32_t da, uin
         b += db >> 4;
     }
 }
+// Warp-wide forms, for code that a whole warp runs: every lane computes the
+// (warp-uniform) descriptors and one elected lane issues the instruction.  A
+// single thread issuing inside a divergent branch took 60-90 cycles per MMA.
+__device__ __forceinline__ void mma_w(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+__device__ __forceinline__ void mma_ts_w(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+        "r"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+__device__ __forceinline__ void mma_seq_w(uint32_t d, uint64_t a, uint32_t da, uint64_t b, uint32_t db, uint32_t idesc,
+                                          int n, bool acc) {
+#pragma unroll 1
+    for (int i = 0; i < n; ++i) {
+        mma_w(d, a, b, idesc, (acc || i > 0) ? 1u : 0u);
+        a += da >> 4;
+        b += db >> 4;
+    }
+}
+__device__ __forceinline__ void mma_commit_w(uint64_t *bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(su32(bar))
+        : "memory");
+}
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(bar))
                  : "memory");
@@ -847,16 +884,17 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
                 drain_wait(&full[cc & 1], (cc >> 1) & 1);
         }
     } else if (warp == kEpiWarps + 1) {
-        // ---------------- MMA issuer: A operands from tensor memory ----------------
-        if (lane == 0) {
+        // ---------------- MMA issuer: A operands from tensor memory; the whole
+        // warp runs the loop (uniform descriptors), one elected lane issues ----------------
+        {
             const uint32_t id1 = idesc_bf16(128, MODE == kFwd ? 128 : 64);
             const uint32_t id64 = idesc_bf16(128, 64);
             const uint32_t id3 = idesc_bf16(128, 128, 0, 1);
             for (int cc = 0; cc < ntot; ++cc) {
                 const int s = cc & 1;
                 char *st = stage0 + s * SL::kBytes;
-                if (!bwait(&full[s], (cc >> 1) & 1, cap, abort)) break;
-                if (!bwait(bar_sb, cc & 1, cap, abort)) break;
+                if (!wbwait(&full[s], (cc >> 1) & 1, cap, abort)) break;
+                if (!wbwait(bar_sb, cc & 1, cap, abort)) break;
                 tc_fence_after();
                 const uint32_t b1 = su32(st + SL::kB1);
                 // MMA1: D1 = S^T [K ; Q]^T over k, 16 k per step (8 packed columns)
@@ -865,46 +903,46 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         const uint32_t ko = (kk & 3) * 32;
-                        mma_ts(tD1, (half ? tSl : tSh) + 8 * kk, sdesc(b1 + (kk >> 2) * SL::kAtom + ko), id1,
+                        mma_ts_w(tD1, (half ? tSl : tSh) + 8 * kk, sdesc(b1 + (kk >> 2) * SL::kAtom + ko), id1,
                                (half | kk) != 0);
                     }
                 }
-                mma_commit(bar_m1);
-                if (!bwait(bar_rt, cc & 1, cap, abort)) break;
+                mma_commit_w(bar_m1);
+                if (!wbwait(bar_rt, cc & 1, cap, abort)) break;
                 tc_fence_after();
                 {
                     const uint32_t ah = su32(st + SL::kA), al = ah + kImg;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint32_t o = kk * 32;
-                        mma_ts(tD1b, tRh + 8 * kk, sdesc(ah + o), id64, kk > 0);
-                        mma_ts(tD1b, tRl + 8 * kk, sdesc(ah + o), id64, 1);
-                        mma_ts(tD1b, tRh + 8 * kk, sdesc(al + o), id64, 1);
+                        mma_ts_w(tD1b, tRh + 8 * kk, sdesc(ah + o), id64, kk > 0);
+                        mma_ts_w(tD1b, tRl + 8 * kk, sdesc(ah + o), id64, 1);
+                        mma_ts_w(tD1b, tRh + 8 * kk, sdesc(al + o), id64, 1);
                     }
                 }
-                mma_commit(bar_m1b);
-                if (!bwait(bar_ut, cc & 1, cap, abort)) break;
+                mma_commit_w(bar_m1b);
+                if (!wbwait(bar_ut, cc & 1, cap, abort)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
-                    mma_ts(tS, tYh + 8 * kk, sdesc(b1 + kk * 2048, SL::kAtom), id3, 1);
-                    mma_ts(tS, tYl + 8 * kk, sdesc(b1 + kk * 2048, SL::kAtom), id3, 1);
+                    mma_ts_w(tS, tYh + 8 * kk, sdesc(b1 + kk * 2048, SL::kAtom), id3, 1);
+                    mma_ts_w(tS, tYl + 8 * kk, sdesc(b1 + kk * 2048, SL::kAtom), id3, 1);
                 }
-                mma_commit(bar_m3);
+                mma_commit_w(bar_m3);
                 if (MODE == kFwd) {  // in issue order before MMA1 of the next chunk overwrites Ut^T
                     const uint32_t ph = su32(st + SL::kP), pl = ph + kImg;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint32_t o = kk * 32;
-                        mma_ts(tD2, tUh + 8 * kk, sdesc(ph + o), id64, kk > 0);
-                        mma_ts(tD2, tUl + 8 * kk, sdesc(ph + o), id64, 1);
-                        mma_ts(tD2, tUh + 8 * kk, sdesc(pl + o), id64, 1);
+                        mma_ts_w(tD2, tUh + 8 * kk, sdesc(ph + o), id64, kk > 0);
+                        mma_ts_w(tD2, tUl + 8 * kk, sdesc(ph + o), id64, 1);
+                        mma_ts_w(tD2, tUh + 8 * kk, sdesc(pl + o), id64, 1);
                     }
-                    mma_commit(bar_m2);
+                    mma_commit_w(bar_m2);
                 }
-                mma_commit(&empty[s]);
+                mma_commit_w(&empty[s]);
             }
-            mma_commit(bar_drain);
+            mma_commit_w(bar_drain);
             drain_wait(bar_drain, 0);
         }
     } else if (MODE == kFwd && warp >= kEpiWarps / 2) {
@@ -1323,7 +1361,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_dh_tc(Params p, const __gri
                 drain_wait(&full[cc & 1], (cc >> 1) & 1);
         }
     } else if (warp == kEpiWarps + 1) {
-        if (lane == 0) {
+        {  // the whole warp runs the loop (uniform descriptors), one elected lane issues
             const uint32_t idK = idesc_bf16(128, 64);           // dS1^T K^T
             const uint32_t idOP = idesc_bf16(128, 64, 1, 1);    // dO^T P
             const uint32_t idA = idesc_bf16(128, 64, 0, 1);     // dUt^T A
@@ -1331,53 +1369,53 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_dh_tc(Params p, const __gri
             for (int cc = 0; cc < nch; ++cc) {
                 const int s = cc & 1;
                 char *st = stage0 + s * SL::kBytes;
-                if (!bwait(&full[s], (cc >> 1) & 1, cap, abort)) break;
+                if (!wbwait(&full[s], (cc >> 1) & 1, cap, abort)) break;
                 const uint32_t qk = su32(st + SL::kQK), kr = qk + 8192;
                 if (!isN) {
                     // the dO term needs no state: issued as soon as the stage lands
                     const uint32_t dO = su32(st + SL::kdO), ph = su32(st + SL::kP), pl = ph + kImg;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        mma(tD1, sdesc(dO + kk * 2048, 8192), sdesc(ph + kk * 2048, 8192), idOP, kk > 0);
-                        mma(tD1, sdesc(dO + kk * 2048, 8192), sdesc(pl + kk * 2048, 8192), idOP, 1);
+                        mma_w(tD1, sdesc(dO + kk * 2048, 8192), sdesc(ph + kk * 2048, 8192), idOP, kk > 0);
+                        mma_w(tD1, sdesc(dO + kk * 2048, 8192), sdesc(pl + kk * 2048, 8192), idOP, 1);
                     }
                 }
-                if (!bwait(bar_sb, cc & 1, cap, abort)) break;
+                if (!wbwait(bar_sb, cc & 1, cap, abort)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         const uint32_t o = (kk >> 2) * 16384 + (kk & 3) * 32;
-                        mma_ts(tD2, (half ? tSl : tSh) + 8 * kk, sdesc(kr + o), idK, (half | kk) != 0);
+                        mma_ts_w(tD2, (half ? tSl : tSh) + 8 * kk, sdesc(kr + o), idK, (half | kk) != 0);
                     }
                 }
-                mma_commit(bar_m1);
-                if (!bwait(bar_ut, cc & 1, cap, abort)) break;
+                mma_commit_w(bar_m1);
+                if (!wbwait(bar_ut, cc & 1, cap, abort)) break;
                 tc_fence_after();
                 {
                     const uint32_t ah = su32(st + SL::kA), al = ah + kImg;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint32_t ob = kk * 2048;
-                        mma_ts(tD2, tUh + 8 * kk, sdesc(ah + ob, 8192), idA, kk > 0);
-                        mma_ts(tD2, tUl + 8 * kk, sdesc(ah + ob, 8192), idA, 1);
-                        mma_ts(tD2, tUh + 8 * kk, sdesc(al + ob, 8192), idA, 1);
+                        mma_ts_w(tD2, tUh + 8 * kk, sdesc(ah + ob, 8192), idA, kk > 0);
+                        mma_ts_w(tD2, tUl + 8 * kk, sdesc(ah + ob, 8192), idA, 1);
+                        mma_ts_w(tD2, tUh + 8 * kk, sdesc(al + ob, 8192), idA, 1);
                     }
                 }
-                mma_commit(bar_m2);
-                if (!bwait(bar_x, cc & 1, cap, abort)) break;
+                mma_commit_w(bar_m2);
+                if (!wbwait(bar_x, cc & 1, cap, abort)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
-                        mma_ts(tS, (half ? tXl : tXh) + 8 * kk, sdesc(qk + kk * 2048, 16384), idQK, 1);
+                        mma_ts_w(tS, (half ? tXl : tXh) + 8 * kk, sdesc(qk + kk * 2048, 16384), idQK, 1);
                 }
-                mma_commit(bar_m3);
-                mma_commit(&empty[s]);
+                mma_commit_w(bar_m3);
+                mma_commit_w(&empty[s]);
             }
-            mma_commit(bar_drain);
+            mma_commit_w(bar_drain);
             drain_wait(bar_drain, 0);
         }
     } else {
@@ -1732,8 +1770,8 @@ __global__ void __launch_bounds__(512) k_combine_tc(Params p) {
 
 // ---------------------------------------------------------------------------
 // Chunk-local gradients of the backward on tcgen05 (K = V = 128).  One CTA of
-// 512 threads per (chunk, v-head); thread 0 issues every MMA, all sixteen
-// warps run the epilogues (warp w reads TMEM lanes 32 (w % 4) .. + 31 and
+// 512 threads per (chunk, v-head); warp 0 issues every MMA (one elected lane),
+// all sixteen warps run the epilogues (warp w reads TMEM lanes 32 (w % 4) .. + 31 and
 // columns [16 (w / 4), + 16)).  The same reverse mode as the warp-MMA kernel, with
 // every product laid out so that its M side is 128 (a value, key or stacked
 // token index in the TMEM lanes):
@@ -2001,29 +2039,29 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
     __syncthreads();
 
     // ---------------- group 1 ----------------
-    if (tid == 0) {
+    if (warp == 0) {  // the whole warp: uniform descriptors, one elected lane issues
         {
             tc_fence_after();
             // KS^T = S0^T K^T: A = S0 image MN-major (M = v in two 64-blocks 16 KiB apart), B = K rows
             for (int tm = 0; tm < 2; ++tm)
                 for (int at = 0; at < 2; ++at)
-                    mma_seq(tmem + kTbKS, sdesc(sS + tm * 32768 + at * 8192, 16384), 2048,
+                    mma_seq_w(tmem + kTbKS, sdesc(sS + tm * 32768 + at * 8192, 16384), 2048,
                             sdesc(sKQ + at * 16384 + 8192), 32, idesc_bf16(128, 64, 1, 0), 4, (tm | at) != 0);
             // dQr^T = S0 dO^T: A = S0 image K-major (M = k), B = dO rows
             for (int tm = 0; tm < 2; ++tm)
                 for (int at = 0; at < 2; ++at)
-                    mma_seq(tmem + kTbDQ, sdesc(sS + tm * 32768 + at * 16384), 32, sdesc(sOR + at * 16384), 32,
+                    mma_seq_w(tmem + kTbDQ, sdesc(sS + tm * 32768 + at * 16384), 32, sdesc(sOR + at * 16384), 32,
                             idesc_bf16(128, 64, 0, 0), 4, (tm | at) != 0);
             {  // dR^T = dUt^T A: A operand dUt^T from TMEM, B = A image MN-major (K = s rows)
                 const uint32_t id = idesc_bf16(128, 64, 0, 1);
-#pragma unroll 1
+#pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
-                    mma_ts(tmem + kTbDR, tmem + kTbU + 8 * kk, sdesc(sA + kk * 2048), id, kk > 0);
-                    mma_ts(tmem + kTbDR, tmem + kTbU + 32 + 8 * kk, sdesc(sA + kk * 2048), id, 1);
-                    mma_ts(tmem + kTbDR, tmem + kTbU + 8 * kk, sdesc(sA + 8192 + kk * 2048), id, 1);
+                    mma_ts_w(tmem + kTbDR, tmem + kTbU + 8 * kk, sdesc(sA + kk * 2048), id, kk > 0);
+                    mma_ts_w(tmem + kTbDR, tmem + kTbU + 32 + 8 * kk, sdesc(sA + kk * 2048), id, 1);
+                    mma_ts_w(tmem + kTbDR, tmem + kTbU + 8 * kk, sdesc(sA + 8192 + kk * 2048), id, 1);
                 }
             }
-            mma_commit(&bars[1]);
+            mma_commit_w(&bars[1]);
             ++ncommit;
         }
     }
@@ -2086,23 +2124,23 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
     tc_fence_before();
     __syncthreads();
     // ---------------- group 2 ----------------
-    if (tid == 0) {
+    if (warp == 0) {  // the whole warp: uniform descriptors, one elected lane issues
         tc_fence_after();
         {  // Ut^T = R^T A^T: A operand R^T from TMEM, B = A image K-major (rows t)
             const uint32_t id = idesc_bf16(128, 64, 0, 0);
-#pragma unroll 1
+#pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-                mma_ts(tmem + kTbKS, tmem + kTbR + 8 * kk, sdesc(sA + kk * 32), id, kk > 0);
-                mma_ts(tmem + kTbKS, tmem + kTbR + 32 + 8 * kk, sdesc(sA + kk * 32), id, 1);
-                mma_ts(tmem + kTbKS, tmem + kTbR + 8 * kk, sdesc(sA + 8192 + kk * 32), id, 1);
+                mma_ts_w(tmem + kTbKS, tmem + kTbR + 8 * kk, sdesc(sA + kk * 32), id, kk > 0);
+                mma_ts_w(tmem + kTbKS, tmem + kTbR + 32 + 8 * kk, sdesc(sA + kk * 32), id, 1);
+                mma_ts_w(tmem + kTbKS, tmem + kTbR + 8 * kk, sdesc(sA + 8192 + kk * 32), id, 1);
             }
         }
         // dK^T = S0 dKS^T: B = dKS^T image MN-major (K = v rows); terms (hi, hi), (lo, hi), (hi, lo)
         for (int m = 0; m < 3; ++m)
             for (int at = 0; at < 2; ++at)
-                mma_seq(tmem + kTbDK, sdesc(sS + (m == 1) * 32768 + at * 16384), 32,
+                mma_seq_w(tmem + kTbDK, sdesc(sS + (m == 1) * 32768 + at * 16384), 32,
                         sdesc(sW + (m == 2) * 16384 + at * 8192), 2048, idesc_bf16(128, 64, 0, 1), 4, (m | at) != 0);
-        mma_commit(&bars[1]);
+        mma_commit_w(&bars[1]);
         ++ncommit;
     }
     // while group 2 runs: row sums dQr.Q (dQr^T stays in TMEM until the end)
@@ -2191,26 +2229,26 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
     tc_fence_before();
     __syncthreads();
     // ---------------- group 3 ----------------
-    if (tid == 0) {
+    if (warp == 0) {  // the whole warp: uniform descriptors, one elected lane issues
         tc_fence_after();
         const uint32_t id = idesc_bf16(128, 64, 0, 1);
         // [dO ; dR_hi] (Ut_hi + Ut_lo)^T, and [. ; dR_lo] Ut_hi^T: B = Ut^T image MN-major
         for (int tb = 0; tb < 2; ++tb)
             for (int at = 0; at < 2; ++at)
-                mma_seq(tmem + kTbP1, sdesc(sOR + at * 16384), 32, sdesc(sW + tb * 16384 + at * 8192), 2048, id, 4,
+                mma_seq_w(tmem + kTbP1, sdesc(sOR + at * 16384), 32, sdesc(sW + tb * 16384 + at * 8192), 2048, id, 4,
                         (tb | at) != 0);
         for (int at = 0; at < 2; ++at)
-            mma_seq(tmem + kTbP1B, sdesc(sRL - 8192 + at * 8192), 32, sdesc(sW + at * 8192), 2048, id, 4, at != 0);
+            mma_seq_w(tmem + kTbP1B, sdesc(sRL - 8192 + at * 8192), 32, sdesc(sW + at * 8192), 2048, id, 4, at != 0);
         // dK2^T = dS1 Ut^T (over the R^T operand, read by group 2)
         for (int m = 0; m < 3; ++m)
             for (int at = 0; at < 2; ++at)
-                mma_seq(tmem + kTbR, sdesc(sS + (m == 1) * 32768 + at * 16384), 32,
+                mma_seq_w(tmem + kTbR, sdesc(sS + (m == 1) * 32768 + at * 16384), 32,
                         sdesc(sW + (m == 2) * 16384 + at * 8192), 2048, id, 4, (m | at) != 0);
         // [Q ; K] K^T
         for (int at = 0; at < 2; ++at)
-            mma_seq(tmem + kTbDR, sdesc(sKQ + at * 16384), 32, sdesc(sKQ + at * 16384 + 8192), 32,
+            mma_seq_w(tmem + kTbDR, sdesc(sKQ + at * 16384), 32, sdesc(sKQ + at * 16384 + 8192), 32,
                     idesc_bf16(128, 64, 0, 0), 4, at != 0);
-        mma_commit(&bars[1]);
+        mma_commit_w(&bars[1]);
         ++ncommit;
     }
     {
@@ -2290,20 +2328,20 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
     tc_fence_before();
     __syncthreads();
     // ---------------- group 4 ----------------
-    if (tid == 0) {
+    if (warp == 0) {  // the whole warp: uniform descriptors, one elected lane issues
         tc_fence_after();
         // A = K^T or Q^T: the K (Q) rows read MN-major (M = k in two 64-blocks 16 KiB apart)
         const uint64_t aK = sdesc(sKQ + 8192, 16384), aQ = sdesc(sKQ, 16384);
         const uint32_t idK = idesc_bf16(128, 64, 1, 0), idM = idesc_bf16(128, 64, 1, 1);
         for (int tb = 0; tb < 2; ++tb) {
             // dq2^T = K^T dP''^T (B = dP'' rows t, K-major)
-            mma_seq(tmem + kTbKS, aK, 2048, sdesc(sW + tb * 8192), 32, idK, 4, tb != 0);
+            mma_seq_w(tmem + kTbKS, aK, 2048, sdesc(sW + tb * 8192), 32, idK, 4, tb != 0);
             // dK^T += Q^T dP'' (B MN-major), K^T MM^T (B K-major), K^T MM (B MN-major)
-            mma_seq(tmem + kTbDK, aQ, 2048, sdesc(sW + tb * 8192), 2048, idM, 4, true);
-            mma_seq(tmem + kTbDK, aK, 2048, sdesc(sW + 16384 + tb * 8192), 32, idK, 4, true);
-            mma_seq(tmem + kTbDK, aK, 2048, sdesc(sW + 16384 + tb * 8192), 2048, idM, 4, true);
+            mma_seq_w(tmem + kTbDK, aQ, 2048, sdesc(sW + tb * 8192), 2048, idM, 4, true);
+            mma_seq_w(tmem + kTbDK, aK, 2048, sdesc(sW + 16384 + tb * 8192), 32, idK, 4, true);
+            mma_seq_w(tmem + kTbDK, aK, 2048, sdesc(sW + 16384 + tb * 8192), 2048, idM, 4, true);
         }
-        mma_commit(&bars[1]);
+        mma_commit_w(&bars[1]);
         ++ncommit;
     }
     ok = bwait(&bars[1], 1, cap, abort);

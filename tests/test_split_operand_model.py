@@ -4,11 +4,11 @@ A numpy model of the chunk algebra the tensor-core kernels evaluate (not their
 code): per 64-token chunk, with gamma the chunk-local cumulative log-gate,
     R  = diag(b) (V - diag(e^gamma) K S0),     Ut = A R,
     Y  = diag(e^{gamma_n - gamma}) Ut,
-    O  = scale diag(e^gamma) Q S0 + P' Y,      P' = scale diag(e^{gamma - gamma_n}) (Q K^T o tril_incl),
+    O  = scale diag(e^gamma) Q S0 + P Ut,      P = scale (Q K^T o D o tril_incl),
     S1 = e^{gamma_n} S0 + K^T Y,
 with the products taken as the MMAs take them: bf16 operands, fp32
 accumulation.  q, k, v enter as the bf16 values they are.  The computed
-operands (S0, R, A, Y, P') are either rounded to bf16 once, or split as
+operands (S0, R, A, Ut, Y, P) are either rounded to bf16 once, or split as
 x = hi + lo (hi = bf16(x), lo = bf16(x - hi)) with three products
 hi*hi + lo*hi + hi*lo.  Both are compared with the same algebra in fp64.
 
@@ -65,19 +65,19 @@ def run(n_chunks, split, seed=0, K=64, V=64, C=64):
         D = np.exp(gam[:, None] - gam[None, :])
         L = np.tril(bc[:, None] * (Kc @ Kc.T) * D, -1)
         A = np.linalg.inv(np.eye(C) + L)
-        Pp = scale * np.exp(gam - gam[-1])[:, None] * np.tril(Q @ Kc.T)
+        P = scale * D * np.tril(Q @ Kc.T)
         eg, en = np.exp(gam), np.exp(gam[-1])
         # fp64 reference of the same algebra
         R = bc[:, None] * (Vc - eg[:, None] * (Kc @ S64))
         Y = np.exp(gam[-1] - gam)[:, None] * (A @ R)
-        O64 = scale * eg[:, None] * (Q @ S64) + Pp @ Y
+        O64 = scale * eg[:, None] * (Q @ S64) + P @ (A @ R)
         S64 = en * S64 + Kc.T @ Y
-        # the model: S0, R, A, Y, P' computed; q, k, v exact bf16
+        # the model: S0, R, A, Ut, Y, P computed; q, k, v exact bf16
         KS = mm(Kc, S32, split)
         R32 = (bc[:, None] * (Vc - eg[:, None] * KS)).astype(np.float32)
         Ut = mm(A.astype(np.float32), R32, split)
         Y32 = (np.exp(gam[-1] - gam)[:, None] * Ut).astype(np.float32)
-        O32 = scale * eg[:, None] * mm(Q, S32, split) + mm(Pp.astype(np.float32), Y32, split)
+        O32 = scale * eg[:, None] * mm(Q, S32, split) + mm(P.astype(np.float32), Ut, split)
         S32 = (en * S32 + mm(Kc.T, Y32, split)).astype(np.float32)
         worst_o = max(worst_o, float(np.max(np.abs(O32 - O64)) / np.sqrt(np.mean(O64 ** 2))))
     err_s = float(np.max(np.abs(S32 - S64)) / np.sqrt(np.mean(S64 ** 2)))

@@ -539,7 +539,8 @@ __global__ void __launch_bounds__(128, 5) k_chunk_tc(Params p, const __grid_cons
             mma_issued = true;
         }
     }
-    const bool ok = bwait(&bars[1], 0, cap, abort);
+    // one decision for the whole CTA: the inverse below synchronises the CTA
+    const bool ok = !__syncthreads_or(!bwait(&bars[1], 0, cap, abort));
     tc_fence_after();
     // rows of [K K^T ; Q K^T]: warps 0-1 -> L (unless from_A), warps 2-3 -> P
     if (ok) {
@@ -785,7 +786,6 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
     uint64_t *bar_ofull = bars + 11;  // output tile staged (kFwd)
     uint64_t *bar_ofree = bars + 12;  // output tile read by its TMA store (kFwd)
     uint64_t *bar_m2 = bars + 13;     // MMA2 done (kFwd)
-    uint64_t *bar_yr = bars + 14;     // every state warp has read its Ut^T columns
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 15);
     volatile int *abort = reinterpret_cast<volatile int *>(bars + 16);
 
@@ -823,7 +823,6 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
         mbar_init(bar_ofull, kEpiWarps / 2);
         mbar_init(bar_ofree, 1);
         mbar_init(bar_m2, 1);
-        mbar_init(bar_yr, MODE == kFwd ? kEpiWarps / 2 : kEpiWarps);
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -842,16 +841,16 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
     //   [256,320) Ut^T                          (MMA1b)
     //   [320,384) (P Ut)^T                      (MMA2)
     //   [384,512) A operands as packed bf16 pairs: S^T hi | lo (64 + 64
-    //             columns) for MMA1, then R^T hi | lo at [384,448) for MMA1b
-    //   [256,320) Y^T hi | lo, in place of Ut^T once (c2) has read it, for
-    //             MMA3
+    //             columns) for MMA1, then R^T hi | lo at [384,448) for MMA1b,
+    //             then Y^T hi | lo at [384,448) for MMA3 (R^T is dead once
+    //             MMA1b has completed, and the next chunk's (a) waits for MMA3)
     //   [128,192) Ut^T hi | lo (kFwd), over (K S)^T once (c) has read it, for
     //             MMA2: the next chunk's (a) touches neither, so MMA2 (the
     //             output's term) runs after MMA3, off the chain, and MMA1 of
     //             the next chunk, issued after it, overwrites them in order
     const uint32_t tS = tmem, tD1 = tmem + 128, tQS = tmem + 192, tD1b = tmem + 256, tD2 = tmem + 320;
-    const uint32_t tSh = tmem + 384, tSl = tmem + 448, tRh = tmem + 384, tRl = tmem + 416, tYh = tmem + 256,
-                   tYl = tmem + 288, tUh = tmem + 128, tUl = tmem + 160;
+    const uint32_t tSh = tmem + 384, tSl = tmem + 448, tRh = tmem + 384, tRl = tmem + 416, tYh = tmem + 384,
+                   tYl = tmem + 416, tUh = tmem + 128, tUl = tmem + 160;
 
     if (warp == kEpiWarps) {
         // ---------------- TMA producer ----------------
@@ -1019,11 +1018,19 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
                 }
                 fence_async_smem();
                 warp_arrive(bar_ofull, lane);
-                if (e0) {
-                    if (!bwait(bar_ofull, ntile & 1, cap, abort)) break;
-                    tma_store3d(&maps.O, ostage, 0, h, ctok0);
-                    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-                    mbar_arrive(bar_ofree);
+                if (warp == kEpiWarps / 2) {
+                    // lane 0 stores the tile; the whole warp leaves together if its
+                    // wait ran out (the next iteration's waits are warp-collective)
+                    bool okw = true;
+                    if (e0) {
+                        okw = bwait(bar_ofull, ntile & 1, cap, abort);
+                        if (okw) {
+                            tma_store3d(&maps.O, ostage, 0, h, ctok0);
+                            asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                            mbar_arrive(bar_ofree);
+                        }
+                    }
+                    if (!__shfl_sync(0xffffffffu, okw, 0)) break;
                 }
                 ++ntile;
             } else {
@@ -1082,8 +1089,11 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
             if (cc > 0 && !wbwait(bar_m3, (cc - 1) & 1, cap, abort)) { live = false; break; }
             tc_fence_after();
             if (!wbwait(&full[s], (cc >> 1) & 1, cap, abort)) { live = false; break; }
+            // (a) S^T -> packed bf16 hi | lo A operands; S^T *= e^{gamma_n}.  With
+            // one 32-column block per thread the state goes out to h after the
+            // arrival, off the chain
+            float fh[32];
             {
-                // (a) S^T -> packed bf16 hi | lo A operands; S^T *= e^{gamma_n}
                 const float dec = eg[63];
 #pragma unroll 1
                 for (int j = 0; j < kSC / 32; ++j) {
@@ -1097,9 +1107,13 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
                     split_pairs<16>(f, hv, lv);
                     tmem_st16(tSh + k0 / 2 + lo, hv);
                     tmem_st16(tSl + k0 / 2 + lo, lv);
-                    if (hdst && cc >= Wc)
+                    if (kSC == 32) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) fh[i] = f[i];
+                    } else if (hdst && cc >= Wc) {
 #pragma unroll
                         for (int i = 0; i < 32; ++i) hdst[(((size_t)c * p.Hv + h) * 128 + k0 + i) * 128 + t] = f[i];
+                    }
 #pragma unroll
                     for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(f[i] * dec);
                     tmem_st32(tS + k0 + lo, r);
@@ -1108,67 +1122,66 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
             }
             tc_fence_before();
             warp_arrive(bar_sb, lane);
-            // (c) R^T[t][s] = b_s (V[s][t] - e^{gamma_s} (K S)^T[t][s])
-            if (!wbwait(bar_m1, cc & 1, cap, abort)) { live = false; break; }
-            tc_fence_after();
+            if (kSC == 32 && hdst && cc >= Wc)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) hdst[(((size_t)c * p.Hv + h) * 128 + sc0 + i) * 128 + t] = fh[i];
+            // (c) R^T[t][s] = b_s (V[s][t] - e^{gamma_s} (K S)^T[t][s]); the V
+            // column is read before the wait for MMA1
             {
                 const __nv_bfloat16 *Vs = reinterpret_cast<const __nv_bfloat16 *>(st + SL::kV);
-#pragma unroll 1
-                for (int j = 0; j < kTC / 16; ++j) {
-                    const int c0 = tc0 + 16 * j;
-                    float vv[16];
+                float vv[kTC];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) vv[i] = isM ? 0.f : __bfloat162float(Vs[(c0 + i) * 128 + t]);
-                    uint32_t r[16];
-                    tmem_ld16_issue(tD1 + c0 + lo, r);
-                    tmem_wait_ld16(r);
+                for (int i = 0; i < kTC; ++i) vv[i] = isM ? 0.f : __bfloat162float(Vs[(tc0 + i) * 128 + t]);
+                if (!wbwait(bar_m1, cc & 1, cap, abort)) { live = false; break; }
+                tc_fence_after();
+                uint32_t r[kTC];
+#pragma unroll
+                for (int j = 0; j < kTC / 16; ++j) tmem_ld16_issue(tD1 + tc0 + 16 * j + lo, *reinterpret_cast<uint32_t(*)[16]>(r + 16 * j));
+                tmem_wait_ld16(*reinterpret_cast<uint32_t(*)[16]>(r));
+                if constexpr (kTC > 16) tmem_hold16(*reinterpret_cast<uint32_t(*)[16]>(r + 16));
+#pragma unroll
+                for (int j = 0; j < kTC / 16; ++j) {
                     float x[16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) x[i] = bet[c0 + i] * (vv[i] - eg[c0 + i] * __uint_as_float(r[i]));
+                    for (int i = 0; i < 16; ++i)
+                        x[i] = bet[tc0 + 16 * j + i] * (vv[16 * j + i] - eg[tc0 + 16 * j + i] * __uint_as_float(r[16 * j + i]));
                     uint32_t hv[8], lv[8];
                     split_pairs<8>(x, hv, lv);
-                    tmem_st8(tRh + c0 / 2 + lo, hv);
-                    tmem_st8(tRl + c0 / 2 + lo, lv);
+                    tmem_st8(tRh + (tc0 + 16 * j) / 2 + lo, hv);
+                    tmem_st8(tRl + (tc0 + 16 * j) / 2 + lo, lv);
                 }
                 tmem_wait_st();
             }
             tc_fence_before();
             warp_arrive(bar_rt, lane);
-            // (c2) Y^T[t][r] = e^{gamma_n - gamma_r} Ut^T[t][r] (and, in kFwd, Ut^T
-            // itself as the A operand of MMA2)
-            if (!wbwait(bar_m1b, cc & 1, cap, abort)) { live = false; break; }
-            tc_fence_after();
+            // (c2) Y^T[t][r] = e^{gamma_n - gamma_r} Ut^T[t][r] over the dead R^T
+            // columns (and, in kFwd, Ut^T itself as the A operand of MMA2)
             {
-                // every state warp reads its Ut^T columns before any writes Y^T
-                // over them (bar_yr, one arrival per state warp)
-                uint32_t hv[kTC / 2], lv[kTC / 2];
+                if (!wbwait(bar_m1b, cc & 1, cap, abort)) { live = false; break; }
+                tc_fence_after();
+                uint32_t r[kTC];
+#pragma unroll
+                for (int j = 0; j < kTC / 16; ++j) tmem_ld16_issue(tD1b + tc0 + 16 * j + lo, *reinterpret_cast<uint32_t(*)[16]>(r + 16 * j));
+                tmem_wait_ld16(*reinterpret_cast<uint32_t(*)[16]>(r));
+                if constexpr (kTC > 16) tmem_hold16(*reinterpret_cast<uint32_t(*)[16]>(r + 16));
 #pragma unroll
                 for (int j = 0; j < kTC / 16; ++j) {
                     const int c0 = tc0 + 16 * j;
-                    uint32_t r[16];
-                    tmem_ld16_issue(tD1b + c0 + lo, r);
-                    tmem_wait_ld16(r);
                     float x[16];
                     if (MODE == kFwd) {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) x[i] = __uint_as_float(r[i]);
+                        for (int i = 0; i < 16; ++i) x[i] = __uint_as_float(r[16 * j + i]);
                         uint32_t uh[8], ul[8];
                         split_pairs<8>(x, uh, ul);
                         tmem_st8(tUh + c0 / 2 + lo, uh);
                         tmem_st8(tUl + c0 / 2 + lo, ul);
                     }
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) x[i] = eL[c0 + i] * __uint_as_float(r[i]);
-                    split_pairs<8>(x, hv + 8 * j, lv + 8 * j);
-                }
-                tc_fence_before();
-                warp_arrive(bar_yr, lane);
-                if (!wbwait(bar_yr, cc & 1, cap, abort)) { live = false; break; }
-                tc_fence_after();
-#pragma unroll
-                for (int j = 0; j < kTC / 16; ++j) {
-                    tmem_st8(tYh + (tc0 + 16 * j) / 2 + lo, hv + 8 * j);
-                    tmem_st8(tYl + (tc0 + 16 * j) / 2 + lo, lv + 8 * j);
+                    for (int i = 0; i < 16; ++i) x[i] = eL[c0 + i] * __uint_as_float(r[16 * j + i]);
+                    uint32_t hv[8], lv[8];
+                    split_pairs<8>(x, hv, lv);
+                    tmem_st8(tYh + c0 / 2 + lo, hv);
+                    tmem_st8(tYl + c0 / 2 + lo, lv);
                 }
                 tmem_wait_st();
             }
@@ -1456,7 +1469,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_dh_tc(Params p, const __gri
             if (cc > 0 && !wbwait(bar_m3, (cc - 1) & 1, cap, abort)) { live = false; break; }
             tc_fence_after();
             if (!wbwait(&full[s], (cc >> 1) & 1, cap, abort)) { live = false; break; }
-            // (a) dS1 = dS (stored for the chunk gradients) -> packed hi | lo; dS *= e^{gamma_n}
+            // (a) dS1 = dS -> packed hi | lo; dS *= e^{gamma_n}; dS1 goes out for the
+            // chunk gradients after the arrival, off the chain
             {
                 const float dec = eg[63];
                 uint32_t r[32];
@@ -1468,6 +1482,12 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_dh_tc(Params p, const __gri
                 split_pairs<16>(f, hv, lv);
                 tmem_st16(tSh + sc0 / 2 + lo, hv);
                 tmem_st16(tSl + sc0 / 2 + lo, lv);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(f[i] * dec);
+                tmem_st32(tS + sc0 + lo, r);
+                tmem_wait_st();
+                tc_fence_before();
+                warp_arrive(bar_sb, lane);
                 if (DM == kDhFull) {
                     // dS1 leaves as the chunk kernel's A operand: a bf16 hi | lo pair of
                     // 128-byte-swizzled images [2 value halves][128 rows k][64 values],
@@ -1488,13 +1508,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_dh_tc(Params p, const __gri
                         *reinterpret_cast<uint32_t *>(img + k * 128 + ((vc ^ (k & 7)) << 4)) = w;
                     }
                 }
-#pragma unroll
-                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(f[i] * dec);
-                tmem_st32(tS + sc0 + lo, r);
-                tmem_wait_st();
             }
-            tc_fence_before();
-            warp_arrive(bar_sb, lane);
             // (c) dUt^T[t][r] = (dO^T P)[t][r] + e^{gamma_n - gamma_r} (dS1^T K^T)[t][r]
             // (rows past the chunk end: 0; P has no entry there)
             if (!wbwait(bar_m1, cc & 1, cap, abort)) { live = false; break; }
@@ -1516,13 +1530,13 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_dh_tc(Params p, const __gri
                 split_pairs<8>(x, hv, lv);
                 tmem_st8(tUh + tc0 / 2 + lo, hv);
                 tmem_st8(tUl + tc0 / 2 + lo, lv);
-                if (DM == kDhFull)
+                tmem_wait_st();
+                tc_fence_before();
+                warp_arrive(bar_ut, lane);
+                if (DM == kDhFull)  // (after the arrival, off the chain)
 #pragma unroll
                     for (int i = 0; i < 16; ++i) p.dubuf[(ch * 64 + tc0 + i) * 128 + t] = x[i];
-                tmem_wait_st();
             }
-            tc_fence_before();
-            warp_arrive(bar_ut, lane);
             // (c2) X^T = [scale e^{gamma_s} dO[s][t] | -b_s e^{gamma_s} dR^T[t][s]]
             {
                 const char *dO = st + SL::kdO + (t >> 6) * 8192;

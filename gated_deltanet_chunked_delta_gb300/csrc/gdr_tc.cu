@@ -161,27 +161,6 @@ __device__ __forceinline__ void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t
         "l"(a), "l"(b), "r"(idesc), "r"(acc)
         : "memory");
 }
-// Same with the A operand (M = 128 lanes x 16 K as 8 packed bf16-pair columns)
-// read from tensor memory at column address a.
-__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
-        "r"(a), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
-}
-// n MMAs into d, the operand descriptors advanced by da / db bytes per step
-// (the start-address field counts 16-byte units); the first accumulates iff acc.
-__device__ __forceinline__ void mma_seq(uint32_t d, uint64_t a, uint32_t da, uint64_t b, uint32_t db, uint32_t idesc,
-                                        int n, bool acc) {
-#pragma unroll 1
-    for (int i = 0; i < n; ++i) {
-        mma(d, a, b, idesc, (acc || i > 0) ? 1u : 0u);
-        a += da >> 4;
-        b += db >> 4;
-    }
-}
 // Warp-wide forms, for code that a whole warp runs: every lane computes the
 // (warp-uniform) descriptors and one elected lane issues the instruction.  A
 // single thread issuing inside a divergent branch took 60-90 cycles per MMA.
@@ -194,6 +173,8 @@ __device__ __forceinline__ void mma_w(uint32_t d, uint64_t a, uint64_t b, uint32
         "l"(a), "l"(b), "r"(idesc), "r"(acc)
         : "memory");
 }
+// (the A operand, M = 128 lanes x 16 K as 8 packed bf16-pair columns, read from
+// tensor memory at column address a)
 __device__ __forceinline__ void mma_ts_w(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
     asm volatile(
         "{\n\t.reg .pred p, e;\n\t"
@@ -203,6 +184,8 @@ __device__ __forceinline__ void mma_ts_w(uint32_t d, uint32_t a, uint64_t b, uin
         "r"(a), "l"(b), "r"(idesc), "r"(acc)
         : "memory");
 }
+// n MMAs into d, the operand descriptors advanced by da / db bytes per step
+// (the start-address field counts 16-byte units); the first accumulates iff acc.
 __device__ __forceinline__ void mma_seq_w(uint32_t d, uint64_t a, uint32_t da, uint64_t b, uint32_t db, uint32_t idesc,
                                           int n, bool acc) {
 #pragma unroll 1
@@ -352,10 +335,11 @@ __device__ __forceinline__ void st_img_half2(char *img, int row, int col0, const
 }
 
 // ---------------------------------------------------------------------------
-// Chunk-parallel kernel: one CTA of 128 threads per (chunk, v-head), several
-// CTAs per SM.  [K ; Q] K^T on tcgen05 (warps 0-1 read the K K^T rows, warps
-// 2-3 the Q K^T rows), the gate cumsum, L = strict_tril(diag(b) (K K^T o D)),
-// P, and the unit-lower-triangular inverse A = (I + L)^-1 on the CUDA cores
+// Chunk-parallel kernel: one CTA of 128 threads per (chunk, qk-head), several
+// CTAs per SM.  [K ; Q] K^T on tcgen05, once for the qk-head's G v-heads
+// (warps 0-1 read the K K^T rows, warps 2-3 the Q K^T rows); then, for each
+// v-head of the group in turn, the gate cumsum, L = strict_tril(diag(b) (K K^T
+// o D)), P, and the unit-lower-triangular inverse A = (I + L)^-1 on the CUDA cores
 // by recursive doubling: the four 16x16 diagonal inverses first (one column
 // per thread), then the two 32x32 diagonal blocks and then the whole matrix,
 // each from its two diagonal halves as
@@ -467,12 +451,13 @@ __global__ void __launch_bounds__(128, 5) k_chunk_tc(Params p, const __grid_cons
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2);
     volatile int *abort = reinterpret_cast<volatile int *>(bars + 3);
 
+    // one CTA per (chunk, qk-head): [K ; Q] K^T is computed once and read by
+    // every v-head of the qk-head's group in turn
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int c = blockIdx.x / p.Hv, h = blockIdx.x - c * p.Hv;
-    const int hq = h / (p.Hv / p.Hq);
+    const int c = blockIdx.x / p.Hq, hq = blockIdx.x - c * p.Hq;
+    const int G = p.Hv / p.Hq;
     const ChunkInfo ci = p.chunk[c];
     const int len = ci.len, tok0 = ci.tok0;
-    const size_t ch = (size_t)c * p.Hv + h;
     const long long cap = p.timeout_spins;
 
     if (tid == 0) {
@@ -498,34 +483,14 @@ __global__ void __launch_bounds__(128, 5) k_chunk_tc(Params p, const __grid_cons
         tma3d(tile + 8192, &maps.Q, 0, hq, tok0, &bars[0]);
         tma3d(tile + 16384 + 8192, &maps.Q, 64, hq, tok0, &bars[0]);
     }
-    // gates while the copies fly: g -> gam (threads 0-63), beta -> bet (64-127)
-    {
+    // the first v-head's gates while the copies fly: g -> gam (threads 0-63), beta -> bet (64-127)
+    auto load_gates = [&](int h) {
         const int t = tid & 63;
         const float x = t < len ? (tid < 64 ? p.g : p.beta)[(size_t)(tok0 + t) * p.Hv + h] : 0.f;
         (tid < 64 ? gam : bet)[t] = x;
-    }
-    __syncthreads();
-    if (tid < 32) {  // inclusive cumsum over 64 values, two per lane
-        const float a = gam[2 * lane], b = gam[2 * lane + 1];
-        float s = a + b;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const float n = __shfl_up_sync(0xffffffffu, s, o);
-            if (lane >= o) s += n;
-        }
-        gam[2 * lane] = s - b;
-        gam[2 * lane + 1] = s;
-    }
-    __syncthreads();
-    const float gC = gam[63];
-    if (tid < 64) {
-        float *aux = reinterpret_cast<float *>(reinterpret_cast<char *>(p.Aux) + ch * kAux);
-        const float gt = gam[tid], bt = bet[tid];
-        aux[tid] = bt;
-        aux[64 + tid] = __expf(gt);
-        aux[128 + tid] = __expf(gC - gt);
-    }
-    if (tid == 0) {  // [K ; Q] K^T once the tiles have landed (the gates' work overlapped the copies)
+    };
+    load_gates(hq * G);
+    if (tid == 0) {  // [K ; Q] K^T once the tiles have landed
         if (bwait(&bars[0], 0, cap, abort)) {
             tc_fence_after();
             const uint32_t id = idesc_bf16(128, 64);
@@ -542,20 +507,80 @@ __global__ void __launch_bounds__(128, 5) k_chunk_tc(Params p, const __grid_cons
     // one decision for the whole CTA: the inverse below synchronises the CTA
     const bool ok = !__syncthreads_or(!bwait(&bars[1], 0, cap, abort));
     tc_fence_after();
-    // rows of [K K^T ; Q K^T]: warps 0-1 -> L (unless from_A), warps 2-3 -> P
-    if (ok) {
-        const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16);
+    // (the K / Q tile is dead from here: the MMA that read it has completed)
+    const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16);
+    for (int j = 0; j < G; ++j) {
+        const int h = hq * G + j;
+        const size_t ch = (size_t)c * p.Hv + h;
+        if (j > 0) {
+            if (tid == 0)  // the previous v-head's A image store has read Ls
+                asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+            load_gates(h);
+        }
+        __syncthreads();
+        if (tid < 32) {  // inclusive cumsum over 64 values, two per lane
+            const float a = gam[2 * lane], b = gam[2 * lane + 1];
+            float s = a + b;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float n = __shfl_up_sync(0xffffffffu, s, o);
+                if (lane >= o) s += n;
+            }
+            gam[2 * lane] = s - b;
+            gam[2 * lane + 1] = s;
+        }
+        __syncthreads();
+        const float gC = gam[63];
         if (tid < 64) {
-            if (!from_A) {
-                // L[r][s] = b_r e^{gamma_r - gamma_s} (k_r . k_s) for s < r: one
-                // exponential per entry, of a non-positive argument (the gates are <= 0)
-                const int rr = tid;
-                const float br = bet[rr], gr = gam[rr];
-                float *lrow = Ls + rr * kLd;
+            float *aux = reinterpret_cast<float *>(reinterpret_cast<char *>(p.Aux) + ch * kAux);
+            const float gt = gam[tid], bt = bet[tid];
+            aux[tid] = bt;
+            aux[64 + tid] = __expf(gt);
+            aux[128 + tid] = __expf(gC - gt);
+        }
+        // rows of [K K^T ; Q K^T]: warps 0-1 -> L (unless from_A), warps 2-3 -> P
+        if (ok) {
+            if (tid < 64) {
+                if (!from_A) {
+                    // L[r][s] = b_r e^{gamma_r - gamma_s} (k_r . k_s) for s < r: one
+                    // exponential per entry, of a non-positive argument (the gates are <= 0)
+                    const int rr = tid;
+                    const float br = bet[rr], gr = gam[rr];
+                    float *lrow = Ls + rr * kLd;
 #pragma unroll 1
+                    for (int hb = 0; hb < 2; ++hb) {
+                        uint32_t rv[32];
+                        tmem_ld32(ta + 32 * hb, rv);
+                        float x[32];
+#pragma unroll
+                        for (int s4 = 0; s4 < 32; s4 += 4) {
+                            const float4 g4 = *reinterpret_cast<const float4 *>(gam + 32 * hb + s4);
+                            const float gs[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                // branch-free: the exponent is clamped to <= 0 and the mask applied after
+                                const int sc = 32 * hb + s4 + e;
+                                const float v = br * __expf(fminf(gr - gs[e], 0.f)) * __uint_as_float(rv[s4 + e]);
+                                x[s4 + e] = sc < rr ? v : 0.f;
+                            }
+                        }
+#pragma unroll
+                        for (int s = 0; s < 32; s += 4)
+                            *reinterpret_cast<float4 *>(lrow + 32 * hb + s) = make_float4(x[s], x[s + 1], x[s + 2], x[s + 3]);
+                    }
+                }
+            } else {
+                // P[r][s] = scale e^{gamma_r - gamma_s} (q_r . k_s) for s <= r: one
+                // exponential per entry, of a non-positive argument, so the entry
+                // stays in range however strongly the gates decay.  Rows past the
+                // chunk end are zero (the backward mixes rows through P^T).
+                const int rr = tid - 64;
+                const float gr = gam[rr], sc = rr < len ? p.scale : 0.f;
+                char *pimg = reinterpret_cast<char *>(As);  // staged for one bulk store
+#pragma unroll
                 for (int hb = 0; hb < 2; ++hb) {
-                    uint32_t rv[32];
-                    tmem_ld32(ta + 32 * hb, rv);
+                    uint32_t r0[32];
+                    tmem_ld32(ta + 32 * hb, r0);
                     float x[32];
 #pragma unroll
                     for (int s4 = 0; s4 < 32; s4 += 4) {
@@ -563,144 +588,114 @@ __global__ void __launch_bounds__(128, 5) k_chunk_tc(Params p, const __grid_cons
                         const float gs[4] = {g4.x, g4.y, g4.z, g4.w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            // branch-free: the exponent is clamped to <= 0 and the mask applied after
-                            const int sc = 32 * hb + s4 + e;
-                            const float v = br * __expf(fminf(gr - gs[e], 0.f)) * __uint_as_float(rv[s4 + e]);
-                            x[s4 + e] = sc < rr ? v : 0.f;
+                            const int s = 32 * hb + s4 + e;
+                            const float v = sc * __expf(fminf(gr - gs[e], 0.f)) * __uint_as_float(r0[s4 + e]);
+                            x[s4 + e] = s <= rr ? v : 0.f;
                         }
                     }
-#pragma unroll
-                    for (int s = 0; s < 32; s += 4)
-                        *reinterpret_cast<float4 *>(lrow + 32 * hb + s) = make_float4(x[s], x[s + 1], x[s + 2], x[s + 3]);
+                    st_img_half2(pimg, rr, 32 * hb, x);
                 }
             }
-        } else {
-            // P[r][s] = scale e^{gamma_r - gamma_s} (q_r . k_s) for s <= r: one
-            // exponential per entry, of a non-positive argument, so the entry
-            // stays in range however strongly the gates decay.  Rows past the
-            // chunk end are zero (the backward mixes rows through P^T).
-            const int rr = tid - 64;
-            const float gr = gam[rr], sc = rr < len ? p.scale : 0.f;
-            char *pimg = reinterpret_cast<char *>(As);  // staged for one bulk store
+        }
+        fence_async_smem();
+        __syncthreads();  // L and the staged P image complete
+        if (tid == 0 && ok) {  // the P image, staged in A's buffer, leaves by one bulk store
+            asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                             reinterpret_cast<char *>(p.Pimg) + ch * kImg2),
+                         "r"(su32(As)), "r"(kImg2)
+                         : "memory");
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+            asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        }
+        __syncthreads();  // the staged P image has been read
+        if (from_A) {
+            // 64 rows x 16 float4, eight per thread, all in flight before the stores
+            float4 av[8];
 #pragma unroll
-            for (int hb = 0; hb < 2; ++hb) {
-                uint32_t r0[32];
-                tmem_ld32(ta + 32 * hb, r0);
-                float x[32];
+            for (int u = 0; u < 8; ++u) {
+                const int e = tid + 128 * u, rr = e >> 4, c4 = (e & 15) * 4;
+                av[u] = rr < len ? *reinterpret_cast<const float4 *>(p.A_in + ((size_t)(tok0 + rr) * p.Hv + h) * 64 + c4)
+                                 : make_float4(rr == c4, rr == c4 + 1, rr == c4 + 2, rr == c4 + 3);
+            }
 #pragma unroll
-                for (int s4 = 0; s4 < 32; s4 += 4) {
-                    const float4 g4 = *reinterpret_cast<const float4 *>(gam + 32 * hb + s4);
-                    const float gs[4] = {g4.x, g4.y, g4.z, g4.w};
+            for (int u = 0; u < 8; ++u) {
+                const int e = tid + 128 * u, rr = e >> 4, c4 = (e & 15) * 4;
+                *reinterpret_cast<float4 *>(As + rr * kLd + c4) = av[u];
+            }
+            __syncthreads();
+        } else if (ok) {
+            if (tid < 64) {
+                // diagonal 16x16 blocks: thread (b, j) solves column j of block b in
+                // registers, x[r] = [r == j] - sum_{s<r} L[b+r][b+s] x[s]
+                // (each row's sum in four partial sums, over vector reads of the row)
+                const int b = 16 * (tid >> 4), jj = tid & 15;
+                float x[16];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int s = 32 * hb + s4 + e;
-                        const float v = sc * __expf(fminf(gr - gs[e], 0.f)) * __uint_as_float(r0[s4 + e]);
-                        x[s4 + e] = s <= rr ? v : 0.f;
+                for (int rr = 0; rr < 16; ++rr) {
+                    const float *lrow = Ls + (b + rr) * kLd + b;
+                    float a[4] = {rr == jj ? 1.f : 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int s4 = 0; s4 < rr; s4 += 4) {
+                        const float4 l4 = *reinterpret_cast<const float4 *>(lrow + s4);
+                        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            if (s4 + e < rr) a[e] = fmaf(-lv[e], x[s4 + e], a[e]);
                     }
+                    x[rr] = rr < jj ? 0.f : (a[0] + a[1]) + (a[2] + a[3]);
                 }
-                st_img_half2(pimg, rr, 32 * hb, x);
-            }
-        }
-    }
-    fence_async_smem();
-    __syncthreads();  // L complete; the K/Q tile is dead (the MMA that read it has completed)
-    if (tid == 0 && ok) {  // the P image, staged in A's buffer, leaves by one bulk store
-        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
-                         reinterpret_cast<char *>(p.Pimg) + ch * kImg2),
-                     "r"(su32(As)), "r"(kImg2)
-                     : "memory");
-        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-    }
-    __syncthreads();  // the staged P image has been read
-    if (from_A) {
-        // 64 rows x 16 float4, eight per thread, all in flight before the stores
-        float4 av[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int e = tid + 128 * u, rr = e >> 4, c4 = (e & 15) * 4;
-            av[u] = rr < len ? *reinterpret_cast<const float4 *>(p.A_in + ((size_t)(tok0 + rr) * p.Hv + h) * 64 + c4)
-                             : make_float4(rr == c4, rr == c4 + 1, rr == c4 + 2, rr == c4 + 3);
-        }
+                for (int rr = 0; rr < 16; ++rr) As[(b + rr) * kLd + b + jj] = x[rr];
+            } else {
+                // zero the strictly upper blocks of A
+                const int t = tid - 64;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int e = tid + 128 * u, rr = e >> 4, c4 = (e & 15) * 4;
-            *reinterpret_cast<float4 *>(As + rr * kLd + c4) = av[u];
-        }
-        __syncthreads();
-    } else if (ok) {
-        if (tid < 64) {
-            // diagonal 16x16 blocks: thread (b, j) solves column j of block b in
-            // registers, x[r] = [r == j] - sum_{s<r} L[b+r][b+s] x[s]
-            // (each row's sum in four partial sums, over vector reads of the row)
-            const int b = 16 * (tid >> 4), jj = tid & 15;
-            float x[16];
-#pragma unroll
-            for (int rr = 0; rr < 16; ++rr) {
-                const float *lrow = Ls + (b + rr) * kLd + b;
-                float a[4] = {rr == jj ? 1.f : 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int s4 = 0; s4 < rr; s4 += 4) {
-                    const float4 l4 = *reinterpret_cast<const float4 *>(lrow + s4);
-                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        if (s4 + e < rr) a[e] = fmaf(-lv[e], x[s4 + e], a[e]);
+                for (int u = 0; u < 6; ++u) {
+                    const int e = t + 64 * u;             // 384 float4 = 6 blocks x 16 rows x 4
+                    const int blk = e >> 6, rr = (e >> 2) & 15, c4 = (e & 3) * 4;
+                    const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+                    const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+                    *reinterpret_cast<float4 *>(As + (16 * bi + rr) * kLd + 16 * bj + c4) = make_float4(0.f, 0.f, 0.f, 0.f);
                 }
-                x[rr] = rr < jj ? 0.f : (a[0] + a[1]) + (a[2] + a[3]);
             }
-#pragma unroll
-            for (int rr = 0; rr < 16; ++rr) As[(b + rr) * kLd + b + jj] = x[rr];
-        } else {
-            // zero the strictly upper blocks of A
-            const int t = tid - 64;
-#pragma unroll
-            for (int u = 0; u < 6; ++u) {
-                const int e = t + 64 * u;             // 384 float4 = 6 blocks x 16 rows x 4
-                const int blk = e >> 6, rr = (e >> 2) & 15, c4 = (e & 3) * 4;
-                const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-                const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-                *reinterpret_cast<float4 *>(As + (16 * bi + rr) * kLd + 16 * bj + c4) = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
+            __syncthreads();
+            inv_level16(Ls, As, Tt, tid);
+            inv_level32(Ls, As, Tt, tid);
         }
-        __syncthreads();
-        inv_level16(Ls, As, Tt, tid);
-        inv_level32(Ls, As, Tt, tid);
-    }
-    if (!*abort) {
-        // the A image (hi | lo: thread -> row tid % 64, 32 columns from 32 (tid
-        // / 64)) staged over L, dead after the inverse, for one bulk store; the
-        // fp32 A output a row per warp at a time (coalesced)
-        const int rr = tid & 63, c0 = 32 * (tid >> 6);
-        float x[32];
-#pragma unroll
-        for (int s = 0; s < 32; s += 4) {
-            const float4 v = *reinterpret_cast<const float4 *>(As + rr * kLd + c0 + s);
-            x[s] = v.x; x[s + 1] = v.y; x[s + 2] = v.z; x[s + 3] = v.w;
-        }
-        st_img_half2(reinterpret_cast<char *>(Ls), rr, c0, x);
-        if (p.A_out && !from_A)
-            for (int r = warp; r < len; r += 4)
-                *reinterpret_cast<float2 *>(p.A_out + ((size_t)(tok0 + r) * p.Hv + h) * 64 + 2 * lane) =
-                    *reinterpret_cast<const float2 *>(As + r * kLd + 2 * lane);
-    }
-    fence_async_smem();
-    if (tid == 0) {  // no copy or MMA of this CTA may still be in flight when it leaves
-        drain_wait(&bars[0], 0);
-        if (mma_issued) drain_wait(&bars[1], 0);
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {
         if (!*abort) {
+            // the A image (hi | lo: thread -> row tid % 64, 32 columns from 32 (tid
+            // / 64)) staged over L, dead after the inverse, for one bulk store; the
+            // fp32 A output a row per warp at a time (coalesced)
+            const int rr = tid & 63, c0 = 32 * (tid >> 6);
+            float x[32];
+#pragma unroll
+            for (int s = 0; s < 32; s += 4) {
+                const float4 v = *reinterpret_cast<const float4 *>(As + rr * kLd + c0 + s);
+                x[s] = v.x; x[s + 1] = v.y; x[s + 2] = v.z; x[s + 3] = v.w;
+            }
+            st_img_half2(reinterpret_cast<char *>(Ls), rr, c0, x);
+            if (p.A_out && !from_A)
+                for (int r = warp; r < len; r += 4)
+                    *reinterpret_cast<float2 *>(p.A_out + ((size_t)(tok0 + r) * p.Hv + h) * 64 + 2 * lane) =
+                        *reinterpret_cast<const float2 *>(As + r * kLd + 2 * lane);
+        }
+        fence_async_smem();
+        __syncthreads();  // the A image staged, As and the gates read
+        if (tid == 0 && !*abort) {
             asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
                              reinterpret_cast<char *>(p.Aimg) + ch * kImg2),
                          "r"(su32(Ls)), "r"(kImg2)
                          : "memory");
             asm volatile("cp.async.bulk.commit_group;" ::: "memory");
         }
+    }
+    if (tid == 0) {  // no copy or MMA of this CTA may still be in flight when it leaves
+        drain_wait(&bars[0], 0);
+        if (mma_issued) drain_wait(&bars[1], 0);
         asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // every bulk store written before the CTA leaves
     }
+    tc_fence_before();
+    __syncthreads();
     if (warp == 0) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(64));
@@ -717,7 +712,7 @@ __global__ void __launch_bounds__(128, 5) k_chunk_tc(Params p, const __grid_cons
 // MMAs read only their B operands from shared memory.  Per chunk, with S^T
 // in TMEM (lane v):
 //   (a)  S^T -> bf16 hi + lo (A operands); S^T *= e^{gamma_n} in place
-//   MMA1 D1 = S^T [K ; Q]^T                               -> (K S)^T, (Q S)^T
+//   MMA1 D1 = S^T K^T -> (K S)^T; then (kFwd) S^T Q^T      -> (Q S)^T, off the chain
 //   (c)  R^T = (diag(b) (V - diag(e^gamma) K S))^T        -> bf16 hi + lo
 //   MMA1b D1b = R^T A^T = Ut^T
 //   (c2) Y^T = (diag(e^{gamma_n - gamma}) Ut)^T           -> bf16 hi + lo
@@ -759,9 +754,16 @@ template <int MODE, typename TO>
 __host__ __device__ constexpr int scan_out_bytes() {
     return MODE == kFwd ? 64 * 128 * (int)sizeof(TO) : 0;
 }
+// The state recompute stages each chunk's start state ([128 k][128 v] fp32)
+// for one bulk copy to the workspace, off the chain.
+template <int MODE>
+__host__ __device__ constexpr int scan_hstage_bytes() {
+    return MODE == kStates ? 65536 : 0;
+}
 template <int MODE, typename TO>
 __host__ __device__ constexpr int scan_smem() {
-    return 1024 + 2 * ScanStage<MODE>::kBytes + scan_out_bytes<MODE, TO>() + 2 * kAux + 256;
+    return 1024 + 2 * ScanStage<MODE>::kBytes + scan_out_bytes<MODE, TO>() + 2 * kAux + 256 +
+           scan_hstage_bytes<MODE>();
 }
 
 template <int MODE, typename TO>
@@ -788,6 +790,11 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
     uint64_t *bar_m2 = bars + 13;     // MMA2 done (kFwd)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 15);
     volatile int *abort = reinterpret_cast<volatile int *>(bars + 16);
+    uint64_t *bar_hfull = bars + 17;  // (kStates) the state warps have staged a chunk's start state
+    uint64_t *bar_hfree = bars + 18;  // (kStates) its bulk copy has read the staging buffer
+    uint64_t *bar_m1q = bars + 19;    // (kFwd) the (Q S)^T half of MMA1 done
+    uint64_t *bar_d2r = bars + 20;    // (kFwd) the output warps have read (P Ut)^T
+    float *hstage = reinterpret_cast<float *>(aux0 + 2 * kAux + 256);  // (kStates) [128 k][128 v]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int sidx = blockIdx.x, h = blockIdx.y;
@@ -823,6 +830,10 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
         mbar_init(bar_ofull, kEpiWarps / 2);
         mbar_init(bar_ofree, 1);
         mbar_init(bar_m2, 1);
+        mbar_init(bar_hfull, kEpiWarps);
+        mbar_init(bar_hfree, 1);
+        mbar_init(bar_m1q, 1);
+        mbar_init(bar_d2r, kEpiWarps / 2);
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -841,16 +852,23 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
     //   [256,320) Ut^T                          (MMA1b)
     //   [320,384) (P Ut)^T                      (MMA2)
     //   [384,512) A operands as packed bf16 pairs: S^T hi | lo (64 + 64
-    //             columns) for MMA1, then R^T hi | lo at [384,448) for MMA1b,
-    //             then Y^T hi | lo at [384,448) for MMA3 (R^T is dead once
-    //             MMA1b has completed, and the next chunk's (a) waits for MMA3)
+    //             columns) for MMA1, then (except kFwd) R^T hi | lo at
+    //             [384,448) for MMA1b, then Y^T hi | lo at [384,448) for MMA3
+    //             (R^T and the S^T operand are dead once MMA1b has completed,
+    //             and the next chunk's (a) waits for MMA3)
+    //   kFwd: MMA1 runs as its (K S)^T half (on the chain, bar_m1) and then its
+    //             (Q S)^T half (bar_m1q), which may still read the S^T operand
+    //             while (c) runs, so R^T goes to [320,384) instead, over
+    //             (P Ut)^T of the previous chunk once the output warps have
+    //             read it (bar_d2r); MMA2 writes there after MMA1b in order
     //   [128,192) Ut^T hi | lo (kFwd), over (K S)^T once (c) has read it, for
     //             MMA2: the next chunk's (a) touches neither, so MMA2 (the
     //             output's term) runs after MMA3, off the chain, and MMA1 of
     //             the next chunk, issued after it, overwrites them in order
     const uint32_t tS = tmem, tD1 = tmem + 128, tQS = tmem + 192, tD1b = tmem + 256, tD2 = tmem + 320;
-    const uint32_t tSh = tmem + 384, tSl = tmem + 448, tRh = tmem + 384, tRl = tmem + 416, tYh = tmem + 384,
-                   tYl = tmem + 416, tUh = tmem + 128, tUl = tmem + 160;
+    const uint32_t tSh = tmem + 384, tSl = tmem + 448, tRh = tmem + (MODE == kFwd ? 320 : 384),
+                   tRl = tmem + (MODE == kFwd ? 352 : 416), tYh = tmem + 384, tYl = tmem + 416, tUh = tmem + 128,
+                   tUl = tmem + 160;
 
     if (warp == kEpiWarps) {
         // ---------------- TMA producer ----------------
@@ -881,12 +899,27 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
             }
             for (int cc = issued - 2 < 0 ? 0 : issued - 2; cc < issued; ++cc)
                 drain_wait(&full[cc & 1], (cc >> 1) & 1);
+        } else if (MODE == kStates && lane == 1 && p.hbuf) {
+            // the start state of every chunk, staged by the state warps, leaves by
+            // one bulk copy; the staging buffer is freed once the copy has read it
+            for (int j = 0; j < ntot - Wc; ++j) {
+                if (!bwait(bar_hfull, j & 1, cap, abort)) break;
+                const int c = cfirst + Wc + j;
+                asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                                 p.hbuf + ((size_t)c * p.Hv + h) * 16384),
+                             "r"(su32(hstage)), "r"(65536)
+                             : "memory");
+                asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                mbar_arrive(bar_hfree);
+            }
+            asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // written before the CTA leaves
         }
     } else if (warp == kEpiWarps + 1) {
         // ---------------- MMA issuer: A operands from tensor memory; the whole
         // warp runs the loop (uniform descriptors), one elected lane issues ----------------
         {
-            const uint32_t id1 = idesc_bf16(128, MODE == kFwd ? 128 : 64);
+            const uint32_t id1 = idesc_bf16(128, 64);
             const uint32_t id64 = idesc_bf16(128, 64);
             const uint32_t id3 = idesc_bf16(128, 128, 0, 1);
             for (int cc = 0; cc < ntot; ++cc) {
@@ -896,7 +929,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
                 if (!wbwait(bar_sb, cc & 1, cap, abort)) break;
                 tc_fence_after();
                 const uint32_t b1 = su32(st + SL::kB1);
-                // MMA1: D1 = S^T [K ; Q]^T over k, 16 k per step (8 packed columns)
+                // MMA1: D1 = S^T K^T over k, 16 k per step (8 packed columns); in
+                // kFwd then (Q S)^T = S^T Q^T from the Q rows (8 KiB into each atom)
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
 #pragma unroll
@@ -907,6 +941,18 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
                     }
                 }
                 mma_commit_w(bar_m1);
+                if (MODE == kFwd) {
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint32_t ko = (kk & 3) * 32;
+                            mma_ts_w(tQS, (half ? tSl : tSh) + 8 * kk,
+                                     sdesc(b1 + 8192 + (kk >> 2) * SL::kAtom + ko), id1, (half | kk) != 0);
+                        }
+                    }
+                    mma_commit_w(bar_m1q);
+                }
                 if (!wbwait(bar_rt, cc & 1, cap, abort)) break;
                 tc_fence_after();
                 {
@@ -973,7 +1019,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] = p.scale * eg[r0 + i];
             warp_arrive(&empty[s], lane);  // done with the stage
-            if (!wbwait(bar_m1, cc & 1, cap, abort)) break;
+            if (!wbwait(bar_m1q, cc & 1, cap, abort)) break;
             tc_fence_after();
             {
                 uint32_t a[16], b[16];
@@ -1005,6 +1051,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
             }
             tc_fence_before();
             warp_arrive(bar_ut, lane);  // (P Ut)^T of cc read
+            warp_arrive(bar_d2r, lane);
             if (cc < Wc) {
                 // a warm-up chunk: no output
             } else if (clen == kChunk) {
@@ -1122,9 +1169,15 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
             }
             tc_fence_before();
             warp_arrive(bar_sb, lane);
-            if (kSC == 32 && hdst && cc >= Wc)
+            if (MODE == kStates && hdst && cc >= Wc) {
+                // staged for the bulk copy once the previous chunk's has read the buffer
+                const int j = cc - Wc;
+                if (j > 0 && !wbwait(bar_hfree, (j - 1) & 1, cap, abort)) { live = false; break; }
 #pragma unroll
-                for (int i = 0; i < 32; ++i) hdst[(((size_t)c * p.Hv + h) * 128 + sc0 + i) * 128 + t] = fh[i];
+                for (int i = 0; i < 32; ++i) hstage[(sc0 + i) * 128 + t] = fh[i];
+                fence_async_smem();
+                warp_arrive(bar_hfull, lane);
+            }
             // (c) R^T[t][s] = b_s (V[s][t] - e^{gamma_s} (K S)^T[t][s]); the V
             // column is read before the wait for MMA1
             {
@@ -1133,6 +1186,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
 #pragma unroll
                 for (int i = 0; i < kTC; ++i) vv[i] = isM ? 0.f : __bfloat162float(Vs[(tc0 + i) * 128 + t]);
                 if (!wbwait(bar_m1, cc & 1, cap, abort)) { live = false; break; }
+                if (MODE == kFwd && cc > 0 && !wbwait(bar_d2r, (cc - 1) & 1, cap, abort)) { live = false; break; }
                 tc_fence_after();
                 uint32_t r[kTC];
 #pragma unroll
@@ -1276,13 +1330,18 @@ struct DhStage {
     static constexpr int kP = 65536;      // P image, hi | lo
     static constexpr int kBytes = 81920;
 };
-constexpr int kDhSmem = 1024 + 2 * DhStage::kBytes + 2 * kAux + 256;
+// The full reverse scan stages each chunk's dS1 image (64 KiB) for one bulk
+// copy to the workspace, off the chain.
+template <int DM>
+__host__ __device__ constexpr int dh_smem() {
+    return 1024 + 2 * DhStage::kBytes + 2 * kAux + 256 + (DM == 0 ? 65536 : 0);
+}
 
 template <int DM>
 __global__ void __launch_bounds__(kScanThreads, 1) k_dh_tc(Params p, const __grid_constant__ DhMaps maps) {
     extern __shared__ __align__(1024) char smraw[];
     char *sm = smem_align1024(smraw);
-    static_assert(kDhSmem <= 227 * 1024, "shared memory budget");
+    static_assert(dh_smem<DM>() <= 227 * 1024, "shared memory budget");
     using SL = DhStage;
     char *stage0 = sm;
     char *aux0 = sm + 2 * SL::kBytes;
@@ -1298,6 +1357,10 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_dh_tc(Params p, const __gri
     uint64_t *bar_drain = bars + 10;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 11);
     volatile int *abort = reinterpret_cast<volatile int *>(bars + 12);
+    // (kDhFull) every chunk's dS1 image (64 KiB) is staged for one bulk copy
+    uint64_t *bar_dfull = bars + 13;  // the epilogue warps have staged a chunk's image
+    uint64_t *bar_dfree = bars + 14;  // its copy has read the staging buffer
+    char *dstage = aux0 + 2 * kAux + 256;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int sidx = blockIdx.x, h = blockIdx.y;
@@ -1325,6 +1388,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_dh_tc(Params p, const __gri
         mbar_init(bar_x, kEpiWarps);
         mbar_init(bar_m3, 1);
         mbar_init(bar_drain, 1);
+        mbar_init(bar_dfull, kEpiWarps);
+        mbar_init(bar_dfree, 1);
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -1372,6 +1437,21 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_dh_tc(Params p, const __gri
             }
             for (int cc = issued - 2 < 0 ? 0 : issued - 2; cc < issued; ++cc)
                 drain_wait(&full[cc & 1], (cc >> 1) & 1);
+        } else if (DM == kDhFull && lane == 1) {
+            // every chunk's dS1 image, staged by the epilogue warps, leaves by one
+            // bulk copy; the staging buffer is freed once the copy has read it
+            for (int cc = 0; cc < nch; ++cc) {
+                if (!bwait(bar_dfull, cc & 1, cap, abort)) break;
+                const size_t ch = (size_t)(cend - 1 - cc) * p.Hv + h;
+                asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                                 reinterpret_cast<char *>(p.dhbuf) + ch * 65536),
+                             "r"(su32(dstage)), "r"(65536)
+                             : "memory");
+                asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                mbar_arrive(bar_dfree);
+            }
+            asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // written before the CTA leaves
         }
     } else if (warp == kEpiWarps + 1) {
         {  // the whole warp runs the loop (uniform descriptors), one elected lane issues
@@ -1465,7 +1545,6 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_dh_tc(Params p, const __gri
             const float *eg = bet + 64, *eL = bet + 128;
             const int c = cend - 1 - cc;
             const int len = min(kChunk, sq.len - kChunk * (c - sq.chunk0));
-            const size_t ch = (size_t)c * p.Hv + h;
             if (cc > 0 && !wbwait(bar_m3, (cc - 1) & 1, cap, abort)) { live = false; break; }
             tc_fence_after();
             if (!wbwait(&full[s], (cc >> 1) & 1, cap, abort)) { live = false; break; }
@@ -1491,11 +1570,13 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_dh_tc(Params p, const __gri
                 if (DM == kDhFull) {
                     // dS1 leaves as the chunk kernel's A operand: a bf16 hi | lo pair of
                     // 128-byte-swizzled images [2 value halves][128 rows k][64 values],
-                    // 64 KiB per (chunk, v-head).  Lanes v, v^1 swap halves so that the
-                    // even lane writes the hi word of the pair, the odd lane the lo word.
+                    // 64 KiB per (chunk, v-head), staged here for one bulk copy once the
+                    // previous chunk's copy has read the buffer.  Lanes v, v^1 swap halves
+                    // so that the even lane writes the hi word of the pair, the odd lane
+                    // the lo word.
+                    if (cc > 0 && !wbwait(bar_dfree, (cc - 1) & 1, cap, abort)) { live = false; break; }
                     const int ve = t & ~1, term = t & 1;
-                    char *img = reinterpret_cast<char *>(p.dhbuf) + ch * 65536 + term * 32768 + (ve >> 6) * 16384 +
-                                (ve & 7) * 2;
+                    char *img = dstage + term * 32768 + (ve >> 6) * 16384 + (ve & 7) * 2;
                     const int vc = (ve & 63) >> 3;
                     // (the bf16 terms are the ones split_pairs packed along k above)
 #pragma unroll
@@ -1507,6 +1588,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_dh_tc(Params p, const __gri
                         const uint32_t w = term ? (other | (lb << 16)) : (hb | (other << 16));
                         *reinterpret_cast<uint32_t *>(img + k * 128 + ((vc ^ (k & 7)) << 4)) = w;
                     }
+                    fence_async_smem();
+                    warp_arrive(bar_dfull, lane);
                 }
             }
             // (c) dUt^T[t][r] = (dO^T P)[t][r] + e^{gamma_n - gamma_r} (dS1^T K^T)[t][r]
@@ -1533,9 +1616,11 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_dh_tc(Params p, const __gri
                 tmem_wait_st();
                 tc_fence_before();
                 warp_arrive(bar_ut, lane);
-                if (DM == kDhFull)  // (after the arrival, off the chain)
+                if (DM == kDhFull) {  // (after the arrival, off the chain)
+                    const size_t ch = (size_t)c * p.Hv + h;
 #pragma unroll
                     for (int i = 0; i < 16; ++i) p.dubuf[(ch * 64 + tc0 + i) * 128 + t] = x[i];
+                }
             }
             // (c2) X^T = [scale e^{gamma_s} dO[s][t] | -b_s e^{gamma_s} dR^T[t][s]]
             {
@@ -2576,7 +2661,7 @@ int launch_chunk(const char *name, const Params &p, int from_A, cudaStream_t st)
     if (cudaFuncSetAttribute(k_chunk_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kChunkSmem) != cudaSuccess)
         return 1;
     tm_begin(p.tm, name, st);
-    k_chunk_tc<<<dim3(p.NT * p.Hv), 128, kChunkSmem, st>>>(p, maps, from_A);
+    k_chunk_tc<<<dim3(p.NT * p.Hq), 128, kChunkSmem, st>>>(p, maps, from_A);
     tm_end(p.tm, st);
     return cudaGetLastError() != cudaSuccess;
 }
@@ -2606,6 +2691,7 @@ int launch_dh(const char *name, const Params &p, cudaStream_t st) {
         !map3(&maps.dO, p.dout, p.Hv, p.Ttot, 64, true))
         return 1;
     auto kern = k_dh_tc<DM>;
+    constexpr int kDhSmem = dh_smem<DM>();
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kDhSmem) != cudaSuccess) return 1;
     tm_begin(p.tm, name, st);
     // the second z-plane (N) only where a v-head may start by warm-up

@@ -166,7 +166,7 @@ size_t al(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Layout {
     size_t seq, chunk, seg, gam, W, U, P, Hseg, Mseg, Nseg, Sstart, hbuf, dhbuf, dubuf, dqp, dkp, warm;
-    size_t Aimg, Pimg, Aux;
+    size_t Aimg, Pimg, Aux, gT, bT;
     bool f32_tiles, bf16_tiles;
     size_t total;
 };
@@ -190,6 +190,8 @@ Layout layout(const gdr_shape *s, const Plan &pl, bool bwd) {
     L.Aimg = L.bf16_tiles ? take((size_t)kTileImgBytes * NT * Hv) : 0;
     L.Pimg = L.bf16_tiles ? take((size_t)kTileImgBytes * NT * Hv) : 0;
     L.Aux = L.bf16_tiles ? take((size_t)kAuxBytes * NT * Hv) : 0;
+    L.gT = L.bf16_tiles ? take(4 * NT * Hv * 64) : 0;
+    L.bT = L.bf16_tiles ? take(4 * NT * Hv * 64) : 0;
     if (pl.use_cp) {
         L.Hseg = take(4 * NS * Hv * K * V);
         L.Mseg = take(4 * NS * Hv * K * K);
@@ -280,6 +282,8 @@ int fill_params(const gdr_shape *s, const Plan &pl, const Layout &L, void *ws, P
     p->Aimg = F(L.Aimg, L.bf16_tiles);
     p->Pimg = F(L.Pimg, L.bf16_tiles);
     p->Aux = F(L.Aux, L.bf16_tiles);
+    p->gT = F(L.gT, L.bf16_tiles);
+    p->bT = F(L.bT, L.bf16_tiles);
     p->Hseg = F(L.Hseg, pl.use_cp);
     p->Mseg = F(L.Mseg, pl.use_cp);
     p->Nseg = F(L.Nseg, L.Nseg != 0);

@@ -92,6 +92,8 @@ struct Params {
     void *Aimg;     // [NT,Hv] x A
     void *Pimg;     // [NT,Hv] x P = scale (Q K^T o D o tril_incl), D_rs = e^{gamma_r - gamma_s}
     void *Aux;      // [NT,Hv] x (beta[64], e^gamma[64], e^{gamma_n - gamma}[64]) fp32
+    float *gT, *bT; // [NT,Hv,64] the gates and beta as one row of 64 per (chunk, v-head),
+                    // zero past the chunk's end (tensor-core path; written first by each call)
     int debug;
     long long timeout_spins;
     Timing *tm;  // host-side only: launch timing (may be null)

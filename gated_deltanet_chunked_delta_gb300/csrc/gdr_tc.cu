@@ -296,6 +296,52 @@ __device__ __forceinline__ bool head_warm(const Params &p, const SeqInfo &sq, in
 }
 
 // ---------------------------------------------------------------------------
+// Gate tiles: one CTA of 256 threads per (chunk, block of 64 v-heads) reads
+// the [64 tokens][64 heads] tiles of g and beta with 16-byte loads along the
+// heads (coalesced rows of the [T, Hv] inputs) and writes them head-major, one
+// row of 64 per (chunk, v-head) in 16-byte stores, zero past the chunk's end.
+// Every later kernel reads a (chunk, v-head)'s gates as 256 contiguous bytes.
+// ---------------------------------------------------------------------------
+constexpr int kGateLd = 65;
+__global__ void __launch_bounds__(256) k_gate_tile(Params p) {
+    __shared__ float tl[2][64 * kGateLd];
+    const int c = blockIdx.x, h0 = 64 * blockIdx.y, tid = threadIdx.x;
+    const ChunkInfo ci = p.chunk[c];
+    const int len = ci.len, tok0 = ci.tok0;
+    const int nh = min(64, p.Hv - h0);
+    if ((p.Hv & 3) == 0) {  // rows start 16 bytes apart: vector loads
+        const int nv = nh >> 2;
+        for (int e = tid; e < 64 * nv; e += 256) {
+            const int t = e / nv, q = 4 * (e - (e / nv) * nv);
+            float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+            if (t < len) {
+                const size_t o = (size_t)(tok0 + t) * p.Hv + h0 + q;
+                a = __ldg(reinterpret_cast<const float4 *>(p.g + o));
+                b = __ldg(reinterpret_cast<const float4 *>(p.beta + o));
+            }
+            float *x = tl[0] + t * kGateLd + q, *y = tl[1] + t * kGateLd + q;
+            x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+            y[0] = b.x; y[1] = b.y; y[2] = b.z; y[3] = b.w;
+        }
+    } else {
+        for (int e = tid; e < 64 * nh; e += 256) {
+            const int t = e / nh, q = e - (e / nh) * nh;
+            const size_t o = (size_t)(tok0 + t) * p.Hv + h0 + q;
+            tl[0][t * kGateLd + q] = t < len ? p.g[o] : 0.f;
+            tl[1][t * kGateLd + q] = t < len ? p.beta[o] : 0.f;
+        }
+    }
+    __syncthreads();
+    for (int e = tid; e < 16 * nh; e += 256) {
+        const int hh = e >> 4, t4 = (e & 15) * 4;
+        const size_t o = ((size_t)c * p.Hv + h0 + hh) * 64 + t4;
+        const float *x = tl[0] + t4 * kGateLd + hh, *y = tl[1] + t4 * kGateLd + hh;
+        *reinterpret_cast<float4 *>(p.gT + o) = make_float4(x[0], x[kGateLd], x[2 * kGateLd], x[3 * kGateLd]);
+        *reinterpret_cast<float4 *>(p.bT + o) = make_float4(y[0], y[kGateLd], y[2 * kGateLd], y[3 * kGateLd]);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // chunk-tile images kept in the workspace (bf16, byte-for-byte the shared-
 // memory image the scan's MMAs read, so the scan fetches them with plain bulk
 // copies).  Each fp32 matrix is stored as two bf16 terms, hi = bf16(x) and
@@ -486,7 +532,7 @@ __global__ void __launch_bounds__(128, 5) k_chunk_tc(Params p, const __grid_cons
     // the first v-head's gates while the copies fly: g -> gam (threads 0-63), beta -> bet (64-127)
     auto load_gates = [&](int h) {
         const int t = tid & 63;
-        const float x = t < len ? (tid < 64 ? p.g : p.beta)[(size_t)(tok0 + t) * p.Hv + h] : 0.f;
+        const float x = (tid < 64 ? p.gT : p.bT)[((size_t)c * p.Hv + h) * 64 + t];  // zero past the end
         (tid < 64 ? gam : bet)[t] = x;
     };
     load_gates(hq * G);
@@ -1729,7 +1775,9 @@ __global__ void __launch_bounds__(128) k_warm_gate(Params p) {
             uint4 u[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) u[i] = kr[i];
-            const float b = p.beta[(size_t)t * p.Hv + h], gt = p.g[(size_t)t * p.Hv + h];
+            // (the window's chunks are whole: it ends at a segment start inside the sequence)
+            const size_t gi = ((size_t)(c0 - W + (t - t0) / kChunk) * p.Hv + h) * 64 + (t - t0) % kChunk;
+            const float b = p.bT[gi], gt = p.gT[gi];
             float kk = 0.f;
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
@@ -2065,8 +2113,8 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
     if (tid == 0 && un < NU) nxt[2] = unit_tok(un, nxt[0], nxt[1]);  // its head, qk-head, first token
     __syncthreads();  // the previous unit's tail is done with the scratch rows
     if (tid < 64) {
-        gam[tid] = tid < len ? p.g[(size_t)(tok0 + tid) * p.Hv + h] : 0.f;
-        bet[tid] = tid < len ? p.beta[(size_t)(tok0 + tid) * p.Hv + h] : 0.f;
+        gam[tid] = p.gT[(size_t)u * 64 + tid];  // zero past the chunk's end
+        bet[tid] = p.bT[(size_t)u * 64 + tid];
         rRV[tid] = rRKS[tid] = rUdU[tid] = rQdq[tid] = rP[tid] = rLK[tid] = cL[tid] = 0.f;
     }
     if (tid < 16) red[tid] = 0.f;
@@ -2758,6 +2806,14 @@ int launch_combine(const char *name, const Params &p, cudaStream_t st) {
 
 int tc_supported(int K, int V) { return K == 128 && V == 128; }
 
+static int launch_gate_tile(const Params &p, cudaStream_t st) {
+    if (p.NT == 0) return 0;
+    tm_begin(p.tm, "tc_gate_tile", st);
+    k_gate_tile<<<dim3(p.NT, (p.Hv + 63) / 64), 256, 0, st>>>(p);
+    tm_end(p.tm, st);
+    return cudaGetLastError() != cudaSuccess;
+}
+
 static int launch_gate(const Params &p, cudaStream_t st) {
     if (!p.warm || p.cp_warmup <= 0) return 0;
     tm_begin(p.tm, "tc_warm_gate", st);
@@ -2767,6 +2823,7 @@ static int launch_gate(const Params &p, cudaStream_t st) {
 }
 
 int tc_fwd(const Params &p, int o_f32, int use_cp, cudaStream_t st) {
+    if (launch_gate_tile(p, st)) return 1;
     if (launch_chunk("tc_chunk", p, 0, st)) return 1;
     if (use_cp) {
         if (launch_gate(p, st)) return 1;
@@ -2778,6 +2835,7 @@ int tc_fwd(const Params &p, int o_f32, int use_cp, cudaStream_t st) {
 
 int tc_bwd(const Params &p, int use_cp, cudaStream_t st) {
     // a8: A image, P image and gates from the forward's A; states before every chunk
+    if (launch_gate_tile(p, st)) return 1;
     if (launch_chunk("tc_chunk_from_A", p, 1, st)) return 1;
     if (use_cp) {
         if (launch_gate(p, st)) return 1;

@@ -64,8 +64,8 @@ int check_shape(const gdr_shape *s) {
     if (s->B < 1 || s->T < 1 || s->Hq < 1 || s->Hv < 1)
         return fail(GDR_ERR_SHAPE, "B, T, Hq, Hv must be >= 1 (got %d, %d, %d, %d)", s->B, s->T, s->Hq, s->Hv);
     if (s->Hv % s->Hq) return fail(GDR_ERR_SHAPE, "Hv (%d) must be a multiple of Hq (%d)", s->Hv, s->Hq);
-    if ((s->K != 64 && s->K != 128) || (s->V != 64 && s->V != 128))
-        return fail(GDR_ERR_SHAPE, "K and V must be 64 or 128 (got %d, %d)", s->K, s->V);
+    if ((s->K != 64 && s->K != 128 && s->K != 192) || (s->V != 64 && s->V != 128 && s->V != 192 && s->V != 256))
+        return fail(GDR_ERR_SHAPE, "K must be 64, 128 or 192 and V 64, 128, 192 or 256 (got %d, %d)", s->K, s->V);
     if ((long long)s->B * s->T * s->Hv * (long long)std::max(s->K, s->V) >= (1LL << 40))
         return fail(GDR_ERR_SHAPE, "problem too large");
     if (s->n_seqs < 0) return fail(GDR_ERR_SHAPE, "n_seqs must be >= 0");

@@ -105,10 +105,11 @@ struct Params {
 namespace gdr {
 int simt_fwd(const Params &p, int in_f32, int o_f32, int use_cp, cudaStream_t st);
 int simt_bwd(const Params &p, int in_f32, int use_cp, cudaStream_t st);
-unsigned simt_take_status(cudaStream_t st);
-int simt_cp_combine(const Params &p, cudaStream_t st);
-int simt_cp_combine_rev(const Params &p, cudaStream_t st);
-int simt_group_sum(const Params &p, cudaStream_t st);   // dq, dk from per-v-head partials (bf16)
-int prep_tables(const int32_t *cu_dev, int N, int T_fixed, int seg_len, SeqInfo *seq,
-                ChunkInfo *chunk, SegInfo *seg, cudaStream_t st);
+unsigned simt_take_status(cudaStream_t st);  // every CUDA-core translation unit's status word
+int simt_fwd_wide_k(const Params &p, int in_f32, int o_f32, int use_cp, cudaStream_t st);  // K = 192
+int simt_bwd_wide_k(const Params &p, int in_f32, int use_cp, cudaStream_t st);
+unsigned simt_wide_k_take_status(cudaStream_t st);
+int simt_fwd_wide_v(const Params &p, int in_f32, int o_f32, int use_cp, cudaStream_t st);  // V in {192, 256}
+int simt_bwd_wide_v(const Params &p, int in_f32, int use_cp, cudaStream_t st);
+unsigned simt_wide_v_take_status(cudaStream_t st);
 }  // namespace gdr

@@ -1639,9 +1639,11 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_dh_tc(Params p, const __gri
                 }
             }
             // (c) dUt^T[t][r] = (dO^T P)[t][r] + e^{gamma_n - gamma_r} (dS1^T K^T)[t][r]
-            // (rows past the chunk end: 0; P has no entry there)
+            // (rows past the chunk end: 0; P has no entry there); the dUt rows go
+            // out while MMA-c runs, off the chain
             if (!wbwait(bar_m1, cc & 1, cap, abort)) { live = false; break; }
             tc_fence_after();
+            float dux[16];
             {
                 float fe[16];
 #pragma unroll
@@ -1659,14 +1661,11 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_dh_tc(Params p, const __gri
                 split_pairs<8>(x, hv, lv);
                 tmem_st8(tUh + tc0 / 2 + lo, hv);
                 tmem_st8(tUl + tc0 / 2 + lo, lv);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) dux[i] = x[i];
                 tmem_wait_st();
                 tc_fence_before();
                 warp_arrive(bar_ut, lane);
-                if (DM == kDhFull) {  // (after the arrival, off the chain)
-                    const size_t ch = (size_t)c * p.Hv + h;
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) p.dubuf[(ch * 64 + tc0 + i) * 128 + t] = x[i];
-                }
             }
             // (c2) X^T = [scale e^{gamma_s} dO[s][t] | -b_s e^{gamma_s} dR^T[t][s]]
             {
@@ -1701,6 +1700,11 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_dh_tc(Params p, const __gri
             tc_fence_before();
             warp_arrive(bar_x, lane);
             warp_arrive(&empty[s], lane);
+            if (DM == kDhFull) {
+                const size_t ch = (size_t)c * p.Hv + h;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) p.dubuf[(ch * 64 + tc0 + i) * 128 + t] = dux[i];
+            }
         }
         // (a segment of an empty sequence has no chunk: its end state is its start state)
         if (__all_sync(0xffffffffu, live && !*abort) && (nch == 0 || wbwait(bar_m3, (nch - 1) & 1, cap, abort))) {

@@ -32,7 +32,9 @@
  * g is the per-token log-gate (<= 0 in the intended use: a_t in (0, 1]);
  * beta is the write strength as passed (already squashed by the caller).
  *
- * Sizes: K, V in {64, 128}; Hq >= 1; Hv a multiple of Hq; T >= 1.
+ * Sizes: K in {64, 128, 192}, V in {64, 128, 192, 256}; Hq >= 1; Hv a
+ * multiple of Hq; T >= 1.  The tensor-core path takes bf16 inputs with
+ * K = V = 128; every other size and fp32 inputs run on the CUDA cores.
  * Varlen sequences may have length 0 (their final state is h0).
  *
  * Ownership: the caller allocates every buffer, including the workspace
@@ -73,7 +75,7 @@ extern "C" {
 /* return codes */
 #define GDR_OK 0
 #define GDR_ERR_ARG 1       /* null or invalid argument */
-#define GDR_ERR_SHAPE 2     /* unsupported sizes: K,V not in {64,128}, Hv % Hq != 0, ... */
+#define GDR_ERR_SHAPE 2     /* unsupported sizes: K, V outside the sets above, Hv % Hq != 0, ... */
 #define GDR_ERR_DTYPE 3     /* unsupported or mismatched element type */
 #define GDR_ERR_ALIGN 4     /* a pointer not 16-byte aligned */
 #define GDR_ERR_WORKSPACE 5 /* workspace missing or too small */

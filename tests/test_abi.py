@@ -52,7 +52,7 @@ def test_workspace_size_and_chunks(lib):
     assert lib.gdr_bwd_workspace_size(ctypes.byref(shape()), ctypes.byref(B.make_opts())) > sizes(lib, shape())
 
 
-@pytest.mark.parametrize("bad", [dict(K=96), dict(V=32), dict(Hq=3, Hv=4), dict(T=0), dict(B_=0),
+@pytest.mark.parametrize("bad", [dict(K=96), dict(V=32), dict(K=256), dict(V=320), dict(Hq=3, Hv=4), dict(T=0), dict(B_=0),
                                  dict(B_=2, n_seqs=2)])
 def test_bad_shapes_rejected(lib, bad):
     assert sizes(lib, shape(**bad)) == 0

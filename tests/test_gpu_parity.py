@@ -210,3 +210,27 @@ def test_bwd_qk_group_summed_in_place(gdr):
     separate head-order sum)."""
     spec = inputs.small(B=1, T=64 * 152, Hq=1, Hv=4, K=128, V=128, bwd=True)
     _check_bwd(gdr, spec, _path(gdr, "tc", spec))
+
+
+# Head sizes beyond 128 (the CUDA-core path: K up to 192, V up to 256), forward
+# and backward, fp32 and bf16 inputs, with a context-parallel split and packed
+# sequences among the cases.
+WIDE = [(128, 256), (64, 256), (192, 192), (192, 64), (192, 256), (64, 192)]
+
+
+@pytest.mark.parametrize("K,V", WIDE)
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_wide_head_dims(gdr, K, V, dt):
+    spec = inputs.small(B=1, T=150, Hq=1, Hv=2, K=K, V=V, in_dtype=dt, bwd=True)
+    _check_fwd(gdr, spec, gdr.GDR_PATH_AUTO)
+    _check_bwd(gdr, spec, gdr.GDR_PATH_AUTO)
+
+
+@pytest.mark.parametrize("K,V", [(128, 256), (192, 192)])
+def test_wide_head_dims_split_and_varlen(gdr, K, V):
+    spec = inputs.small(B=1, T=64 * 9 + 5, Hq=1, Hv=2, K=K, V=V, bwd=True, name="wide_cp")
+    _check_fwd(gdr, spec, gdr.GDR_PATH_AUTO, cp=3)
+    _check_bwd(gdr, spec, gdr.GDR_PATH_AUTO, cp=3)
+    spec = inputs.small(lengths=(64, 1, 130, 65), Hq=1, Hv=2, K=K, V=V, bwd=True, name="wide_varlen")
+    _check_fwd(gdr, spec, gdr.GDR_PATH_AUTO)
+    _check_bwd(gdr, spec, gdr.GDR_PATH_AUTO)

@@ -105,3 +105,11 @@ def test_bad_arguments():
     bad = B.gdr_shape(1, 64, 3, 4, 128, 128, 0, None, None)
     out = B.gdr_plan()
     assert gdr.load().gdr_get_plan(bad, 0, None, out) == 2
+
+
+@pytest.mark.parametrize("K,V", [(128, 256), (192, 192), (64, 256), (192, 64)])
+def test_wide_head_sizes_take_the_cuda_core_path(K, V):
+    """Head sizes beyond 128 are accepted and planned on the CUDA-core path,
+    bf16 inputs included (the tensor-core path takes K = V = 128 only)."""
+    assert plan(problem(K=K, V=V))["path"] == B.GDR_PATH_SIMT
+    assert plan(problem(K=K, V=V), B.GDR_F32)["path"] == B.GDR_PATH_SIMT

@@ -153,47 +153,52 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn = 0, in
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
-__device__ __forceinline__ void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+// MMA issue.  A warp runs the issuing code (uniform descriptors) and one
+// elected lane issues, four MMAs into d per call, the operand descriptors
+// advanced in place by DA / DB bytes per step (compile-time; the start-address
+// field counts 16-byte units); the first accumulates iff acc.  The issue rate
+// is set by the instructions between the MMAs: measured on one warp, a rolled
+// loop that rebuilds its descriptors took ~165 cycles per MMA, one thread
+// issuing inside a divergent branch ~107, and these forms reach the operand
+// fetch's own rate (~49 cycles for a 128 x 64 x 16 MMA with both operands in
+// shared memory, ~34 with A in tensor memory, the tensor pipe's peak for N >= 128).
+template <uint32_t DA, uint32_t DB>
+__device__ __forceinline__ void mma4_w(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\t"
+        "{\n\t.reg .pred p, q, e;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-        "l"(a), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
-}
-// Warp-wide forms, for code that a whole warp runs: every lane computes the
-// (warp-uniform) descriptors and one elected lane issues the instruction.  A
-// single thread issuing inside a divergent branch took 60-90 cycles per MMA.
-__device__ __forceinline__ void mma_w(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-    asm volatile(
-        "{\n\t.reg .pred p, e;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.eq.b32 q, %4, %4;\n\t"
         "elect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+        "add.s64 %1, %1, %5;\n\tadd.s64 %2, %2, %6;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, q;\n\t"
+        "add.s64 %1, %1, %5;\n\tadd.s64 %2, %2, %6;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, q;\n\t"
+        "add.s64 %1, %1, %5;\n\tadd.s64 %2, %2, %6;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, q;\n\t}"
+        : "+r"(d), "+l"(a), "+l"(b)
+        : "r"(idesc), "r"(acc), "n"(DA >> 4), "n"(DB >> 4)
         : "memory");
 }
-// (the A operand, M = 128 lanes x 16 K as 8 packed bf16-pair columns, read from
-// tensor memory at column address a)
-__device__ __forceinline__ void mma_ts_w(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+// The same with the A operand in tensor memory at column a, advanced by 8
+// columns (16 packed bf16 K values) per step.
+template <uint32_t DB>
+__device__ __forceinline__ void mma4_ts_w(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
     asm volatile(
-        "{\n\t.reg .pred p, e;\n\t"
+        "{\n\t.reg .pred p, q, e;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.eq.b32 q, %4, %4;\n\t"
         "elect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
-        "r"(a), "l"(b), "r"(idesc), "r"(acc)
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+        "add.s32 %1, %1, 8;\n\tadd.s64 %2, %2, %5;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, q;\n\t"
+        "add.s32 %1, %1, 8;\n\tadd.s64 %2, %2, %5;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, q;\n\t"
+        "add.s32 %1, %1, 8;\n\tadd.s64 %2, %2, %5;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, q;\n\t}"
+        : "+r"(d), "+r"(a), "+l"(b)
+        : "r"(idesc), "r"(acc), "n"(DB >> 4)
         : "memory");
-}
-// n MMAs into d, the operand descriptors advanced by da / db bytes per step
-// (the start-address field counts 16-byte units); the first accumulates iff acc.
-__device__ __forceinline__ void mma_seq_w(uint32_t d, uint64_t a, uint32_t da, uint64_t b, uint32_t db, uint32_t idesc,
-                                          int n, bool acc) {
-#pragma unroll 1
-    for (int i = 0; i < n; ++i) {
-        mma_w(d, a, b, idesc, (acc || i > 0) ? 1u : 0u);
-        a += da >> 4;
-        b += db >> 4;
-    }
 }
 __device__ __forceinline__ void mma_commit_w(uint64_t *bar) {
     asm volatile(
@@ -201,10 +206,6 @@ __device__ __forceinline__ void mma_commit_w(uint64_t *bar) {
         "elect.sync _|e, 0xffffffff;\n\t"
         "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(su32(bar))
         : "memory");
-}
-__device__ __forceinline__ void mma_commit(uint64_t *bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(bar))
-                 : "memory");
 }
 
 #define R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), "=r"(r[i + 4]), "=r"(r[i + 5]), \
@@ -536,17 +537,14 @@ __global__ void __launch_bounds__(128, 5) k_chunk_tc(Params p, const __grid_cons
         (tid < 64 ? gam : bet)[t] = x;
     };
     load_gates(hq * G);
-    if (tid == 0) {  // [K ; Q] K^T once the tiles have landed
-        if (bwait(&bars[0], 0, cap, abort)) {
+    if (warp == 0) {  // [K ; Q] K^T once the tiles have landed (the whole warp, one elected lane issues)
+        if (wbwait(&bars[0], 0, cap, abort)) {
             tc_fence_after();
             const uint32_t id = idesc_bf16(128, 64);
             const uint32_t a0 = su32(tile);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                mma(tmem, sdesc(a0 + off), sdesc(a0 + off), id, kk > 0);
-            }
-            mma_commit(&bars[1]);
+            mma4_w<32, 32>(tmem, sdesc(a0), sdesc(a0), id, 0);
+            mma4_w<32, 32>(tmem, sdesc(a0 + 16384), sdesc(a0 + 16384), id, 1);
+            mma_commit_w(&bars[1]);
             mma_issued = true;
         }
     }
@@ -978,57 +976,39 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
                 // MMA1: D1 = S^T K^T over k, 16 k per step (8 packed columns); in
                 // kFwd then (Q S)^T = S^T Q^T from the Q rows (8 KiB into each atom)
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
+                for (int half = 0; half < 2; ++half)
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t ko = (kk & 3) * 32;
-                        mma_ts_w(tD1, (half ? tSl : tSh) + 8 * kk, sdesc(b1 + (kk >> 2) * SL::kAtom + ko), id1,
-                               (half | kk) != 0);
-                    }
-                }
+                    for (int q = 0; q < 2; ++q)
+                        mma4_ts_w<32>(tD1, (half ? tSl : tSh) + 32 * q, sdesc(b1 + q * SL::kAtom), id1, (half | q) != 0);
                 mma_commit_w(bar_m1);
                 if (MODE == kFwd) {
 #pragma unroll
-                    for (int half = 0; half < 2; ++half) {
+                    for (int half = 0; half < 2; ++half)
 #pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
-                            const uint32_t ko = (kk & 3) * 32;
-                            mma_ts_w(tQS, (half ? tSl : tSh) + 8 * kk,
-                                     sdesc(b1 + 8192 + (kk >> 2) * SL::kAtom + ko), id1, (half | kk) != 0);
-                        }
-                    }
+                        for (int q = 0; q < 2; ++q)
+                            mma4_ts_w<32>(tQS, (half ? tSl : tSh) + 32 * q, sdesc(b1 + 8192 + q * SL::kAtom), id1,
+                                          (half | q) != 0);
                     mma_commit_w(bar_m1q);
                 }
                 if (!wbwait(bar_rt, cc & 1, cap, abort)) break;
                 tc_fence_after();
                 {
                     const uint32_t ah = su32(st + SL::kA), al = ah + kImg;
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint32_t o = kk * 32;
-                        mma_ts_w(tD1b, tRh + 8 * kk, sdesc(ah + o), id64, kk > 0);
-                        mma_ts_w(tD1b, tRl + 8 * kk, sdesc(ah + o), id64, 1);
-                        mma_ts_w(tD1b, tRh + 8 * kk, sdesc(al + o), id64, 1);
-                    }
+                    mma4_ts_w<32>(tD1b, tRh, sdesc(ah), id64, 0);
+                    mma4_ts_w<32>(tD1b, tRl, sdesc(ah), id64, 1);
+                    mma4_ts_w<32>(tD1b, tRh, sdesc(al), id64, 1);
                 }
                 mma_commit_w(bar_m1b);
                 if (!wbwait(bar_ut, cc & 1, cap, abort)) break;
                 tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    mma_ts_w(tS, tYh + 8 * kk, sdesc(b1 + kk * 2048, SL::kAtom), id3, 1);
-                    mma_ts_w(tS, tYl + 8 * kk, sdesc(b1 + kk * 2048, SL::kAtom), id3, 1);
-                }
+                mma4_ts_w<2048>(tS, tYh, sdesc(b1, SL::kAtom), id3, 1);
+                mma4_ts_w<2048>(tS, tYl, sdesc(b1, SL::kAtom), id3, 1);
                 mma_commit_w(bar_m3);
                 if (MODE == kFwd) {  // in issue order before MMA1 of the next chunk overwrites Ut^T
                     const uint32_t ph = su32(st + SL::kP), pl = ph + kImg;
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint32_t o = kk * 32;
-                        mma_ts_w(tD2, tUh + 8 * kk, sdesc(ph + o), id64, kk > 0);
-                        mma_ts_w(tD2, tUl + 8 * kk, sdesc(ph + o), id64, 1);
-                        mma_ts_w(tD2, tUh + 8 * kk, sdesc(pl + o), id64, 1);
-                    }
+                    mma4_ts_w<32>(tD2, tUh, sdesc(ph), id64, 0);
+                    mma4_ts_w<32>(tD2, tUl, sdesc(ph), id64, 1);
+                    mma4_ts_w<32>(tD2, tUh, sdesc(pl), id64, 1);
                     mma_commit_w(bar_m2);
                 }
                 mma_commit_w(&empty[s]);
@@ -1513,44 +1493,33 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_dh_tc(Params p, const __gri
                 if (!isN) {
                     // the dO term needs no state: issued as soon as the stage lands
                     const uint32_t dO = su32(st + SL::kdO), ph = su32(st + SL::kP), pl = ph + kImg;
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        mma_w(tD1, sdesc(dO + kk * 2048, 8192), sdesc(ph + kk * 2048, 8192), idOP, kk > 0);
-                        mma_w(tD1, sdesc(dO + kk * 2048, 8192), sdesc(pl + kk * 2048, 8192), idOP, 1);
-                    }
+                    mma4_w<2048, 2048>(tD1, sdesc(dO, 8192), sdesc(ph, 8192), idOP, 0);
+                    mma4_w<2048, 2048>(tD1, sdesc(dO, 8192), sdesc(pl, 8192), idOP, 1);
                 }
                 if (!wbwait(bar_sb, cc & 1, cap, abort)) break;
                 tc_fence_after();
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
+                for (int half = 0; half < 2; ++half)
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t o = (kk >> 2) * 16384 + (kk & 3) * 32;
-                        mma_ts_w(tD2, (half ? tSl : tSh) + 8 * kk, sdesc(kr + o), idK, (half | kk) != 0);
-                    }
-                }
+                    for (int q = 0; q < 2; ++q)
+                        mma4_ts_w<32>(tD2, (half ? tSl : tSh) + 32 * q, sdesc(kr + q * 16384), idK, (half | q) != 0);
                 mma_commit_w(bar_m1);
                 if (!wbwait(bar_ut, cc & 1, cap, abort)) break;
                 tc_fence_after();
                 {
                     const uint32_t ah = su32(st + SL::kA), al = ah + kImg;
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint32_t ob = kk * 2048;
-                        mma_ts_w(tD2, tUh + 8 * kk, sdesc(ah + ob, 8192), idA, kk > 0);
-                        mma_ts_w(tD2, tUl + 8 * kk, sdesc(ah + ob, 8192), idA, 1);
-                        mma_ts_w(tD2, tUh + 8 * kk, sdesc(al + ob, 8192), idA, 1);
-                    }
+                    mma4_ts_w<2048>(tD2, tUh, sdesc(ah, 8192), idA, 0);
+                    mma4_ts_w<2048>(tD2, tUl, sdesc(ah, 8192), idA, 1);
+                    mma4_ts_w<2048>(tD2, tUh, sdesc(al, 8192), idA, 1);
                 }
                 mma_commit_w(bar_m2);
                 if (!wbwait(bar_x, cc & 1, cap, abort)) break;
                 tc_fence_after();
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
+                for (int half = 0; half < 2; ++half)
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_ts_w(tS, (half ? tXl : tXh) + 8 * kk, sdesc(qk + kk * 2048, 16384), idQK, 1);
-                }
+                    for (int q = 0; q < 2; ++q)
+                        mma4_ts_w<2048>(tS, (half ? tXl : tXh) + 32 * q, sdesc(qk + q * 8192, 16384), idQK, 1);
                 mma_commit_w(bar_m3);
                 mma_commit_w(&empty[s]);
             }
@@ -2194,23 +2163,20 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
         {
             tc_fence_after();
             // KS^T = S0^T K^T: A = S0 image MN-major (M = v in two 64-blocks 16 KiB apart), B = K rows
+            #pragma unroll 1
             for (int tm = 0; tm < 2; ++tm)
                 for (int at = 0; at < 2; ++at)
-                    mma_seq_w(tmem + kTbKS, sdesc(sS + tm * 32768 + at * 8192, 16384), 2048,
-                            sdesc(sKQ + at * 16384 + 8192), 32, idesc_bf16(128, 64, 1, 0), 4, (tm | at) != 0);
+                    mma4_w<2048, 32>(tmem + kTbKS, sdesc(sS + tm * 32768 + at * 8192, 16384), sdesc(sKQ + at * 16384 + 8192), idesc_bf16(128, 64, 1, 0), (tm | at) != 0);
             // dQr^T = S0 dO^T: A = S0 image K-major (M = k), B = dO rows
+            #pragma unroll 1
             for (int tm = 0; tm < 2; ++tm)
                 for (int at = 0; at < 2; ++at)
-                    mma_seq_w(tmem + kTbDQ, sdesc(sS + tm * 32768 + at * 16384), 32, sdesc(sOR + at * 16384), 32,
-                            idesc_bf16(128, 64, 0, 0), 4, (tm | at) != 0);
+                    mma4_w<32, 32>(tmem + kTbDQ, sdesc(sS + tm * 32768 + at * 16384), sdesc(sOR + at * 16384), idesc_bf16(128, 64, 0, 0), (tm | at) != 0);
             {  // dR^T = dUt^T A: A operand dUt^T from TMEM, B = A image MN-major (K = s rows)
                 const uint32_t id = idesc_bf16(128, 64, 0, 1);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    mma_ts_w(tmem + kTbDR, tmem + kTbU + 8 * kk, sdesc(sA + kk * 2048), id, kk > 0);
-                    mma_ts_w(tmem + kTbDR, tmem + kTbU + 32 + 8 * kk, sdesc(sA + kk * 2048), id, 1);
-                    mma_ts_w(tmem + kTbDR, tmem + kTbU + 8 * kk, sdesc(sA + 8192 + kk * 2048), id, 1);
-                }
+                mma4_ts_w<2048>(tmem + kTbDR, tmem + kTbU, sdesc(sA), id, 0);
+                mma4_ts_w<2048>(tmem + kTbDR, tmem + kTbU + 32, sdesc(sA), id, 1);
+                mma4_ts_w<2048>(tmem + kTbDR, tmem + kTbU, sdesc(sA + 8192), id, 1);
             }
             mma_commit_w(&bars[1]);
             ++ncommit;
@@ -2279,18 +2245,15 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
         tc_fence_after();
         {  // Ut^T = R^T A^T: A operand R^T from TMEM, B = A image K-major (rows t)
             const uint32_t id = idesc_bf16(128, 64, 0, 0);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                mma_ts_w(tmem + kTbKS, tmem + kTbR + 8 * kk, sdesc(sA + kk * 32), id, kk > 0);
-                mma_ts_w(tmem + kTbKS, tmem + kTbR + 32 + 8 * kk, sdesc(sA + kk * 32), id, 1);
-                mma_ts_w(tmem + kTbKS, tmem + kTbR + 8 * kk, sdesc(sA + 8192 + kk * 32), id, 1);
-            }
+            mma4_ts_w<32>(tmem + kTbKS, tmem + kTbR, sdesc(sA), id, 0);
+            mma4_ts_w<32>(tmem + kTbKS, tmem + kTbR + 32, sdesc(sA), id, 1);
+            mma4_ts_w<32>(tmem + kTbKS, tmem + kTbR, sdesc(sA + 8192), id, 1);
         }
         // dK^T = S0 dKS^T: B = dKS^T image MN-major (K = v rows); terms (hi, hi), (lo, hi), (hi, lo)
+        #pragma unroll 1
         for (int m = 0; m < 3; ++m)
             for (int at = 0; at < 2; ++at)
-                mma_seq_w(tmem + kTbDK, sdesc(sS + (m == 1) * 32768 + at * 16384), 32,
-                        sdesc(sW + (m == 2) * 16384 + at * 8192), 2048, idesc_bf16(128, 64, 0, 1), 4, (m | at) != 0);
+                mma4_w<32, 2048>(tmem + kTbDK, sdesc(sS + (m == 1) * 32768 + at * 16384), sdesc(sW + (m == 2) * 16384 + at * 8192), idesc_bf16(128, 64, 0, 1), (m | at) != 0);
         mma_commit_w(&bars[1]);
         ++ncommit;
     }
@@ -2384,21 +2347,22 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
         tc_fence_after();
         const uint32_t id = idesc_bf16(128, 64, 0, 1);
         // [dO ; dR_hi] (Ut_hi + Ut_lo)^T, and [. ; dR_lo] Ut_hi^T: B = Ut^T image MN-major
+        #pragma unroll 1
         for (int tb = 0; tb < 2; ++tb)
             for (int at = 0; at < 2; ++at)
-                mma_seq_w(tmem + kTbP1, sdesc(sOR + at * 16384), 32, sdesc(sW + tb * 16384 + at * 8192), 2048, id, 4,
-                        (tb | at) != 0);
+                mma4_w<32, 2048>(tmem + kTbP1, sdesc(sOR + at * 16384), sdesc(sW + tb * 16384 + at * 8192), id, (tb | at) != 0);
+        #pragma unroll 1
         for (int at = 0; at < 2; ++at)
-            mma_seq_w(tmem + kTbP1B, sdesc(sRL - 8192 + at * 8192), 32, sdesc(sW + at * 8192), 2048, id, 4, at != 0);
+            mma4_w<32, 2048>(tmem + kTbP1B, sdesc(sRL - 8192 + at * 8192), sdesc(sW + at * 8192), id, at != 0);
         // dK2^T = dS1 Ut^T (over the R^T operand, read by group 2)
+        #pragma unroll 1
         for (int m = 0; m < 3; ++m)
             for (int at = 0; at < 2; ++at)
-                mma_seq_w(tmem + kTbR, sdesc(sS + (m == 1) * 32768 + at * 16384), 32,
-                        sdesc(sW + (m == 2) * 16384 + at * 8192), 2048, id, 4, (m | at) != 0);
+                mma4_w<32, 2048>(tmem + kTbR, sdesc(sS + (m == 1) * 32768 + at * 16384), sdesc(sW + (m == 2) * 16384 + at * 8192), id, (m | at) != 0);
         // [Q ; K] K^T
+        #pragma unroll 1
         for (int at = 0; at < 2; ++at)
-            mma_seq_w(tmem + kTbDR, sdesc(sKQ + at * 16384), 32, sdesc(sKQ + at * 16384 + 8192), 32,
-                    idesc_bf16(128, 64, 0, 0), 4, at != 0);
+            mma4_w<32, 32>(tmem + kTbDR, sdesc(sKQ + at * 16384), sdesc(sKQ + at * 16384 + 8192), idesc_bf16(128, 64, 0, 0), at != 0);
         mma_commit_w(&bars[1]);
         ++ncommit;
     }
@@ -2484,13 +2448,14 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
         // A = K^T or Q^T: the K (Q) rows read MN-major (M = k in two 64-blocks 16 KiB apart)
         const uint64_t aK = sdesc(sKQ + 8192, 16384), aQ = sdesc(sKQ, 16384);
         const uint32_t idK = idesc_bf16(128, 64, 1, 0), idM = idesc_bf16(128, 64, 1, 1);
+        #pragma unroll 1
         for (int tb = 0; tb < 2; ++tb) {
             // dq2^T = K^T dP''^T (B = dP'' rows t, K-major)
-            mma_seq_w(tmem + kTbKS, aK, 2048, sdesc(sW + tb * 8192), 32, idK, 4, tb != 0);
+            mma4_w<2048, 32>(tmem + kTbKS, aK, sdesc(sW + tb * 8192), idK, tb != 0);
             // dK^T += Q^T dP'' (B MN-major), K^T MM^T (B K-major), K^T MM (B MN-major)
-            mma_seq_w(tmem + kTbDK, aQ, 2048, sdesc(sW + tb * 8192), 2048, idM, 4, true);
-            mma_seq_w(tmem + kTbDK, aK, 2048, sdesc(sW + 16384 + tb * 8192), 32, idK, 4, true);
-            mma_seq_w(tmem + kTbDK, aK, 2048, sdesc(sW + 16384 + tb * 8192), 2048, idM, 4, true);
+            mma4_w<2048, 2048>(tmem + kTbDK, aQ, sdesc(sW + tb * 8192), idM, true);
+            mma4_w<2048, 32>(tmem + kTbDK, aK, sdesc(sW + 16384 + tb * 8192), idK, true);
+            mma4_w<2048, 2048>(tmem + kTbDK, aK, sdesc(sW + 16384 + tb * 8192), idM, true);
         }
         mma_commit_w(&bars[1]);
         ++ncommit;

@@ -247,6 +247,24 @@ __device__ __forceinline__ void tmem_ld8_issue(uint32_t ta, uint32_t (&r)[8]) {
                  : "r"(ta));
 }
 __device__ __forceinline__ void tmem_hold8(uint32_t (&r)[8]) { asm volatile("" : W4(0), W4(4)::"memory"); }
+// 16 lanes x 16 columns (lane base in ta, inside the warp's quadrant), as the
+// fragments of 8 x 8 blocks of 16-bit pairs: register 2j holds lane
+// base + lane / 4, column 4 j + lane % 4; register 2j + 1 the lane 8 further.
+// Waits for the load.
+__device__ __forceinline__ void tmem_ld16x128b_x4(uint32_t ta, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.16x128b.x4.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(ta));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" : W4(0), W4(4)::"memory");
+}
+// Four 8 x 8 blocks of 16-bit values, stored transposed: lanes 8 m .. 8 m + 7
+// address the eight 16-byte rows of block m; a thread's register m holds row
+// lane / 4, columns 2 (lane % 4), + 1 of block m before the transpose.
+__device__ __forceinline__ void stmatrix_x4_trans(uint32_t saddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(a),
+                 "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
 // Orders the use of a second load's registers after a wait already issued.
 __device__ __forceinline__ void tmem_st32(uint32_t ta, const uint32_t (&r)[32]) {
     asm volatile(
@@ -1329,10 +1347,12 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
 //                                           issued as soon as the stage lands)
 //   (a)  store dS1; dS1^T -> bf16 hi + lo; dS^T *= e^{gamma_n} in place
 //   MMA-a E  = dS1^T K^T
+//   (b)  X^T dO part = (diag(scale e^gamma) dO)^T -> hi + lo  (no state)
+//   MMA-c (dO half) dS^T += X^T[:, :64] Q  (off the chain: runs while (c) works)
 //   (c)  dUt^T = D1 + E diag(e^{gamma_n - gamma}); store dUt; -> bf16 hi + lo
 //   MMA-b D2 = dUt^T A                     = dR^T  (A read MN-major)
-//   (c2) X^T = [ (diag(scale e^gamma) dO)^T | -(diag(b e^gamma) dR)^T ] -> hi + lo
-//   MMA-c dS^T += X^T [Q ; K]              (the stacked Q, K tile read MN-major)
+//   (c2) X^T dR part = -(diag(b e^gamma) dR)^T -> hi + lo
+//   MMA-c (dR half) dS^T += X^T[:, 64:] K  (Q and K rows of the stacked tile read MN-major)
 // which is dS0 = e^{gamma_n} dS1 + Qt^T dO - W^T dUt with W = A diag(b e^gamma) K.
 //
 // The map dS1 -> dS0 is affine, so the reverse scan splits into segments
@@ -1386,6 +1406,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_dh_tc(Params p, const __gri
     // (kDhFull) every chunk's dS1 image (64 KiB) is staged for one bulk copy
     uint64_t *bar_dfull = bars + 13;  // the epilogue warps have staged a chunk's image
     uint64_t *bar_dfree = bars + 14;  // its copy has read the staging buffer
+    uint64_t *bar_xo = bars + 15;     // the dO part of X^T is in tensor memory
     char *dstage = aux0 + 2 * kAux + 256;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1416,6 +1437,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_dh_tc(Params p, const __gri
         mbar_init(bar_drain, 1);
         mbar_init(bar_dfull, kEpiWarps);
         mbar_init(bar_dfree, 1);
+        mbar_init(bar_xo, kEpiWarps);
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -1504,6 +1526,12 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_dh_tc(Params p, const __gri
                     for (int q = 0; q < 2; ++q)
                         mma4_ts_w<32>(tD2, (half ? tSl : tSh) + 32 * q, sdesc(kr + q * 16384), idK, (half | q) != 0);
                 mma_commit_w(bar_m1);
+                // the dO half of MMA-c (the Q rows of [Q ; K]) needs no state beyond
+                // (a)'s rescaling of dS: it runs while (c) works, off the chain
+                if (!wbwait(bar_xo, cc & 1, cap, abort)) break;
+                tc_fence_after();
+                mma4_ts_w<2048>(tS, tXh, sdesc(qk, 16384), idQK, 1);
+                mma4_ts_w<2048>(tS, tXl, sdesc(qk, 16384), idQK, 1);
                 if (!wbwait(bar_ut, cc & 1, cap, abort)) break;
                 tc_fence_after();
                 {
@@ -1515,11 +1543,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_dh_tc(Params p, const __gri
                 mma_commit_w(bar_m2);
                 if (!wbwait(bar_x, cc & 1, cap, abort)) break;
                 tc_fence_after();
-#pragma unroll
-                for (int half = 0; half < 2; ++half)
-#pragma unroll
-                    for (int q = 0; q < 2; ++q)
-                        mma4_ts_w<2048>(tS, (half ? tXl : tXh) + 32 * q, sdesc(qk + q * 8192, 16384), idQK, 1);
+                mma4_ts_w<2048>(tS, tXh + 32, sdesc(qk + 8192, 16384), idQK, 1);  // the dR half (K rows)
+                mma4_ts_w<2048>(tS, tXl + 32, sdesc(qk + 8192, 16384), idQK, 1);
                 mma_commit_w(bar_m3);
                 mma_commit_w(&empty[s]);
             }
@@ -1582,30 +1607,57 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_dh_tc(Params p, const __gri
                 tmem_wait_st();
                 tc_fence_before();
                 warp_arrive(bar_sb, lane);
-                if (DM == kDhFull) {
-                    // dS1 leaves as the chunk kernel's A operand: a bf16 hi | lo pair of
-                    // 128-byte-swizzled images [2 value halves][128 rows k][64 values],
-                    // 64 KiB per (chunk, v-head), staged here for one bulk copy once the
-                    // previous chunk's copy has read the buffer.  Lanes v, v^1 swap halves
-                    // so that the even lane writes the hi word of the pair, the odd lane
-                    // the lo word.
-                    if (cc > 0 && !wbwait(bar_dfree, (cc - 1) & 1, cap, abort)) { live = false; break; }
-                    const int ve = t & ~1, term = t & 1;
-                    char *img = dstage + term * 32768 + (ve >> 6) * 16384 + (ve & 7) * 2;
-                    const int vc = (ve & 63) >> 3;
-                    // (the bf16 terms are the ones split_pairs packed along k above)
+            }
+            if (DM == kDhFull) {
+                // dS1 leaves as the chunk kernel's A operand: a bf16 hi | lo pair of
+                // 128-byte-swizzled images [2 value halves][128 rows k][64 values],
+                // 64 KiB per (chunk, v-head), staged for one bulk copy once the
+                // previous chunk's copy has read the buffer.  The packed pairs (a) left
+                // in tensor memory come back as 8 x 8 blocks of (v, k-pair) fragments
+                // and leave transposed, each block as eight 16-byte rows k of eight
+                // values v: one image chunk per row.  This warp: lanes v of quadrant
+                // q, k in [sc0, sc0 + 32).
+                if (cc > 0 && !wbwait(bar_dfree, (cc - 1) & 1, cap, abort)) { live = false; break; }
+                const int q = warp & 3, mb = lane >> 3, rr = lane & 7;  // the block row this lane addresses
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int k = sc0 + i;
-                        const uint32_t hb = (i & 1) ? (hv[i >> 1] >> 16) : (hv[i >> 1] & 0xffffu);
-                        const uint32_t lb = (i & 1) ? (lv[i >> 1] >> 16) : (lv[i >> 1] & 0xffffu);
-                        const uint32_t other = __shfl_xor_sync(0xffffffffu, term ? hb : lb, 1);
-                        const uint32_t w = term ? (other | (lb << 16)) : (hb | (other << 16));
-                        *reinterpret_cast<uint32_t *>(img + k * 128 + ((vc ^ (k & 7)) << 4)) = w;
+                for (int term = 0; term < 2; ++term)
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        uint32_t f[8];  // f[2j]: v = 32q + 16hf + lane/4, k pair group j; f[2j+1]: v + 8
+                        tmem_ld16x128b_x4((term ? tSl : tSh) + sc0 / 2 + ((uint32_t)(32 * q + 16 * hf) << 16), f);
+#pragma unroll
+                        for (int jp = 0; jp < 2; ++jp) {  // blocks (v group, k group 2jp), (+1, 2jp), (, 2jp+1), (+1, 2jp+1)
+                            const int v8 = 32 * q + 16 * hf + 8 * (mb & 1);
+                            const int k = sc0 + 8 * (2 * jp + (mb >> 1)) + rr;
+                            const char *row = dstage + term * 32768 + (v8 >> 6) * 16384 + k * 128 +
+                                              ((((v8 & 63) >> 3) ^ (k & 7)) << 4);
+                            stmatrix_x4_trans(su32(row), f[4 * jp], f[4 * jp + 1], f[4 * jp + 2], f[4 * jp + 3]);
+                        }
                     }
-                    fence_async_smem();
-                    warp_arrive(bar_dfull, lane);
+                fence_async_smem();
+                warp_arrive(bar_dfull, lane);
+            }
+            // (b) the dO part of X^T, scale e^{gamma_s} dO[s][t]: read by MMA-c's dO
+            // half, which runs while (c) works (the previous chunk's MMA-c has read
+            // these columns: (a) waited for it)
+            {
+                const char *dO = st + SL::kdO + (t >> 6) * 8192;
+                const int cv = t & 63;
+                float xo[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int s2 = tc0 + i;
+                    const __nv_bfloat16 dv = *reinterpret_cast<const __nv_bfloat16 *>(
+                        dO + s2 * 128 + ((((cv >> 3) ^ (s2 & 7)) << 4) | ((cv & 7) << 1)));
+                    xo[i] = (s2 < len && !isN) ? p.scale * eg[s2] * __bfloat162float(dv) : 0.f;
                 }
+                uint32_t hv[8], lv[8];
+                split_pairs<8>(xo, hv, lv);
+                tmem_st8(tXh + tc0 / 2 + lo, hv);
+                tmem_st8(tXl + tc0 / 2 + lo, lv);
+                tmem_wait_st();
+                tc_fence_before();
+                warp_arrive(bar_xo, lane);
             }
             // (c) dUt^T[t][r] = (dO^T P)[t][r] + e^{gamma_n - gamma_r} (dS1^T K^T)[t][r]
             // (rows past the chunk end: 0; P has no entry there); the dUt rows go
@@ -1636,23 +1688,12 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_dh_tc(Params p, const __gri
                 tc_fence_before();
                 warp_arrive(bar_ut, lane);
             }
-            // (c2) X^T = [scale e^{gamma_s} dO[s][t] | -b_s e^{gamma_s} dR^T[t][s]]
+            // (c2) X^T = [scale e^{gamma_s} dO[s][t] | -b_s e^{gamma_s} dR^T[t][s]]: the dR part
             {
-                const char *dO = st + SL::kdO + (t >> 6) * 8192;
-                const int cv = t & 63;
-                float xo[16], fr[16];
+                float fr[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int s2 = tc0 + i;
-                    const __nv_bfloat16 dv = *reinterpret_cast<const __nv_bfloat16 *>(
-                        dO + s2 * 128 + ((((cv >> 3) ^ (s2 & 7)) << 4) | ((cv & 7) << 1)));
-                    xo[i] = (s2 < len && !isN) ? p.scale * eg[s2] * __bfloat162float(dv) : 0.f;
-                    fr[i] = -bet[s2] * eg[s2];
-                }
+                for (int i = 0; i < 16; ++i) fr[i] = -bet[tc0 + i] * eg[tc0 + i];
                 uint32_t hv[8], lv[8];
-                split_pairs<8>(xo, hv, lv);
-                tmem_st8(tXh + tc0 / 2 + lo, hv);
-                tmem_st8(tXl + tc0 / 2 + lo, lv);
                 if (!wbwait(bar_m2, cc & 1, cap, abort)) { live = false; break; }
                 tc_fence_after();
                 uint32_t r[16];

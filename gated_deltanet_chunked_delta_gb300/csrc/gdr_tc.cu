@@ -249,13 +249,12 @@ __device__ __forceinline__ void tmem_ld8_issue(uint32_t ta, uint32_t (&r)[8]) {
 __device__ __forceinline__ void tmem_hold8(uint32_t (&r)[8]) { asm volatile("" : W4(0), W4(4)::"memory"); }
 // 16 lanes x 16 columns (lane base in ta, inside the warp's quadrant), as the
 // fragments of 8 x 8 blocks of 16-bit pairs: register 2j holds lane
-// base + lane / 4, column 4 j + lane % 4; register 2j + 1 the lane 8 further.
-// Waits for the load.
-__device__ __forceinline__ void tmem_ld16x128b_x4(uint32_t ta, uint32_t (&r)[8]) {
+// base + lane / 4, column 4 j + lane % 4; register 2j + 1 the lane 8 further
+// (issue only: tcgen05.wait::ld before use).
+__device__ __forceinline__ void tmem_ld16x128b_x4_issue(uint32_t ta, uint32_t *r) {
     asm volatile("tcgen05.ld.sync.aligned.16x128b.x4.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
                  : "r"(ta));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" : W4(0), W4(4)::"memory");
 }
 // Four 8 x 8 blocks of 16-bit values, stored transposed: lanes 8 m .. 8 m + 7
 // address the eight 16-byte rows of block m; a thread's register m holds row
@@ -264,6 +263,47 @@ __device__ __forceinline__ void stmatrix_x4_trans(uint32_t saddr, uint32_t a, ui
     asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(a),
                  "r"(b), "r"(c), "r"(d)
                  : "memory");
+}
+// A state handed to the chunk-gradient kernel as its MMA operand: the bf16
+// hi | lo pair of 128-byte-swizzled images [2 terms][2 value halves][128 rows
+// k][64 values v] (64 KiB).  A scan's state warp holds, in tensor memory, the
+// packed hi | lo words (k pairs) of the state columns k in [sc0, sc0 + 32) for
+// the 32 lanes v of its quadrant q; state_frag_ld reads them back as 8 x 8
+// blocks of (v, k-pair) fragments, state_frag_st writes each block transposed
+// as eight 16-byte rows k of eight values v (one image chunk per row).
+struct StateFrags {
+    uint32_t f[2][2][8];  // [term][16-lane half][fragments]
+};
+__device__ __forceinline__ void state_frag_ld(uint32_t tSh, uint32_t tSl, int sc0, int q, StateFrags &x) {
+#pragma unroll
+    for (int term = 0; term < 2; ++term)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf)
+            tmem_ld16x128b_x4_issue((term ? tSl : tSh) + sc0 / 2 + ((uint32_t)(32 * q + 16 * hf) << 16),
+                                    x.f[term][hf]);
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int term = 0; term < 2; ++term)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf)
+            asm volatile("" : "+r"(x.f[term][hf][0]), "+r"(x.f[term][hf][1]), "+r"(x.f[term][hf][2]),
+                         "+r"(x.f[term][hf][3]), "+r"(x.f[term][hf][4]), "+r"(x.f[term][hf][5]),
+                         "+r"(x.f[term][hf][6]), "+r"(x.f[term][hf][7])::"memory");
+}
+__device__ __forceinline__ void state_frag_st(char *img, int sc0, int q, int lane, const StateFrags &x) {
+    const int mb = lane >> 3, rr = lane & 7;  // the block and row this lane addresses
+#pragma unroll
+    for (int term = 0; term < 2; ++term)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+            for (int jp = 0; jp < 2; ++jp) {  // blocks (v group, k group 2 jp), (+1, 2 jp), (, 2 jp + 1), (+1, 2 jp + 1)
+                const int v8 = 32 * q + 16 * hf + 8 * (mb & 1);
+                const int k = sc0 + 8 * (2 * jp + (mb >> 1)) + rr;
+                const char *row = img + term * 32768 + (v8 >> 6) * 16384 + k * 128 + ((((v8 & 63) >> 3) ^ (k & 7)) << 4);
+                const uint32_t *f = x.f[term][hf];
+                stmatrix_x4_trans(su32(row), f[4 * jp], f[4 * jp + 1], f[4 * jp + 2], f[4 * jp + 3]);
+            }
 }
 // Orders the use of a second load's registers after a wait already issued.
 __device__ __forceinline__ void tmem_st32(uint32_t ta, const uint32_t (&r)[32]) {
@@ -816,8 +856,9 @@ template <int MODE, typename TO>
 __host__ __device__ constexpr int scan_out_bytes() {
     return MODE == kFwd ? 64 * 128 * (int)sizeof(TO) : 0;
 }
-// The state recompute stages each chunk's start state ([128 k][128 v] fp32)
-// for one bulk copy to the workspace, off the chain.
+// The state recompute stages each chunk's start state (the bf16 hi | lo image
+// the chunk-gradient kernel reads, 64 KiB) for one bulk copy to the workspace,
+// off the chain.
 template <int MODE>
 __host__ __device__ constexpr int scan_hstage_bytes() {
     return MODE == kStates ? 65536 : 0;
@@ -856,7 +897,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
     uint64_t *bar_hfree = bars + 18;  // (kStates) its bulk copy has read the staging buffer
     uint64_t *bar_m1q = bars + 19;    // (kFwd) the (Q S)^T half of MMA1 done
     uint64_t *bar_d2r = bars + 20;    // (kFwd) the output warps have read (P Ut)^T
-    float *hstage = reinterpret_cast<float *>(aux0 + 2 * kAux + 256);  // (kStates) [128 k][128 v]
+    char *hstage = aux0 + 2 * kAux + 256;  // (kStates) a chunk's start state as the bf16 hi | lo image
+    uint64_t *bar_sld = bars + 21;    // (kStates) every state warp has read its packed words back for the staging
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int sidx = blockIdx.x, h = blockIdx.y;
@@ -894,6 +936,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
         mbar_init(bar_m2, 1);
         mbar_init(bar_hfull, kEpiWarps);
         mbar_init(bar_hfree, 1);
+        mbar_init(bar_sld, kEpiWarps);
         mbar_init(bar_m1q, 1);
         mbar_init(bar_d2r, kEpiWarps / 2);
         *abort = 0;
@@ -1183,7 +1226,6 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
             // (a) S^T -> packed bf16 hi | lo A operands; S^T *= e^{gamma_n}.  With
             // one 32-column block per thread the state goes out to h after the
             // arrival, off the chain
-            float fh[32];
             {
                 const float dec = eg[63];
 #pragma unroll 1
@@ -1198,10 +1240,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
                     split_pairs<16>(f, hv, lv);
                     tmem_st16(tSh + k0 / 2 + lo, hv);
                     tmem_st16(tSl + k0 / 2 + lo, lv);
-                    if (kSC == 32) {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) fh[i] = f[i];
-                    } else if (hdst && cc >= Wc) {
+                    if (MODE == kFwd && hdst && cc >= Wc) {
 #pragma unroll
                         for (int i = 0; i < 32; ++i) hdst[(((size_t)c * p.Hv + h) * 128 + k0 + i) * 128 + t] = f[i];
                     }
@@ -1214,11 +1253,17 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
             tc_fence_before();
             warp_arrive(bar_sb, lane);
             if (MODE == kStates && hdst && cc >= Wc) {
-                // staged for the bulk copy once the previous chunk's has read the buffer
+                // the start state leaves as the chunk-gradient kernel's A operand (64 KiB
+                // image), staged for one bulk copy once the previous chunk's copy has
+                // read the buffer; (c) of every warp waits for bar_sld before it writes
+                // R^T over the packed words read back here
                 const int j = cc - Wc;
+                StateFrags fr;
+                state_frag_ld(tSh, tSl, sc0, warp & 3, fr);
+                tc_fence_before();
+                warp_arrive(bar_sld, lane);
                 if (j > 0 && !wbwait(bar_hfree, (j - 1) & 1, cap, abort)) { live = false; break; }
-#pragma unroll
-                for (int i = 0; i < 32; ++i) hstage[(sc0 + i) * 128 + t] = fh[i];
+                state_frag_st(hstage, sc0, warp & 3, lane, fr);
                 fence_async_smem();
                 warp_arrive(bar_hfull, lane);
             }
@@ -1237,6 +1282,10 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_scan_tc(Params p, const __g
                 for (int j = 0; j < kTC / 16; ++j) tmem_ld16_issue(tD1 + tc0 + 16 * j + lo, *reinterpret_cast<uint32_t(*)[16]>(r + 16 * j));
                 tmem_wait_ld16(*reinterpret_cast<uint32_t(*)[16]>(r));
                 if constexpr (kTC > 16) tmem_hold16(*reinterpret_cast<uint32_t(*)[16]>(r + 16));
+                if (MODE == kStates && hdst && cc >= Wc) {  // R^T goes over the staged state's packed words
+                    if (!wbwait(bar_sld, (cc - Wc) & 1, cap, abort)) { live = false; break; }
+                    tc_fence_after();
+                }
 #pragma unroll
                 for (int j = 0; j < kTC / 16; ++j) {
                     float x[16];
@@ -1407,6 +1456,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_dh_tc(Params p, const __gri
     uint64_t *bar_dfull = bars + 13;  // the epilogue warps have staged a chunk's image
     uint64_t *bar_dfree = bars + 14;  // its copy has read the staging buffer
     uint64_t *bar_xo = bars + 15;     // the dO part of X^T is in tensor memory
+    uint64_t *bar_sld = bars + 16;    // (kDhFull) every warp has read its dS1 words back for the staging
     char *dstage = aux0 + 2 * kAux + 256;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1438,6 +1488,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_dh_tc(Params p, const __gri
         mbar_init(bar_dfull, kEpiWarps);
         mbar_init(bar_dfree, 1);
         mbar_init(bar_xo, kEpiWarps);
+        mbar_init(bar_sld, kEpiWarps);
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -1609,31 +1660,16 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_dh_tc(Params p, const __gri
                 warp_arrive(bar_sb, lane);
             }
             if (DM == kDhFull) {
-                // dS1 leaves as the chunk kernel's A operand: a bf16 hi | lo pair of
-                // 128-byte-swizzled images [2 value halves][128 rows k][64 values],
-                // 64 KiB per (chunk, v-head), staged for one bulk copy once the
-                // previous chunk's copy has read the buffer.  The packed pairs (a) left
-                // in tensor memory come back as 8 x 8 blocks of (v, k-pair) fragments
-                // and leave transposed, each block as eight 16-byte rows k of eight
-                // values v: one image chunk per row.  This warp: lanes v of quadrant
-                // q, k in [sc0, sc0 + 32).
+                // dS1 leaves as the chunk kernel's A operand (64 KiB image), staged for
+                // one bulk copy once the previous chunk's copy has read the buffer.
+                // Its packed words are read back before bar_sld: (c) of every warp
+                // waits for it before it writes dUt over them.
+                StateFrags fr;
+                state_frag_ld(tSh, tSl, sc0, warp & 3, fr);
+                tc_fence_before();
+                warp_arrive(bar_sld, lane);
                 if (cc > 0 && !wbwait(bar_dfree, (cc - 1) & 1, cap, abort)) { live = false; break; }
-                const int q = warp & 3, mb = lane >> 3, rr = lane & 7;  // the block row this lane addresses
-#pragma unroll
-                for (int term = 0; term < 2; ++term)
-#pragma unroll
-                    for (int hf = 0; hf < 2; ++hf) {
-                        uint32_t f[8];  // f[2j]: v = 32q + 16hf + lane/4, k pair group j; f[2j+1]: v + 8
-                        tmem_ld16x128b_x4((term ? tSl : tSh) + sc0 / 2 + ((uint32_t)(32 * q + 16 * hf) << 16), f);
-#pragma unroll
-                        for (int jp = 0; jp < 2; ++jp) {  // blocks (v group, k group 2jp), (+1, 2jp), (, 2jp+1), (+1, 2jp+1)
-                            const int v8 = 32 * q + 16 * hf + 8 * (mb & 1);
-                            const int k = sc0 + 8 * (2 * jp + (mb >> 1)) + rr;
-                            const char *row = dstage + term * 32768 + (v8 >> 6) * 16384 + k * 128 +
-                                              ((((v8 & 63) >> 3) ^ (k & 7)) << 4);
-                            stmatrix_x4_trans(su32(row), f[4 * jp], f[4 * jp + 1], f[4 * jp + 2], f[4 * jp + 3]);
-                        }
-                    }
+                state_frag_st(dstage, sc0, warp & 3, lane, fr);
                 fence_async_smem();
                 warp_arrive(bar_dfull, lane);
             }
@@ -1680,6 +1716,10 @@ __global__ void __launch_bounds__(kScanThreads, 1) k_dh_tc(Params p, const __gri
                     x[i] = fe[i] * __uint_as_float(r[i]) + (isN ? 0.f : __uint_as_float(ro[i]));
                 uint32_t hv[8], lv[8];
                 split_pairs<8>(x, hv, lv);
+                if (DM == kDhFull) {
+                    if (!wbwait(bar_sld, cc & 1, cap, abort)) { live = false; break; }
+                    tc_fence_after();
+                }
                 tmem_st8(tUh + tc0 / 2 + lo, hv);
                 tmem_st8(tUl + tc0 / 2 + lo, lv);
 #pragma unroll
@@ -1960,7 +2000,7 @@ __global__ void __launch_bounds__(512) k_combine_tc(Params p) {
 // ---------------------------------------------------------------------------
 struct BcMaps {
     CUtensorMap Q, K, dO;  // 3-D (x, head, token), box 64 x 1 x 64, 128-byte swizzle
-    CUtensorMap S0, dU;    // fp32 3-D (v, k or t, unit), box 32 x 128 (64) x 1, 128-byte swizzle
+    CUtensorMap dU;        // fp32 3-D (v, t, unit), box 32 x 64 x 1, 128-byte swizzle
     CUtensorMap A;         // fp32 3-D (s, head, token), box 32 x 1 x 64, 128-byte swizzle
     CUtensorMap V;         // 3-D (v, head, token), box 128 x 1 x 64, plain rows
 };
@@ -2089,8 +2129,7 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
         tma3d(sm + kBcV, &maps.V, 0, hn, tk, &bars[0]);
     };
     auto copy_S0_dO = [&](int un, int hn, int hqn, int tk) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) tma3d(Sim + q * 16384, &maps.S0, 32 * q, 0, un, &bars[0]);
+        bulk_g2s(Sim, reinterpret_cast<const char *>(p.hbuf) + (size_t)un * 65536, 65536, &bars[0]);  // the S0 image
         tma3d(OR, &maps.dO, 0, hn, tk, &bars[0]);
         tma3d(OR + 16384, &maps.dO, 64, hn, tk, &bars[0]);
     };
@@ -2136,21 +2175,13 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
     if (__syncthreads_or(!ok)) goto out;
     if (tid == 0) pf_phase = -1;
     {
-        // This unit's copies have landed (128-byte-swizzled fp32 rows: 16-byte
-        // chunk j of row r at j ^ (r % 8)).  Every thread reads its share into
-        // registers, then, after a barrier, writes the bf16 hi | lo images over
-        // them: one S0 item (row k, 32 columns), the A row half (threads
-        // 0-127; rows past the chunk end become identity rows), the dUt^T column.
-        const int k = tid & 127, sq = tid >> 7;  // a warp: 32 consecutive rows of one quarter
-        float xs[32], xa[32], du[16];
-        {
-            const char *src = Sim + sq * 16384 + k * 128;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float4 v = *reinterpret_cast<const float4 *>(src + ((j ^ (k & 7)) << 4));
-                xs[4 * j] = v.x; xs[4 * j + 1] = v.y; xs[4 * j + 2] = v.z; xs[4 * j + 3] = v.w;
-            }
-        }
+        // This unit's copies have landed: S0 as the bf16 hi | lo image the state
+        // recompute staged, the A rows and dUt as 128-byte-swizzled fp32 rows
+        // (16-byte chunk j of row r at j ^ (r % 8)).  Every thread reads its share
+        // of those into registers, then, after a barrier, writes the A image over
+        // them (threads 0-127; rows past the chunk end become identity rows) and
+        // its dUt^T column into tensor memory.
+        float xa[32], du[16];
         const int rr = tid & 63, ah = (tid >> 6) & 1;
         if (tid < 128) {
             const char *src = Aim + ah * 8192 + rr * 128;
@@ -2185,7 +2216,6 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
             gam[2 * lane] = sc - b;
             gam[2 * lane + 1] = sc;
         }
-        st_img_hl(Sim + (sq >> 1) * 16384, Sim + 32768 + (sq >> 1) * 16384, k, 32 * (sq & 1), xs);
         if (tid < 128) st_img_hl(Aim, Aim + 8192, rr, 32 * ah, xa);
         uint32_t hv[8], lv[8];
         split_pairs<8>(du, hv, lv);
@@ -2765,7 +2795,6 @@ int launch_bwd_chunk(const Params &p, cudaStream_t st) {
     BcMaps maps;
     if (!map3(&maps.Q, p.q, p.Hq, p.Ttot, 64, true) || !map3(&maps.K, p.k, p.Hq, p.Ttot, 64, true) ||
         !map3(&maps.dO, p.dout, p.Hv, p.Ttot, 64, true) ||
-        !mapf32(&maps.S0, p.hbuf, 128, 128, NU, 512, 65536, 32, 128, 1) ||
         !mapf32(&maps.dU, p.dubuf, 128, 64, NU, 512, 32768, 32, 64, 1) ||
         !mapf32(&maps.A, p.A_in, 64, p.Hv, p.Ttot, 256, (cuuint64_t)p.Hv * 256, 32, 1, 64) ||
         !map3(&maps.V, p.v, p.Hv, p.Ttot, 128, false))

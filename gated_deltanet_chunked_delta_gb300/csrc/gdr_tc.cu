@@ -2261,6 +2261,7 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
     if (__syncthreads_or(!ok)) goto out;
     tc_fence_after();
     // ---------------- epilogue 1 ----------------
+    float a1[16], a2[16];  // this thread's terms of the row sums dR.V, dR.KS (summed while group 2 runs)
     {
         // lane v: R^T, dv, dKS^T, dR (as rows of the [dO ; dR] operand), row sums dR.V, dR.KS
         const int v = row_v;
@@ -2279,7 +2280,6 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
             tmem_st8(tmem + kTbR + t0 / 2 + lq, hv);
             tmem_st8(tmem + kTbR + 32 + t0 / 2 + lq, lv);
         }
-        float a1[16], a2[16];
         __nv_bfloat16 *dvo = reinterpret_cast<__nv_bfloat16 *>(p.dv) + ((size_t)tok0 * p.Hv + h) * 128 + v;
         // rows 64 + t of the v half's [dO ; dR_hi] atom and row t of its dR_lo atom;
         // t0 is a multiple of 8, so row t's 16-byte chunk is (v % 64) / 8 ^ (j % 8)
@@ -2300,12 +2300,6 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
             *reinterpret_cast<__nv_bfloat16 *>(orl + off) = __float2bfloat16_rn(dr - __uint_as_float(hw << 16));
         }
         st_img_hl16(Wim, Wim + 16384, v, t0, x);  // dKS^T row v
-        const float s1 = warp_rs16(a1, lane);
-        const float s2 = warp_rs16(a2, lane);
-        if (lane < 16) {
-            atomicAdd(&rRV[t0 + lane], s1);
-            atomicAdd(&rRKS[t0 + lane], s2);
-        }
     }
     tmem_wait_st();
     fence_async_smem();
@@ -2328,7 +2322,16 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
         mma_commit_w(&bars[1]);
         ++ncommit;
     }
-    // while group 2 runs: row sums dQr.Q (dQr^T stays in TMEM until the end)
+    // while group 2 runs: row sums dR.V, dR.KS (epilogue 1's terms) and dQr.Q
+    // (dQr^T stays in TMEM until the end)
+    {
+        const float s1 = warp_rs16(a1, lane);
+        const float s2 = warp_rs16(a2, lane);
+        if (lane < 16) {
+            atomicAdd(&rRV[t0 + lane], s1);
+            atomicAdd(&rRKS[t0 + lane], s2);
+        }
+    }
     {
         // lane k: row sums dQr.Q (Q from the [Q ; K] image)
         const int k = row_v;
@@ -2388,28 +2391,6 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
     }
     ok = bwait(&bars[6], (ds1_parity++) & 1, cap, abort);
     if (__syncthreads_or(!ok)) goto out;
-    {
-        const int k = tid & 127, sq = tid >> 7;
-        const char *ih = Sim + (sq >> 1) * 16384 + k * 128, *il = ih + 32768;
-        const int c0 = 32 * (sq & 1);
-        float part = 0.f;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int off = ((((c0 >> 3) + j) ^ (k & 7)) << 4);
-            const uint4 wh = *reinterpret_cast<const uint4 *>(ih + off);
-            const uint4 wl = *reinterpret_cast<const uint4 *>(il + off);
-            const uint32_t dh[4] = {wh.x, wh.y, wh.z, wh.w}, dl[4] = {wl.x, wl.y, wl.z, wl.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const uint32_t sh = s0w[8 * j + e], sl = s0w[8 * j + 4 + e];
-                part += (bf_lo(dh[e]) + bf_lo(dl[e])) * (bf_lo(sh) + bf_lo(sl)) +
-                        (bf_hi(dh[e]) + bf_hi(dl[e])) * (bf_hi(sh) + bf_hi(sl));
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-        if (lane == 0) atomicAdd(&red[0], part);
-    }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -2436,6 +2417,31 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
             mma4_w<32, 32>(tmem + kTbDR, sdesc(sKQ + at * 16384), sdesc(sKQ + at * 16384 + 8192), idesc_bf16(128, 64, 0, 0), at != 0);
         mma_commit_w(&bars[1]);
         ++ncommit;
+    }
+    {
+        // while group 3 runs: <dS1, S0> (this thread's S0 terms, read before the
+        // dS1 image was copied over them, against the dS1 terms; group 3 reads
+        // the same image)
+        const int k = tid & 127, sq = tid >> 7;
+        const char *ih = Sim + (sq >> 1) * 16384 + k * 128, *il = ih + 32768;
+        const int c0 = 32 * (sq & 1);
+        float part = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int off = ((((c0 >> 3) + j) ^ (k & 7)) << 4);
+            const uint4 wh = *reinterpret_cast<const uint4 *>(ih + off);
+            const uint4 wl = *reinterpret_cast<const uint4 *>(il + off);
+            const uint32_t dh[4] = {wh.x, wh.y, wh.z, wh.w}, dl[4] = {wl.x, wl.y, wl.z, wl.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const uint32_t sh = s0w[8 * j + e], sl = s0w[8 * j + 4 + e];
+                part += (bf_lo(dh[e]) + bf_lo(dl[e])) * (bf_lo(sh) + bf_lo(sl)) +
+                        (bf_hi(dh[e]) + bf_hi(dl[e])) * (bf_hi(sh) + bf_hi(sl));
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+        if (lane == 0) atomicAdd(&red[0], part);
     }
     {
         // while group 3 runs: row sums dUt.Ut (lane v; dUt^T packed in TMEM, Ut^T in TMEM)
@@ -2531,6 +2537,38 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
         mma_commit_w(&bars[1]);
         ++ncommit;
     }
+    // ---------------- gate and beta gradients, while group 4 runs: every row
+    // and column sum they read is complete (epilogues 1-3 and the windows of
+    // groups 2 and 3) ----------------
+    if (tid < 64) {
+        const int r = tid;
+        const float br = bet[r], egr = egv[r];
+        const float db = rRV[r] - egr * rRKS[r] + rLK[r];
+        const float dgam = -br * egr * rRKS[r] - rUdU[r] + p.scale * egr * rQdq[r] + rP[r] + br * rLK[r] - cL[r];
+        if (r < len) p.dbeta[(size_t)(tok0 + r) * p.Hv + h] = db;
+        dgm[r] = r < len ? dgam : 0.f;
+        tnp[r] = rUdU[r] - rP[r];
+    }
+    __syncthreads();
+    if (tid < 32) {
+        // dgamma_n collects e^{gamma_n} <dS1, S0> and the rows' shares; dg is the
+        // reverse cumulative sum of dgamma over the chunk
+        float tn = tnp[2 * lane] + tnp[2 * lane + 1];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) tn += __shfl_xor_sync(0xffffffffu, tn, o);
+        tn += __expf(gam[63]) * red[0];
+        float a = dgm[2 * lane], b = dgm[2 * lane + 1];
+        if (2 * lane == len - 1) a += tn;
+        if (2 * lane + 1 == len - 1) b += tn;
+        float s = a + b;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float n = __shfl_down_sync(0xffffffffu, s, o);
+            if (lane + o < 32) s += n;
+        }
+        if (2 * lane < len) p.dg[(size_t)(tok0 + 2 * lane) * p.Hv + h] = s;
+        if (2 * lane + 1 < len) p.dg[(size_t)(tok0 + 2 * lane + 1) * p.Hv + h] = s - a;
+    }
     ok = bwait(&bars[1], 1, cap, abort);
     if (__syncthreads_or(!ok)) goto out;
     tc_fence_after();
@@ -2612,36 +2650,6 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
                     dko[o] = __float2bfloat16_rn(dkv[j]);
                 }
         }
-    }
-    // ---------------- gate and beta gradients ----------------
-    if (tid < 64) {
-        const int r = tid;
-        const float br = bet[r], egr = egv[r];
-        const float db = rRV[r] - egr * rRKS[r] + rLK[r];
-        const float dgam = -br * egr * rRKS[r] - rUdU[r] + p.scale * egr * rQdq[r] + rP[r] + br * rLK[r] - cL[r];
-        if (r < len) p.dbeta[(size_t)(tok0 + r) * p.Hv + h] = db;
-        dgm[r] = r < len ? dgam : 0.f;
-        tnp[r] = rUdU[r] - rP[r];
-    }
-    __syncthreads();
-    if (tid < 32) {
-        // dgamma_n collects e^{gamma_n} <dS1, S0> and the rows' shares; dg is the
-        // reverse cumulative sum of dgamma over the chunk
-        float tn = tnp[2 * lane] + tnp[2 * lane + 1];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) tn += __shfl_xor_sync(0xffffffffu, tn, o);
-        tn += __expf(gam[63]) * red[0];
-        float a = dgm[2 * lane], b = dgm[2 * lane + 1];
-        if (2 * lane == len - 1) a += tn;
-        if (2 * lane + 1 == len - 1) b += tn;
-        float s = a + b;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const float n = __shfl_down_sync(0xffffffffu, s, o);
-            if (lane + o < 32) s += n;
-        }
-        if (2 * lane < len) p.dg[(size_t)(tok0 + 2 * lane) * p.Hv + h] = s;
-        if (2 * lane + 1 < len) p.dg[(size_t)(tok0 + 2 * lane + 1) * p.Hv + h] = s - a;
     }
     }  // units
 out:

@@ -2177,24 +2177,15 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
     {
         // This unit's copies have landed: S0 as the bf16 hi | lo image the state
         // recompute staged, the A rows and dUt as 128-byte-swizzled fp32 rows
-        // (16-byte chunk j of row r at j ^ (r % 8)).  Every thread reads its share
-        // of those into registers, then, after a barrier, writes the A image over
-        // them (threads 0-127; rows past the chunk end become identity rows) and
-        // its dUt^T column into tensor memory.
-        float xa[32], du[16];
-        const int rr = tid & 63, ah = (tid >> 6) & 1;
-        if (tid < 128) {
-            const char *src = Aim + ah * 8192 + rr * 128;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float4 v = *reinterpret_cast<const float4 *>(src + ((j ^ (rr & 7)) << 4));
-                xa[4 * j] = v.x; xa[4 * j + 1] = v.y; xa[4 * j + 2] = v.z; xa[4 * j + 3] = v.w;
-            }
-            if (rr >= len)
-#pragma unroll
-                for (int j = 0; j < 32; ++j) xa[j] = (32 * ah + j == rr) ? 1.f : 0.f;
-        }
+        // (16-byte chunk j of row r at j ^ (r % 8)).  Every thread moves its dUt^T
+        // column into tensor memory; warps 4-7 read the A rows and, after a
+        // barrier of their own, write the A image over them (rows past the chunk
+        // end become identity rows); warp 1 takes the gate cumsum.  Warp 0 first
+        // moves its dUt column, then issues the part of group 1 that needs none of
+        // this (KS^T and dQr^T read the S0 image and the K and dO tiles as they
+        // landed), so those MMAs run while the others convert.
         {
+            float du[16];
             const int v = row_v;
             const char *src = Wim + (v >> 5) * 8192 + (v & 3) * 4;
 #pragma unroll
@@ -2203,9 +2194,41 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
                 du[j] = t < len ? *reinterpret_cast<const float *>(src + t * 128 + ((((v & 31) >> 2) ^ (t & 7)) << 4))
                                 : 0.f;
             }
+            uint32_t hv[8], lv[8];
+            split_pairs<8>(du, hv, lv);
+            tmem_st8(tmem + kTbU + t0 / 2 + lq, hv);
+            tmem_st8(tmem + kTbU + 32 + t0 / 2 + lq, lv);
+            tmem_wait_st();
         }
-        __syncthreads();  // every raw row read
-        if (tid < 32) {  // inclusive cumsum of the gates, two per lane
+        if (warp == 0) {  // group 1, first part (the whole warp; one elected lane issues)
+            tc_fence_after();
+            // KS^T = S0^T K^T: A = S0 image MN-major (M = v in two 64-blocks 16 KiB apart), B = K rows
+#pragma unroll 1
+            for (int tm = 0; tm < 2; ++tm)
+                for (int at = 0; at < 2; ++at)
+                    mma4_w<2048, 32>(tmem + kTbKS, sdesc(sS + tm * 32768 + at * 8192, 16384),
+                                     sdesc(sKQ + at * 16384 + 8192), idesc_bf16(128, 64, 1, 0), (tm | at) != 0);
+            // dQr^T = S0 dO^T: A = S0 image K-major (M = k), B = dO rows
+#pragma unroll 1
+            for (int tm = 0; tm < 2; ++tm)
+                for (int at = 0; at < 2; ++at)
+                    mma4_w<32, 32>(tmem + kTbDQ, sdesc(sS + tm * 32768 + at * 16384), sdesc(sOR + at * 16384),
+                                   idesc_bf16(128, 64, 0, 0), (tm | at) != 0);
+        } else if (warp >= 4 && warp < 8) {
+            const int a = tid - 128, rr = a & 63, ah = (a >> 6) & 1;
+            float xa[32];
+            const char *src = Aim + ah * 8192 + rr * 128;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float4 v4 = *reinterpret_cast<const float4 *>(src + ((j ^ (rr & 7)) << 4));
+                xa[4 * j] = v4.x; xa[4 * j + 1] = v4.y; xa[4 * j + 2] = v4.z; xa[4 * j + 3] = v4.w;
+            }
+            if (rr >= len)
+#pragma unroll
+                for (int j = 0; j < 32; ++j) xa[j] = (32 * ah + j == rr) ? 1.f : 0.f;
+            asm volatile("bar.sync 1, 128;" ::: "memory");  // every raw A row read (warps 4-7)
+            st_img_hl(Aim, Aim + 8192, rr, 32 * ah, xa);
+        } else if (warp == 1) {  // inclusive cumsum of the gates, two per lane
             const float a = gam[2 * lane], b = gam[2 * lane + 1];
             float sc = a + b;
 #pragma unroll
@@ -2216,12 +2239,6 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
             gam[2 * lane] = sc - b;
             gam[2 * lane + 1] = sc;
         }
-        if (tid < 128) st_img_hl(Aim, Aim + 8192, rr, 32 * ah, xa);
-        uint32_t hv[8], lv[8];
-        split_pairs<8>(du, hv, lv);
-        tmem_st8(tmem + kTbU + t0 / 2 + lq, hv);
-        tmem_st8(tmem + kTbU + 32 + t0 / 2 + lq, lv);
-        tmem_wait_st();
     }
     __syncthreads();  // gates
     if (tid < 64) egv[tid] = __expf(gam[tid]);
@@ -2229,29 +2246,17 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
     tc_fence_before();
     __syncthreads();
 
-    // ---------------- group 1 ----------------
+    // ---------------- group 1, second part ----------------
     if (warp == 0) {  // the whole warp: uniform descriptors, one elected lane issues
-        {
-            tc_fence_after();
-            // KS^T = S0^T K^T: A = S0 image MN-major (M = v in two 64-blocks 16 KiB apart), B = K rows
-            #pragma unroll 1
-            for (int tm = 0; tm < 2; ++tm)
-                for (int at = 0; at < 2; ++at)
-                    mma4_w<2048, 32>(tmem + kTbKS, sdesc(sS + tm * 32768 + at * 8192, 16384), sdesc(sKQ + at * 16384 + 8192), idesc_bf16(128, 64, 1, 0), (tm | at) != 0);
-            // dQr^T = S0 dO^T: A = S0 image K-major (M = k), B = dO rows
-            #pragma unroll 1
-            for (int tm = 0; tm < 2; ++tm)
-                for (int at = 0; at < 2; ++at)
-                    mma4_w<32, 32>(tmem + kTbDQ, sdesc(sS + tm * 32768 + at * 16384), sdesc(sOR + at * 16384), idesc_bf16(128, 64, 0, 0), (tm | at) != 0);
-            {  // dR^T = dUt^T A: A operand dUt^T from TMEM, B = A image MN-major (K = s rows)
-                const uint32_t id = idesc_bf16(128, 64, 0, 1);
-                mma4_ts_w<2048>(tmem + kTbDR, tmem + kTbU, sdesc(sA), id, 0);
-                mma4_ts_w<2048>(tmem + kTbDR, tmem + kTbU + 32, sdesc(sA), id, 1);
-                mma4_ts_w<2048>(tmem + kTbDR, tmem + kTbU, sdesc(sA + 8192), id, 1);
-            }
-            mma_commit_w(&bars[1]);
-            ++ncommit;
+        tc_fence_after();
+        {  // dR^T = dUt^T A: A operand dUt^T from TMEM, B = A image MN-major (K = s rows)
+            const uint32_t id = idesc_bf16(128, 64, 0, 1);
+            mma4_ts_w<2048>(tmem + kTbDR, tmem + kTbU, sdesc(sA), id, 0);
+            mma4_ts_w<2048>(tmem + kTbDR, tmem + kTbU + 32, sdesc(sA), id, 1);
+            mma4_ts_w<2048>(tmem + kTbDR, tmem + kTbU, sdesc(sA + 8192), id, 1);
         }
+        mma_commit_w(&bars[1]);
+        ++ncommit;
     }
     // this thread's V column (lane v, tokens t0..; the tile landed with the unit's copies)
     float vv[16];

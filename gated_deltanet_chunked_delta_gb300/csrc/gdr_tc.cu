@@ -2026,22 +2026,22 @@ constexpr uint32_t kTbU = 320;    // dUt^T hi | lo (packed A operand)
 constexpr uint32_t kTbR = 384;    // R^T hi | lo (packed A operand) -> dK2^T
 constexpr uint32_t kTbP1B = 448;  // [. ; dR_lo Ut_hi^T]
 
-// Per lane x[0..15] -> the sum over the warp's 32 lanes of x[lane % 16]
-// (an all-reduce over lane bit 4, then a reduce-scatter; x is consumed).
+// Per lane x[0..15] -> the sum over the warp's 32 lanes of x[lane / 2] (lanes
+// 2c and 2c + 1 both hold column c).  A reduce-scatter: each round a lane keeps
+// the half of its columns selected by one lane bit and sends the other half to
+// the lane differing in that bit (16 shuffles and 16 adds; x is consumed).
 __device__ __forceinline__ float warp_rs16(float (&x)[16], int lane) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) x[i] += __shfl_xor_sync(0xffffffffu, x[i], 16);
-#pragma unroll
-    for (int o = 8; o >= 1; o >>= 1) {
+    for (int o = 16, n = 8; o >= 2; o >>= 1, n >>= 1) {
         const bool up = (lane & o) != 0;
 #pragma unroll
-        for (int i = 0; i < o; ++i) {
-            const float send = up ? x[i] : x[i + o];
-            const float keep = up ? x[i + o] : x[i];
+        for (int i = 0; i < n; ++i) {
+            const float send = up ? x[i] : x[i + n];
+            const float keep = up ? x[i + n] : x[i];
             x[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
         }
     }
-    return x[0];
+    return x[0] + __shfl_xor_sync(0xffffffffu, x[0], 1);
 }
 // 16 columns [col0, col0 + 16) of row `row` (col0 a multiple of 8, inside one
 // 64-column atom) of a pair of 128-byte-swizzled bf16 images (hi, lo).
@@ -2332,9 +2332,9 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
     {
         const float s1 = warp_rs16(a1, lane);
         const float s2 = warp_rs16(a2, lane);
-        if (lane < 16) {
-            atomicAdd(&rRV[t0 + lane], s1);
-            atomicAdd(&rRKS[t0 + lane], s2);
+        if (!(lane & 1)) {
+            atomicAdd(&rRV[t0 + (lane >> 1)], s1);
+            atomicAdd(&rRKS[t0 + (lane >> 1)], s2);
         }
     }
     {
@@ -2350,7 +2350,7 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
             a[j] = __uint_as_float(dqu[j]) *
                    __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(qa + j * 128 + ((xc ^ (j & 7)) << 4)));
         const float s = warp_rs16(a, lane);
-        if (lane < 16) atomicAdd(&rQdq[t0 + lane], s);
+        if (!(lane & 1)) atomicAdd(&rQdq[t0 + (lane >> 1)], s);
     }
     ok = bwait(&bars[1], 1, cap, abort);
     if (__syncthreads_or(!ok)) goto out;
@@ -2464,7 +2464,7 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
             a[2 * i + 1] = (bf_hi(dh[i]) + bf_hi(dl[i])) * __uint_as_float(uu[2 * i + 1]);
         }
         const float rs = warp_rs16(a, lane);
-        if (lane < 16) atomicAdd(&rUdU[t0 + lane], rs);
+        if (!(lane & 1)) atomicAdd(&rUdU[t0 + (lane >> 1)], rs);
     }
     ok = bwait(&bars[1], 0, cap, abort);
     if (__syncthreads_or(!ok)) goto out;
@@ -2519,7 +2519,7 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
         st_img_hl16(Wim + 16384, Wim + 24576, t, t0, mmx);
         atomicAdd(&rLK[t], rl);
         const float s = warp_rs16(col, lane);
-        if (lane < 16) atomicAdd(&cL[t0 + lane], s);
+        if (!(lane & 1)) atomicAdd(&cL[t0 + (lane >> 1)], s);
     }
     fence_async_smem();
     tc_fence_before();
@@ -2544,18 +2544,19 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
     }
     // ---------------- gate and beta gradients, while group 4 runs: every row
     // and column sum they read is complete (epilogues 1-3 and the windows of
-    // groups 2 and 3) ----------------
-    if (tid < 64) {
-        const int r = tid;
+    // groups 2 and 3).  Warps 1-2 (warp 0 is issuing), with a barrier of
+    // their own ----------------
+    if (warp == 1 || warp == 2) {
+        const int r = tid - 32;
         const float br = bet[r], egr = egv[r];
         const float db = rRV[r] - egr * rRKS[r] + rLK[r];
         const float dgam = -br * egr * rRKS[r] - rUdU[r] + p.scale * egr * rQdq[r] + rP[r] + br * rLK[r] - cL[r];
         if (r < len) p.dbeta[(size_t)(tok0 + r) * p.Hv + h] = db;
         dgm[r] = r < len ? dgam : 0.f;
         tnp[r] = rUdU[r] - rP[r];
+        asm volatile("bar.sync 2, 64;" ::: "memory");
     }
-    __syncthreads();
-    if (tid < 32) {
+    if (warp == 1) {
         // dgamma_n collects e^{gamma_n} <dS1, S0> and the rows' shares; dg is the
         // reverse cumulative sum of dgamma over the chunk
         float tn = tnp[2 * lane] + tnp[2 * lane + 1];

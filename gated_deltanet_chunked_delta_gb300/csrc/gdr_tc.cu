@@ -108,6 +108,11 @@ __device__ __forceinline__ void drain_wait(uint64_t *b, uint32_t parity) {
         if (mbar_try(b, parity)) return;
 }
 
+// Brings a tensor map (a kernel parameter) into the descriptor cache ahead of
+// the copies that use it.
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *m) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
 __device__ __forceinline__ void tma3d(void *dst, const CUtensorMap *m, int x, int y, int z, uint64_t *bar) {
     asm volatile(
         "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
@@ -2000,7 +2005,6 @@ __global__ void __launch_bounds__(512) k_combine_tc(Params p) {
 // ---------------------------------------------------------------------------
 struct BcMaps {
     CUtensorMap Q, K, dO;  // 3-D (x, head, token), box 64 x 1 x 64, 128-byte swizzle
-    CUtensorMap dU;        // fp32 3-D (v, t, unit), box 32 x 64 x 1, 128-byte swizzle
     CUtensorMap A;         // fp32 3-D (s, head, token), box 32 x 1 x 64, 128-byte swizzle
     CUtensorMap V;         // 3-D (v, head, token), box 128 x 1 x 64, plain rows
 };
@@ -2123,33 +2127,45 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
         hqn = hn / (p.Hv / p.Hq);
         return p.chunk[cn].tok0;
     };
-    auto copy_A = [&](int un, int hn, int hqn, int tk) {  // the A rows and the V tile
-        tma3d(Aim, &maps.A, 0, hn, tk, &bars[0]);
-        tma3d(Aim + 8192, &maps.A, 32, hn, tk, &bars[0]);
-        tma3d(sm + kBcV, &maps.V, 0, hn, tk, &bars[0]);
-    };
-    auto copy_S0_dO = [&](int un, int hn, int hqn, int tk) {
-        bulk_g2s(Sim, reinterpret_cast<const char *>(p.hbuf) + (size_t)un * 65536, 65536, &bars[0]);  // the S0 image
-        tma3d(OR, &maps.dO, 0, hn, tk, &bars[0]);
-        tma3d(OR + 16384, &maps.dO, 64, hn, tk, &bars[0]);
-    };
-    auto copy_KQ_dU = [&](int un, int hn, int hqn, int tk) {
-#pragma unroll
-        for (int a = 0; a < 2; ++a) {
-            tma3d(KQ + a * 16384, &maps.Q, 64 * a, hqn, tk, &bars[0]);
-            tma3d(KQ + a * 16384 + 8192, &maps.K, 64 * a, hqn, tk, &bars[0]);
+    // One batch of the next unit's copies, issued by warp 0 with one copy per
+    // lane (a copy instruction costs its thread ~120 cycles; a warp's lanes issue
+    // theirs together): batch 0 the A rows (two boxes) and the V tile, batch 1
+    // the S0 image and the dO tile (two boxes), batch 2 [Q ; K] (four boxes) and
+    // dUt (fp32 rows [64 t][128 v], read as they are).
+    auto issue_copies = [&](int batch, int un, int hn, int hqn, int tk) {
+        if (batch == 0) {
+            if (lane < 3)
+                tma3d(lane < 2 ? Aim + lane * 8192 : sm + kBcV, lane < 2 ? &maps.A : &maps.V, 32 * (lane & 1), hn, tk,
+                      &bars[0]);
+        } else if (batch == 1) {
+            if (lane == 0)
+                bulk_g2s(Sim, reinterpret_cast<const char *>(p.hbuf) + (size_t)un * 65536, 65536, &bars[0]);
+            else if (lane < 3)
+                tma3d(OR + (lane - 1) * 16384, &maps.dO, 64 * (lane - 1), hn, tk, &bars[0]);
+        } else {
+            if (lane < 4)
+                tma3d(KQ + (lane >> 1) * 16384 + (lane & 1) * 8192, (lane & 1) ? &maps.K : &maps.Q, 64 * (lane >> 1),
+                      hqn, tk, &bars[0]);
+            else if (lane == 4)
+                bulk_g2s(Wim, reinterpret_cast<const char *>(p.dubuf) + (size_t)un * 32768, 32768, &bars[0]);
         }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) tma3d(Wim + q * 8192, &maps.dU, 32 * q, 0, un, &bars[0]);
     };
-    if (tid == 0 && (int)blockIdx.x < NQ) {
+    if (tid == 0) {
+        prefetch_tmap(&maps.Q);
+        prefetch_tmap(&maps.K);
+        prefetch_tmap(&maps.dO);
+        prefetch_tmap(&maps.A);
+        prefetch_tmap(&maps.V);
+    }
+    if (warp == 0 && (int)blockIdx.x < NQ) {
         const int u0 = blockIdx.x * gsteps;
         int hn, hqn;
         const int tk = unit_tok(u0, hn, hqn);
-        mbar_expect_tx(&bars[0], kBcPrefetch);
-        copy_A(u0, hn, hqn, tk);
-        copy_S0_dO(u0, hn, hqn, tk);
-        copy_KQ_dU(u0, hn, hqn, tk);
+        if (lane == 0) mbar_expect_tx(&bars[0], kBcPrefetch);
+        __syncwarp();
+        issue_copies(0, u0, hn, hqn, tk);
+        issue_copies(1, u0, hn, hqn, tk);
+        issue_copies(2, u0, hn, hqn, tk);
         pf_phase = 0;
     }
     bool ok = true;
@@ -2176,8 +2192,8 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
     if (tid == 0) pf_phase = -1;
     {
         // This unit's copies have landed: S0 as the bf16 hi | lo image the state
-        // recompute staged, the A rows and dUt as 128-byte-swizzled fp32 rows
-        // (16-byte chunk j of row r at j ^ (r % 8)).  Every thread moves its dUt^T
+        // recompute staged, the A rows as 128-byte-swizzled fp32 rows (16-byte
+        // chunk j of row r at j ^ (r % 8)), dUt as plain fp32 rows.  Every thread moves its dUt^T
         // column into tensor memory; warps 4-7 read the A rows and, after a
         // barrier of their own, write the A image over them (rows past the chunk
         // end become identity rows); warp 1 takes the gate cumsum.  Warp 0 first
@@ -2186,14 +2202,9 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
         // landed), so those MMAs run while the others convert.
         {
             float du[16];
-            const int v = row_v;
-            const char *src = Wim + (v >> 5) * 8192 + (v & 3) * 4;
+            const float *src = reinterpret_cast<const float *>(Wim) + row_v;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int t = t0 + j;
-                du[j] = t < len ? *reinterpret_cast<const float *>(src + t * 128 + ((((v & 31) >> 2) ^ (t & 7)) << 4))
-                                : 0.f;
-            }
+            for (int j = 0; j < 16; ++j) du[j] = t0 + j < len ? src[(t0 + j) * 128] : 0.f;
             uint32_t hv[8], lv[8];
             split_pairs<8>(du, hv, lv);
             tmem_st8(tmem + kTbU + t0 / 2 + lq, hv);
@@ -2355,12 +2366,6 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
     ok = bwait(&bars[1], 1, cap, abort);
     if (__syncthreads_or(!ok)) goto out;
     tc_fence_after();
-    if (tid == 0 && un < NU) {  // the next unit's A rows, over the A image groups 1-2 have read
-        mbar_expect_tx_only(&bars[0], 16384 + 16384);
-        copy_A(un, nxt[0], nxt[1], nxt[2]);
-        pf_phase = (it + 1) & 1;
-        pf_arrived = false;
-    }
     // ---------------- epilogue 2 ----------------
     // <dS1, S0>: this thread's S0 terms (row k, 32 values) are read before the
     // dS1 image, which the reverse scan stored ready for the MMA, is copied
@@ -2384,6 +2389,10 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
         mbar_expect_tx(&bars[6], 65536);
         bulk_g2s(Sim, reinterpret_cast<const char *>(p.dhbuf) + ch * 65536, 65536, &bars[6]);
         ++ds1_copies;
+        if (un < NU) {  // the phase of bars[0] the next unit's copies (issued below by warp 3) complete
+            pf_phase = (it + 1) & 1;
+            pf_arrived = false;
+        }
     }
     {
         // lane v: Ut^T -> image (B operand of group 3)
@@ -2393,6 +2402,11 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
 #pragma unroll
         for (int j = 0; j < 16; ++j) x[j] = __uint_as_float(uu[j]);
         st_img_hl16(Wim, Wim + 16384, row_v, t0, x);
+    }
+    if (warp == 3 && un < NU) {  // the next unit's A rows, over the A image groups 1-2 have read (while dS1 lands)
+        if (lane == 0) mbar_expect_tx_only(&bars[0], 16384 + 16384);
+        __syncwarp();
+        issue_copies(0, un, nxt[0], nxt[1], nxt[2]);
     }
     ok = bwait(&bars[6], (ds1_parity++) & 1, cap, abort);
     if (__syncthreads_or(!ok)) goto out;
@@ -2469,10 +2483,6 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
     ok = bwait(&bars[1], 0, cap, abort);
     if (__syncthreads_or(!ok)) goto out;
     tc_fence_after();
-    if (tid == 0 && un < NU) {  // the next S0 and dO, over dS1 and [dO ; dR] that group 3 has read
-        mbar_expect_tx_only(&bars[0], 65536 + 16384);
-        copy_S0_dO(un, nxt[0], nxt[1], nxt[2]);
-    }
     // ---------------- epilogue 3: token lanes ----------------
     if (q4 < 2) {
         // row t of dP'' = scale e^{gamma_t - gamma_s} (dO Ut^T)[t][s], s <= t < len; row sum dP''.QK
@@ -2542,6 +2552,11 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
         mma_commit_w(&bars[1]);
         ++ncommit;
     }
+    if (warp == 3 && un < NU) {  // while group 4 runs: the next S0 and dO, over dS1 and [dO ; dR] that group 3 read
+        if (lane == 0) mbar_expect_tx_only(&bars[0], 65536 + 16384);
+        __syncwarp();
+        issue_copies(1, un, nxt[0], nxt[1], nxt[2]);
+    }
     // ---------------- gate and beta gradients, while group 4 runs: every row
     // and column sum they read is complete (epilogues 1-3 and the windows of
     // groups 2 and 3).  Warps 1-2 (warp 0 is issuing), with a barrier of
@@ -2578,9 +2593,10 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
     ok = bwait(&bars[1], 1, cap, abort);
     if (__syncthreads_or(!ok)) goto out;
     tc_fence_after();
-    if (tid == 0 && un < NU) {  // the next [Q ; K] and dUt, over the tiles group 4 has read; the phase's arrival
-        mbar_expect_tx(&bars[0], 32768 + 32768);
-        copy_KQ_dU(un, nxt[0], nxt[1], nxt[2]);
+    if (warp == 0 && un < NU) {  // the next [Q ; K] and dUt, over the tiles group 4 has read; the phase's arrival
+        if (lane == 0) mbar_expect_tx(&bars[0], 32768 + 32768);
+        __syncwarp();
+        issue_copies(2, un, nxt[0], nxt[1], nxt[2]);
         pf_arrived = true;
     }
     // ---------------- epilogue 4: lane k ----------------
@@ -2809,7 +2825,6 @@ int launch_bwd_chunk(const Params &p, cudaStream_t st) {
     BcMaps maps;
     if (!map3(&maps.Q, p.q, p.Hq, p.Ttot, 64, true) || !map3(&maps.K, p.k, p.Hq, p.Ttot, 64, true) ||
         !map3(&maps.dO, p.dout, p.Hv, p.Ttot, 64, true) ||
-        !mapf32(&maps.dU, p.dubuf, 128, 64, NU, 512, 32768, 32, 64, 1) ||
         !mapf32(&maps.A, p.A_in, 64, p.Hv, p.Ttot, 256, (cuuint64_t)p.Hv * 256, 32, 1, 64) ||
         !map3(&maps.V, p.v, p.Hv, p.Ttot, 128, false))
         return 1;

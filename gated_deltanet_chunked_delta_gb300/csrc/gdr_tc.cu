@@ -256,6 +256,11 @@ __device__ __forceinline__ void tmem_hold8(uint32_t (&r)[8]) { asm volatile("" :
 // fragments of 8 x 8 blocks of 16-bit pairs: register 2j holds lane
 // base + lane / 4, column 4 j + lane % 4; register 2j + 1 the lane 8 further
 // (issue only: tcgen05.wait::ld before use).
+__device__ __forceinline__ void tmem_ld16x128b_x2_issue(uint32_t ta, uint32_t *r) {
+    asm volatile("tcgen05.ld.sync.aligned.16x128b.x2.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(ta));
+}
 __device__ __forceinline__ void tmem_ld16x128b_x4_issue(uint32_t ta, uint32_t *r) {
     asm volatile("tcgen05.ld.sync.aligned.16x128b.x4.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
@@ -2127,12 +2132,13 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
         hqn = hn / (p.Hv / p.Hq);
         return p.chunk[cn].tok0;
     };
-    // One batch of the next unit's copies, issued by warp 0 with one copy per
+    // One batch of the next unit's copies, issued by one warp with one copy per
     // lane (a copy instruction costs its thread ~120 cycles; a warp's lanes issue
     // theirs together): batch 0 the A rows (two boxes) and the V tile, batch 1
-    // the S0 image and the dO tile (two boxes), batch 2 [Q ; K] (four boxes) and
-    // dUt (fp32 rows [64 t][128 v], read as they are).
-    auto issue_copies = [&](int batch, int un, int hn, int hqn, int tk) {
+    // the S0 image and the dO tile (two boxes), batch 2 [Q ; K] (four boxes;
+    // skipped when the next unit is the same (chunk, qk-head): nothing writes the
+    // tile) and dUt (fp32 rows [64 t][128 v], read as they are).
+    auto issue_copies = [&](int batch, int un, int hn, int hqn, int tk, bool keep_kq = false) {
         if (batch == 0) {
             if (lane < 3)
                 tma3d(lane < 2 ? Aim + lane * 8192 : sm + kBcV, lane < 2 ? &maps.A : &maps.V, 32 * (lane & 1), hn, tk,
@@ -2143,7 +2149,7 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
             else if (lane < 3)
                 tma3d(OR + (lane - 1) * 16384, &maps.dO, 64 * (lane - 1), hn, tk, &bars[0]);
         } else {
-            if (lane < 4)
+            if (lane < 4 && !keep_kq)
                 tma3d(KQ + (lane >> 1) * 16384 + (lane & 1) * 8192, (lane & 1) ? &maps.K : &maps.Q, 64 * (lane >> 1),
                       hqn, tk, &bars[0]);
             else if (lane == 4)
@@ -2296,12 +2302,43 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
             tmem_st8(tmem + kTbR + t0 / 2 + lq, hv);
             tmem_st8(tmem + kTbR + 32 + t0 / 2 + lq, lv);
         }
+        {
+            // the dR rows of the [dO ; dR] operand: rows 64 + t of the v half's
+            // [dO ; dR_hi] atom (hi) and row t of its dR_lo atom (lo).  The packed
+            // (t, t + 1) pairs go into this warp's own KS^T columns, already read
+            // above, and come back as 8 x 8 (v, t-pair) fragments that leave by
+            // transposed stmatrix stores, each block as eight 16-byte rows t of
+            // eight values v (one swizzled chunk per row)
+            float d[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) d[j] = __uint_as_float(dru[j]);
+            uint32_t hv[8], lv[8];
+            split_pairs<8>(d, hv, lv);
+            tmem_st8(tmem + kTbKS + t0 + lq, hv);
+            tmem_st8(tmem + kTbKS + t0 + 8 + lq, lv);
+            tmem_wait_st();
+            uint32_t f[2][2][4];  // [term][16-lane half]: blocks (v group, t group) (0,0) (1,0) (0,1) (1,1)
+#pragma unroll
+            for (int term = 0; term < 2; ++term)
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf)
+                    tmem_ld16x128b_x2_issue(tmem + kTbKS + t0 + 8 * term + ((uint32_t)(32 * q4 + 16 * hf) << 16),
+                                            f[term][hf]);
+            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+            const int mb = lane >> 3, rr = lane & 7;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                asm volatile("" : "+r"(f[0][hf][0]), "+r"(f[0][hf][1]), "+r"(f[0][hf][2]), "+r"(f[0][hf][3]),
+                             "+r"(f[1][hf][0]), "+r"(f[1][hf][1]), "+r"(f[1][hf][2]), "+r"(f[1][hf][3])::"memory");
+                const int v8 = 32 * q4 + 16 * hf + 8 * (mb & 1), t = t0 + 8 * (mb >> 1) + rr;
+                const int off = t * 128 + ((((v8 & 63) >> 3) ^ (t & 7)) << 4);
+                stmatrix_x4_trans(su32(OR + (v8 >> 6) * 16384 + 8192 + off), f[0][hf][0], f[0][hf][1], f[0][hf][2],
+                                  f[0][hf][3]);
+                stmatrix_x4_trans(su32(RL + (v8 >> 6) * 8192 + off), f[1][hf][0], f[1][hf][1], f[1][hf][2],
+                                  f[1][hf][3]);
+            }
+        }
         __nv_bfloat16 *dvo = reinterpret_cast<__nv_bfloat16 *>(p.dv) + ((size_t)tok0 * p.Hv + h) * 128 + v;
-        // rows 64 + t of the v half's [dO ; dR_hi] atom and row t of its dR_lo atom;
-        // t0 is a multiple of 8, so row t's 16-byte chunk is (v % 64) / 8 ^ (j % 8)
-        const int xc = ((v & 63) >> 3), xb = (v & 7) * 2;
-        char *orh = OR + (v >> 6) * 16384 + 8192 + t0 * 128 + xb;
-        char *orl = RL + (v >> 6) * 8192 + t0 * 128 + xb;
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
             const int t = t0 + j;
@@ -2310,10 +2347,6 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
             a2[j] = dr * __uint_as_float(ksu[j]);
             if (t < len) dvo[(size_t)t * tstride] = __float2bfloat16_rn(bet[t] * dr);
             x[j] = -bet[t] * egv[t] * dr;
-            const uint32_t hw = pack_bf16(dr, 0.f);
-            const int off = j * 128 + ((xc ^ (j & 7)) << 4);
-            *reinterpret_cast<uint16_t *>(orh + off) = (uint16_t)hw;
-            *reinterpret_cast<__nv_bfloat16 *>(orl + off) = __float2bfloat16_rn(dr - __uint_as_float(hw << 16));
         }
         st_img_hl16(Wim, Wim + 16384, v, t0, x);  // dKS^T row v
     }
@@ -2594,9 +2627,10 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
     if (__syncthreads_or(!ok)) goto out;
     tc_fence_after();
     if (warp == 0 && un < NU) {  // the next [Q ; K] and dUt, over the tiles group 4 has read; the phase's arrival
-        if (lane == 0) mbar_expect_tx(&bars[0], 32768 + 32768);
+        const bool keep_kq = gj + 1 < gsteps;  // the next unit: the same chunk and qk-head
+        if (lane == 0) mbar_expect_tx(&bars[0], (keep_kq ? 0 : 32768) + 32768);
         __syncwarp();
-        issue_copies(2, un, nxt[0], nxt[1], nxt[2]);
+        issue_copies(2, un, nxt[0], nxt[1], nxt[2], keep_kq);
         pf_arrived = true;
     }
     // ---------------- epilogue 4: lane k ----------------

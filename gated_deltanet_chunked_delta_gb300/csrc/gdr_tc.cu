@@ -2086,6 +2086,7 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
           *rLK = scr + 512, *cL = scr + 576, *dgm = scr + 640, *tnp = scr + 704;
     float *red = scr + 768;  // [16]
     uint64_t *bars = reinterpret_cast<uint64_t *>(scr + 784);  // tma, mma
+    float *eLv = scr + 832;  // [64] e^{gamma_n - gamma_t}
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2);
     volatile int *abort = reinterpret_cast<volatile int *>(bars + 3);
     int *nxt = reinterpret_cast<int *>(bars + 4);  // [3] the next unit's coordinates (thread 0)
@@ -2258,7 +2259,10 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
         }
     }
     __syncthreads();  // gates
-    if (tid < 64) egv[tid] = __expf(gam[tid]);
+    if (tid < 64) {
+        egv[tid] = __expf(gam[tid]);
+        eLv[tid] = __expf(gam[63] - gam[tid]);
+    }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -2636,7 +2640,6 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
     // ---------------- epilogue 4: lane k ----------------
     {
         const int k = row_v;
-        const float gC = gam[63];
         uint32_t qr[16], q2[16], kd[16], k2[16];
         tmem_ld16_issue(tmem + kTbDQ + t0 + lq, qr);
         tmem_ld16_issue(tmem + kTbKS + t0 + lq, q2);
@@ -2651,7 +2654,7 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
         for (int j = 0; j < 16; ++j) {
             const int t = t0 + j;
             dqv[j] = p.scale * egv[t] * __uint_as_float(qr[j]) + __uint_as_float(q2[j]);
-            dkv[j] = __uint_as_float(kd[j]) + __expf(gC - gam[t]) * __uint_as_float(k2[j]);
+            dkv[j] = __uint_as_float(kd[j]) + eLv[t] * __uint_as_float(k2[j]);
         }
         // dq, dk summed over the G v-heads of the qk-head in head order: with
         // gsteps = G this CTA takes the group's units one after another, and each

@@ -317,8 +317,10 @@ def inputs_make(spec):
 
 def timed_steps(w, steps, warmup, flush, stream, world, clocks=None):
     """W warm-up steps, then `steps` timed ones (barrier + synchronize on both
-    sides, an L2 flush before each, CUDA events on the launching stream); then
-    as many steps again with every kernel bracketed by caller-owned events.
+    sides of the run, an L2 flush before each step, CUDA events on the
+    launching stream; the steps are enqueued back to back, so that a host-side
+    stall cannot fall between a step's start event and its kernels); then as
+    many steps again with every kernel bracketed by caller-owned events.
     Returns (per-step ms, per-kernel ms lists, launches, wall seconds, clocks)."""
     gdr = w.gdr
     for _ in range(warmup):
@@ -340,7 +342,6 @@ def timed_steps(w, steps, warmup, flush, stream, world, clocks=None):
         e0[i].record(stream)
         w.step()
         e1[i].record(stream)
-        torch.cuda.synchronize()
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()

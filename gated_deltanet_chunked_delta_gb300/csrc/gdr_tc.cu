@@ -2431,14 +2431,51 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
             pf_arrived = false;
         }
     }
+    float udu[16];  // this thread's terms of the row sums dUt.Ut
     {
-        // lane v: Ut^T -> image (B operand of group 3)
-        uint32_t uu[16];
-        tmem_ld16w(tmem + kTbKS + t0 + lq, uu);
+        // lane v: Ut^T -> image (B operand of group 3); the dUt.Ut terms (dUt^T
+        // packed in TMEM) while Ut^T is in registers
+        uint32_t uu[16], dh[8], dl[8];
+        tmem_ld16_issue(tmem + kTbKS + t0 + lq, uu);
+        tmem_ld8_issue(tmem + kTbU + t0 / 2 + lq, dh);
+        tmem_ld8_issue(tmem + kTbU + 32 + t0 / 2 + lq, dl);
+        tmem_wait_ld16(uu);
+        tmem_hold8(dh);
+        tmem_hold8(dl);
         float x[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) x[j] = __uint_as_float(uu[j]);
         st_img_hl16(Wim, Wim + 16384, row_v, t0, x);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            udu[2 * i] = (bf_lo(dh[i]) + bf_lo(dl[i])) * x[2 * i];
+            udu[2 * i + 1] = (bf_hi(dh[i]) + bf_hi(dl[i])) * x[2 * i + 1];
+        }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();  // the Ut^T image complete
+    // ---------------- group 3, first part, while dS1 lands: the products
+    // that do not read it ----------------
+    if (warp == 0) {  // the whole warp: uniform descriptors, one elected lane issues
+        tc_fence_after();
+        const uint32_t id = idesc_bf16(128, 64, 0, 1);
+        // [dO ; dR_hi] (Ut_hi + Ut_lo)^T, and [. ; dR_lo] Ut_hi^T: B = Ut^T image MN-major
+        #pragma unroll 1
+        for (int tb = 0; tb < 2; ++tb)
+            for (int at = 0; at < 2; ++at)
+                mma4_w<32, 2048>(tmem + kTbP1, sdesc(sOR + at * 16384), sdesc(sW + tb * 16384 + at * 8192), id, (tb | at) != 0);
+        #pragma unroll 1
+        for (int at = 0; at < 2; ++at)
+            mma4_w<32, 2048>(tmem + kTbP1B, sdesc(sRL - 8192 + at * 8192), sdesc(sW + at * 8192), id, at != 0);
+        // [Q ; K] K^T
+        #pragma unroll 1
+        for (int at = 0; at < 2; ++at)
+            mma4_w<32, 32>(tmem + kTbDR, sdesc(sKQ + at * 16384), sdesc(sKQ + at * 16384 + 8192), idesc_bf16(128, 64, 0, 0), at != 0);
+    }
+    {
+        const float rs = warp_rs16(udu, lane);
+        if (!(lane & 1)) atomicAdd(&rUdU[t0 + (lane >> 1)], rs);
     }
     if (warp == 3 && un < NU) {  // the next unit's A rows, over the A image groups 1-2 have read (while dS1 lands)
         if (lane == 0) mbar_expect_tx_only(&bars[0], 16384 + 16384);
@@ -2454,24 +2491,12 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
     if (warp == 0) {  // the whole warp: uniform descriptors, one elected lane issues
         tc_fence_after();
         const uint32_t id = idesc_bf16(128, 64, 0, 1);
-        // [dO ; dR_hi] (Ut_hi + Ut_lo)^T, and [. ; dR_lo] Ut_hi^T: B = Ut^T image MN-major
-        #pragma unroll 1
-        for (int tb = 0; tb < 2; ++tb)
-            for (int at = 0; at < 2; ++at)
-                mma4_w<32, 2048>(tmem + kTbP1, sdesc(sOR + at * 16384), sdesc(sW + tb * 16384 + at * 8192), id, (tb | at) != 0);
-        #pragma unroll 1
-        for (int at = 0; at < 2; ++at)
-            mma4_w<32, 2048>(tmem + kTbP1B, sdesc(sRL - 8192 + at * 8192), sdesc(sW + at * 8192), id, at != 0);
         // dK2^T = dS1 Ut^T (over the R^T operand, read by group 2)
         #pragma unroll 1
         for (int m = 0; m < 3; ++m)
             for (int at = 0; at < 2; ++at)
                 mma4_w<32, 2048>(tmem + kTbR, sdesc(sS + (m == 1) * 32768 + at * 16384), sdesc(sW + (m == 2) * 16384 + at * 8192), id, (m | at) != 0);
-        // [Q ; K] K^T
-        #pragma unroll 1
-        for (int at = 0; at < 2; ++at)
-            mma4_w<32, 32>(tmem + kTbDR, sdesc(sKQ + at * 16384), sdesc(sKQ + at * 16384 + 8192), idesc_bf16(128, 64, 0, 0), at != 0);
-        mma_commit_w(&bars[1]);
+        mma_commit_w(&bars[1]);  // the first part's MMAs complete with these
         ++ncommit;
     }
     {
@@ -2498,24 +2523,6 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
         if (lane == 0) atomicAdd(&red[0], part);
-    }
-    {
-        // while group 3 runs: row sums dUt.Ut (lane v; dUt^T packed in TMEM, Ut^T in TMEM)
-        uint32_t uu[16], dh[8], dl[8];
-        tmem_ld16_issue(tmem + kTbKS + t0 + lq, uu);
-        tmem_ld8_issue(tmem + kTbU + t0 / 2 + lq, dh);
-        tmem_ld8_issue(tmem + kTbU + 32 + t0 / 2 + lq, dl);
-        tmem_wait_ld16(uu);
-        tmem_hold8(dh);
-        tmem_hold8(dl);
-        float a[16];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            a[2 * i] = (bf_lo(dh[i]) + bf_lo(dl[i])) * __uint_as_float(uu[2 * i]);
-            a[2 * i + 1] = (bf_hi(dh[i]) + bf_hi(dl[i])) * __uint_as_float(uu[2 * i + 1]);
-        }
-        const float rs = warp_rs16(a, lane);
-        if (!(lane & 1)) atomicAdd(&rUdU[t0 + (lane >> 1)], rs);
     }
     ok = bwait(&bars[1], 0, cap, abort);
     if (__syncthreads_or(!ok)) goto out;

@@ -2527,6 +2527,12 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
     ok = bwait(&bars[1], 0, cap, abort);
     if (__syncthreads_or(!ok)) goto out;
     tc_fence_after();
+    if (warp == 1 && un < NU) {  // the next S0 and dO, over dS1 and [dO ; dR] that group 3 has read (warp 1 has
+                                 // the lighter half of epilogue 3)
+        if (lane == 0) mbar_expect_tx_only(&bars[0], 65536 + 16384);
+        __syncwarp();
+        issue_copies(1, un, nxt[0], nxt[1], nxt[2]);
+    }
     // ---------------- epilogue 3: token lanes ----------------
     if (q4 < 2) {
         // row t of dP'' = scale e^{gamma_t - gamma_s} (dO Ut^T)[t][s], s <= t < len; row sum dP''.QK
@@ -2595,11 +2601,6 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
         }
         mma_commit_w(&bars[1]);
         ++ncommit;
-    }
-    if (warp == 3 && un < NU) {  // while group 4 runs: the next S0 and dO, over dS1 and [dO ; dR] that group 3 read
-        if (lane == 0) mbar_expect_tx_only(&bars[0], 65536 + 16384);
-        __syncwarp();
-        issue_copies(1, un, nxt[0], nxt[1], nxt[2]);
     }
     // ---------------- gate and beta gradients, while group 4 runs: every row
     // and column sum they read is complete (epilogues 1-3 and the windows of

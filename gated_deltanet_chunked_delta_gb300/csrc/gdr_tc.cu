@@ -2013,7 +2013,7 @@ struct BcMaps {
     CUtensorMap A;         // fp32 3-D (s, head, token), box 32 x 1 x 64, 128-byte swizzle
     CUtensorMap V;         // 3-D (v, head, token), box 128 x 1 x 64, plain rows
 };
-constexpr uint32_t kBcPrefetch = 16384 + 16384 + 65536 + 16384 + 32768 + 32768;  // A, V, S0, dO, [Q ; K], dUt
+constexpr uint32_t kBcPrefetch = 16384 + 16384 + 512 + 65536 + 16384 + 32768 + 32768;  // A, V, gates, S0, dO, [Q ; K], dUt
 constexpr int kBcThreads = 512;
 // shared memory (bytes from the 1024-aligned base)
 constexpr int kBcKQ = 0;        // [Q ; K]: 2 atoms (k halves) x [128 rows][128 B]: Q rows 0-63, K rows 64-127
@@ -2087,6 +2087,7 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
     float *red = scr + 768;  // [16]
     uint64_t *bars = reinterpret_cast<uint64_t *>(scr + 784);  // tma, mma
     float *eLv = scr + 832;  // [64] e^{gamma_n - gamma_t}
+    float *gnx = scr + 896, *bnx = scr + 960;  // [64] each: the gate and beta rows, copied in with a unit's tiles
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2);
     volatile int *abort = reinterpret_cast<volatile int *>(bars + 3);
     int *nxt = reinterpret_cast<int *>(bars + 4);  // [3] the next unit's coordinates (thread 0)
@@ -2136,25 +2137,30 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
     // One batch of the next unit's copies, issued by one warp with one copy per
     // lane (a copy instruction costs its thread ~120 cycles; a warp's lanes issue
     // theirs together): batch 0 the A rows (two boxes) and the V tile, batch 1
-    // the S0 image and the dO tile (two boxes), batch 2 [Q ; K] (four boxes;
+    // the S0 image, the dO tile (two boxes) and dUt rows 0-31 (into the dR_lo
+    // region, free from group 3 to epilogue 1), batch 2 [Q ; K] (four boxes;
     // skipped when the next unit is the same (chunk, qk-head): nothing writes the
-    // tile) and dUt (fp32 rows [64 t][128 v], read as they are).
+    // tile) and dUt rows 32-63.  dUt arrives as its fp32 rows [t][128 v].
     auto issue_copies = [&](int batch, int un, int hn, int hqn, int tk, bool keep_kq = false) {
         if (batch == 0) {
             if (lane < 3)
                 tma3d(lane < 2 ? Aim + lane * 8192 : sm + kBcV, lane < 2 ? &maps.A : &maps.V, 32 * (lane & 1), hn, tk,
                       &bars[0]);
+            else if (lane < 5)
+                bulk_g2s(lane == 3 ? gnx : bnx, (lane == 3 ? p.gT : p.bT) + (size_t)un * 64, 256, &bars[0]);
         } else if (batch == 1) {
             if (lane == 0)
                 bulk_g2s(Sim, reinterpret_cast<const char *>(p.hbuf) + (size_t)un * 65536, 65536, &bars[0]);
             else if (lane < 3)
                 tma3d(OR + (lane - 1) * 16384, &maps.dO, 64 * (lane - 1), hn, tk, &bars[0]);
+            else if (lane == 3)
+                bulk_g2s(RL, reinterpret_cast<const char *>(p.dubuf) + (size_t)un * 32768, 16384, &bars[0]);
         } else {
             if (lane < 4 && !keep_kq)
                 tma3d(KQ + (lane >> 1) * 16384 + (lane & 1) * 8192, (lane & 1) ? &maps.K : &maps.Q, 64 * (lane >> 1),
                       hqn, tk, &bars[0]);
             else if (lane == 4)
-                bulk_g2s(Wim, reinterpret_cast<const char *>(p.dubuf) + (size_t)un * 32768, 32768, &bars[0]);
+                bulk_g2s(Wim, reinterpret_cast<const char *>(p.dubuf) + (size_t)un * 32768 + 16384, 16384, &bars[0]);
         }
     };
     if (tid == 0) {
@@ -2188,11 +2194,7 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
     const int un = gj + 1 < gsteps ? u + 1 : (q + (int)gridDim.x < NQ ? (q + (int)gridDim.x) * gsteps : NU);  // next unit
     if (tid == 0 && un < NU) nxt[2] = unit_tok(un, nxt[0], nxt[1]);  // its head, qk-head, first token
     __syncthreads();  // the previous unit's tail is done with the scratch rows
-    if (tid < 64) {
-        gam[tid] = p.gT[(size_t)u * 64 + tid];  // zero past the chunk's end
-        bet[tid] = p.bT[(size_t)u * 64 + tid];
-        rRV[tid] = rRKS[tid] = rUdU[tid] = rQdq[tid] = rP[tid] = rLK[tid] = cL[tid] = 0.f;
-    }
+    if (tid < 64) rRV[tid] = rRKS[tid] = rUdU[tid] = rQdq[tid] = rP[tid] = rLK[tid] = cL[tid] = 0.f;
     if (tid < 16) red[tid] = 0.f;
     ok = bwait(&bars[0], it & 1, cap, abort);
     if (__syncthreads_or(!ok)) goto out;
@@ -2208,10 +2210,10 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
         // this (KS^T and dQr^T read the S0 image and the K and dO tiles as they
         // landed), so those MMAs run while the others convert.
         {
-            float du[16];
-            const float *src = reinterpret_cast<const float *>(Wim) + row_v;
+            float du[16];  // rows 0-31 in the dR_lo region, 32-63 at the start of the W region
+            const float *src = reinterpret_cast<const float *>(t0 < 32 ? RL : Wim) + (t0 & 31) * 128 + row_v;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) du[j] = t0 + j < len ? src[(t0 + j) * 128] : 0.f;
+            for (int j = 0; j < 16; ++j) du[j] = t0 + j < len ? src[j * 128] : 0.f;
             uint32_t hv[8], lv[8];
             split_pairs<8>(du, hv, lv);
             tmem_st8(tmem + kTbU + t0 / 2 + lq, hv);
@@ -2246,8 +2248,11 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
                 for (int j = 0; j < 32; ++j) xa[j] = (32 * ah + j == rr) ? 1.f : 0.f;
             asm volatile("bar.sync 1, 128;" ::: "memory");  // every raw A row read (warps 4-7)
             st_img_hl(Aim, Aim + 8192, rr, 32 * ah, xa);
-        } else if (warp == 1) {  // inclusive cumsum of the gates, two per lane
-            const float a = gam[2 * lane], b = gam[2 * lane + 1];
+        } else if (warp == 1) {  // the gate and beta rows (copied in with the tiles; zero past the
+                                 // chunk's end) and the inclusive cumsum of the gates, two per lane
+            bet[2 * lane] = bnx[2 * lane];
+            bet[2 * lane + 1] = bnx[2 * lane + 1];
+            const float a = gnx[2 * lane], b = gnx[2 * lane + 1];
             float sc = a + b;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -2478,7 +2483,7 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
         if (!(lane & 1)) atomicAdd(&rUdU[t0 + (lane >> 1)], rs);
     }
     if (warp == 3 && un < NU) {  // the next unit's A rows, over the A image groups 1-2 have read (while dS1 lands)
-        if (lane == 0) mbar_expect_tx_only(&bars[0], 16384 + 16384);
+        if (lane == 0) mbar_expect_tx_only(&bars[0], 16384 + 16384 + 512);
         __syncwarp();
         issue_copies(0, un, nxt[0], nxt[1], nxt[2]);
     }
@@ -2529,7 +2534,7 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
     tc_fence_after();
     if (warp == 1 && un < NU) {  // the next S0 and dO, over dS1 and [dO ; dR] that group 3 has read (warp 1 has
                                  // the lighter half of epilogue 3)
-        if (lane == 0) mbar_expect_tx_only(&bars[0], 65536 + 16384);
+        if (lane == 0) mbar_expect_tx_only(&bars[0], 65536 + 16384 + 16384);
         __syncwarp();
         issue_copies(1, un, nxt[0], nxt[1], nxt[2]);
     }
@@ -2640,7 +2645,7 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
     tc_fence_after();
     if (warp == 0 && un < NU) {  // the next [Q ; K] and dUt, over the tiles group 4 has read; the phase's arrival
         const bool keep_kq = gj + 1 < gsteps;  // the next unit: the same chunk and qk-head
-        if (lane == 0) mbar_expect_tx(&bars[0], (keep_kq ? 0 : 32768) + 32768);
+        if (lane == 0) mbar_expect_tx(&bars[0], (keep_kq ? 0 : 32768) + 16384);
         __syncwarp();
         issue_copies(2, un, nxt[0], nxt[1], nxt[2], keep_kq);
         pf_arrived = true;

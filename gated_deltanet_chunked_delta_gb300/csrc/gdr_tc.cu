@@ -2311,13 +2311,14 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
             tmem_st8(tmem + kTbR + t0 / 2 + lq, hv);
             tmem_st8(tmem + kTbR + 32 + t0 / 2 + lq, lv);
         }
+        // the dR rows of the [dO ; dR] operand: rows 64 + t of the v half's
+        // [dO ; dR_hi] atom (hi) and row t of its dR_lo atom (lo).  The packed
+        // (t, t + 1) pairs go into this warp's own KS^T columns, already read
+        // above, and come back as 8 x 8 (v, t-pair) fragments that leave by
+        // transposed stmatrix stores, each block as eight 16-byte rows t of
+        // eight values v (one swizzled chunk per row); dv and the dKS^T row are
+        // done while the tensor-memory stores complete
         {
-            // the dR rows of the [dO ; dR] operand: rows 64 + t of the v half's
-            // [dO ; dR_hi] atom (hi) and row t of its dR_lo atom (lo).  The packed
-            // (t, t + 1) pairs go into this warp's own KS^T columns, already read
-            // above, and come back as 8 x 8 (v, t-pair) fragments that leave by
-            // transposed stmatrix stores, each block as eight 16-byte rows t of
-            // eight values v (one swizzled chunk per row)
             float d[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) d[j] = __uint_as_float(dru[j]);
@@ -2325,7 +2326,20 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
             split_pairs<8>(d, hv, lv);
             tmem_st8(tmem + kTbKS + t0 + lq, hv);
             tmem_st8(tmem + kTbKS + t0 + 8 + lq, lv);
-            tmem_wait_st();
+        }
+        __nv_bfloat16 *dvo = reinterpret_cast<__nv_bfloat16 *>(p.dv) + ((size_t)tok0 * p.Hv + h) * 128 + v;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const int t = t0 + j;
+            const float dr = __uint_as_float(dru[j]);
+            a1[j] = dr * vv[j];
+            a2[j] = dr * __uint_as_float(ksu[j]);
+            if (t < len) dvo[(size_t)t * tstride] = __float2bfloat16_rn(bet[t] * dr);
+            x[j] = -bet[t] * egv[t] * dr;
+        }
+        st_img_hl16(Wim, Wim + 16384, v, t0, x);  // dKS^T row v
+        tmem_wait_st();
+        {
             uint32_t f[2][2][4];  // [term][16-lane half]: blocks (v group, t group) (0,0) (1,0) (0,1) (1,1)
 #pragma unroll
             for (int term = 0; term < 2; ++term)
@@ -2347,17 +2361,6 @@ __global__ void __launch_bounds__(kBcThreads, 1) k_bwd_chunk_tc(Params p, const 
                                   f[1][hf][3]);
             }
         }
-        __nv_bfloat16 *dvo = reinterpret_cast<__nv_bfloat16 *>(p.dv) + ((size_t)tok0 * p.Hv + h) * 128 + v;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const int t = t0 + j;
-            const float dr = __uint_as_float(dru[j]);
-            a1[j] = dr * vv[j];
-            a2[j] = dr * __uint_as_float(ksu[j]);
-            if (t < len) dvo[(size_t)t * tstride] = __float2bfloat16_rn(bet[t] * dr);
-            x[j] = -bet[t] * egv[t] * dr;
-        }
-        st_img_hl16(Wim, Wim + 16384, v, t0, x);  // dKS^T row v
     }
     tmem_wait_st();
     fence_async_smem();

@@ -1980,12 +1980,13 @@ __global__ void __launch_bounds__(512) k_combine_tc(Params p) {
 }
 
 // ---------------------------------------------------------------------------
-// Chunk-local gradients of the backward on tcgen05 (K = V = 128).  One CTA of
-// 512 threads per (chunk, v-head); warp 0 issues every MMA (one elected lane),
-// all sixteen warps run the epilogues (warp w reads TMEM lanes 32 (w % 4) .. + 31 and
-// columns [16 (w / 4), + 16)).  The same reverse mode as the warp-MMA kernel, with
-// every product laid out so that its M side is 128 (a value, key or stacked
-// token index in the TMEM lanes):
+// Chunk-local gradients of the backward on tcgen05 (K = V = 128).  A persistent
+// CTA of 512 threads per SM takes units (chunk, v-head) in turn, a qk-head's G
+// v-heads one after another where that keeps the CTAs balanced; warp 0 issues
+// every MMA (one elected lane), all sixteen warps run the epilogues (warp w
+// reads TMEM lanes 32 (w % 4) .. + 31 and columns [16 (w / 4), + 16)).  The same
+// reverse mode as the CUDA-core kernel, with every product laid out so that
+// its M side is 128 (a value, key or stacked token index in the TMEM lanes):
 //   group 1  KS^T   = S0^T K^T          (S0 image read MN-major)
 //            dQr^T  = S0 dO^T
 //            dR^T   = dUt^T A           (dUt^T from TMEM, A read MN-major)
@@ -2007,6 +2008,11 @@ __global__ void __launch_bounds__(512) k_combine_tc(Params p) {
 // X A^T = A^T dUt R^T A^T = dR Ut^T, so the 64 x 64 products X = A^T dA and
 // dL = X A^T need no separate pass.  Operands that are not exact bf16 inputs
 // enter as hi + lo bf16 pairs with three products (hi hi, lo hi, hi lo).
+// Schedule: KS^T and dQr^T are issued as soon as the unit's tiles land, under
+// the A-row and dUt conversion; group 3's products that do not read dS1 run
+// while the dS1 copy lands; the row and column sums that only feed dbeta and
+// dg, and dbeta, dg themselves, run under groups 2-4; the next unit's copies
+// are issued as soon as the regions they land in are free.
 // ---------------------------------------------------------------------------
 struct BcMaps {
     CUtensorMap Q, K, dO;  // 3-D (x, head, token), box 64 x 1 x 64, 128-byte swizzle

@@ -819,7 +819,8 @@ __global__ void __launch_bounds__(128, 5) k_chunk_tc(Params p, const __grid_cons
 // states run in separate CTAs).  Warps 0-15: epilogue (in kFwd, warps 0-7
 // carry the state chain and warps 8-15 write the output; otherwise all 16
 // carry the chain), warp 16: TMA producer (two-stage ring), warp 17: tensor-
-// memory allocation and the MMA issue (one thread).  Every A operand comes
+// memory allocation and the MMA issue (the whole warp runs it, one elected
+// lane issues, four MMAs per instruction group).  Every A operand comes
 // from tensor memory as packed bf16 pairs written by the epilogue, so the
 // MMAs read only their B operands from shared memory.  Per chunk, with S^T
 // in TMEM (lane v):

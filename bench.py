@@ -19,7 +19,7 @@ steps follow with every kernel bracketed by caller-owned events
 (gdr_opts.events; kept out of the timed steps, whose time the extra event
 records would inflate): the dominant kernel's algorithmic work over its
 measured duration gives the roofline fraction, and their launch count (the
-same calls as the timed steps) is gpu_launches.
+same calls as the K timed steps) is gpu_launches, the count over the K steps.
 
 ``--impl reference`` times the fp64 CPU oracle (the pages ship no code to
 run, so the oracle is the reference arm) on a bounded sample of the same
@@ -289,18 +289,30 @@ class Workload:
         if mode == "bwd":
             self.run_fwd()  # A for the backward, untimed
 
-    def run_fwd(self, timer=None):
-        d = self.d
+    def buffers(self):
+        """This workload's device inputs and outputs: (d, out_f, out_b)."""
+        return self.d, self.out_f, self.out_b
+
+    def clone_buffers(self):
+        """A second set of device inputs and outputs of the same shapes (contents
+        copied), for steps whose copies overlap another step's kernels."""
+        d = {k: (v.clone() if torch.is_tensor(v) else v) for k, v in self.d.items()}
+        out_f = {k: v.clone() for k, v in self.out_f.items()}
+        out_b = {k: v.clone() for k, v in self.out_b.items()} if self.out_b else None
+        return d, out_f, out_b
+
+    def run_fwd(self, timer=None, bufs=None):
+        d, out_f, _ = bufs or self.buffers()
         self.gdr.gdr_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], self.x["scale"], h0=d["h0"],
-                         cu_seqlens=d["cu_seqlens"], cu_seqlens_host=self.cu_host, out=self.out_f,
+                         cu_seqlens=d["cu_seqlens"], cu_seqlens_host=self.cu_host, out=out_f,
                          workspace=self.ws_f, cp_segments=self.cp, path=self.path, timer=timer,
                          cp_warmup=self.cp_warmup)
 
-    def run_bwd(self, timer=None):
-        d = self.d
-        self.gdr.gdr_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], self.out_f["A"], d["do"], dht=d["dht"],
+    def run_bwd(self, timer=None, bufs=None):
+        d, out_f, out_b = bufs or self.buffers()
+        self.gdr.gdr_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], out_f["A"], d["do"], dht=d["dht"],
                          scale=self.x["scale"], h0=d["h0"], cu_seqlens=d["cu_seqlens"],
-                         cu_seqlens_host=self.cu_host, out=self.out_b, workspace=self.ws_b, cp_segments=self.cp,
+                         cu_seqlens_host=self.cu_host, out=out_b, workspace=self.ws_b, cp_segments=self.cp,
                          path=self.path, timer=timer, cp_warmup=self.cp_warmup)
 
     def step(self, timer_f=None, timer_b=None):
@@ -308,6 +320,94 @@ class Workload:
             self.run_fwd(timer_f)
         if self.mode in ("both", "bwd"):
             self.run_bwd(timer_b)
+
+
+def e2e_pipelined(w, mode, steps, stream, dev):
+    """End-to-end steps through the public calls: each step copies its inputs
+    in from pinned host memory and its results out to pinned host memory, and
+    every copy lies between the timed region's two events.  The steps run as a
+    software pipeline over two device buffer sets, the way a training loop
+    prefetches its next batch: step i + 1's inputs go in on a copy-in stream
+    and step i's results come out on a copy-out stream while the kernels of
+    the neighbouring steps run (the link carries both directions at once).
+    The results are o and final_state of the forward and every gradient of
+    the backward; A, which the backward reads, stays on the device.  Returns
+    (total ms of `steps` steps, h2d bytes per step, d2h bytes per step)."""
+    x = w.x
+    in_f = [k for k in ("q", "k", "v", "g", "beta", "h0") if torch.is_tensor(x.get(k))]
+    in_b = [k for k in ("do", "dht") if torch.is_tensor(x.get(k))] if mode != "fwd" else []
+    out_f_keys = ["o", "final_state"] if mode != "bwd" else []
+    out_b_keys = ["dq", "dk", "dv", "dbeta", "dg", "dh0"] if mode != "fwd" else []
+    sets = [w.buffers(), w.clone_buffers()]
+
+    def dst(bufs, k):
+        d, out_f, _ = bufs
+        return out_f["A"] if k == "A" else d[k]
+
+    def src(bufs, k):
+        _, out_f, out_b = bufs
+        return out_f[k] if k in out_f else out_b[k]
+
+    hin = {k: x[k].pin_memory() for k in in_f + in_b}
+    if mode == "bwd":  # the backward alone reads the forward's A as an input
+        in_f.append("A")
+        hin["A"] = w.out_f["A"].cpu().pin_memory()
+    hout = {k: torch.empty(src(sets[0], k).shape, dtype=src(sets[0], k).dtype, pin_memory=True)
+            for k in out_f_keys + out_b_keys}
+    h2d = sum(t.numel() * t.element_size() for t in hin.values())
+    d2h = sum(t.numel() * t.element_size() for t in hout.values())
+    cin, cout = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def run(n):
+        e_in_f, e_in_b, e_fwd, e_done, e_out = ([None] * n for _ in range(5))
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        cin.wait_event(t0)
+        cout.wait_event(t0)
+        for i in range(n):
+            b = sets[i % 2]
+            with torch.cuda.stream(cin):
+                if i >= 2:
+                    cin.wait_event(e_done[i - 2])  # step i - 2 has read this set's inputs
+                for k in in_f:
+                    dst(b, k).copy_(hin[k], non_blocking=True)
+                e_in_f[i] = torch.cuda.Event()
+                e_in_f[i].record(cin)
+                for k in in_b:
+                    dst(b, k).copy_(hin[k], non_blocking=True)
+                e_in_b[i] = torch.cuda.Event()
+                e_in_b[i].record(cin)
+            stream.wait_event(e_in_f[i])
+            if i >= 2:
+                stream.wait_event(e_out[i - 2])  # step i - 2's results are out of this set
+            if mode != "bwd":
+                w.run_fwd(bufs=b)
+            e_fwd[i] = torch.cuda.Event()
+            e_fwd[i].record(stream)
+            if mode != "fwd":
+                stream.wait_event(e_in_b[i])
+                w.run_bwd(bufs=b)
+            e_done[i] = torch.cuda.Event()
+            e_done[i].record(stream)
+            with torch.cuda.stream(cout):
+                cout.wait_event(e_fwd[i])
+                for k in out_f_keys:
+                    hout[k].copy_(src(b, k), non_blocking=True)
+                cout.wait_event(e_done[i])
+                for k in out_b_keys:
+                    hout[k].copy_(src(b, k), non_blocking=True)
+                e_out[i] = torch.cuda.Event()
+                e_out[i].record(cout)
+        stream.wait_event(e_out[n - 1])
+        t1.record(stream)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1)
+
+    run(2)  # warm-up: first touch of the pinned buffers and the second set
+    total = run(steps)
+    del sets[1]
+    return total, h2d, d2h
 
 
 def inputs_make(spec):
@@ -321,7 +421,8 @@ def timed_steps(w, steps, warmup, flush, stream, world, clocks=None):
     launching stream; the steps are enqueued back to back, so that a host-side
     stall cannot fall between a step's start event and its kernels); then as
     many steps again with every kernel bracketed by caller-owned events.
-    Returns (per-step ms, per-kernel ms lists, launches, wall seconds, clocks)."""
+    Returns (per-step ms, per-kernel ms lists, launches over the `steps` steps,
+    wall seconds, clocks)."""
     gdr = w.gdr
     for _ in range(warmup):
         flush.zero_()
@@ -361,7 +462,7 @@ def timed_steps(w, steps, warmup, flush, stream, world, clocks=None):
             for nm, ms in timer.elapsed():
                 per_kernel.setdefault(nm, []).append(ms)
     gdr.check_status()
-    return step_ms, per_kernel, launches // steps, t1 - t0, clk
+    return step_ms, per_kernel, launches, t1 - t0, clk
 
 
 def rooflines(spec, mode, per_kernel, peaks, nch_heads, step_ms_mean):
@@ -433,7 +534,8 @@ def fwd_extra(gdr, name, args, dev, path, flush, stream, peaks):
         roof, frac, sroof, kernels = rooflines(spec, "fwd", per_kernel, peaks, w.prob.num_chunks() * spec.Hv, ms)
         r = {"value": spec.tokens / (ms / 1e3) / 1e6, "unit": "Mtokens/s", "ms_per_step": ms,
              "step_roofline_frac": frac, "cp_warmup": w.plan["cp_warmup"], "cp_segments": w.plan["n_segments"],
-             "seg_len": w.plan["seg_len"], "gpu_launches": launches, "kernels": kernels}
+             "seg_len": w.plan["seg_len"], "gpu_launches": launches, "gpu_launches_per_step": launches // steps,
+             "kernels": kernels}
         if key == "planned":
             r.update({"roofline": roof, "step_roofline": sroof})
         res[key] = r
@@ -501,65 +603,11 @@ def main():
     tokens = spec.tokens
     value, total_ms = aggregate(sum(step_ms), tokens, args.steps, dev)
 
-    # e2e: pinned host buffers, copies inside the timed region (every input of
-    # the timed calls in, every output out)
-    in_keys = ["q", "k", "v", "g", "beta", "h0"] + (["do", "dht"] if args.mode != "fwd" else [])
-    hin = {k: x[k].pin_memory() for k in in_keys if torch.is_tensor(x[k])}
-    dev_out = {**(out_f if args.mode != "bwd" else {}), **(out_b if args.mode != "fwd" else {})}
-    if args.mode == "bwd":
-        hin["A"] = out_f["A"].cpu().pin_memory()
-    hout = {k: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for k, t in dev_out.items()}
-    h2d = sum(t.numel() * t.element_size() for t in hin.values())
-    d2h = sum(t.numel() * t.element_size() for t in hout.values())
-    dst_of = {**d, "A": out_f["A"]}
-    ee0 = torch.cuda.Event(enable_timing=True)
-    ee1 = torch.cuda.Event(enable_timing=True)
-    # forward + backward: the backward-only inputs (do, dht) go in on a second
-    # stream after the forward's own inputs (the host-to-device link is shared,
-    # ~210 GB/s) while the forward runs, and the forward's outputs come out on it
-    # while the backward runs; every copy stays inside [ee0, ee1]
-    cs = torch.cuda.Stream(dev)
-    overlap = args.mode == "both"
-    bwd_only = [k for k in ("do", "dht") if k in hin]
-    e2e_ms = []
-    for i in range(max(3, args.steps // 2)):
-        ee0.record(stream)
-        if not overlap:
-            for k, t in hin.items():
-                dst_of[k].copy_(t, non_blocking=True)
-            w.step()
-            for k, t in dev_out.items():
-                hout[k].copy_(t, non_blocking=True)
-        else:
-            for k, t in hin.items():
-                if k not in bwd_only:
-                    dst_of[k].copy_(t, non_blocking=True)
-            ev_fin = torch.cuda.Event()
-            ev_fin.record(stream)
-            cs.wait_event(ev_fin)
-            with torch.cuda.stream(cs):
-                for k in bwd_only:
-                    dst_of[k].copy_(hin[k], non_blocking=True)
-            ev_in = torch.cuda.Event()
-            ev_in.record(cs)
-            w.run_fwd()
-            ev_f = torch.cuda.Event()
-            ev_f.record(stream)
-            cs.wait_event(ev_f)
-            with torch.cuda.stream(cs):
-                for k, t in out_f.items():
-                    hout[k].copy_(t, non_blocking=True)
-            ev_o = torch.cuda.Event()
-            ev_o.record(cs)
-            stream.wait_event(ev_in)
-            w.run_bwd()
-            for k, t in out_b.items():
-                hout[k].copy_(t, non_blocking=True)
-            stream.wait_event(ev_o)
-        ee1.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms.append(ee0.elapsed_time(ee1))
-    e2e_val = tokens * world / (statistics.mean(e2e_ms) / 1e3) / 1e6
+    # e2e: every step's inputs in from pinned host memory and its results out,
+    # inside the timed region, steps pipelined over two buffer sets
+    e2e_steps = max(4, args.steps)
+    e2e_total, h2d, d2h = e2e_pipelined(w, args.mode, e2e_steps, stream, dev)
+    e2e_val, _ = aggregate(e2e_total, tokens, e2e_steps, dev)
     gdr.check_status()
 
     roof, step_frac, sroof, kernels = rooflines(spec, args.mode, per_kernel, peaks,
@@ -576,10 +624,13 @@ def main():
             "step_roofline": sroof,
             "kernels": kernels,
             "e2e": {"value": e2e_val, "unit": "Mtokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "copies": ("do, dht in during the forward and the forward's outputs out during the backward, "
-                               "on a second stream; the rest in line" if overlap else "in line")},
-            "gpu_launches": launches, "clocks": clk}
-    del hin, hout, dst_of, dev_out, out_f, out_b, d
+                    "steps": e2e_steps, "ms_per_step": e2e_total / e2e_steps,
+                    "copies": ("pinned host buffers; steps pipelined over two device buffer sets: the next "
+                               "step's inputs in on a copy-in stream and each step's results out on a copy-out "
+                               "stream while kernels run; results are o, final_state and the gradients "
+                               "(A stays on the device)")},
+            "gpu_launches": launches, "gpu_launches_per_step": launches // args.steps, "clocks": clk}
+    del out_f, out_b, d
     if rank == 0 and world == 1 and not args.no_extras and args.workload == DEFAULT_WORKLOAD:
         del w
         torch.cuda.empty_cache()

@@ -526,6 +526,20 @@ def rooflines(spec, mode, per_kernel, peaks, nch_heads, step_ms_mean):
     return roof, step_roof_ms / step_ms_mean, step, kernels
 
 
+def unflushed_steps(w, steps, stream):
+    """Per-step ms of `steps` more steps enqueued back to back with no L2 flush
+    between them (reported beside the flushed value, not as it)."""
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    torch.cuda.synchronize()
+    for i in range(steps):
+        e0[i].record(stream)
+        w.step()
+        e1[i].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in zip(e0, e1)]
+
+
 def fwd_extra(gdr, name, args, dev, path, flush, stream, peaks):
     """Forward-only figures of one workload: with the planner's warm-up starts
     and with the exact context-parallel split only."""
@@ -608,6 +622,7 @@ def main():
     step_ms, per_kernel, launches, _, clk = timed_steps(w, args.steps, args.warmup, flush, stream, world, clocks)
     tokens = spec.tokens
     value, total_ms = aggregate(sum(step_ms), tokens, args.steps, dev)
+    unfl_ms = statistics.median(unflushed_steps(w, args.steps, stream))
 
     # e2e: every step's inputs in from pinned host memory and its results out,
     # inside the timed region, steps pipelined over two buffer sets
@@ -635,7 +650,9 @@ def main():
                                "step's inputs in on a copy-in stream and each step's results out on a copy-out "
                                "stream while kernels run; results are o, final_state and the gradients "
                                "(A stays on the device)")},
-            "gpu_launches": launches, "gpu_launches_per_step": launches // args.steps, "clocks": clk}
+            "gpu_launches": launches, "gpu_launches_per_step": launches // args.steps, "clocks": clk,
+            "unflushed": {"ms_per_step": unfl_ms, "value": tokens * world / (unfl_ms / 1e3) / 1e6,
+                          "note": "median of as many steps again with no L2 flush between them (this rank)"}}
     del out_f, out_b, d
     if rank == 0 and world == 1 and not args.no_extras and args.workload == DEFAULT_WORKLOAD:
         del w

@@ -65,8 +65,9 @@ def _peaks():
 C = 64
 
 
-def kernel_work(name, spec, in_bytes, o_bytes, nchunk_heads):
-    """(flops, bytes) of one launch of kernel `name` over the whole problem.
+def kernel_work(name, spec, in_bytes, o_bytes, nchunk_heads, with_A=True):
+    """(flops, bytes) of one launch of kernel `name` over the whole problem
+    (`with_A`: the forward's chunk kernel writes A for a backward).
 
     Unit: one (chunk, v-head) pair of C = 64 tokens.  Flops count the dense
     contractions the kernel's step of the method needs (2 per MAC, causal
@@ -96,16 +97,18 @@ def kernel_work(name, spec, in_bytes, o_bytes, nchunk_heads):
         "bwd_chunk": n * (4 * C * K * V + 3.5 * C * C * V + 6 * C * C * K + 2 * C ** 3),
     }
     byt = {
-        "chunk": 2 * qk + 2 * gb + A,
+        "chunk": 2 * qk + 2 * gb + (A if with_A else 0),
+        "chunk_from_A": 2 * qk + 2 * gb + A,
         "scan": 2 * qk + vv + th * V * o_bytes + st,
         "scan_states": qk + vv,
         "dh": 2 * qk + vv + 2 * st,
         "bwd_chunk": 2 * qk + 2 * vv + A + 2 * gb + (2 * qk + vv) + 2 * gb,
     }
-    base = name.split("_", 1)[1] if name.startswith(("tc_", "mma_", "simt_")) else name
-    base = {"chunk_from_A": "chunk", "wy": "chunk", "wy_from_A": "chunk"}.get(base, base)
+    raw = name.split("_", 1)[1] if name.startswith(("tc_", "mma_", "simt_")) else name
+    from_A = raw in ("chunk_from_A", "wy_from_A")  # the backward's pass reads A
+    base = {"chunk_from_A": "chunk", "wy": "chunk", "wy_from_A": "chunk"}.get(raw, raw)
     if base in mac:
-        return 2.0 * mac[base], float(byt[base])
+        return 2.0 * mac[base], float(byt["chunk_from_A" if from_A else base])
     return 0.0, 0.0
 
 
@@ -245,7 +248,7 @@ def aggregate(total_ms, tokens, steps, device):
 
 
 STEP_DESC = {"both": "gdr_fwd(o, final_state, A) + gdr_bwd(dq, dk, dv, dbeta, dg, dh0)",
-             "fwd": "gdr_fwd(o, final_state, A)",
+             "fwd": "gdr_fwd(o, final_state)",
              "bwd": "gdr_bwd(dq, dk, dv, dbeta, dg, dh0)"}
 
 
@@ -278,9 +281,12 @@ class Workload:
         self.ws_f = gdr.alloc_workspace(gdr.fwd_workspace_size(prob, opts), dev)
         self.ws_b = gdr.alloc_workspace(gdr.bwd_workspace_size(prob, opts), dev) if mode != "fwd" else None
         N, B, T, Hv, K, V = prob.N, spec.B, spec.T, spec.Hv, spec.K, spec.V
+        # A is written only where a backward reads it: the forward-only workloads
+        # return o and final_state
+        self.want_A = mode != "fwd"
         self.out_f = {"o": torch.empty(B, T, Hv, V, device=dev, dtype=o_dtype),
                       "final_state": torch.empty(N, Hv, K, V, device=dev),
-                      "A": torch.empty(B, T, Hv, 64, device=dev)}
+                      "A": torch.empty(B, T, Hv, 64, device=dev) if self.want_A else None}
         self.out_b = None
         if mode != "fwd":
             self.out_b = {"dq": torch.empty_like(d["q"]), "dk": torch.empty_like(d["k"]),
@@ -297,7 +303,7 @@ class Workload:
         """A second set of device inputs and outputs of the same shapes (contents
         copied), for steps whose copies overlap another step's kernels."""
         d = {k: (v.clone() if torch.is_tensor(v) else v) for k, v in self.d.items()}
-        out_f = {k: v.clone() for k, v in self.out_f.items()}
+        out_f = {k: (v.clone() if v is not None else None) for k, v in self.out_f.items()}
         out_b = {k: v.clone() for k, v in self.out_b.items()} if self.out_b else None
         return d, out_f, out_b
 
@@ -305,8 +311,8 @@ class Workload:
         d, out_f, _ = bufs or self.buffers()
         self.gdr.gdr_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], self.x["scale"], h0=d["h0"],
                          cu_seqlens=d["cu_seqlens"], cu_seqlens_host=self.cu_host, out=out_f,
-                         workspace=self.ws_f, cp_segments=self.cp, path=self.path, timer=timer,
-                         cp_warmup=self.cp_warmup)
+                         want_A=self.want_A, workspace=self.ws_f, cp_segments=self.cp, path=self.path,
+                         timer=timer, cp_warmup=self.cp_warmup)
 
     def run_bwd(self, timer=None, bufs=None):
         d, out_f, out_b = bufs or self.buffers()
@@ -476,10 +482,10 @@ def rooflines(spec, mode, per_kernel, peaks, nch_heads, step_ms_mean):
     # the dominant kernel among those with algorithmic work (the context-parallel
     # summaries and combines, the tables and the group sums count none)
     top = max(agg, key=lambda n: agg[n][0])
-    working = [n for n in agg if kernel_work(n, spec, in_b, o_b, nch_heads) != (0.0, 0.0)]
+    working = [n for n in agg if kernel_work(n, spec, in_b, o_b, nch_heads, mode != "fwd") != (0.0, 0.0)]
     dom = max(working, key=lambda n: agg[n][0]) if working else top
     dom_ms = agg[dom][0] / agg[dom][1]
-    fl, by = kernel_work(dom, spec, in_b, o_b, nch_heads)
+    fl, by = kernel_work(dom, spec, in_b, o_b, nch_heads, with_A=mode != "fwd")
     tc_peak = peaks["bf16_tflops"]
     alu_peak = 152 * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12  # fp32 FFMA, TFLOP/s
     if dom.startswith("simt"):
@@ -512,7 +518,9 @@ def rooflines(spec, mode, per_kernel, peaks, nch_heads, step_ms_mean):
     qk_b, v_b, gb_b = tokens * spec.Hq * K * in_b, tokens * Hv * V * in_b, tokens * Hv * 4
     A_b, st_b = tokens * Hv * 64 * 4, N * Hv * K * V * 4
     f_fl, b_fl = th * 166.6e3, th * 491.5e3
-    f_by = 2 * qk_b + v_b + 2 * gb_b + (st_b if spec.h0 else 0) + tokens * Hv * V * o_b + st_b + A_b
+    # the forward writes A only when a backward follows in the step
+    f_by = (2 * qk_b + v_b + 2 * gb_b + (st_b if spec.h0 else 0) + tokens * Hv * V * o_b + st_b
+            + (A_b if mode != "fwd" else 0))
     b_by = (2 * qk_b + 2 * v_b + 2 * gb_b + A_b + (2 * st_b if spec.h0 else st_b)
             + 2 * qk_b + v_b + 2 * gb_b + st_b)
     step_flops = (f_fl if mode != "bwd" else 0) + (b_fl if mode != "fwd" else 0)

@@ -473,8 +473,10 @@ constexpr int kChunkSmem = 1024 + (kChunkScratch > 32768 ? kChunkScratch : 32768
 // row tid % 16, four columns 4 ((tid / 16) % 4) (eight consecutive lanes on
 // eight rows: conflict-free vector accesses).
 __device__ __forceinline__ void inv_level16(const float *Ls, float *As, float *Tt, int tid) {
+    // column pairs (c4, c4 + 1) and (c4 + 2, c4 + 3) in packed fp32 FMAs: per
+    // element the same fused multiply-adds in the same order as scalar ones
     const int b = tid >> 6, r = tid & 15, c4 = ((tid >> 4) & 3) * 4, o = 32 * b;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
     const float *lrow = Ls + (o + 16 + r) * kLd + o;
 #pragma unroll
     for (int k = 0; k < 16; k += 4) {
@@ -483,14 +485,15 @@ __device__ __forceinline__ void inv_level16(const float *Ls, float *As, float *T
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const float4 a4 = *reinterpret_cast<const float4 *>(As + (o + k + q) * kLd + o + c4);
-            acc[0] = fmaf(lv[q], a4.x, acc[0]); acc[1] = fmaf(lv[q], a4.y, acc[1]);
-            acc[2] = fmaf(lv[q], a4.z, acc[2]); acc[3] = fmaf(lv[q], a4.w, acc[3]);
+            const float2 ll = make_float2(lv[q], lv[q]);
+            acc[0] = __ffma2_rn(ll, make_float2(a4.x, a4.y), acc[0]);
+            acc[1] = __ffma2_rn(ll, make_float2(a4.z, a4.w), acc[1]);
         }
     }
     float *t = Tt + (b * 16 + r) * kTLd + c4;
-    *reinterpret_cast<float4 *>(t) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    *reinterpret_cast<float4 *>(t) = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
     __syncthreads();
-    acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+    acc[0] = acc[1] = make_float2(0.f, 0.f);
     const float *drow = As + (o + 16 + r) * kLd + o + 16;
 #pragma unroll
     for (int m = 0; m < 16; m += 4) {
@@ -499,11 +502,13 @@ __device__ __forceinline__ void inv_level16(const float *Ls, float *As, float *T
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const float4 t4 = *reinterpret_cast<const float4 *>(Tt + (b * 16 + m + q) * kTLd + c4);
-            acc[0] = fmaf(dv[q], t4.x, acc[0]); acc[1] = fmaf(dv[q], t4.y, acc[1]);
-            acc[2] = fmaf(dv[q], t4.z, acc[2]); acc[3] = fmaf(dv[q], t4.w, acc[3]);
+            const float2 dd = make_float2(dv[q], dv[q]);
+            acc[0] = __ffma2_rn(dd, make_float2(t4.x, t4.y), acc[0]);
+            acc[1] = __ffma2_rn(dd, make_float2(t4.z, t4.w), acc[1]);
         }
     }
-    *reinterpret_cast<float4 *>(As + (o + 16 + r) * kLd + o + c4) = make_float4(-acc[0], -acc[1], -acc[2], -acc[3]);
+    *reinterpret_cast<float4 *>(As + (o + 16 + r) * kLd + o + c4) =
+        make_float4(-acc[0].x, -acc[0].y, -acc[1].x, -acc[1].y);
     __syncthreads();
 }
 // The whole matrix from its two 32x32 diagonal blocks: T = L[32:, :32]
@@ -511,7 +516,9 @@ __device__ __forceinline__ void inv_level16(const float *Ls, float *As, float *T
 // + 1, four columns 4 (tid % 8).
 __device__ __forceinline__ void inv_level32(const float *Ls, float *As, float *Tt, int tid) {
     const int r = 2 * (tid >> 3), c4 = (tid & 7) * 4;
-    float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
+    // rows r, r + 1; column pairs (c4, c4 + 1), (c4 + 2, c4 + 3) in packed FMAs
+    float2 a0[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    float2 a1[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
     const float *l0 = Ls + (32 + r) * kLd, *l1 = l0 + kLd;
 #pragma unroll 2
     for (int k = 0; k < 32; k += 4) {
@@ -521,17 +528,18 @@ __device__ __forceinline__ void inv_level32(const float *Ls, float *As, float *T
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const float4 a4 = *reinterpret_cast<const float4 *>(As + (k + q) * kLd + c4);
-            a0[0] = fmaf(xv[q], a4.x, a0[0]); a0[1] = fmaf(xv[q], a4.y, a0[1]);
-            a0[2] = fmaf(xv[q], a4.z, a0[2]); a0[3] = fmaf(xv[q], a4.w, a0[3]);
-            a1[0] = fmaf(yv[q], a4.x, a1[0]); a1[1] = fmaf(yv[q], a4.y, a1[1]);
-            a1[2] = fmaf(yv[q], a4.z, a1[2]); a1[3] = fmaf(yv[q], a4.w, a1[3]);
+            const float2 p0 = make_float2(a4.x, a4.y), p1 = make_float2(a4.z, a4.w);
+            const float2 xx = make_float2(xv[q], xv[q]), yy = make_float2(yv[q], yv[q]);
+            a0[0] = __ffma2_rn(xx, p0, a0[0]);
+            a0[1] = __ffma2_rn(xx, p1, a0[1]);
+            a1[0] = __ffma2_rn(yy, p0, a1[0]);
+            a1[1] = __ffma2_rn(yy, p1, a1[1]);
         }
     }
-    *reinterpret_cast<float4 *>(Tt + r * kTLd + c4) = make_float4(a0[0], a0[1], a0[2], a0[3]);
-    *reinterpret_cast<float4 *>(Tt + (r + 1) * kTLd + c4) = make_float4(a1[0], a1[1], a1[2], a1[3]);
+    *reinterpret_cast<float4 *>(Tt + r * kTLd + c4) = make_float4(a0[0].x, a0[0].y, a0[1].x, a0[1].y);
+    *reinterpret_cast<float4 *>(Tt + (r + 1) * kTLd + c4) = make_float4(a1[0].x, a1[0].y, a1[1].x, a1[1].y);
     __syncthreads();
-#pragma unroll
-    for (int e = 0; e < 4; ++e) a0[e] = a1[e] = 0.f;
+    a0[0] = a0[1] = a1[0] = a1[1] = make_float2(0.f, 0.f);
     const float *d0 = As + (32 + r) * kLd + 32, *d1 = d0 + kLd;
 #pragma unroll 2
     for (int m = 0; m < 32; m += 4) {
@@ -541,14 +549,16 @@ __device__ __forceinline__ void inv_level32(const float *Ls, float *As, float *T
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const float4 t4 = *reinterpret_cast<const float4 *>(Tt + (m + q) * kTLd + c4);
-            a0[0] = fmaf(xv[q], t4.x, a0[0]); a0[1] = fmaf(xv[q], t4.y, a0[1]);
-            a0[2] = fmaf(xv[q], t4.z, a0[2]); a0[3] = fmaf(xv[q], t4.w, a0[3]);
-            a1[0] = fmaf(yv[q], t4.x, a1[0]); a1[1] = fmaf(yv[q], t4.y, a1[1]);
-            a1[2] = fmaf(yv[q], t4.z, a1[2]); a1[3] = fmaf(yv[q], t4.w, a1[3]);
+            const float2 p0 = make_float2(t4.x, t4.y), p1 = make_float2(t4.z, t4.w);
+            const float2 xx = make_float2(xv[q], xv[q]), yy = make_float2(yv[q], yv[q]);
+            a0[0] = __ffma2_rn(xx, p0, a0[0]);
+            a0[1] = __ffma2_rn(xx, p1, a0[1]);
+            a1[0] = __ffma2_rn(yy, p0, a1[0]);
+            a1[1] = __ffma2_rn(yy, p1, a1[1]);
         }
     }
-    *reinterpret_cast<float4 *>(As + (32 + r) * kLd + c4) = make_float4(-a0[0], -a0[1], -a0[2], -a0[3]);
-    *reinterpret_cast<float4 *>(As + (33 + r) * kLd + c4) = make_float4(-a1[0], -a1[1], -a1[2], -a1[3]);
+    *reinterpret_cast<float4 *>(As + (32 + r) * kLd + c4) = make_float4(-a0[0].x, -a0[0].y, -a0[1].x, -a0[1].y);
+    *reinterpret_cast<float4 *>(As + (33 + r) * kLd + c4) = make_float4(-a1[0].x, -a1[0].y, -a1[1].x, -a1[1].y);
     __syncthreads();
 }
 

@@ -16,6 +16,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -117,16 +118,26 @@ int make_plan(const gdr_shape *s, const gdr_opts *o, int want_path, int in_f32, 
     } else if (forced == 0 && maxc > 1 && path == GDR_PATH_TC) {
         // One scan CTA per (segment, v-head), one CTA per SM.  Estimated time in
         // chunk steps of the longest segment: the scan's waves times the segment
-        // length, plus (when split) the summary's waves (two states, each ~0.8 of
-        // a scan step) and the sequential combine (~0.7 of a step per segment).
+        // length (and its warm-up chunks), plus (when split) the summary's waves
+        // (two states, each ~0.8 of a scan step) and the sequential combine (~0.7
+        // of a step per segment).  With warm-up starts (the rule of
+        // warmup_chunks) only the heads whose gates barely decay run the summary:
+        // taken as 0.3 of them, since 60-80 % of the heads have a gate that is not
+        // identically one (FlashQLA pages, page 1 "two fused kernels and automatic
+        // CP", the gate-decay paragraph; a wrong guess costs a few percent either
+        // way).
         const long long B = (long long)pl->N * s->Hv, S = device_sms();
+        const int req = o ? o->cp_warmup : 0;
         double best = 1e300;
         for (int nseg = 1; nseg <= 64 && nseg <= maxc; ++nseg) {
             const int L = (maxc + nseg - 1) / nseg;
             if (nseg > 1 && L < 4) break;
+            const int Wc = nseg == 1 || req < 0 ? 0 : (req > 0 ? req : (L >= 4 * 8 ? 8 : 0));
+            const double f = Wc > 0 ? 0.3 : 1.0;
             const double waves = (double)((B * nseg + S - 1) / S);
-            double t = waves * L;
-            if (nseg > 1) t += (double)((2 * B * nseg + S - 1) / S) * L * 0.8 + 0.7 * nseg;
+            double t = waves * (L + Wc);
+            if (nseg > 1)
+                t += std::ceil(2.0 * f * (double)(B * nseg) / (double)S) * L * 0.8 + 0.7 * nseg;
             if (t < best - 1e-9) {
                 best = t;
                 seg_len = L;

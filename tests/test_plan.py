@@ -65,6 +65,42 @@ def test_long_sequence_takes_warm_up_starts():
     assert plan(problem(T=262144, Hq=8, Hv=16), cp_warmup=3)["cp_warmup"] == 3
 
 
+def _model(n_scans, maxc, nseg, warm_req=0, share=0.3, sms=152):
+    # the planner's estimate in chunk steps, written out: the scan's waves times
+    # the segment (with its warm-up chunks), the summary's waves for the share
+    # of heads that run it (all of them without warm-up starts), the combine
+    L = math.ceil(maxc / nseg)
+    wc = 0 if nseg == 1 or warm_req < 0 else (warm_req if warm_req > 0 else (8 if L >= 32 else 0))
+    f = share if wc > 0 else 1.0
+    t = math.ceil(n_scans * nseg / sms) * (L + wc)
+    if nseg > 1:
+        t += math.ceil(2 * f * n_scans * nseg / sms) * L * 0.8 + 0.7 * nseg
+    return t, L
+
+
+def _best(n_scans, maxc, warm_req=0):
+    best = None
+    for nseg in range(1, 65):
+        t, L = _model(n_scans, maxc, nseg, warm_req)
+        if nseg > 1 and L < 4:
+            break
+        if best is None or t < best[0] - 1e-9:
+            best = (t, L)
+    return best[1]
+
+
+@pytest.mark.parametrize("T,Hv,warm", [(262144, 16, 0), (262144, 16, -1), (32768, 16, 0), (8192, 8, 0),
+                                       (16384 * 2, 64, 0), (65536, 4, 0)])
+def test_split_follows_the_cost_model(T, Hv, warm):
+    # with warm-up starts only the heads whose gates barely decay run the
+    # summary, so the long forward takes more, shorter segments than the exact
+    # split alone would (28 of 147 chunks against 19 of 216)
+    p = plan(problem(T=T, Hq=max(1, Hv // 2), Hv=Hv), cp_warmup=warm)
+    assert p["seg_len"] == _best(Hv, math.ceil(T / 64), warm)
+    if (T, Hv) == (262144, 16):
+        assert p["n_segments"] == (28 if warm == 0 else 19)
+
+
 @pytest.mark.parametrize("n", [1, 2, 5, 19, 128, 500])
 def test_forced_segment_count(n):
     p = plan(problem(), cp_segments=n)
